@@ -1,0 +1,673 @@
+/*
+ * oracle/ar_oracle.c — plain, slow CPU oracle of the gradient AllReduce.
+ *
+ * TEST INFRASTRUCTURE ONLY. The test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference arms are the only callers. It shares
+ * no code, header, table or helper with the CUDA library, and the library
+ * never calls it. Build: gcc -O2 -std=c11 -ffp-contract=off (no fast-math,
+ * no FMA contraction), so every float operation below is one IEEE binary32
+ * operation rounded to nearest even.
+ *
+ * Sources (web pages on AllReduce), cited by title and section:
+ *   [GL] "AllReduce（オールリデュース）" — jisaku.com glossary
+ *   [VL] "All-Reduce・All-Gather・All-to-Allとは？LLM分散推論のGPU通信を整理する" — vasteelab
+ *   [EN] "All-Reduce" — intelion.cloud encyclopedia
+ *   [AW] "AllReduce" — astro-wiki
+ *   [WP] "All-reduce" — wikiprompt
+ *
+ * Where the pages leave a step open, the reading taken is named here by a
+ * short tag (ring schedule, uneven split, avg, wrap, nan-order, widen, fp8,
+ * bucket, tree); each is one plain choice consistent with the pages.
+ *
+ * Pins: every function here is checked by tests against values the pages
+ * print (the worked example of [VL] §All-Reduce), hand-computed cases,
+ * closed forms, invariants (reduce-scatter then all-gather equals allreduce,
+ * replicas identical), brute force and library conversions. The FP8 block
+ * semantics are not given by the pages (they only say FP8 halves the traffic
+ * and needs quantise/dequantise plus a scale exchange, [GL] §NCCLにおける
+ * AllReduce, §勾配圧縮技術, [VL] §data typeと圧縮): parity unpinned for the
+ * choice of block size and scale rule; the arithmetic itself is pinned by
+ * format anchors, brute-force rounding and error bounds.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_I32 = 3 };
+enum { OR_SUM = 0, OR_AVG = 1, OR_MIN = 2, OR_MAX = 3 };
+
+#define OR_OK 0
+#define OR_EINVAL (-1)
+#define OR_ENOMEM (-2)
+
+static size_t or_esize(int dt) { return (dt == OR_F16 || dt == OR_BF16) ? 2u : 4u; }
+
+static float or_bits_f(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t or_f_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+/* ------------------------------------------------------------------------- */
+/* Number formats, written from their definitions.                           */
+/*   binary32: 1 sign, 8 exponent (bias 127), 23 fraction bits.              */
+/*   bfloat16: the upper 16 bits of binary32 (8 exponent, 7 fraction bits).  */
+/*   binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits, inf/NaN at 31. */
+/*   OCP FP8 E4M3: 1 sign, 4 exponent (bias 7), 3 fraction bits, no inf,     */
+/*   NaN = S.1111.111, largest finite 448, smallest normal 2^-6, smallest    */
+/*   subnormal 2^-9.                                                         */
+/* Canonical NaNs (reading nan-order): f32 0x7FC00000, bf16 0x7FC0,          */
+/* f16 0x7E00, e4m3 0x7F.                                                    */
+/* ------------------------------------------------------------------------- */
+
+uint16_t or_f32_to_bf16(float f)
+{
+    uint32_t u = or_f_bits(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return 0x7FC0;
+    /* keep the upper half, round the dropped 16 bits to nearest, ties to even;
+       a carry out of the fraction moves into the exponent (and to inf) as it should */
+    uint32_t keep = u >> 16, rem = u & 0xFFFFu;
+    if (rem > 0x8000u || (rem == 0x8000u && (keep & 1u))) keep += 1u;
+    return (uint16_t)keep;
+}
+
+float or_bf16_to_f32(uint16_t h) { return or_bits_f((uint32_t)h << 16); }
+
+/* Split a finite, non-zero |x| (as binary32) into x = m * 2^(e-23), m < 2^24. */
+static void or_split(uint32_t a, uint32_t *m, int *e)
+{
+    uint32_t ef = a >> 23;
+    if (ef == 0) { *m = a & 0x7FFFFFu; *e = -126; }           /* binary32 subnormal */
+    else { *m = (a & 0x7FFFFFu) | 0x800000u; *e = (int)ef - 127; }
+}
+
+/* k = m * 2^(e-23) / 2^q rounded to nearest integer, ties to even. */
+static uint32_t or_round_to_quantum(uint32_t m, int e, int q)
+{
+    int s = q - (e - 23);                  /* right shift that leaves units of 2^q */
+    if (s <= 0) return m << (-s);          /* not reached for the formats below */
+    if (s > 25) return 0;                  /* below half a unit: rounds to zero */
+    uint32_t k = m >> s;
+    uint32_t rem = m & ((1u << s) - 1u);
+    uint32_t half = 1u << (s - 1);
+    if (rem > half || (rem == half && (k & 1u))) k += 1u;
+    return k;
+}
+
+uint16_t or_f32_to_f16(float f)
+{
+    uint32_t u = or_f_bits(f);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return 0x7E00;                  /* NaN */
+    if (a == 0x7F800000u) return sign | 0x7C00;          /* inf */
+    if (a == 0) return sign;
+    uint32_t m; int e;
+    or_split(a, &m, &e);
+    if (e > 15) return sign | 0x7C00;                    /* >= 2^16: overflows to inf */
+    int q = (e < -14 ? -14 : e) - 10;                    /* unit in the last place at x */
+    uint32_t k = or_round_to_quantum(m, e, q);
+    /* normal: biased exponent (q+10+15), fraction k-1024; the same formula gives
+       the subnormal encoding k when q = -24, and a rounding carry lands in the
+       next binade (or on inf, 0x7C00) */
+    int32_t bits = ((q + 25) << 10) + (int32_t)k - 1024;
+    if (bits >= 0x7C00) bits = 0x7C00;
+    return (uint16_t)(sign | (uint16_t)bits);
+}
+
+float or_f16_to_f32(uint16_t h)
+{
+    int s = (h >> 15) & 1, E = (h >> 10) & 31, M = h & 1023;
+    double v;
+    if (E == 31) return M ? or_bits_f(0x7FC00000u) : (s ? -INFINITY : INFINITY);
+    if (E == 0) v = ldexp((double)M, -24);
+    else v = ldexp((double)(1024 + M), E - 25);
+    return (float)(s ? -v : v);
+}
+
+/* binary32 -> E4M3, round to nearest even, saturating to +-448 (no inf in E4M3);
+   NaN -> 0x7F. */
+uint8_t or_f32_to_e4m3(float f)
+{
+    uint32_t u = or_f_bits(f);
+    uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return 0x7F;
+    if (a == 0x7F800000u) return sign | 0x7E;
+    if (a == 0) return sign;
+    uint32_t m; int e;
+    or_split(a, &m, &e);
+    if (e >= 9) return sign | 0x7E;                      /* >= 512 > 448 */
+    int q = (e < -6 ? -6 : e) - 3;
+    uint32_t k = or_round_to_quantum(m, e, q);
+    int32_t bits = ((q + 10) << 3) + (int32_t)k - 8;     /* subnormal: q = -9 gives k */
+    if (bits > 0x7E) bits = 0x7E;                        /* saturate to the largest finite */
+    return (uint8_t)(sign | (uint8_t)bits);
+}
+
+float or_e4m3_to_f32(uint8_t b)
+{
+    int s = (b >> 7) & 1, E = (b >> 3) & 15, M = b & 7;
+    double v;
+    if (E == 15 && M == 7) return or_bits_f(0x7FC00000u);
+    if (E == 0) v = ldexp((double)M, -9);
+    else v = ldexp((double)(8 + M), E - 10);
+    return (float)(s ? -v : v);
+}
+
+void or_f32_to_bf16_n(const float *x, uint16_t *y, size_t n) { for (size_t i = 0; i < n; ++i) y[i] = or_f32_to_bf16(x[i]); }
+void or_f32_to_f16_n(const float *x, uint16_t *y, size_t n) { for (size_t i = 0; i < n; ++i) y[i] = or_f32_to_f16(x[i]); }
+void or_f32_to_e4m3_n(const float *x, uint8_t *y, size_t n) { for (size_t i = 0; i < n; ++i) y[i] = or_f32_to_e4m3(x[i]); }
+void or_bf16_to_f32_n(const uint16_t *x, float *y, size_t n) { for (size_t i = 0; i < n; ++i) y[i] = or_bf16_to_f32(x[i]); }
+void or_f16_to_f32_n(const uint16_t *x, float *y, size_t n) { for (size_t i = 0; i < n; ++i) y[i] = or_f16_to_f32(x[i]); }
+void or_e4m3_to_f32_n(const uint8_t *x, float *y, size_t n) { for (size_t i = 0; i < n; ++i) y[i] = or_e4m3_to_f32(x[i]); }
+
+/* ------------------------------------------------------------------------- */
+/* Element values and the reduction operator.                                */
+/* ------------------------------------------------------------------------- */
+
+/* One element widened for reduction. Floating types reduce in binary32
+   (reading widen: bf16/f16 widen exactly, one rounding at the end);
+   int32 reduces as a 32-bit two's-complement word (reading wrap). */
+typedef union { float f; uint32_t u; } or_val;
+
+static or_val or_load(int dt, const void *p, size_t i)
+{
+    or_val v;
+    const unsigned char *b = (const unsigned char *)p;
+    uint16_t h;
+    switch (dt) {
+    case OR_F32: memcpy(&v.f, b + 4 * i, 4); break;
+    case OR_I32: memcpy(&v.u, b + 4 * i, 4); break;
+    case OR_BF16: memcpy(&h, b + 2 * i, 2); v.f = or_bf16_to_f32(h); break;
+    default: memcpy(&h, b + 2 * i, 2); v.f = or_f16_to_f32(h); break;
+    }
+    return v;
+}
+
+static void or_store(int dt, void *p, size_t i, or_val v)
+{
+    unsigned char *b = (unsigned char *)p;
+    uint16_t h;
+    switch (dt) {
+    case OR_F32: memcpy(b + 4 * i, &v.f, 4); break;
+    case OR_I32: memcpy(b + 4 * i, &v.u, 4); break;
+    case OR_BF16: h = or_f32_to_bf16(v.f); memcpy(b + 2 * i, &h, 2); break;
+    default: h = or_f32_to_f16(v.f); memcpy(b + 2 * i, &h, 2); break;
+    }
+}
+
+/* a < b in the total order of reading nan-order: -0 < +0 (NaN handled by the caller). */
+static int or_less(float a, float b)
+{
+    return a < b || (a == b && signbit(a) && !signbit(b));
+}
+
+/* The element-wise reduction of [WP] (sum, min, max, average) and [AW]
+   §定义 ("通常是求和"). `acc` is the partial result so far, `x` the next rank's
+   value; average sums here and divides once at the end ([AW] §在 DDP 中的角色). */
+static or_val or_combine(int dt, int op, or_val acc, or_val x)
+{
+    or_val r;
+    if (dt == OR_I32) {
+        int32_t a = (int32_t)acc.u, b = (int32_t)x.u;
+        if (op == OR_SUM || op == OR_AVG) r.u = acc.u + x.u;      /* wraps modulo 2^32 */
+        else if (op == OR_MIN) r.u = (uint32_t)(b < a ? b : a);
+        else r.u = (uint32_t)(b > a ? b : a);
+        return r;
+    }
+    if (op == OR_SUM || op == OR_AVG) { r.f = acc.f + x.f; return r; }
+    if (acc.f != acc.f || x.f != x.f) { r.u = 0x7FC00000u; return r; }
+    if (op == OR_MIN) r = or_less(x.f, acc.f) ? x : acc;
+    else r = or_less(acc.f, x.f) ? x : acc;
+    return r;
+}
+
+/* average: divide the finished sum by N once (reading avg): binary32 IEEE
+   division for floats, C division (truncation toward zero) for int32. */
+static or_val or_finish(int dt, int op, or_val acc, int nranks)
+{
+    if (op != OR_AVG) return acc;
+    if (dt == OR_I32) acc.u = (uint32_t)((int32_t)acc.u / (int32_t)nranks);
+    else acc.f = acc.f / (float)nranks;
+    return acc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Chunking (reading uneven split). [GL] §Ring-AllReduceの仕組み and [AW]     */
+/* §Ring AllReduce split each rank's data into N chunks "evenly". Chunk c     */
+/* covers [c*L, min((c+1)*L, count)) with L = ceil(count/N) rounded up to a   */
+/* multiple of V = 16 bytes / element size; trailing chunks may be short or   */
+/* empty.                                                                    */
+/* ------------------------------------------------------------------------- */
+
+size_t or_chunk_len(size_t count, int nranks, size_t vec_elems)
+{
+    size_t q = (count + (size_t)nranks - 1) / (size_t)nranks;
+    return (q + vec_elems - 1) / vec_elems * vec_elems;
+}
+
+static void or_chunk(size_t count, size_t L, int c, size_t *lo, size_t *hi)
+{
+    size_t a = (size_t)c * L, b = a + L;
+    *lo = a < count ? a : count;
+    *hi = b < count ? b : count;
+}
+
+static int or_mod(int a, int n) { int m = a % n; return m < 0 ? m + n : m; }
+
+/* ------------------------------------------------------------------------- */
+/* Literal ring simulator ([GL] §Ring-AllReduceの仕組み, [AW] §Ring AllReduce  */
+/* 阶段一/阶段二, [EN] §Ring All-Reduce).                                       */
+/*                                                                           */
+/* Reading ring schedule: at reduce-scatter step s (0..N-2) every rank r     */
+/* sends its partial of chunk (r-s-1) mod N to rank r+1, which combines the  */
+/* received partial with its own value (received first). Chunk c therefore   */
+/* starts at rank c+1 and finishes at rank c after N-1 steps, folded in the  */
+/* order x_{c+1}, x_{c+2}, ..., x_{c+N=c}; rank r ends holding chunk r, the  */
+/* placement of [VL] §Reduce-Scatter (rank 0 holds the first part). At       */
+/* all-gather step s every rank r forwards chunk (r-s) mod N to r+1, which   */
+/* overwrites its copy ([AW] §阶段二: "直接覆盖本地对应位置").                    */
+/* All ranks send "at once": a step first fills every send buffer, then      */
+/* delivers them.                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* Reduce-scatter over per-rank working arrays st[r][0..count). */
+static int or_ring_rs_phase(or_val **st, int N, size_t count, size_t L, int dt, int op)
+{
+    or_val **sb = (or_val **)calloc((size_t)N, sizeof(or_val *));
+    if (!sb) return OR_ENOMEM;
+    int rc = OR_OK;
+    for (int r = 0; r < N; ++r)
+        if (!(sb[r] = (or_val *)malloc((L ? L : 1) * sizeof(or_val)))) rc = OR_ENOMEM;
+    for (int s = 0; rc == OR_OK && s < N - 1; ++s) {
+        for (int r = 0; r < N; ++r) {                     /* every rank fills its send buffer */
+            size_t lo, hi;
+            or_chunk(count, L, or_mod(r - s - 1, N), &lo, &hi);
+            memcpy(sb[r], st[r] + lo, (hi - lo) * sizeof(or_val));
+        }
+        for (int r = 0; r < N; ++r) {                     /* rank r+1 receives and combines */
+            int dst = (r + 1) % N;
+            size_t lo, hi;
+            or_chunk(count, L, or_mod(r - s - 1, N), &lo, &hi);
+            for (size_t i = lo; i < hi; ++i)
+                st[dst][i] = or_combine(dt, op, sb[r][i - lo], st[dst][i]);
+        }
+    }
+    for (int r = 0; r < N; ++r) free(sb[r]);
+    free(sb);
+    return rc;
+}
+
+/* All-gather over per-rank byte buffers buf[r][0..count*esize): rank c's
+   chunk c is complete on entry. */
+static int or_ring_ag_phase(unsigned char **buf, int N, size_t count, size_t L, size_t es)
+{
+    unsigned char **sb = (unsigned char **)calloc((size_t)N, sizeof(unsigned char *));
+    if (!sb) return OR_ENOMEM;
+    int rc = OR_OK;
+    for (int r = 0; r < N; ++r)
+        if (!(sb[r] = (unsigned char *)malloc((L ? L : 1) * es))) rc = OR_ENOMEM;
+    for (int s = 0; rc == OR_OK && s < N - 1; ++s) {
+        for (int r = 0; r < N; ++r) {
+            size_t lo, hi;
+            or_chunk(count, L, or_mod(r - s, N), &lo, &hi);
+            memcpy(sb[r], buf[r] + lo * es, (hi - lo) * es);
+        }
+        for (int r = 0; r < N; ++r) {
+            size_t lo, hi;
+            or_chunk(count, L, or_mod(r - s, N), &lo, &hi);
+            memcpy(buf[(r + 1) % N] + lo * es, sb[r], (hi - lo) * es);
+        }
+    }
+    for (int r = 0; r < N; ++r) free(sb[r]);
+    free(sb);
+    return rc;
+}
+
+static or_val **or_alloc_state(int N, size_t count)
+{
+    or_val **st = (or_val **)calloc((size_t)N, sizeof(or_val *));
+    if (!st) return NULL;
+    for (int r = 0; r < N; ++r) {
+        st[r] = (or_val *)malloc((count ? count : 1) * sizeof(or_val));
+        if (!st[r]) {
+            for (int q = 0; q < r; ++q) free(st[q]);
+            free(st);
+            return NULL;
+        }
+    }
+    return st;
+}
+
+static void or_free_state(or_val **st, int N)
+{
+    if (!st) return;
+    for (int r = 0; r < N; ++r) free(st[r]);
+    free(st);
+}
+
+static int or_check(int N, int dt, int op)
+{
+    if (N < 1 || N > 64 || dt < OR_F32 || dt > OR_I32 || op < OR_SUM || op > OR_MAX) return OR_EINVAL;
+    return OR_OK;
+}
+
+/* Ring allreduce = ring reduce-scatter + ring all-gather ([AW] §集合通信原语一览:
+   AllReduce decomposes into Reduce-Scatter + All-Gather). Every recv[r] ends
+   with the same `count` values ([GL] §AllReduceの基本動作). send[r] may equal
+   recv[r] (in place). */
+int or_ring_allreduce(const void *const *send, void *const *recv, int N, size_t count, int dt, int op)
+{
+    if (or_check(N, dt, op)) return OR_EINVAL;
+    size_t es = or_esize(dt), L = or_chunk_len(count, N, 16 / es);
+    or_val **st = or_alloc_state(N, count);
+    if (!st) return OR_ENOMEM;
+    for (int r = 0; r < N; ++r)
+        for (size_t i = 0; i < count; ++i) st[r][i] = or_load(dt, send[r], i);
+    int rc = or_ring_rs_phase(st, N, count, L, dt, op);
+    if (rc == OR_OK) {
+        for (int c = 0; c < N; ++c) {                 /* rank c finishes and rounds chunk c */
+            size_t lo, hi;
+            or_chunk(count, L, c, &lo, &hi);
+            for (size_t i = lo; i < hi; ++i) or_store(dt, recv[c], i, or_finish(dt, op, st[c][i], N));
+        }
+        rc = or_ring_ag_phase((unsigned char **)recv, N, count, L, es);
+    }
+    or_free_state(st, N);
+    return rc;
+}
+
+/* Reduce-scatter ([VL] §Reduce-Scatter, [AW] primitives table): each rank
+   holds N*recvcount values; rank c receives chunk c of the reduction
+   (recvcount values). Same ring schedule, chunk length = recvcount. */
+int or_ring_reduce_scatter(const void *const *send, void *const *recv, int N, size_t recvcount, int dt, int op)
+{
+    if (or_check(N, dt, op)) return OR_EINVAL;
+    size_t count = (size_t)N * recvcount;
+    or_val **st = or_alloc_state(N, count);
+    if (!st) return OR_ENOMEM;
+    for (int r = 0; r < N; ++r)
+        for (size_t i = 0; i < count; ++i) st[r][i] = or_load(dt, send[r], i);
+    int rc = or_ring_rs_phase(st, N, count, recvcount, dt, op);
+    if (rc == OR_OK)
+        for (int c = 0; c < N; ++c)
+            for (size_t j = 0; j < recvcount; ++j)
+                or_store(dt, recv[c], j, or_finish(dt, op, st[c][(size_t)c * recvcount + j], N));
+    or_free_state(st, N);
+    return rc;
+}
+
+/* All-gather ([VL] §All-Gather: [A],[B],[C],[D] -> [A,B,C,D] on every rank, in
+   rank order; the output is N times the input). Each rank first places its
+   own slice at slot r, then the ring all-gather phase forwards slices. */
+int or_ring_all_gather(const void *const *send, void *const *recv, int N, size_t sendcount, int dt)
+{
+    if (N < 1 || N > 64 || dt < OR_F32 || dt > OR_I32) return OR_EINVAL;
+    size_t es = or_esize(dt);
+    for (int r = 0; r < N; ++r)
+        memmove((unsigned char *)recv[r] + (size_t)r * sendcount * es, send[r], sendcount * es);
+    return or_ring_ag_phase((unsigned char **)recv, N, (size_t)N * sendcount, sendcount, es);
+}
+
+/* ------------------------------------------------------------------------- */
+/* The same ring order written per element: y[i] folds x_{c+1}[i], ...,      */
+/* x_{c+N}[i] for the chunk c holding i. Used as the cross-check of the       */
+/* simulator and for evaluating sampled elements of large problems.           */
+/* ------------------------------------------------------------------------- */
+
+static or_val or_fold_one(const or_val *x, int N, int c, int dt, int op)
+{
+    int start = (c + 1) % N;
+    or_val acc = x[start];
+    for (int k = 1; k < N; ++k) acc = or_combine(dt, op, acc, x[(start + k) % N]);
+    return or_finish(dt, op, acc, N);
+}
+
+int or_fold_allreduce(const void *const *send, void *const *recv, int N, size_t count, int dt, int op)
+{
+    if (or_check(N, dt, op)) return OR_EINVAL;
+    size_t L = or_chunk_len(count, N, 16 / or_esize(dt));
+    or_val x[64];
+    for (size_t i = 0; i < count; ++i) {
+        for (int r = 0; r < N; ++r) x[r] = or_load(dt, send[r], i);
+        or_val y = or_fold_one(x, N, (int)(i / L), dt, op);
+        for (int r = 0; r < N; ++r) or_store(dt, recv[r], i, y);
+    }
+    return OR_OK;
+}
+
+/* vals: n rows of N values (dtype dt, row-major); gidx[j]: the element's index
+   in a problem of `count` elements per rank; out[j]: the result (dtype dt). */
+int or_fold_points(const void *vals, const int64_t *gidx, size_t n, size_t count, int N, int dt, int op, void *out)
+{
+    if (or_check(N, dt, op)) return OR_EINVAL;
+    size_t L = or_chunk_len(count, N, 16 / or_esize(dt));
+    or_val x[64];
+    for (size_t j = 0; j < n; ++j) {
+        for (int r = 0; r < N; ++r) x[r] = or_load(dt, vals, j * (size_t)N + (size_t)r);
+        or_store(dt, out, j, or_fold_one(x, N, (int)((size_t)gidx[j] / L), dt, op));
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Recursive-halving order ([GL] algorithm table "Recursive Halving-Doubling",*/
+/* [AW] §其他 AllReduce 算法, [WP] §算法与实现 "成对交换"). Reading tree:          */
+/* v_r = x_r; for d = N/2, N/4, ..., 1: v_r = v_r (+) v_{r+d} for r < d;      */
+/* y = v_0. N must be a power of two.                                         */
+/* ------------------------------------------------------------------------- */
+
+static or_val or_tree_one(or_val *v, int N, int dt, int op)
+{
+    for (int d = N / 2; d >= 1; d /= 2)
+        for (int r = 0; r < d; ++r) v[r] = or_combine(dt, op, v[r], v[r + d]);
+    return or_finish(dt, op, v[0], N);
+}
+
+static int or_pow2(int N) { return N >= 1 && (N & (N - 1)) == 0; }
+
+int or_tree_allreduce(const void *const *send, void *const *recv, int N, size_t count, int dt, int op)
+{
+    if (or_check(N, dt, op) || !or_pow2(N)) return OR_EINVAL;
+    or_val v[64];
+    for (size_t i = 0; i < count; ++i) {
+        for (int r = 0; r < N; ++r) v[r] = or_load(dt, send[r], i);
+        or_val y = or_tree_one(v, N, dt, op);
+        for (int r = 0; r < N; ++r) or_store(dt, recv[r], i, y);
+    }
+    return OR_OK;
+}
+
+int or_tree_points(const void *vals, size_t n, int N, int dt, int op, void *out)
+{
+    if (or_check(N, dt, op) || !or_pow2(N)) return OR_EINVAL;
+    or_val v[64];
+    for (size_t j = 0; j < n; ++j) {
+        for (int r = 0; r < N; ++r) v[r] = or_load(dt, vals, j * (size_t)N + (size_t)r);
+        or_store(dt, out, j, or_tree_one(v, N, dt, op));
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* fp64 reference for tolerances: y*_i = sum_r x_r[i] (divided by N for avg) */
+/* and the conditioning scale S_i = sum_r |x_r[i]| (divided by N for avg).   */
+/* Floating dtypes, sum/avg only.                                            */
+/* ------------------------------------------------------------------------- */
+
+int or_reference_f64(const void *const *send, int N, size_t count, int dt, int op, double *y, double *S)
+{
+    if (or_check(N, dt, op) || dt == OR_I32 || (op != OR_SUM && op != OR_AVG)) return OR_EINVAL;
+    for (size_t i = 0; i < count; ++i) {
+        double s = 0.0, a = 0.0;
+        for (int r = 0; r < N; ++r) {
+            double x = (double)or_load(dt, send[r], i).f;
+            s += x;
+            a += fabs(x);
+        }
+        if (op == OR_AVG) { s /= N; a /= N; }
+        y[i] = s;
+        S[i] = a;
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8-compressed allreduce (reading fp8). [GL] §NCCLにおけるAllReduce and    */
+/* §勾配圧縮技術: FP8 halves the bytes of FP16; [VL] §data typeと圧縮: it needs  */
+/* quantise, dequantise and a scale exchange, and the aggregation precision   */
+/* must be managed. Each rank quantises once, before the reduction: per      */
+/* contiguous block of 128 elements (the last block may be shorter),         */
+/* amax = max|x| in binary32, s = amax / 448, q = E4M3(x / s) with rounding   */
+/* to nearest even and saturation; amax = 0 gives s = 0 and q = 0. The wire   */
+/* carries q and s. Dequantisation is one binary32 multiply float(q) * s;    */
+/* the dequantised values are reduced in the ring order in binary32 (sum or  */
+/* avg), rounded once to the output type, and all-gathered. Chunks use       */
+/* V = 16 bytes / output element size. Non-finite inputs are outside the     */
+/* method's domain.                                                          */
+/* ------------------------------------------------------------------------- */
+
+#define OR_FP8_BLOCK 128
+
+void or_fp8_quantize(const void *x, int in_dt, size_t count, uint8_t *q, float *scales)
+{
+    size_t nb = (count + OR_FP8_BLOCK - 1) / OR_FP8_BLOCK;
+    for (size_t b = 0; b < nb; ++b) {
+        size_t lo = b * OR_FP8_BLOCK, hi = lo + OR_FP8_BLOCK < count ? lo + OR_FP8_BLOCK : count;
+        float amax = 0.0f;
+        for (size_t i = lo; i < hi; ++i) {
+            float a = fabsf(or_load(in_dt, x, i).f);
+            if (a > amax) amax = a;
+        }
+        float s = amax / 448.0f;
+        scales[b] = s;
+        for (size_t i = lo; i < hi; ++i)
+            q[i] = (amax == 0.0f) ? 0 : or_f32_to_e4m3(or_load(in_dt, x, i).f / s);
+    }
+}
+
+static float or_fp8_deq(uint8_t q, float s) { return or_e4m3_to_f32(q) * s; }
+
+static int or_fp8_check(int N, int in_dt, int out_dt, int op)
+{
+    if (N < 1 || N > 64 || in_dt == OR_I32 || in_dt < OR_F32 || in_dt > OR_BF16 ||
+        out_dt == OR_I32 || out_dt < OR_F32 || out_dt > OR_BF16 || (op != OR_SUM && op != OR_AVG))
+        return OR_EINVAL;
+    return OR_OK;
+}
+
+/* Dequantised working state for every rank (quantise, then dequantise). */
+static or_val **or_fp8_state(const void *const *send, int N, size_t count, int in_dt)
+{
+    size_t nb = (count + OR_FP8_BLOCK - 1) / OR_FP8_BLOCK;
+    uint8_t *q = (uint8_t *)malloc(count ? count : 1);
+    float *s = (float *)malloc((nb ? nb : 1) * sizeof(float));
+    or_val **st = or_alloc_state(N, count);
+    if (!q || !s || !st) { free(q); free(s); or_free_state(st, N); return NULL; }
+    for (int r = 0; r < N; ++r) {
+        or_fp8_quantize(send[r], in_dt, count, q, s);
+        for (size_t i = 0; i < count; ++i) st[r][i].f = or_fp8_deq(q[i], s[i / OR_FP8_BLOCK]);
+    }
+    free(q);
+    free(s);
+    return st;
+}
+
+int or_fp8_ring_allreduce(const void *const *send, void *const *recv, int N, size_t count,
+                          int in_dt, int out_dt, int op)
+{
+    if (or_fp8_check(N, in_dt, out_dt, op)) return OR_EINVAL;
+    size_t es = or_esize(out_dt), L = or_chunk_len(count, N, 16 / es);
+    or_val **st = or_fp8_state(send, N, count, in_dt);
+    if (!st) return OR_ENOMEM;
+    int rc = or_ring_rs_phase(st, N, count, L, OR_F32, op);
+    if (rc == OR_OK) {
+        for (int c = 0; c < N; ++c) {
+            size_t lo, hi;
+            or_chunk(count, L, c, &lo, &hi);
+            for (size_t i = lo; i < hi; ++i) or_store(out_dt, recv[c], i, or_finish(OR_F32, op, st[c][i], N));
+        }
+        rc = or_ring_ag_phase((unsigned char **)recv, N, count, L, es);
+    }
+    or_free_state(st, N);
+    return rc;
+}
+
+int or_fp8_tree_allreduce(const void *const *send, void *const *recv, int N, size_t count,
+                          int in_dt, int out_dt, int op)
+{
+    if (or_fp8_check(N, in_dt, out_dt, op) || !or_pow2(N)) return OR_EINVAL;
+    or_val **st = or_fp8_state(send, N, count, in_dt);
+    if (!st) return OR_ENOMEM;
+    or_val v[64];
+    for (size_t i = 0; i < count; ++i) {
+        for (int r = 0; r < N; ++r) v[r] = st[r][i];
+        or_val y = or_tree_one(v, N, OR_F32, op);
+        for (int r = 0; r < N; ++r) or_store(out_dt, recv[r], i, y);
+    }
+    or_free_state(st, N);
+    return OR_OK;
+}
+
+/* Sampled evaluation of the FP8 ring result. blocks: nb groups of N rows of
+   `blen[j]` (<= 128) input values, each row one rank's whole quantisation
+   block j, which starts at element first[j] of a `count`-element problem.
+   out: nb rows of 128 output values (only the first blen[j] are written). */
+int or_fp8_ring_blocks(const void *blocks, const int64_t *first, const int32_t *blen, size_t nb,
+                       size_t count, int N, int in_dt, int out_dt, int op, void *out)
+{
+    if (or_fp8_check(N, in_dt, out_dt, op)) return OR_EINVAL;
+    size_t ies = or_esize(in_dt), L = or_chunk_len(count, N, 16 / or_esize(out_dt));
+    uint8_t q[OR_FP8_BLOCK];
+    float s, deq[64][OR_FP8_BLOCK];
+    for (size_t j = 0; j < nb; ++j) {
+        size_t n = (size_t)blen[j];
+        if (n > OR_FP8_BLOCK) return OR_EINVAL;
+        for (int r = 0; r < N; ++r) {
+            const unsigned char *row = (const unsigned char *)blocks + (j * (size_t)N + (size_t)r) * OR_FP8_BLOCK * ies;
+            or_fp8_quantize(row, in_dt, n, q, &s);
+            for (size_t k = 0; k < n; ++k) deq[r][k] = or_fp8_deq(q[k], s);
+        }
+        for (size_t k = 0; k < n; ++k) {
+            or_val x[64];
+            for (int r = 0; r < N; ++r) x[r].f = deq[r][k];
+            int c = (int)(((size_t)first[j] + k) / L);
+            or_store(out_dt, out, j * OR_FP8_BLOCK + k, or_fold_one(x, N, c, OR_F32, op));
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Gradient bucketing ([GL] §パフォーマンスチューニング: DDP packs many small   */
+/* tensors into one bucket per allreduce, 25 MB by default; [AW] §计算-通信重叠: */
+/* gradients become ready from the output layer backwards). Reading bucket:   */
+/* walk tensors in reverse registration order; a tensor joins the open bucket */
+/* if the bucket is empty or if its aligned end stays within cap_bytes;       */
+/* otherwise the bucket closes and a new one opens with it. Offsets are in    */
+/* elements, each rounded up to V = 16 bytes / element size. bucket_counts[b] */
+/* is the end of the last tensor in bucket b.                                 */
+/* ------------------------------------------------------------------------- */
+
+int or_bucket_plan(const uint64_t *counts, int ntensors, int esize, uint64_t cap_bytes,
+                   int32_t *bucket_of, uint64_t *offset_of, uint64_t *bucket_counts, int32_t *nbuckets)
+{
+    if (ntensors < 0 || (esize != 1 && esize != 2 && esize != 4 && esize != 8)) return OR_EINVAL;
+    uint64_t V = 16u / (uint64_t)esize, fill = 0;
+    int nb = 0, open = 0;
+    for (int t = ntensors - 1; t >= 0; --t) {
+        uint64_t start = (fill + V - 1) / V * V;
+        if (open && (start + counts[t]) * (uint64_t)esize > cap_bytes) {
+            bucket_counts[nb++] = fill;
+            fill = 0;
+            start = 0;
+        }
+        bucket_of[t] = nb;
+        offset_of[t] = start;
+        fill = start + counts[t];
+        open = 1;
+    }
+    if (open) bucket_counts[nb++] = fill;
+    *nbuckets = nb;
+    return OR_OK;
+}

@@ -1,0 +1,333 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix (no GPU).
+
+Each test pins the oracle to something other than itself: values the pages
+print, hand-computed cases, closed forms, invariants, library routines,
+error bounds, or an independent algorithm (literal ring simulator vs the
+per-element fold).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthgen
+from tests import _golden as G
+
+ALL_DT = ("f32", "bf16", "f16", "i32")
+FLOAT_DT = ("f32", "bf16", "f16")
+
+
+def _as(dtype, vals):
+    if dtype == "i32":
+        return np.array(vals, dtype=np.int32)
+    x = np.array(vals, dtype=np.float32)
+    return x if dtype == "f32" else synthgen.to_dtype(x, dtype)
+
+
+def _to_f32(dtype, a):
+    if dtype == "bf16":
+        return oracle.bf16_to_f32(a)
+    if dtype == "f16":
+        return oracle.f16_to_f32(a)
+    return a.astype(np.float32)
+
+
+def _rand(dtype, n, count, seed=0, sigma=1.0):
+    if dtype == "i32":
+        return synthgen.ranks_int(n, count, -(2**20), 2**20, base_seed=seed)
+    return synthgen.ranks_normal(n, count, sigma, base_seed=seed, dtype=dtype)
+
+
+# ---------------------------------------------------------------- page values
+
+@pytest.mark.parametrize("dtype", ["i32", "f32", "bf16", "f16"])
+@pytest.mark.parametrize("fn", ["ring", "fold", "tree"])
+def test_worked_example(dtype, fn):
+    g = G.load("worked_example_allreduce.txt")
+    send = [_as(dtype, G.nums(g[f"rank{r}"])) for r in range(4)]
+    out = getattr(oracle, f"{fn}_allreduce")(send, dtype, g["op"])
+    want = G.nums(g["expect"])
+    if dtype == "bf16":
+        # the inputs are exact in bf16 but 1111 and 2222 are not (8 significant bits):
+        # the page's exact result, rounded once by the library's conversion
+        import torch
+        want = torch.tensor(want).to(torch.bfloat16).float().tolist()
+    for y in out:
+        assert _to_f32(dtype, y).tolist() == want
+
+
+def test_all_gather_rank_order():
+    g = G.load("all_gather_rank_order.txt")
+    send = [_as("i32", G.nums(g[f"rank{r}"], int)) for r in range(4)]
+    for y in oracle.ring_all_gather(send, "i32"):
+        assert y.tolist() == G.nums(g["expect"], int)
+
+
+def test_reduce_scatter_placement():
+    g = G.load("reduce_scatter_placement.txt")
+    send = [_as("i32", G.nums(g[f"rank{r}"], int)) for r in range(2)]
+    out = oracle.ring_reduce_scatter(send, "i32", g["op"])
+    assert out[0].tolist() == G.nums(g["expect_rank0"], int)
+    assert out[1].tolist() == G.nums(g["expect_rank1"], int)
+
+
+# ---------------------------------------------------------- hand-computed pins
+
+def test_ring_start_rank():
+    g = G.load("ring_start_rank.txt")
+    n = int(g["count"])
+    send = [np.full(n, float(g[f"rank{r}"]), dtype=np.float32) for r in range(3)]
+    for fn in (oracle.ring_allreduce, oracle.fold_allreduce):
+        for y in fn(send, "f32", g["op"]):
+            assert y.tolist() == G.nums(g["expect"])
+
+
+def test_tree_order():
+    g = G.load("tree_order.txt")
+    send = [np.array([float(g[f"rank{r}"])], dtype=np.float32) for r in range(4)]
+    assert oracle.tree_allreduce(send, "f32", "sum")[0].tolist() == G.nums(g["expect_tree"])
+    assert oracle.ring_allreduce(send, "f32", "sum")[0].tolist() == G.nums(g["expect_ring"])
+
+
+def test_gpt2_buckets():
+    g = G.load("gpt2_buckets.txt")
+    shapes = synthgen.gpt2_small_param_shapes()
+    counts = [math.prod(s) for _, s in shapes]
+    assert len(counts) == 148 and sum(counts) == 124_439_808
+    esize = int(g["esize"])
+    bucket_of, offset_of, bucket_counts = oracle.bucket_plan(counts, esize, int(g["cap_bytes"]))
+    assert (bucket_counts * esize).tolist() == G.nums(g["expect_bytes"], int)
+    # every tensor lies inside its bucket, 16-byte aligned, tensors do not overlap,
+    # and bucket b holds tensors later in registration order than bucket b+1
+    for b in range(len(bucket_counts)):
+        ts = sorted((int(offset_of[t]), counts[t], t) for t in range(148) if bucket_of[t] == b)
+        end = 0
+        for off, c, t in ts:
+            assert off % (16 // esize) == 0 and off >= end
+            end = off + c
+        assert end == bucket_counts[b]
+    assert all(bucket_of[t] >= bucket_of[t + 1] for t in range(147))
+
+
+def test_fp8_block_example():
+    g = G.load("fp8_block_example.txt")
+    send = [_as("bf16", G.nums(g[f"rank{r}"])) for r in range(2)]
+    for op in ("sum", "avg"):
+        for y in oracle.fp8_ring_allreduce(send, "bf16", "bf16", op):
+            assert oracle.bf16_to_f32(y).tolist() == G.nums(g[f"expect_{op}"])
+
+
+def test_nan_and_signed_zero_min_max():
+    pz, nz = np.float32(0.0), np.float32(-0.0)
+    send = [np.array([pz, nz, 1.0, np.nan], dtype=np.float32),
+            np.array([nz, pz, np.nan, 2.0], dtype=np.float32)]
+    for fn in (oracle.ring_allreduce, oracle.tree_allreduce):
+        mn = fn(send, "f32", "min")[0].view(np.uint32).tolist()
+        mx = fn(send, "f32", "max")[0].view(np.uint32).tolist()
+        assert mn == [0x80000000, 0x80000000, 0x7FC00000, 0x7FC00000]
+        assert mx == [0x00000000, 0x00000000, 0x7FC00000, 0x7FC00000]
+    for dt, canon in (("bf16", 0x7FC0), ("f16", 0x7E00)):
+        s2 = [synthgen.to_dtype(a, dt) for a in send]
+        assert oracle.ring_allreduce(s2, dt, "min")[0].tolist() == [0x8000, 0x8000, canon, canon]
+        assert oracle.ring_allreduce(s2, dt, "max")[0].tolist() == [0x0000, 0x0000, canon, canon]
+
+
+def test_int32_wrap_and_truncating_average():
+    send = [np.array([2**31 - 1, -7, 7, -8], dtype=np.int32), np.array([1, 0, 0, 1], dtype=np.int32)]
+    assert oracle.ring_allreduce(send, "i32", "sum")[0].tolist() == [-(2**31), -7, 7, -7]
+    assert oracle.ring_allreduce(send, "i32", "avg")[0].tolist() == [-(2**30), -3, 3, -3]
+
+
+# ------------------------------------------------------------------ closed form
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("op", ["sum", "avg"])
+def test_sum_closed_form(n, op):
+    count = 2 * 1024 + 37
+    i = np.arange(count)
+    send = [(r * 1024 + (i % 1024)).astype(np.float32) for r in range(n)]
+    exact = 1024 * n * (n - 1) // 2 + n * (i % 1024)
+    want = exact / n if op == "avg" else exact
+    fns = [oracle.ring_allreduce, oracle.fold_allreduce] + ([oracle.tree_allreduce] if n & (n - 1) == 0 else [])
+    for fn in fns:
+        for y in fn(send, "f32", op):
+            assert np.array_equal(y.astype(np.float64), want.astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_low_precision_closed_form(dtype):
+    # small integers are exact in both formats and their sum is exact in binary32, so the
+    # result is the library's rounding of the exact sum (torch for bf16, numpy for fp16)
+    import torch
+    n, count = 8, 1000
+    i = np.arange(count)
+    send = [synthgen.to_dtype((r * 16 + (i % 8)).astype(np.float32) * 3, dtype) for r in range(n)]
+    exact = (3 * (16 * n * (n - 1) // 2 + n * (i % 8))).astype(np.float32)
+    if dtype == "bf16":
+        want = torch.from_numpy(exact).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    else:
+        want = exact.astype(np.float16).view(np.uint16)
+    for y in oracle.ring_allreduce(send, dtype, "sum"):
+        assert np.array_equal(y, want)
+
+
+# -------------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("dtype", ALL_DT)
+@pytest.mark.parametrize("op", ["sum", "avg", "min", "max"])
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 16])
+def test_simulator_equals_fold(dtype, op, n):
+    for count in (0, 1, 7, 33, 1021):
+        send = _rand(dtype, n, count, seed=11 * n + count)
+        ring = oracle.ring_allreduce(send, dtype, op)
+        fold = oracle.fold_allreduce(send, dtype, op)
+        for r in range(n):
+            assert np.array_equal(ring[r].view(np.uint8), ring[0].view(np.uint8))  # replicas identical
+            assert np.array_equal(fold[r].view(np.uint8), ring[0].view(np.uint8))
+
+
+@pytest.mark.parametrize("dtype", ALL_DT)
+@pytest.mark.parametrize("n", [1, 2, 4, 7, 8])
+def test_reduce_scatter_then_all_gather_is_allreduce(dtype, n):
+    v = 16 // (4 if dtype in ("f32", "i32") else 2)
+    for per in (v, 5 * v):
+        count = n * per
+        send = _rand(dtype, n, count, seed=3 + n)
+        for op in ("sum", "avg", "max"):
+            rs = oracle.ring_reduce_scatter(send, dtype, op)
+            ag = oracle.ring_all_gather(rs, dtype)
+            ar = oracle.ring_allreduce(send, dtype, op)
+            for r in range(n):
+                assert np.array_equal(ag[r].view(np.uint8), ar[r].view(np.uint8))
+
+
+@pytest.mark.parametrize("dtype", ALL_DT)
+def test_min_max_match_numpy_and_are_order_free(dtype):
+    n, count = 8, 4099
+    send = _rand(dtype, n, count, seed=5)
+    f = np.stack([_to_f32(dtype, a) if dtype != "i32" else a for a in send])
+    for op, ref in (("min", f.min(axis=0)), ("max", f.max(axis=0))):
+        outs = [oracle.ring_allreduce(send, dtype, op)[0], oracle.tree_allreduce(send, dtype, op)[0],
+                oracle.fold_allreduce(send, dtype, op)[0]]
+        for y in outs:
+            assert np.array_equal(y.view(np.uint8), outs[0].view(np.uint8))
+        got = _to_f32(dtype, outs[0]) if dtype != "i32" else outs[0]
+        assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("dtype", ALL_DT)
+@pytest.mark.parametrize("op", ["sum", "avg", "min", "max"])
+def test_single_rank_is_identity(dtype, op):
+    x = _rand(dtype, 1, 777, seed=9)
+    for fn in (oracle.ring_allreduce, oracle.tree_allreduce):
+        assert np.array_equal(fn(x, dtype, op)[0], x[0])
+
+
+def test_points_match_full_problem():
+    n, count = 8, 50_003
+    for dtype in ("f32", "bf16", "i32"):
+        send = _rand(dtype, n, count, seed=21)
+        full = oracle.ring_allreduce(send, dtype, "sum")[0]
+        idx = np.random.default_rng(0).choice(count, 500, replace=False)
+        vals = np.stack([a[idx] for a in send], axis=1)
+        assert np.array_equal(oracle.fold_points(vals, idx, count, dtype, "sum"), full[idx])
+        tfull = oracle.tree_allreduce(send, dtype, "sum")[0]
+        assert np.array_equal(oracle.tree_points(vals, dtype, "sum"), tfull[idx])
+
+
+# ------------------------------------------------------------------ error bounds
+
+def _gamma(k):
+    u = 2.0**-24
+    return k * u / (1 - k * u)
+
+
+@pytest.mark.parametrize("n", [2, 4, 8, 16])
+@pytest.mark.parametrize("op", ["sum", "avg"])
+def test_f32_error_bound(n, op):
+    # recursive summation: |fl(sum) - sum| <= gamma_{n-1} * sum|x| (Higham, Accuracy and
+    # Stability of Numerical Algorithms, 2nd ed., §4.2); a pairwise tree needs gamma_{log2 n};
+    # the final division adds one more rounding
+    count = 20_011
+    send = synthgen.ranks_normal(n, count, 1e-3, base_seed=n)
+    ystar, S = oracle.reference_f64(send, "f32", op)
+    extra = 1 if op == "avg" else 0
+    for fn, k in ((oracle.ring_allreduce, n - 1), (oracle.tree_allreduce, int(math.log2(n)))):
+        y = fn(send, "f32", op)[0].astype(np.float64)
+        bound = _gamma(k + extra) * S
+        assert np.all(np.abs(y - ystar) <= bound + 1e-300)
+        assert np.max(np.abs(y - ystar) / S) <= 1e-6
+
+
+def test_bf16_output_error_bound():
+    n, count = 8, 30_000
+    send = synthgen.ranks_normal(n, count, 1e-4, base_seed=100, dtype="bf16")
+    ystar, S = oracle.reference_f64(send, "bf16", "avg")
+    y = oracle.bf16_to_f32(oracle.ring_allreduce(send, "bf16", "avg")[0]).astype(np.float64)
+    # one bf16 rounding (relative 2^-8) on top of the binary32 sum and division
+    bound = 2.0**-8 * np.abs(ystar) + (1 + 2.0**-8) * _gamma(n) * S
+    assert np.all(np.abs(y - ystar) <= bound)
+    assert np.max(np.abs(y - ystar) / S) <= 1e-2
+
+
+def test_fp8_error_bounds():
+    n, count = 16, 128 * 300 + 77
+    send = synthgen.ranks_normal(n, count, 1e-3, base_seed=0, dtype="bf16", outlier_p=1e-3, outlier_scale=100.0)
+    ystar, S = oracle.reference_f64(send, "bf16", "sum")
+    y = oracle.bf16_to_f32(oracle.fp8_ring_allreduce(send, "bf16", "bf16", "sum")[0]).astype(np.float64)
+    # a-priori bound: E4M3 rounding (relative 2^-4 for normals, so u/(1+u) of |x|) plus
+    # half an E4M3 subnormal step s*2^-10 per element, the dequantise multiply, the
+    # binary32 sum and one bf16 rounding
+    x = np.stack([oracle.bf16_to_f32(a).astype(np.float64) for a in send])
+    sc = np.stack([np.repeat(oracle.fp8_quantize(a, "bf16")[1].astype(np.float64), 128)[:count] for a in send])
+    per = (0.0589 * np.abs(x) + sc * 2.0**-10).sum(axis=0)
+    bound = per * (1 + 2.0**-23) + _gamma(n) * (S + per) + 2.0**-8 * (np.abs(ystar) + per + _gamma(n) * S)
+    assert np.all(np.abs(y - ystar) <= bound)
+    assert np.linalg.norm(y - ystar) / np.linalg.norm(ystar) <= 6e-2
+
+
+def test_fp8_quantize_block_rules():
+    # zero block -> scale 0, codes 0; block max maps to 448 (0x7E); partial last block
+    x = np.zeros(128 + 5, dtype=np.float32)
+    x[128:] = [3.0, -1.0, 0.5, 0.0, 6.0]
+    q, s = oracle.fp8_quantize(x, "f32")
+    assert s.tolist()[0] == 0.0 and not q[:128].any()
+    assert s[1] == np.float32(6.0) / np.float32(448.0)
+    assert q[132] == 0x7E and oracle.e4m3_to_f32(q[128:133]).tolist()[4] == 448.0
+    # codes are the E4M3 rounding of x/s
+    assert np.array_equal(q[128:], oracle.f32_to_e4m3(x[128:] / s[1]))
+
+
+def test_fp8_blocks_match_full():
+    n, count = 4, 128 * 40 + 50
+    send = synthgen.ranks_normal(n, count, 1e-3, base_seed=3, dtype="bf16", outlier_p=1e-2, outlier_scale=100.0)
+    full = oracle.fp8_ring_allreduce(send, "bf16", "bf16", "sum")[0]
+    blocks_idx = [0, 7, 20, 39, 40]
+    blk = np.zeros((len(blocks_idx), n, 128), dtype=np.uint16)
+    first, blen = [], []
+    for j, b in enumerate(blocks_idx):
+        lo, hi = b * 128, min(b * 128 + 128, count)
+        for r in range(n):
+            blk[j, r, : hi - lo] = send[r][lo:hi]
+        first.append(lo)
+        blen.append(hi - lo)
+    out = oracle.fp8_ring_blocks(blk, np.array(first), np.array(blen), count, "bf16", "bf16", "sum")
+    for j, b in enumerate(blocks_idx):
+        assert np.array_equal(out[j, : blen[j]], full[first[j]: first[j] + blen[j]])
+
+
+def test_fp8_tree_and_ring_agree_up_to_order():
+    n, count = 8, 4096
+    send = synthgen.ranks_normal(n, count, 1e-3, base_seed=8, dtype="bf16")
+    a = oracle.bf16_to_f32(oracle.fp8_ring_allreduce(send, "bf16", "bf16", "avg")[0])
+    b = oracle.bf16_to_f32(oracle.fp8_tree_allreduce(send, "bf16", "bf16", "avg")[0])
+    assert np.max(np.abs(a - b)) <= 2.0**-7 * np.max(np.abs(a)) + 1e-12
+
+
+def test_empty_inputs():
+    for dtype in ALL_DT:
+        send = _rand(dtype, 4, 0)
+        assert all(y.size == 0 for y in oracle.ring_allreduce(send, dtype, "sum"))
+        assert all(y.size == 0 for y in oracle.tree_allreduce(send, dtype, "sum"))
+    assert oracle.bucket_plan([], 2, 1 << 20)[2].size == 0
