@@ -1,0 +1,203 @@
+/*
+ * ar.h — C ABI of the GB300 gradient allreduce library (libar.so).
+ *
+ * N "virtual ranks" live in one GPU's memory: rank r owns an input and an
+ * output buffer, and a collective combines all ranks' buffers element by
+ * element so that every rank ends with the same result.
+ *
+ * Sources (web pages on AllReduce), cited by title and section:
+ *   [GL] "AllReduce（オールリデュース）" — jisaku.com glossary
+ *   [VL] "All-Reduce・All-Gather・All-to-Allとは？LLM分散推論のGPU通信を整理する" — vasteelab
+ *   [AW] "AllReduce" — astro-wiki
+ *   [WP] "All-reduce" — wikiprompt
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * Memory and ownership: the caller owns every device buffer, the FP8
+ *   workspace and the stream; the library allocates no memory and never
+ *   synchronises. Pointer arrays (`sendbufs`, `recvbufs`, `tensors`) and the
+ *   count/offset arrays are HOST memory, read during the call only; the
+ *   buffers they point to are DEVICE memory of the current device (the
+ *   device selected in the calling thread), and `stream` must belong to it
+ *   (0 = the legacy default stream).
+ * Asynchrony: work is enqueued on `stream` and the call returns at once
+ *   (stream separation, [GL] §パフォーマンスチューニング; [VL] §communicationと
+ *   computeを重ねる条件). Results are valid after the stream reaches them.
+ * Errors: argument errors are detected before anything is enqueued and
+ *   return synchronously: AR_ERR_INVALID_ARGUMENT (null pointer, nranks
+ *   outside 1..AR_MAX_RANKS, unknown enum, a buffer not aligned to its
+ *   element size, workspace too small), AR_ERR_UNSUPPORTED (TREE with a
+ *   nranks that is not a power of two; MIN/MAX on the FP8 path; FP8 output
+ *   type I32), AR_ERR_ALIAS (buffers overlap other than in the documented
+ *   in-place forms). A failed launch returns AR_ERR_CUDA; ar_last_error()
+ *   holds the CUDA message. Faults inside kernels surface at the caller's
+ *   next synchronisation, as with any CUDA work. On any error nothing has
+ *   been written.
+ * Counts: `count == 0` (or an empty tensor list) is a successful no-op.
+ * Alignment: any element-aligned address works. When every pointer and the
+ *   chunk length allow 16-byte vectors the kernels use them; otherwise they
+ *   fall back to element-wide accesses with bit-identical results.
+ * Numerics: bf16/fp16 inputs widen exactly to binary32, reduce in binary32,
+ *   and round once to the output type (nearest even). int32 sums wrap modulo
+ *   2^32; int32 AVG truncates toward zero. AVG divides the finished sum once
+ *   by nranks (IEEE division for floats). MIN/MAX order -0 below +0 and turn
+ *   any NaN input into the canonical quiet NaN of the type (f32 0x7FC00000,
+ *   bf16 0x7FC0, fp16 0x7E00). SUM/AVG with NaN inputs return a NaN of
+ *   unspecified payload.
+ */
+#ifndef AR_GB300_H
+#define AR_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the runtime's cudaStream_t). */
+typedef struct CUstream_st *ar_stream_t;
+
+typedef enum {
+    AR_SUCCESS = 0,
+    AR_ERR_INVALID_ARGUMENT = 1,
+    AR_ERR_UNSUPPORTED = 2,
+    AR_ERR_ALIAS = 3,
+    AR_ERR_CUDA = 4,
+    AR_ERR_TIMEOUT = 5,
+    AR_ERR_MISMATCH = 6
+} ar_status_t;
+
+typedef enum { AR_F32 = 0, AR_F16 = 1, AR_BF16 = 2, AR_I32 = 3 } ar_dtype_t;
+
+/* Element-wise operators named in [WP] §definition (sum, min, max, average). */
+typedef enum { AR_SUM = 0, AR_AVG = 1, AR_MIN = 2, AR_MAX = 3 } ar_op_t;
+
+/* Summation orders / kernel shapes:
+ *   AR_ALGO_RING  — ring reduce-scatter kernel, then ring all-gather kernel
+ *                   ([GL] §Ring-AllReduceの仕組み; [AW] §Ring AllReduce).
+ *   AR_ALGO_FUSED — one pass: the same ring order, every element reduced once
+ *                   and stored to all N outputs. Bit-identical to RING.
+ *   AR_ALGO_TREE  — one pass in recursive-halving order ([GL] algorithm table,
+ *                   "Recursive Halving-Doubling"; [AW] §其他 AllReduce 算法):
+ *                   v_r = x_r; for d = N/2, ..., 1: v_r = v_r (+) v_{r+d}, r < d.
+ * Ring order: the ranks' data are split into N chunks ([GL] §Ring-AllReduce
+ * の仕組み, "N個のチャンクに分割"); chunk c covers elements
+ * [c*L, min((c+1)*L, count)), L = ceil(count/N) rounded up to a multiple of
+ * 16 bytes / element size (trailing chunks may be short or empty). Chunk c is
+ * folded starting at rank c+1: x_{c+1}, x_{c+2}, ..., x_{c+N} (mod N), and
+ * rank c ends holding it. */
+typedef enum { AR_ALGO_RING = 0, AR_ALGO_FUSED = 1, AR_ALGO_TREE = 2 } ar_algo_t;
+
+#define AR_MAX_RANKS 64
+#define AR_FP8_BLOCK 128
+
+/* Allreduce ([GL] §AllReduceの基本動作: every process ends with the same
+ * reduced tensor; [VL] §All-Reduceは全rankの値を集約して全rankへ返す; [AW]
+ * §定义: N processes with equal-length data).
+ *   sendbufs[r] — rank r's input: `count` elements of `dtype` (device).
+ *   recvbufs[r] — rank r's output: `count` elements (device). After the call
+ *                 every recvbufs[r] holds the same bytes.
+ * In place: recvbufs[r] == sendbufs[r] is allowed for any r. Otherwise the
+ * output buffers must not overlap each other or any input; inputs may
+ * overlap each other (they are only read). */
+ar_status_t ar_allreduce(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
+                         ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, ar_stream_t stream);
+
+/* Reduce-scatter ([VL] §Reduce-Scatterは集約後の結果をrankへ分ける: reduce
+ * element-wise, split into equal chunks, rank r keeps chunk r; [AW]
+ * primitives table). Ring order with chunk length `recvcount`.
+ *   sendbufs[r] — nranks*recvcount elements (device).
+ *   recvbufs[c] — recvcount elements: chunk c of the reduction (device).
+ * In place: recvbufs[c] == sendbufs[c] + c*recvcount elements. */
+ar_status_t ar_reduce_scatter(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t recvcount,
+                              ar_dtype_t dtype, ar_op_t op, ar_stream_t stream);
+
+/* All-gather ([VL] §All-Gatherは分割dataを連結して全rankへ配る: every rank
+ * receives all slices concatenated in rank order; [AW] primitives table).
+ *   sendbufs[r] — sendcount elements (device).
+ *   recvbufs[q] — nranks*sendcount elements; slice r lands at
+ *                 recvbufs[q] + r*sendcount for every q (device).
+ * In place: sendbufs[r] == recvbufs[r] + r*sendcount elements. A pure copy:
+ * dtype only fixes the element size. */
+ar_status_t ar_all_gather(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t sendcount,
+                          ar_dtype_t dtype, ar_stream_t stream);
+
+/* Bucket plan (host only, no CUDA call). [GL] §パフォーマンスチューニング:
+ * several small gradient tensors are packed into one bucket per allreduce,
+ * 25 MB by default in PyTorch DDP; [AW] §计算-通信重叠: gradients become ready
+ * from the output layer backwards. Tensors are walked in reverse index order;
+ * a tensor joins the open bucket if it is empty or if the tensor's end
+ * (offset rounded up to 16 bytes, plus its size) stays within cap_bytes;
+ * otherwise the bucket closes and a new one starts with it.
+ *   counts[t]         — elements of tensor t (host, ntensors entries).
+ *   bucket_of[t]      — out: bucket index of tensor t.
+ *   offset_of[t]      — out: element offset of tensor t in its bucket
+ *                       (a multiple of 16 bytes / element size).
+ *   bucket_counts[b]  — out: elements in bucket b (end of its last tensor);
+ *                       the caller provides room for ntensors entries.
+ *   nbuckets          — out: number of buckets.
+ * Padding elements between tensors are not written by flatten. */
+ar_status_t ar_bucket_plan(const size_t *counts, int ntensors, ar_dtype_t dtype, size_t cap_bytes,
+                           int *bucket_of, size_t *offset_of, size_t *bucket_counts, int *nbuckets);
+
+/* Flatten: bucket[offsets[t] + i] = tensors[t][i] for i < counts[t].
+ *   tensors[t] — device pointers (host array of ntensors); offsets in
+ *   elements of `dtype` from `bucket` (device). Offsets may address several
+ *   ranks' buckets laid out back to back, so one call can flatten every rank.
+ * Destination ranges must not overlap each other or any source. */
+ar_status_t ar_bucket_flatten(const void *const *tensors, const size_t *counts, const size_t *offsets, int ntensors,
+                              ar_dtype_t dtype, void *bucket, ar_stream_t stream);
+
+/* Unflatten: tensors[t][i] = bucket[offsets[t] + i]. Same layout rules. */
+ar_status_t ar_bucket_unflatten(const void *bucket, void *const *tensors, const size_t *counts, const size_t *offsets,
+                                int ntensors, ar_dtype_t dtype, ar_stream_t stream);
+
+/* FP8 gradient compression ([GL] §NCCLにおけるAllReduce: FP8 AllReduce halves
+ * the traffic; §勾配圧縮技術: FP8 quantisation; [VL] §data typeと圧縮は品質だけ
+ * の問題ではない: quantise, dequantise and a scale exchange are needed and the
+ * aggregation precision must be managed). Each rank's flat buffer is cut
+ * into blocks of AR_FP8_BLOCK = 128 consecutive elements (the last block may
+ * be shorter); per block amax = max|x| in binary32, s = amax / 448, and
+ * q = E4M3(x / s) rounded to nearest even with saturation to +-448
+ * (amax == 0 gives s = 0 and q = 0). Non-finite inputs give unspecified
+ * values in their block.
+ *
+ * Workspace layout (bytes, all regions 256-byte aligned):
+ *   [0, N*QS)            q of rank r at r*QS,  QS = round_up(count, 256)
+ *   [N*QS, N*QS + N*SS)  scales of rank r at N*QS + r*SS,
+ *                        SS = round_up(ceil(count/128), 64) * 4 */
+size_t ar_fp8_workspace_bytes(int nranks, size_t count);
+
+/* Quantise one buffer: in (count elements of in_dtype, F32/F16/BF16) ->
+ * q (count bytes, E4M3) and scales (ceil(count/128) floats). Device memory. */
+ar_status_t ar_quantize_fp8_blocks(const void *in, ar_dtype_t in_dtype, size_t count, uint8_t *q, float *scales,
+                                   ar_stream_t stream);
+
+/* FP8-compressed allreduce: every rank is quantised once into `workspace`
+ * (the wire format), then the dequantised values float(q)*s (one binary32
+ * multiply) are reduced in binary32 in the order `algo` names, SUM or AVG,
+ * rounded once to out_dtype (F32/F16/BF16) and written to every recvbufs[r].
+ * RING = reduce-scatter into each owner's chunk, then all-gather copies;
+ * FUSED = one pass writing all N outputs; TREE = recursive halving.
+ * Chunks use 16 bytes / out_dtype size. recvbufs must not overlap sendbufs
+ * or the workspace; ws_bytes >= ar_fp8_workspace_bytes(nranks, count). */
+ar_status_t ar_allreduce_fp8(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
+                             ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
+                             void *workspace, size_t ws_bytes, ar_stream_t stream);
+
+/* Static text for a status code. */
+const char *ar_status_string(ar_status_t status);
+
+/* Detail of the last error returned to the calling thread (e.g. the CUDA
+ * error text); "" if none. Valid until the thread's next library call. */
+const char *ar_last_error(void);
+
+/* Library version string. */
+const char *ar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_GB300_H */

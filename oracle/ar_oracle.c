@@ -226,6 +226,10 @@ static or_val or_combine(int dt, int op, or_val acc, or_val x)
    division for floats, C division (truncation toward zero) for int32. */
 static or_val or_finish(int dt, int op, or_val acc, int nranks)
 {
+    if ((op == OR_MIN || op == OR_MAX) && dt != OR_I32 && acc.f != acc.f) {
+        acc.u = 0x7FC00000u;                 /* a lone NaN (N = 1) is canonical too */
+        return acc;
+    }
     if (op != OR_AVG) return acc;
     if (dt == OR_I32) acc.u = (uint32_t)((int32_t)acc.u / (int32_t)nranks);
     else acc.f = acc.f / (float)nranks;

@@ -133,6 +133,13 @@ def test_nan_and_signed_zero_min_max():
         assert oracle.ring_allreduce(s2, dt, "max")[0].tolist() == [0x0000, 0x0000, canon, canon]
 
 
+def test_single_rank_nan_is_canonical():
+    x = np.array([np.float32(np.nan), 1.0], dtype=np.float32)
+    x.view(np.uint32)[0] = 0x7FA00001  # a NaN with a payload
+    for op in ("min", "max"):
+        assert oracle.ring_allreduce([x], "f32", op)[0].view(np.uint32).tolist() == [0x7FC00000, 0x3F800000]
+
+
 def test_int32_wrap_and_truncating_average():
     send = [np.array([2**31 - 1, -7, 7, -8], dtype=np.int32), np.array([1, 0, 0, 1], dtype=np.int32)]
     assert oracle.ring_allreduce(send, "i32", "sum")[0].tolist() == [-(2**31), -7, 7, -7]
@@ -219,7 +226,7 @@ def test_min_max_match_numpy_and_are_order_free(dtype):
 @pytest.mark.parametrize("dtype", ALL_DT)
 @pytest.mark.parametrize("op", ["sum", "avg", "min", "max"])
 def test_single_rank_is_identity(dtype, op):
-    x = _rand(dtype, 1, 777, seed=9)
+    x = _rand(dtype, 1, 777, seed=9)  # finite values
     for fn in (oracle.ring_allreduce, oracle.tree_allreduce):
         assert np.array_equal(fn(x, dtype, op)[0], x[0])
 
