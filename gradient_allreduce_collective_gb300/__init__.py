@@ -1,0 +1,193 @@
+"""GB300-native gradient allreduce: thin Python binding of libar.so.
+
+Each function here has the name of the C entry point it calls (include/ar.h)
+and only marshals arguments: tensor -> device pointer, dtype -> enum, the
+current PyTorch stream -> cudaStream_t. All work runs in the library's sm_103a
+kernels; there is no fallback path. PyTorch supplies device memory and
+streams, and must be imported before the library is loaded so that both use
+one CUDA runtime (and one current device).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+import torch  # noqa: F401  (loads the shared CUDA runtime first)
+
+from ._build import build, lib_path
+
+__all__ = [
+    "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_reduce_scatter", "ar_all_gather",
+    "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_fp8_workspace_bytes",
+    "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_status_string", "ar_last_error", "ar_version",
+    "DTYPES", "OPS", "ALGOS",
+]
+
+AR_SUCCESS, AR_ERR_INVALID_ARGUMENT, AR_ERR_UNSUPPORTED, AR_ERR_ALIAS, AR_ERR_CUDA, AR_ERR_TIMEOUT, \
+    AR_ERR_MISMATCH = range(7)
+DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3}
+DTYPE_NAMES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
+OPS = {"sum": 0, "avg": 1, "min": 2, "max": 3}
+ALGOS = {"ring": 0, "fused": 1, "tree": 2}
+FP8_BLOCK = 128
+
+
+class ArError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        self.detail = detail
+        super().__init__(f"{_status_text(status)} ({status}): {detail}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libar.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not path.exists():
+        raise ImportError(f"libar.so is not built ({path}); run gradient_allreduce_collective_gb300.build()")
+    L = ctypes.CDLL(str(path))
+    vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    L.ar_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
+    L.ar_reduce_scatter.argtypes = [pp, pp, ci, sz, ci, ci, vp]
+    L.ar_all_gather.argtypes = [pp, pp, ci, sz, ci, vp]
+    L.ar_bucket_plan.argtypes = [vp, ci, ci, sz, vp, vp, vp, vp]
+    L.ar_bucket_flatten.argtypes = [pp, vp, vp, ci, ci, vp, vp]
+    L.ar_bucket_unflatten.argtypes = [vp, pp, vp, vp, ci, ci, vp]
+    L.ar_fp8_workspace_bytes.argtypes = [ci, sz]
+    L.ar_fp8_workspace_bytes.restype = sz
+    L.ar_quantize_fp8_blocks.argtypes = [vp, ci, sz, vp, vp, vp]
+    L.ar_allreduce_fp8.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp, sz, vp]
+    for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
+                 "ar_bucket_unflatten", "ar_quantize_fp8_blocks", "ar_allreduce_fp8"):
+        getattr(L, name).restype = ci
+    L.ar_status_string.argtypes = [ci]
+    L.ar_status_string.restype = ctypes.c_char_p
+    L.ar_last_error.argtypes = []
+    L.ar_last_error.restype = ctypes.c_char_p
+    L.ar_version.argtypes = []
+    L.ar_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _status_text(st: int) -> str:
+    try:
+        return lib().ar_status_string(st).decode()
+    except Exception:  # pragma: no cover
+        return "status"
+
+
+def ar_status_string(st: int) -> str:
+    return lib().ar_status_string(st).decode()
+
+
+def ar_last_error() -> str:
+    return lib().ar_last_error().decode()
+
+
+def ar_version() -> str:
+    return lib().ar_version().decode()
+
+
+def _check(st: int) -> None:
+    if st != AR_SUCCESS:
+        raise ArError(st, ar_last_error())
+
+
+def _ptrs(ts: Sequence) -> ctypes.Array:
+    return (ctypes.c_void_p * len(ts))(*[t if isinstance(t, int) else t.data_ptr() for t in ts])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _same(ts: Sequence[torch.Tensor], what: str):
+    if len(ts) == 0:
+        raise ValueError(f"{what}: empty list")
+    t0 = ts[0]
+    for t in ts:
+        if t.dtype != t0.dtype or t.numel() != t0.numel() or not t.is_contiguous():
+            raise ValueError(f"{what}: tensors must be contiguous with one dtype and size")
+    return t0.dtype, t0.numel()
+
+
+def ar_allreduce(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], op: str = "sum",
+                 algo: str = "fused", stream=None) -> None:
+    dt, n = _same(sendbufs, "sendbufs")
+    if len(recvbufs) != len(sendbufs):
+        raise ValueError("one output per rank")
+    _same(recvbufs, "recvbufs")
+    _check(lib().ar_allreduce(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], OPS[op],
+                              ALGOS[algo], _stream(stream)))
+
+
+def ar_reduce_scatter(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], op: str = "sum",
+                      stream=None) -> None:
+    dt, n = _same(sendbufs, "sendbufs")
+    _, rc = _same(recvbufs, "recvbufs")
+    _check(lib().ar_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), rc, DTYPES[dt], OPS[op],
+                                   _stream(stream)))
+
+
+def ar_all_gather(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], stream=None) -> None:
+    dt, sc = _same(sendbufs, "sendbufs")
+    _same(recvbufs, "recvbufs")
+    _check(lib().ar_all_gather(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), sc, DTYPES[dt], _stream(stream)))
+
+
+def ar_bucket_plan(counts: Sequence[int], dtype: torch.dtype, cap_bytes: int):
+    """Host-only: (bucket_of, offset_of, bucket_counts) lists."""
+    t = len(counts)
+    c = (ctypes.c_size_t * max(t, 1))(*counts)
+    bucket_of = (ctypes.c_int * max(t, 1))()
+    offset_of = (ctypes.c_size_t * max(t, 1))()
+    bucket_counts = (ctypes.c_size_t * max(t, 1))()
+    nb = ctypes.c_int(0)
+    _check(lib().ar_bucket_plan(c, t, DTYPES[dtype], cap_bytes, bucket_of, offset_of, bucket_counts,
+                                ctypes.byref(nb)))
+    return list(bucket_of)[:t], list(offset_of)[:t], list(bucket_counts)[: nb.value]
+
+
+def ar_bucket_flatten(tensors: Sequence[torch.Tensor], offsets: Sequence[int], bucket: torch.Tensor,
+                      stream=None) -> None:
+    t = len(tensors)
+    counts = (ctypes.c_size_t * max(t, 1))(*[x.numel() for x in tensors])
+    offs = (ctypes.c_size_t * max(t, 1))(*offsets)
+    _check(lib().ar_bucket_flatten(_ptrs(tensors), counts, offs, t, DTYPES[bucket.dtype], bucket.data_ptr(),
+                                   _stream(stream)))
+
+
+def ar_bucket_unflatten(bucket: torch.Tensor, tensors: Sequence[torch.Tensor], offsets: Sequence[int],
+                        stream=None) -> None:
+    t = len(tensors)
+    counts = (ctypes.c_size_t * max(t, 1))(*[x.numel() for x in tensors])
+    offs = (ctypes.c_size_t * max(t, 1))(*offsets)
+    _check(lib().ar_bucket_unflatten(bucket.data_ptr(), _ptrs(tensors), counts, offs, t, DTYPES[bucket.dtype],
+                                     _stream(stream)))
+
+
+def ar_fp8_workspace_bytes(nranks: int, count: int) -> int:
+    return int(lib().ar_fp8_workspace_bytes(nranks, count))
+
+
+def ar_quantize_fp8_blocks(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    _check(lib().ar_quantize_fp8_blocks(x.data_ptr(), DTYPES[x.dtype], x.numel(), q.data_ptr(), scales.data_ptr(),
+                                        _stream(stream)))
+
+
+def ar_allreduce_fp8(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], workspace: torch.Tensor,
+                     op: str = "sum", algo: str = "fused", stream=None) -> None:
+    dt, n = _same(sendbufs, "sendbufs")
+    odt, _ = _same(recvbufs, "recvbufs")
+    _check(lib().ar_allreduce_fp8(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], DTYPES[odt],
+                                  OPS[op], ALGOS[algo], workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))

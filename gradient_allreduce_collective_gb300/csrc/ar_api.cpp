@@ -1,0 +1,531 @@
+// ar_api.cpp — the C ABI declared in include/ar.h: argument validation,
+// aliasing rules, the chunk plan, the bucket plan, and packing of the
+// by-value kernel argument blocks. Everything here runs on the host; nothing
+// allocates device memory or synchronises.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "ar.h"
+#include "ar_internal.h"
+
+namespace gar {
+
+int sm_count() {
+  static std::atomic<int> cache[kMaxRanks];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const bool cacheable = dev >= 0 && dev < kMaxRanks;
+  if (cacheable) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+  if (cacheable) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// in ar_reduce_<type>.cu
+cudaError_t launch_reduce_f32(int op, int mode, const ReduceArgs& a, cudaStream_t stream);
+cudaError_t launch_reduce_f16(int op, int mode, const ReduceArgs& a, cudaStream_t stream);
+cudaError_t launch_reduce_bf16(int op, int mode, const ReduceArgs& a, cudaStream_t stream);
+cudaError_t launch_reduce_i32(int op, int mode, const ReduceArgs& a, cudaStream_t stream);
+
+cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cudaStream_t stream) {
+  switch (dtype) {
+    case DT_F32: return launch_reduce_f32(op, mode, a, stream);
+    case DT_F16: return launch_reduce_f16(op, mode, a, stream);
+    case DT_BF16: return launch_reduce_bf16(op, mode, a, stream);
+    case DT_I32: return launch_reduce_i32(op, mode, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gar
+
+namespace {
+
+using namespace gar;
+
+thread_local std::string g_last_error;
+
+ar_status_t fail(ar_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+ar_status_t ok() {
+  g_last_error.clear();
+  return AR_SUCCESS;
+}
+
+ar_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(AR_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+size_t elem_size(int dt) {
+  switch (dt) {
+    case AR_F32: case AR_I32: return 4;
+    case AR_F16: case AR_BF16: return 2;
+    default: return 0;
+  }
+}
+
+bool valid_op(int op) { return op >= AR_SUM && op <= AR_MAX; }
+bool valid_algo(int a) { return a >= AR_ALGO_RING && a <= AR_ALGO_TREE; }
+bool pow2(int n) { return n >= 1 && (n & (n - 1)) == 0; }
+uintptr_t addr(const void* p) { return reinterpret_cast<uintptr_t>(p); }
+bool aligned(const void* p, size_t a) { return (addr(p) % a) == 0; }
+
+// chunk length (elements): ceil(count / N) rounded up to a multiple of `vec` elements
+size_t chunk_len(size_t count, int n, size_t vec) {
+  const size_t q = count / (size_t)n + (count % (size_t)n != 0);
+  return (q + vec - 1) / vec * vec;
+}
+
+// Overlap rules. Inputs may overlap each other (read only). An output may not
+// overlap another output, nor an input, except output o and input `pair_in[o]`
+// when the output starts exactly `pair_off[o]` bytes into that input (the
+// documented in-place forms). pair_in[o] = -1: no in-place form.
+struct Span {
+  uintptr_t lo, hi;
+  bool out;
+  int idx;
+};
+
+bool overlap_ok(const std::vector<Span>& spans, const std::vector<int>& pair_in,
+                const std::vector<uintptr_t>& pair_off) {
+  std::vector<Span> s;
+  s.reserve(spans.size());
+  for (const Span& x : spans)
+    if (x.hi > x.lo) s.push_back(x);
+  std::sort(s.begin(), s.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+  for (size_t i = 0; i < s.size(); ++i) {
+    for (size_t j = i + 1; j < s.size() && s[j].lo < s[i].hi; ++j) {
+      const Span& a = s[i];
+      const Span& b = s[j];
+      if (!a.out && !b.out) continue;
+      if (a.out && b.out) return false;
+      const Span& o = a.out ? a : b;
+      const Span& in = a.out ? b : a;
+      if (pair_in.empty() || pair_in[o.idx] != in.idx || o.lo != in.lo + pair_off[o.idx]) return false;
+    }
+  }
+  return true;
+}
+
+ar_status_t check_ptrs(const void* const* p, int n, size_t es, const char* what) {
+  for (int r = 0; r < n; ++r) {
+    if (!p[r]) return fail(AR_ERR_INVALID_ARGUMENT, std::string(what) + "[" + std::to_string(r) + "] is null");
+    if (!aligned(p[r], es))
+      return fail(AR_ERR_INVALID_ARGUMENT,
+                  std::string(what) + "[" + std::to_string(r) + "] is not aligned to the element size");
+  }
+  return AR_SUCCESS;
+}
+
+bool all_aligned16(const void* const* p, int n) {
+  for (int r = 0; r < n; ++r)
+    if (!aligned(p[r], 16)) return false;
+  return true;
+}
+
+ar_status_t common_checks(const void* const* send, void* const* recv, int n, int dtype) {
+  if (!send || !recv) return fail(AR_ERR_INVALID_ARGUMENT, "null buffer array");
+  if (n < 1 || n > AR_MAX_RANKS) return fail(AR_ERR_INVALID_ARGUMENT, "nranks must be in 1..64");
+  if (elem_size(dtype) == 0) return fail(AR_ERR_INVALID_ARGUMENT, "unknown dtype");
+  return AR_SUCCESS;
+}
+
+// Ring all-gather of chunk c (owned by rank c, already in recv[c]) to every
+// other rank; `es` bytes per element, chunk length L elements.
+ar_status_t ring_gather(void* const* recv, int n, size_t count, size_t L, size_t es, bool vec, cudaStream_t s) {
+  if (n == 1) return AR_SUCCESS;
+  GatherArgs g{};
+  g.nranks = n;
+  g.skip_mask = (n == 64) ? ~0ull : ((1ull << n) - 1);
+  for (int c = 0; c < n; ++c) {
+    const size_t off = (size_t)c * L < count ? (size_t)c * L * es : 0;
+    g.src[c] = static_cast<const char*>(recv[c]) + off;
+    g.dst[c] = recv[c];
+  }
+  int unit;
+  if (vec) {
+    unit = 16;
+    g.units = count * es / 16;
+    g.Lu = L * es / 16;
+    g.tail_bytes = count * es % 16;
+    g.Lb = L * es;
+  } else {
+    unit = (int)es;
+    g.units = count;
+    g.Lu = L;
+  }
+  const cudaError_t e = launch_gather(unit, g, s);
+  return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "all-gather launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ar_version(void) { return "gradient-allreduce-gb300 0.1.0 (sm_103a)"; }
+
+const char* ar_status_string(ar_status_t st) {
+  switch (st) {
+    case AR_SUCCESS: return "success";
+    case AR_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case AR_ERR_UNSUPPORTED: return "unsupported combination";
+    case AR_ERR_ALIAS: return "buffers overlap";
+    case AR_ERR_CUDA: return "CUDA error";
+    case AR_ERR_TIMEOUT: return "timed out";
+    case AR_ERR_MISMATCH: return "collective calls do not match";
+    default: return "unknown status";
+  }
+}
+
+const char* ar_last_error(void) { return g_last_error.c_str(); }
+
+ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                         ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, ar_stream_t stream) {
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
+  if (st != AR_SUCCESS) return st;
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if (algo == AR_ALGO_TREE && !pow2(nranks))
+    return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
+  if (count == 0) return ok();
+  const size_t es = elem_size(dtype);
+  if (count > SIZE_MAX / es / 2) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if ((st = check_ptrs(sendbufs, nranks, es, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, es, "recvbufs")) != AR_SUCCESS) return st;
+  const size_t bytes = count * es;
+  std::vector<Span> spans;
+  spans.reserve(2 * (size_t)nranks);
+  std::vector<int> pair_in(nranks);
+  std::vector<uintptr_t> pair_off(nranks, 0);
+  for (int r = 0; r < nranks; ++r) {
+    spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + bytes, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + bytes, true, r});
+    pair_in[r] = r;  // in place: recvbufs[r] == sendbufs[r]
+  }
+  if (!overlap_ok(spans, pair_in, pair_off)) return fail(AR_ERR_ALIAS, "buffers overlap");
+
+  const size_t L = chunk_len(count, nranks, 16 / es);
+  const bool vec = all_aligned16(sendbufs, nranks) && all_aligned16(recvbufs, nranks);
+  ReduceArgs a{};
+  a.nranks = nranks;
+  a.count = count;
+  a.L = L;
+  a.vec = vec ? 1 : 0;
+  for (int r = 0; r < nranks; ++r) a.src[r] = sendbufs[r];
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (algo == AR_ALGO_RING) {
+    for (int c = 0; c < nranks; ++c)
+      a.dst[c] = static_cast<char*>(recvbufs[c]) + ((size_t)c * L < count ? (size_t)c * L * es : 0);
+    const cudaError_t e = launch_reduce(dtype, op, MODE_RS, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter launch");
+    if ((st = ring_gather(recvbufs, nranks, count, L, es, vec, s)) != AR_SUCCESS) return st;
+    return ok();
+  }
+  for (int r = 0; r < nranks; ++r) a.dst[r] = recvbufs[r];
+  const cudaError_t e = launch_reduce(dtype, op, algo == AR_ALGO_TREE ? MODE_FUSED_TREE : MODE_FUSED_RING, a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "allreduce launch");
+  return ok();
+}
+
+ar_status_t ar_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t recvcount,
+                              ar_dtype_t dtype, ar_op_t op, ar_stream_t stream) {
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
+  if (st != AR_SUCCESS) return st;
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (recvcount == 0) return ok();
+  const size_t es = elem_size(dtype);
+  if (recvcount > SIZE_MAX / es / (size_t)nranks / 2) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if ((st = check_ptrs(sendbufs, nranks, es, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, es, "recvbufs")) != AR_SUCCESS) return st;
+  const size_t rb = recvcount * es;
+  std::vector<Span> spans;
+  std::vector<int> pair_in(nranks);
+  std::vector<uintptr_t> pair_off(nranks);
+  for (int r = 0; r < nranks; ++r) {
+    spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + rb * (size_t)nranks, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + rb, true, r});
+    pair_in[r] = r;  // in place: recvbufs[c] == sendbufs[c] + c*recvcount
+    pair_off[r] = (uintptr_t)r * rb;
+  }
+  if (!overlap_ok(spans, pair_in, pair_off)) return fail(AR_ERR_ALIAS, "buffers overlap");
+  ReduceArgs a{};
+  a.nranks = nranks;
+  a.count = recvcount * (size_t)nranks;
+  a.L = recvcount;
+  a.vec = (all_aligned16(sendbufs, nranks) && all_aligned16(recvbufs, nranks) && rb % 16 == 0) ? 1 : 0;
+  for (int r = 0; r < nranks; ++r) {
+    a.src[r] = sendbufs[r];
+    a.dst[r] = recvbufs[r];
+  }
+  const cudaError_t e = launch_reduce(dtype, op, MODE_RS, a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "reduce-scatter launch");
+}
+
+ar_status_t ar_all_gather(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t sendcount,
+                          ar_dtype_t dtype, ar_stream_t stream) {
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
+  if (st != AR_SUCCESS) return st;
+  if (sendcount == 0) return ok();
+  const size_t es = elem_size(dtype);
+  if (sendcount > SIZE_MAX / es / (size_t)nranks / 2) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if ((st = check_ptrs(sendbufs, nranks, es, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, es, "recvbufs")) != AR_SUCCESS) return st;
+  const size_t sb = sendcount * es;
+  std::vector<Span> spans;
+  // in place: sendbufs[r] == recvbufs[r] + r*sendcount (the input lies inside the output)
+  std::vector<int> pair_in;
+  std::vector<uintptr_t> pair_off;
+  GatherArgs g{};
+  g.nranks = nranks;
+  for (int r = 0; r < nranks; ++r) {
+    const bool inplace = addr(sendbufs[r]) == addr(recvbufs[r]) + (uintptr_t)r * sb;
+    if (inplace) g.skip_mask |= 1ull << r;
+    else spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + sb, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + sb * (size_t)nranks, true, r});
+    g.src[r] = sendbufs[r];
+    g.dst[r] = recvbufs[r];
+  }
+  if (!overlap_ok(spans, pair_in, pair_off)) return fail(AR_ERR_ALIAS, "buffers overlap");
+  int unit;
+  if (all_aligned16(sendbufs, nranks) && all_aligned16(recvbufs, nranks) && sb % 16 == 0) {
+    unit = 16;
+    g.units = sb * (size_t)nranks / 16;
+    g.Lu = sb / 16;
+  } else {
+    unit = (int)es;
+    g.units = sendcount * (size_t)nranks;
+    g.Lu = sendcount;
+  }
+  const cudaError_t e = launch_gather(unit, g, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "all-gather launch");
+}
+
+ar_status_t ar_bucket_plan(const size_t* counts, int ntensors, ar_dtype_t dtype, size_t cap_bytes, int* bucket_of,
+                           size_t* offset_of, size_t* bucket_counts, int* nbuckets) {
+  if (ntensors < 0) return fail(AR_ERR_INVALID_ARGUMENT, "ntensors < 0");
+  if (!nbuckets || (ntensors > 0 && (!counts || !bucket_of || !offset_of || !bucket_counts)))
+    return fail(AR_ERR_INVALID_ARGUMENT, "null pointer");
+  const size_t es = elem_size(dtype);
+  if (es == 0) return fail(AR_ERR_INVALID_ARGUMENT, "unknown dtype");
+  const size_t vec = 16 / es;
+  size_t fill = 0;  // elements used in the open bucket
+  int nb = 0;
+  bool open = false;
+  for (int t = ntensors - 1; t >= 0; --t) {  // gradients are ready from the last layer backwards
+    if (counts[t] > SIZE_MAX / es / 4) return fail(AR_ERR_INVALID_ARGUMENT, "tensor too large");
+    size_t start = (fill + vec - 1) / vec * vec;
+    if (open && (start + counts[t]) * es > cap_bytes) {
+      bucket_counts[nb++] = fill;
+      start = 0;
+    }
+    bucket_of[t] = nb;
+    offset_of[t] = start;
+    fill = start + counts[t];
+    open = true;
+  }
+  if (open) bucket_counts[nb++] = fill;
+  *nbuckets = nb;
+  return ok();
+}
+
+}  // extern "C"
+
+namespace {
+
+// Flatten (to_bucket = true) or unflatten: batched range copies.
+ar_status_t bucket_copy(const void* const* srcs_or_null, void* const* dsts_or_null, const void* bucket_src,
+                        void* bucket_dst, const size_t* counts, const size_t* offsets, int ntensors, int dtype,
+                        cudaStream_t s) {
+  const bool flatten = bucket_dst != nullptr;
+  const size_t es = elem_size(dtype);
+  if (es == 0) return fail(AR_ERR_INVALID_ARGUMENT, "unknown dtype");
+  if (ntensors < 0) return fail(AR_ERR_INVALID_ARGUMENT, "ntensors < 0");
+  if (ntensors == 0) return ok();
+  if (!counts || !offsets) return fail(AR_ERR_INVALID_ARGUMENT, "null counts/offsets");
+  const void* const* tens_in = srcs_or_null;
+  void* const* tens_out = dsts_or_null;
+  if (flatten ? !tens_in : !tens_out) return fail(AR_ERR_INVALID_ARGUMENT, "null tensor array");
+  const char* bucket = flatten ? static_cast<const char*>(bucket_dst) : static_cast<const char*>(bucket_src);
+  if (!bucket) return fail(AR_ERR_INVALID_ARGUMENT, "null bucket");
+  if (!aligned(bucket, es)) return fail(AR_ERR_INVALID_ARGUMENT, "bucket is not aligned to the element size");
+  std::vector<Span> spans;
+  spans.reserve(2 * (size_t)ntensors);
+  for (int t = 0; t < ntensors; ++t) {
+    if (counts[t] == 0) continue;
+    const void* tp = flatten ? tens_in[t] : tens_out[t];
+    if (!tp) return fail(AR_ERR_INVALID_ARGUMENT, "tensor " + std::to_string(t) + " is null");
+    if (!aligned(tp, es))
+      return fail(AR_ERR_INVALID_ARGUMENT, "tensor " + std::to_string(t) + " is not aligned to the element size");
+    if (counts[t] > SIZE_MAX / es / 4 || offsets[t] > SIZE_MAX / es / 4)
+      return fail(AR_ERR_INVALID_ARGUMENT, "tensor too large");
+    const uintptr_t b = addr(bucket) + offsets[t] * es, n = counts[t] * es;
+    spans.push_back({addr(tp), addr(tp) + n, !flatten, t});
+    spans.push_back({b, b + n, flatten, t});
+  }
+  if (!overlap_ok(spans, {}, {})) return fail(AR_ERR_ALIAS, "buffers overlap");
+  MultiCopyArgs a{};
+  auto flush = [&]() -> ar_status_t {
+    if (a.nitems == 0) return AR_SUCCESS;
+    const cudaError_t e = launch_multicopy(a, s);
+    a.nitems = 0;
+    return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "bucket copy launch");
+  };
+  uint64_t tiles = 0;
+  for (int t = 0; t < ntensors; ++t) {
+    if (counts[t] == 0) continue;
+    const uint64_t n = counts[t] * es;
+    const uint64_t nt = (n + kCopyTile - 1) / kCopyTile;
+    if (a.nitems == kMaxCopyItems || tiles + nt > 0xFFFFFFFFull) {
+      if (ar_status_t st = flush(); st != AR_SUCCESS) return st;
+      tiles = 0;
+    }
+    char* b = const_cast<char*>(bucket) + offsets[t] * es;
+    CopyItem& it = a.item[a.nitems];
+    it.src = flatten ? tens_in[t] : b;
+    it.dst = flatten ? static_cast<void*>(b) : tens_out[t];
+    it.bytes = n;
+    a.tile_start[a.nitems] = (uint32_t)tiles;
+    tiles += nt;
+    a.nitems += 1;
+    a.tile_start[a.nitems] = (uint32_t)tiles;
+  }
+  if (ar_status_t st = flush(); st != AR_SUCCESS) return st;
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+ar_status_t ar_bucket_flatten(const void* const* tensors, const size_t* counts, const size_t* offsets, int ntensors,
+                              ar_dtype_t dtype, void* bucket, ar_stream_t stream) {
+  if (!bucket && ntensors > 0) return fail(AR_ERR_INVALID_ARGUMENT, "null bucket");
+  return bucket_copy(tensors, nullptr, nullptr, bucket, counts, offsets, ntensors, dtype,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+ar_status_t ar_bucket_unflatten(const void* bucket, void* const* tensors, const size_t* counts, const size_t* offsets,
+                                int ntensors, ar_dtype_t dtype, ar_stream_t stream) {
+  if (!bucket && ntensors > 0) return fail(AR_ERR_INVALID_ARGUMENT, "null bucket");
+  return bucket_copy(nullptr, tensors, bucket, nullptr, counts, offsets, ntensors, dtype,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t ar_fp8_workspace_bytes(int nranks, size_t count) {
+  if (nranks < 1 || nranks > AR_MAX_RANKS || count > (SIZE_MAX >> 8) / AR_MAX_RANKS) return 0;
+  const size_t qs = (count + 255) / 256 * 256;
+  const size_t nblocks = (count + AR_FP8_BLOCK - 1) / AR_FP8_BLOCK;
+  const size_t ss = (nblocks + 63) / 64 * 64 * sizeof(float);
+  return (size_t)nranks * (qs + ss);
+}
+
+ar_status_t ar_quantize_fp8_blocks(const void* in, ar_dtype_t in_dtype, size_t count, uint8_t* q, float* scales,
+                                   ar_stream_t stream) {
+  if (in_dtype != AR_F32 && in_dtype != AR_F16 && in_dtype != AR_BF16)
+    return fail(AR_ERR_INVALID_ARGUMENT, "in_dtype must be F32, F16 or BF16");
+  if (count == 0) return ok();
+  if (!in || !q || !scales) return fail(AR_ERR_INVALID_ARGUMENT, "null pointer");
+  const size_t es = elem_size(in_dtype);
+  if (count > SIZE_MAX / es / 4) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if (!aligned(in, es) || !aligned(scales, 4))
+    return fail(AR_ERR_INVALID_ARGUMENT, "buffer not aligned to its element size");
+  const size_t nblocks = (count + AR_FP8_BLOCK - 1) / AR_FP8_BLOCK;
+  std::vector<Span> spans = {{addr(in), addr(in) + count * es, false, 0},
+                             {addr(q), addr(q) + count, true, 0},
+                             {addr(scales), addr(scales) + nblocks * 4, true, 1}};
+  if (!overlap_ok(spans, {}, {})) return fail(AR_ERR_ALIAS, "buffers overlap");
+  Fp8QuantArgs a{};
+  a.src[0] = in;
+  a.q[0] = q;
+  a.s[0] = scales;
+  a.count = count;
+  a.nranks = 1;
+  const bool vec = aligned(in, 16) && aligned(q, 8);
+  const cudaError_t e = launch_fp8_quant(in_dtype, vec, a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "quantise launch");
+}
+
+ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                             ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo, void* workspace,
+                             size_t ws_bytes, ar_stream_t stream) {
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, in_dtype);
+  if (st != AR_SUCCESS) return st;
+  if (in_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating input type");
+  if (elem_size(out_dtype) == 0) return fail(AR_ERR_INVALID_ARGUMENT, "unknown out_dtype");
+  if (out_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating output type");
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (op != AR_SUM && op != AR_AVG) return fail(AR_ERR_UNSUPPORTED, "FP8 path supports SUM and AVG");
+  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if (algo == AR_ALGO_TREE && !pow2(nranks))
+    return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
+  if (count == 0) return ok();
+  const size_t need = ar_fp8_workspace_bytes(nranks, count);
+  if (need == 0) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if (!workspace) return fail(AR_ERR_INVALID_ARGUMENT, "null workspace");
+  if (ws_bytes < need) return fail(AR_ERR_INVALID_ARGUMENT, "workspace too small");
+  if (!aligned(workspace, 16)) return fail(AR_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+  const size_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
+  if ((st = check_ptrs(sendbufs, nranks, ies, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, oes, "recvbufs")) != AR_SUCCESS) return st;
+  std::vector<Span> spans;
+  for (int r = 0; r < nranks; ++r) {
+    spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + count * ies, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + count * oes, true, r});
+  }
+  spans.push_back({addr(workspace), addr(workspace) + need, true, nranks});
+  if (!overlap_ok(spans, {}, {})) return fail(AR_ERR_ALIAS, "buffers overlap");
+
+  const size_t qs = (count + 255) / 256 * 256;
+  const size_t ss = ((count + AR_FP8_BLOCK - 1) / AR_FP8_BLOCK + 63) / 64 * 64 * sizeof(float);
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  Fp8QuantArgs qa{};
+  qa.nranks = nranks;
+  qa.count = count;
+  for (int r = 0; r < nranks; ++r) {
+    qa.src[r] = sendbufs[r];
+    qa.q[r] = reinterpret_cast<uint8_t*>(ws + (size_t)r * qs);
+    qa.s[r] = reinterpret_cast<float*>(ws + (size_t)nranks * qs + (size_t)r * ss);
+  }
+  cudaError_t e = launch_fp8_quant(in_dtype, all_aligned16(sendbufs, nranks), qa, s);
+  if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
+
+  const size_t L = chunk_len(count, nranks, 16 / oes);
+  const bool vec = all_aligned16(recvbufs, nranks);
+  Fp8ReduceArgs ra{};
+  ra.nranks = nranks;
+  ra.count = count;
+  ra.L = L;
+  ra.vec = vec ? 1 : 0;
+  for (int r = 0; r < nranks; ++r) {
+    ra.q[r] = qa.q[r];
+    ra.s[r] = qa.s[r];
+  }
+  if (algo == AR_ALGO_RING) {
+    for (int c = 0; c < nranks; ++c)
+      ra.dst[c] = static_cast<char*>(recvbufs[c]) + ((size_t)c * L < count ? (size_t)c * L * oes : 0);
+    e = launch_fp8_reduce(out_dtype, op, MODE_RS, ra, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8 reduce-scatter launch");
+    if ((st = ring_gather(recvbufs, nranks, count, L, oes, vec, s)) != AR_SUCCESS) return st;
+    return ok();
+  }
+  for (int r = 0; r < nranks; ++r) ra.dst[r] = recvbufs[r];
+  e = launch_fp8_reduce(out_dtype, op, algo == AR_ALGO_TREE ? MODE_FUSED_TREE : MODE_FUSED_RING, ra, s);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "fp8 allreduce launch");
+}
+
+}  // extern "C"

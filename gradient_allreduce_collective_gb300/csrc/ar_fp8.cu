@@ -1,0 +1,311 @@
+// ar_fp8.cu — FP8 (E4M3) gradient compression for the allreduce (sm_103a).
+//
+// FP8 on the wire halves the bytes of FP16 ("AllReduce（オールリデュース）"
+// glossary, §NCCLにおけるAllReduce and §勾配圧縮技術) at the cost of quantise /
+// dequantise work and a scale exchange ("All-Reduce・All-Gather・All-to-All
+// とは？" vasteelab, §data typeと圧縮は品質だけの問題ではない). Each rank is
+// quantised once, before the reduction, per block of 128 consecutive
+// elements: amax = max|x| (binary32), s = amax / 448, q = E4M3(x / s) with
+// round-to-nearest-even and saturation; amax = 0 gives s = 0, q = 0.
+//
+//  k_fp8_quant_vec     one group of 128/V lanes per block (16 lanes of 8 bf16
+//                      or fp16, 32 lanes of 4 fp32): 16-byte loads, amax by
+//                      xor shuffles inside the group, V code bytes per lane.
+//  k_fp8_quant_scalar  one warp per block, for a short last block or inputs
+//                      that are not 16-byte aligned.
+//  k_fp8_reduce        dequantise float(q) * s (one binary32 multiply),
+//                      fold in ring or tree order in binary32, SUM or AVG,
+//                      round once to the output type, store to the chunk
+//                      owner or to all N outputs.
+#include <cstdint>
+
+#include "ar_device.cuh"
+
+namespace gar {
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+  return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constant__ Fp8QuantArgs A) {
+  constexpr int B = Fmt<DT>::bytes, V = 16 / B, G = kFp8Block / V, GPW = 32 / G;
+  const uint64_t nfull = A.count / kFp8Block;
+  const uint64_t tasks = (uint64_t)A.nranks * nfull;  // (rank, block) pairs
+  const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
+  const uint64_t warp0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+  const uint64_t wtasks = (tasks + GPW - 1) / GPW;
+  for (uint64_t w = warp0; w < wtasks; w += nwarps) {  // uniform across the warp
+    const uint64_t task = w * GPW + g;
+    const bool valid = task < tasks;
+    int r = 0;
+    uint64_t b = 0;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (valid) {
+      r = (int)(task / nfull);
+      b = task - (uint64_t)r * nfull;
+      raw = __ldcs(reinterpret_cast<const uint4*>(static_cast<const char*>(A.src[r]) +
+                                                  (b * kFp8Block + (uint64_t)gl * V) * B));
+    }
+    float x[V];
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      x[k] = to_f32<DT>(get_lane<B>(raw, k));
+      amax = fmaxf(amax, fabsf(x[k]));
+    }
+#pragma unroll
+    for (int o = G / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = __fdiv_rn(amax, 448.0f);
+    uint32_t word[(V + 3) / 4] = {};
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const uint32_t q = (amax == 0.0f) ? 0u : f32_to_e4m3(__fdiv_rn(x[k], s));
+      word[k >> 2] |= q << ((k & 3) * 8);
+    }
+    if (valid) {
+      uint8_t* qp = A.q[r] + b * kFp8Block + (uint64_t)gl * V;
+      if constexpr (V == 8) __stcs(reinterpret_cast<uint2*>(qp), make_uint2(word[0], word[1]));
+      else __stcs(reinterpret_cast<unsigned int*>(qp), word[0]);
+      if (gl == 0) A.s[r][b] = s;
+    }
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_fp8_quant_scalar(const __grid_constant__ Fp8QuantArgs A) {
+  constexpr int B = Fmt<DT>::bytes;
+  const uint64_t nblocks = (A.count + kFp8Block - 1) / kFp8Block;
+  const uint64_t nb = nblocks - A.first_block;
+  const uint64_t tasks = (uint64_t)A.nranks * nb;
+  const int lane = threadIdx.x & 31;
+  const uint64_t warp0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+  for (uint64_t w = warp0; w < tasks; w += nwarps) {
+    const int r = (int)(w / nb);
+    const uint64_t b = A.first_block + (w - (uint64_t)r * nb);
+    const uint64_t lo = b * kFp8Block;
+    const char* src = static_cast<const char*>(A.src[r]);
+    float x[4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t e = lo + lane + 32 * k;
+      uint32_t bits = 0;
+      if (e < A.count) {
+        if constexpr (B == 4) bits = *reinterpret_cast<const uint32_t*>(src + e * 4);
+        else bits = *reinterpret_cast<const uint16_t*>(src + e * 2);
+      }
+      x[k] = to_f32<DT>(bits);
+      amax = fmaxf(amax, fabsf(x[k]));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = __fdiv_rn(amax, 448.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t e = lo + lane + 32 * k;
+      if (e < A.count) A.q[r][e] = (uint8_t)((amax == 0.0f) ? 0u : f32_to_e4m3(__fdiv_rn(x[k], s)));
+    }
+    if (lane == 0) A.s[r][b] = s;
+  }
+}
+
+template <class K> static int resident_blocks(K kernel) {
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1) b = 1;
+  return b;
+}
+
+template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& a, cudaStream_t stream) {
+  static const int res_v = resident_blocks(k_fp8_quant_vec<DT>);
+  static const int res_s = resident_blocks(k_fp8_quant_scalar<DT>);
+  constexpr int GPW = 32 / (kFp8Block / (16 / Fmt<DT>::bytes));
+  const uint64_t nblocks = (a.count + kFp8Block - 1) / kFp8Block;
+  Fp8QuantArgs b = a;
+  if (vec) {
+    const uint64_t nfull = a.count / kFp8Block;
+    if (nfull > 0) {
+      const uint64_t warps = ((uint64_t)a.nranks * nfull + GPW - 1) / GPW;
+      k_fp8_quant_vec<DT><<<grid_for(warps * 32, res_v), kThreads, 0, stream>>>(a);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    b.first_block = nfull;
+  } else {
+    b.first_block = 0;
+  }
+  if (b.first_block < nblocks) {
+    const uint64_t warps = (uint64_t)a.nranks * (nblocks - b.first_block);
+    k_fp8_quant_scalar<DT><<<grid_for(warps * 32, res_s), kThreads, 0, stream>>>(b);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream) {
+  switch (in_dtype) {
+    case DT_F32: return launch_fp8_quant_dt<DT_F32>(vec, a, stream);
+    case DT_F16: return launch_fp8_quant_dt<DT_F16>(vec, a, stream);
+    case DT_BF16: return launch_fp8_quant_dt<DT_BF16>(vec, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// ---------------------------------------------------------------- dequantise + reduce
+
+template <int VV> struct Fp8Ld {
+  static constexpr int V = VV;
+  using Acc = float;
+  struct Raw {
+    uint32_t q[(V + 3) / 4];
+    float s;
+  };
+  const Fp8ReduceArgs& A;
+  uint64_t e0;  // first element of the item
+
+  __device__ __forceinline__ Raw load(int r) const {
+    Raw w;
+    const uint8_t* qp = A.q[r] + e0;
+    if constexpr (V == 8) {
+      const uint2 t = __ldcs(reinterpret_cast<const uint2*>(qp));
+      w.q[0] = t.x;
+      w.q[1] = t.y;
+    } else if constexpr (V == 4) {
+      w.q[0] = __ldcs(reinterpret_cast<const unsigned int*>(qp));
+    } else {
+      w.q[0] = *qp;
+    }
+    w.s = __ldg(A.s[r] + (e0 / kFp8Block));
+    return w;
+  }
+  __device__ __forceinline__ void unpack(const Raw& w, Acc (&a)[V]) const {
+#pragma unroll
+    for (int k = 0; k < V; ++k) a[k] = __fmul_rn(e4m3_to_f32((w.q[k >> 2] >> ((k & 3) * 8)) & 0xFFu), w.s);
+  }
+  __device__ __forceinline__ static Acc comb(Acc a, Acc b) { return __fadd_rn(a, b); }
+};
+
+template <int ODT, int OP, int MODE, int MAXN, bool VEC>
+__device__ __forceinline__ void fp8_item(const Fp8ReduceArgs& A, uint64_t i, int c, uint64_t ci) {
+  constexpr int B = Fmt<ODT>::bytes;
+  constexpr int V = VEC ? 16 / B : 1;
+  using Ld = Fp8Ld<V>;
+  const int N = A.nranks;
+  const Ld ld{A, i * V};
+  float acc[V];
+  if constexpr (MODE == MODE_FUSED_TREE) {
+    Fold<Ld>::template tree<MAXN>(ld, N, acc);
+  } else {
+    const int s = (c + 1 == N) ? 0 : c + 1;
+    Fold<Ld>::template ring<MAXN>(ld, N, s, acc);
+  }
+  uint32_t bits[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) bits[k] = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(acc[k], (float)N) : acc[k]);
+  if constexpr (VEC) {
+    uint4 out = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < V; ++k) set_lane<B>(out, k, bits[k]);
+    if constexpr (MODE == MODE_RS) {
+      __stcs(reinterpret_cast<uint4*>(A.dst[c]) + ci, out);
+    } else {
+      for (int r = 0; r < N; ++r) __stcs(reinterpret_cast<uint4*>(A.dst[r]) + i, out);
+    }
+  } else {
+    auto put = [&](void* base, uint64_t j) {
+      if constexpr (B == 4) reinterpret_cast<uint32_t*>(base)[j] = bits[0];
+      else reinterpret_cast<uint16_t*>(base)[j] = (uint16_t)bits[0];
+    };
+    if constexpr (MODE == MODE_RS) {
+      put(A.dst[c], ci);
+    } else {
+      for (int r = 0; r < N; ++r) put(A.dst[r], i);
+    }
+  }
+}
+
+template <int ODT, int OP, int MODE, int MAXN, bool VEC>
+__device__ __forceinline__ void fp8_range(const Fp8ReduceArgs& A, uint64_t t0, uint64_t nt, uint64_t items,
+                                          uint64_t Litems) {
+  if (t0 >= items) return;
+  int c = (int)(t0 / Litems);
+  uint64_t cbeg = (uint64_t)c * Litems, cend = cbeg + Litems;
+  for (uint64_t i = t0; i < items; i += nt) {
+    while (i >= cend) {
+      ++c;
+      cbeg = cend;
+      cend += Litems;
+    }
+    fp8_item<ODT, OP, MODE, MAXN, VEC>(A, i, c, i - cbeg);
+  }
+}
+
+template <int ODT, int OP, int MODE, int MAXN>
+__global__ void __launch_bounds__(kThreads) k_fp8_reduce(const __grid_constant__ Fp8ReduceArgs A) {
+  const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t nt = (uint64_t)gridDim.x * blockDim.x;
+  if (A.vec) {
+    constexpr int V = 16 / Fmt<ODT>::bytes;
+    const uint64_t items = A.count / V;
+    fp8_range<ODT, OP, MODE, MAXN, true>(A, t0, nt, items, A.L / V);
+    const uint64_t done = items * V;
+    if (t0 < A.count - done) {
+      const uint64_t e = done + t0;
+      const int c = (int)(e / A.L);
+      fp8_item<ODT, OP, MODE, MAXN, false>(A, e, c, e - (uint64_t)c * A.L);
+    }
+  } else {
+    fp8_range<ODT, OP, MODE, MAXN, false>(A, t0, nt, A.count, A.L);
+  }
+}
+
+template <int ODT, int OP, int MODE, int MAXN>
+cudaError_t launch_fp8_reduce_n(const Fp8ReduceArgs& a, cudaStream_t stream) {
+  static const int resident = resident_blocks(k_fp8_reduce<ODT, OP, MODE, MAXN>);
+  const uint64_t items = a.vec ? a.count / (16 / Fmt<ODT>::bytes) : a.count;
+  k_fp8_reduce<ODT, OP, MODE, MAXN><<<grid_for(items, resident), kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int ODT, int OP>
+cudaError_t launch_fp8_reduce_op(int mode, const Fp8ReduceArgs& a, cudaStream_t stream) {
+  const bool small = a.nranks <= 8;
+  switch (mode) {
+    case MODE_RS:
+      return small ? launch_fp8_reduce_n<ODT, OP, MODE_RS, 8>(a, stream)
+                   : launch_fp8_reduce_n<ODT, OP, MODE_RS, kMaxRanks>(a, stream);
+    case MODE_FUSED_RING:
+      return small ? launch_fp8_reduce_n<ODT, OP, MODE_FUSED_RING, 8>(a, stream)
+                   : launch_fp8_reduce_n<ODT, OP, MODE_FUSED_RING, kMaxRanks>(a, stream);
+    case MODE_FUSED_TREE:
+      return small ? launch_fp8_reduce_n<ODT, OP, MODE_FUSED_TREE, 8>(a, stream)
+                   : launch_fp8_reduce_n<ODT, OP, MODE_FUSED_TREE, kMaxRanks>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int ODT> cudaError_t launch_fp8_reduce_dt(int op, int mode, const Fp8ReduceArgs& a, cudaStream_t s) {
+  switch (op) {
+    case OP_SUM: return launch_fp8_reduce_op<ODT, OP_SUM>(mode, a, s);
+    case OP_AVG: return launch_fp8_reduce_op<ODT, OP_AVG>(mode, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream) {
+  switch (out_dtype) {
+    case DT_F32: return launch_fp8_reduce_dt<DT_F32>(op, mode, a, stream);
+    case DT_F16: return launch_fp8_reduce_dt<DT_F16>(op, mode, a, stream);
+    case DT_BF16: return launch_fp8_reduce_dt<DT_BF16>(op, mode, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gar

@@ -1,0 +1,110 @@
+// ar_internal.h — launch interface between the host planner (ar_api.cpp) and
+// the sm_103a kernels. Every per-launch argument block is passed by value in
+// kernel parameter space (read through the constant cache with
+// __grid_constant__), so a call needs no device allocation and no copy.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace gar {
+
+constexpr int kMaxRanks = 64;
+constexpr int kThreads = 256;
+
+enum Dt { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_I32 = 3 };
+enum Op { OP_SUM = 0, OP_AVG = 1, OP_MIN = 2, OP_MAX = 3 };
+
+// How a reduction kernel orders the fold and where it stores.
+enum Mode {
+  MODE_RS = 0,          // ring order, store chunk c only to its owner dst[c]
+  MODE_FUSED_RING = 1,  // ring order, store every element to all N outputs
+  MODE_FUSED_TREE = 2,  // recursive-halving order, store to all N outputs
+};
+
+// Reduction over N ranks of `count` elements each. Chunk c covers elements
+// [c*L, min((c+1)*L, count)).
+//   MODE_RS:     element i of chunk c goes to dst[c] + (i - c*L).
+//   MODE_FUSED_*: element i goes to dst[r] + i for every r.
+struct ReduceArgs {
+  const void* src[kMaxRanks];
+  void* dst[kMaxRanks];
+  uint64_t count;
+  uint64_t L;
+  int nranks;
+  int vec;  // 1: all pointers 16-byte aligned and L a multiple of the vector width
+};
+
+// All-gather copy in units of `unit` bytes. Output q, unit i (chunk c = i / Lu)
+// comes from src[c] + (i - c*Lu). Destinations whose bit c is set in skip_mask
+// already hold chunk c (the owner, or an in-place slot) and are not written.
+struct GatherArgs {
+  const void* src[kMaxRanks];
+  void* dst[kMaxRanks];
+  uint64_t units;      // units per output buffer
+  uint64_t Lu;         // chunk length in units
+  uint64_t skip_mask;  // bit c: skip dst[c] for chunk c
+  uint64_t tail_bytes; // bytes after units*unit still to copy (byte-wise)
+  uint64_t Lb;         // chunk length in bytes (for the byte tail)
+  int nranks;
+};
+
+// Batched memcpy of up to kMaxCopyItems ranges, cut into kCopyTile-byte tiles;
+// tile_start[k] is the first tile of item k, tile_start[nitems] the total.
+constexpr int kMaxCopyItems = 256;
+constexpr uint32_t kCopyTile = 16384;
+struct CopyItem {
+  const void* src;
+  void* dst;
+  uint64_t bytes;
+};
+struct MultiCopyArgs {
+  CopyItem item[kMaxCopyItems];
+  uint32_t tile_start[kMaxCopyItems + 1];
+  int nitems;
+};
+
+// FP8 block quantisation of N ranks: rank r's `count` inputs -> q[r] (bytes)
+// and s[r] (one float per 128-element block).
+constexpr int kFp8Block = 128;
+struct Fp8QuantArgs {
+  const void* src[kMaxRanks];
+  uint8_t* q[kMaxRanks];
+  float* s[kMaxRanks];
+  uint64_t count;
+  uint64_t first_block;  // blocks [first_block, ceil(count/128)) of every rank
+  int nranks;
+};
+
+// Dequantise + reduce + store, same modes as ReduceArgs, with q/s per rank.
+struct Fp8ReduceArgs {
+  const uint8_t* q[kMaxRanks];
+  const float* s[kMaxRanks];
+  void* dst[kMaxRanks];
+  uint64_t count;
+  uint64_t L;
+  int nranks;
+  int vec;
+};
+
+// Launchers: enqueue on `stream`, return the launch status.
+cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cudaStream_t stream);
+cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream);
+cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream);
+cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream);
+
+// Streaming multiprocessors of the calling thread's current device (cached).
+int sm_count();
+
+// Grid for a grid-stride kernel: enough blocks for `items` (one per thread),
+// at most `resident` blocks per SM on every SM.
+inline unsigned grid_for(uint64_t items, int resident) {
+  uint64_t need = (items + kThreads - 1) / kThreads;
+  uint64_t cap = (uint64_t)sm_count() * (uint64_t)(resident > 0 ? resident : 1);
+  if (need > cap) need = cap;
+  return (unsigned)(need > 0 ? need : 1);
+}
+
+}  // namespace gar

@@ -1,0 +1,154 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/ar.h declares, and its host-only logic (status text, bucket plan,
+argument and aliasing checks that return before anything is enqueued)
+behaves as documented. Fake device addresses are used where a check must
+fire before any pointer is dereferenced."""
+import ctypes
+import math
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import gradient_allreduce_collective_gb300 as gar
+import oracle
+import synthgen
+from tests import _golden as G
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "ar.h"
+
+
+@pytest.fixture(scope="module")
+def L():
+    gar.build()
+    return gar.lib()
+
+
+def _declared():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(encoding="utf-8"), flags=re.S)
+    return sorted(set(re.findall(r"\b(ar_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    for st in range(7):
+        assert gar.ar_status_string(st)
+    assert gar.ar_status_string(99) == "unknown status"
+    assert "sm_103a" in gar.ar_version()
+
+
+P = ctypes.POINTER(ctypes.c_void_p)
+
+
+def _arr(addrs):
+    return (ctypes.c_void_p * len(addrs))(*addrs)
+
+
+def _ar(L, send, recv, n, count, dt=0, op=0, algo=1):
+    return L.ar_allreduce(_arr(send), _arr(recv), n, count, dt, op, algo, None)
+
+
+def test_allreduce_argument_errors(L):
+    s = [0x100000 * (r + 1) for r in range(8)]
+    d = [0x8000000 + 0x100000 * r for r in range(8)]
+    assert L.ar_allreduce(None, _arr(d), 8, 16, 0, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert _ar(L, s, d, 0, 16) == gar.AR_ERR_INVALID_ARGUMENT
+    assert L.ar_allreduce(_arr(s * 9), _arr(d * 9), 65, 16, 0, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert _ar(L, s, d, 8, 16, dt=7) == gar.AR_ERR_INVALID_ARGUMENT
+    assert _ar(L, s, d, 8, 16, op=9) == gar.AR_ERR_INVALID_ARGUMENT
+    assert _ar(L, s, d, 8, 16, algo=5) == gar.AR_ERR_INVALID_ARGUMENT
+    assert _ar(L, s[:3], d[:3], 3, 16, algo=2) == gar.AR_ERR_UNSUPPORTED
+    assert "power of two" in gar.ar_last_error()
+    assert _ar(L, s[:3], d[:3], 3, 0, algo=1) == gar.AR_SUCCESS  # count 0: no-op
+    bad = list(s)
+    bad[2] = 0
+    assert _ar(L, bad, d, 8, 16) == gar.AR_ERR_INVALID_ARGUMENT
+    assert "sendbufs[2] is null" in gar.ar_last_error()
+    mis = list(d)
+    mis[5] += 2  # not 4-byte aligned for f32
+    assert _ar(L, s, mis, 8, 16) == gar.AR_ERR_INVALID_ARGUMENT
+
+
+def test_allreduce_alias_rules(L):
+    n, count = 4, 1024
+    s = [0x1000000 * (r + 1) for r in range(n)]
+    d = [0x20000000 + 0x1000000 * r for r in range(n)]
+    over = list(d)
+    over[1] = d[0] + 8  # two outputs overlap
+    assert _ar(L, s, over, n, count) == gar.AR_ERR_ALIAS
+    cross = list(d)
+    cross[1] = s[0]  # an output on another rank's input
+    assert _ar(L, s, cross, n, count) == gar.AR_ERR_ALIAS
+    shifted = list(d)
+    shifted[2] = s[2] + 16  # overlaps its own input but not exactly
+    assert _ar(L, s, shifted, n, count) == gar.AR_ERR_ALIAS
+
+
+def test_reduce_scatter_and_all_gather_alias_rules(L):
+    n, rc = 4, 64
+    s = [0x1000000 * (r + 1) for r in range(n)]
+    # in place is recvbufs[c] == sendbufs[c] + c*recvcount; recvbufs[c] == sendbufs[c] is not
+    wrong = [s[c] for c in range(n)]
+    wrong[0] = 0x30000000
+    assert L.ar_reduce_scatter(_arr(s), _arr(wrong), n, rc, 0, 0, None) == gar.AR_ERR_ALIAS
+    d = [0x20000000 + 0x1000000 * r for r in range(n)]
+    assert L.ar_all_gather(_arr([d[0] + 4] + s[1:]), _arr(d), n, rc, 0, None) == gar.AR_ERR_ALIAS
+
+
+def test_fp8_argument_errors(L):
+    n, count = 4, 1000
+    s = [0x1000000 * (r + 1) for r in range(n)]
+    d = [0x20000000 + 0x1000000 * r for r in range(n)]
+    need = gar.ar_fp8_workspace_bytes(n, count)
+    qs = math.ceil(count / 256) * 256
+    ss = math.ceil(math.ceil(count / 128) / 64) * 64 * 4
+    assert need == n * (qs + ss)
+    ws = 0x40000000
+    f = L.ar_allreduce_fp8
+    assert f(_arr(s), _arr(d), n, count, 2, 2, 2, 1, ws, need, None) == gar.AR_ERR_UNSUPPORTED  # MIN
+    assert f(_arr(s), _arr(d), n, count, 3, 2, 0, 1, ws, need, None) == gar.AR_ERR_UNSUPPORTED  # int input
+    assert f(_arr(s), _arr(d), n, count, 2, 2, 0, 1, ws, need - 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(_arr(s), _arr(d), n, count, 2, 2, 0, 1, ws + 8, need, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(_arr(s[:3]), _arr(d[:3]), 3, count, 2, 2, 0, 2, ws, need, None) == gar.AR_ERR_UNSUPPORTED
+    assert f(_arr(s), _arr(d), n, count, 2, 2, 0, 1, d[1] + 64, need, None) == gar.AR_ERR_ALIAS
+    assert gar.ar_fp8_workspace_bytes(0, 10) == 0
+
+
+def test_bucket_plan_matches_hand_derivation(L):
+    import torch
+    g = G.load("gpt2_buckets.txt")
+    counts = [math.prod(s) for _, s in synthgen.gpt2_small_param_shapes()]
+    bucket_of, offset_of, bucket_counts = gar.ar_bucket_plan(counts, torch.bfloat16, int(g["cap_bytes"]))
+    assert [b * 2 for b in bucket_counts] == G.nums(g["expect_bytes"], int)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_bucket_plan_matches_oracle(L, seed):
+    import torch
+    rng = np.random.default_rng(seed)
+    counts = [int(x) for x in rng.integers(0, 5000, size=int(rng.integers(1, 60)))]
+    for dt, es in ((torch.float32, 4), (torch.bfloat16, 2)):
+        for cap in (1, 64, 4096, 40000):
+            b1, o1, c1 = gar.ar_bucket_plan(counts, dt, cap)
+            b2, o2, c2 = oracle.bucket_plan(counts, es, cap)
+            assert b1 == b2.tolist() and o1 == o2.tolist() and c1 == c2.tolist()
+
+
+def test_bucket_copy_errors(L):
+    import torch
+    t = [0x1000000, 0x2000000]
+    counts = (ctypes.c_size_t * 2)(100, 100)
+    offs = (ctypes.c_size_t * 2)(0, 50)  # the two tensors overlap inside the bucket
+    assert L.ar_bucket_flatten(_arr(t), counts, offs, 2, 2, 0x4000000, None) == gar.AR_ERR_ALIAS
+    offs_ok = (ctypes.c_size_t * 2)(0, 100)
+    assert L.ar_bucket_flatten(_arr(t), counts, offs_ok, 2, 2, 0, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert L.ar_bucket_flatten(_arr(t), counts, offs_ok, 0, 2, 0x4000000, None) == gar.AR_SUCCESS
+    del torch

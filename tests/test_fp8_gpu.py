@@ -1,0 +1,124 @@
+"""GPU parity of the FP8 (E4M3, per-128-element block scale) path against the
+oracle, bit for bit, plus the tolerance against the fp64 reference. The full
+16 x 134,217,728 bf16 workload is checked on sampled whole blocks, which the
+oracle evaluates one by one, and by properties (replicas identical, ring ==
+fused bitwise, normwise error)."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_allreduce_collective_gb300 as gar
+import oracle
+import synthgen
+from tests import _golden as G
+from tests._dev import ESIZE, TORCH, Guarded, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gar.build()
+    gar.lib()
+
+
+def _same_bits(a, b):
+    return np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
+def _ws(n, count):
+    return torch.empty(gar.ar_fp8_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("in_dtype", ["bf16", "f16", "f32"])
+def test_quantize_matches_oracle(in_dtype):
+    for count in (1, 5, 127, 128, 129, 128 * 1000 + 77):
+        x = synthgen.ranks_normal(1, count, 1e-3, base_seed=count, dtype=in_dtype, outlier_p=1e-2,
+                                  outlier_scale=100.0)[0]
+        x[: min(count, 128)] = 0  # an all-zero block (scale 0)
+        for off in (0, ESIZE[in_dtype]):  # aligned, and the element path
+            g = Guarded(1, count, in_dtype, off)
+            g.views[0].copy_(to_dev(x, in_dtype))
+            q = torch.empty(count, dtype=torch.uint8, device="cuda")
+            s = torch.empty((count + 127) // 128, dtype=torch.float32, device="cuda")
+            gar.ar_quantize_fp8_blocks(g.views[0], q, s)
+            wq, ws = oracle.fp8_quantize(x, in_dtype)
+            assert _same_bits(from_dev(q), wq) and _same_bits(from_dev(s), ws), (count, off)
+
+
+def test_fp8_block_example():
+    g = G.load("fp8_block_example.txt")
+    send = [to_dev(synthgen.to_dtype(np.array(G.nums(g[f"rank{r}"]), dtype=np.float32), "bf16"), "bf16")
+            for r in range(2)]
+    for op in ("sum", "avg"):
+        for algo in ("ring", "fused", "tree"):
+            recv = [torch.empty(4, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+            gar.ar_allreduce_fp8(send, recv, _ws(2, 4), op, algo)
+            for y in recv:
+                assert y.float().cpu().tolist() == G.nums(g[f"expect_{op}"]), (op, algo)
+
+
+@pytest.mark.parametrize("in_dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("out_dtype", ["bf16", "f16", "f32"])
+def test_fp8_allreduce_matches_oracle(in_dtype, out_dtype):
+    for n in (1, 2, 3, 4, 8, 16):
+        for count in (1, 100, 128 * 50 + 3, 128 * 300):
+            send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=n + count, dtype=in_dtype, outlier_p=1e-2,
+                                            outlier_scale=100.0)
+            send = [to_dev(a, in_dtype) for a in send_np]
+            for op in ("sum", "avg"):
+                algos = ("ring", "fused", "tree") if n & (n - 1) == 0 else ("ring", "fused")
+                for algo in algos:
+                    if algo == "tree":
+                        want = oracle.fp8_tree_allreduce(send_np, in_dtype, out_dtype, op)[0]
+                    else:
+                        want = oracle.fp8_ring_allreduce(send_np, in_dtype, out_dtype, op)[0]
+                    out = Guarded(n, count, out_dtype)
+                    gar.ar_allreduce_fp8(send, out.views, _ws(n, count), op, algo)
+                    out.check()
+                    for v in out.views:
+                        assert _same_bits(from_dev(v), want), (n, count, op, algo)
+
+
+def test_fp8_unaligned_outputs():
+    n, count = 4, 128 * 20 + 9
+    send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=5, dtype="bf16")
+    send = [to_dev(a, "bf16") for a in send_np]
+    want = oracle.fp8_ring_allreduce(send_np, "bf16", "bf16", "sum")[0]
+    for algo in ("ring", "fused"):
+        out = Guarded(n, count, "bf16", 2)
+        gar.ar_allreduce_fp8(send, out.views, _ws(n, count), "sum", algo)
+        out.check()
+        for v in out.views:
+            assert _same_bits(from_dev(v), want)
+
+
+def test_config5_full_size_sampled():
+    n, count = 16, 134_217_728
+    send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=0, dtype="bf16", outlier_p=1e-3, outlier_scale=100.0)
+    send = [to_dev(a, "bf16") for a in send_np]
+    ws = _ws(n, count)
+    fused = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    gar.ar_allreduce_fp8(send, fused, ws, "sum", "fused")
+    ring = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    gar.ar_allreduce_fp8(send, ring, ws, "sum", "ring")
+    torch.cuda.synchronize()
+    f0 = fused[0].view(torch.int16)
+    for r in range(n):
+        assert torch.equal(fused[r].view(torch.int16), f0)
+        assert torch.equal(ring[r].view(torch.int16), f0)
+    del ring
+    rng = np.random.default_rng(0)
+    nblocks = count // 128
+    blocks = np.unique(np.concatenate([rng.choice(nblocks, 3000, replace=False), [0, nblocks - 1],
+                                       # blocks at every chunk boundary
+                                       [(c * (count // n)) // 128 for c in range(n)]]))
+    blk = np.stack([np.stack([send_np[r][b * 128:(b + 1) * 128] for r in range(n)]) for b in blocks])
+    want = oracle.fp8_ring_blocks(blk, blocks * 128, np.full(len(blocks), 128), count, "bf16", "bf16", "sum")
+    got = from_dev(fused[0]).reshape(-1, 128)[blocks]
+    assert _same_bits(got, want)
+    # tolerance against fp64 on the sample (normwise, as the FP8 bound is stated)
+    x = np.stack([oracle.bf16_to_f32(blk[:, r, :].ravel()).astype(np.float64) for r in range(n)])
+    ystar = x.sum(axis=0)
+    y = oracle.bf16_to_f32(got.ravel()).astype(np.float64)
+    assert np.linalg.norm(y - ystar) / np.linalg.norm(ystar) <= 6e-2
