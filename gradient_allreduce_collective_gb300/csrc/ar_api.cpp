@@ -529,3 +529,9 @@ ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs,
 }
 
 }  // extern "C"
+
+namespace gar {
+// Lets other translation units of the library report an error through
+// ar_last_error() for the calling thread.
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace gar

@@ -186,6 +186,35 @@ ar_status_t ar_allreduce_fp8(const void *const *sendbufs, void *const *recvbufs,
                              ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
                              void *workspace, size_t ws_bytes, ar_stream_t stream);
 
+/* Bytes of the FP8 workspace built into the library (16 MiB per device). */
+#define AR_FP8_STATIC_WS_BYTES (16u * 1024u * 1024u)
+
+/* FP8-compressed allreduce for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot obtain a workspace for ar_allreduce_fp8: code running inside an
+ * allocator's or memory pool's own callbacks, on a framework path where
+ * allocation is forbidden, or a host program with no access to the CUDA
+ * allocation API. It computes exactly what ar_allreduce_fp8 computes (same
+ * kernels, same bits) but keeps the quantised codes and scales in a fixed
+ * array inside the library, AR_FP8_STATIC_WS_BYTES bytes on every device that
+ * loads it, held until the process exits. It calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ *   Limit: ar_fp8_workspace_bytes(nranks, count) must not exceed
+ *   AR_FP8_STATIC_WS_BYTES (for example 8 ranks x 2,000,000 elements fit);
+ *   larger calls return AR_ERR_INVALID_ARGUMENT and ar_last_error() says why.
+ *   Set-up: the first call made while a device is current looks up that
+ *   device's address of the array (cudaGetSymbolAddress) and caches it; make
+ *   that first call before any stream capture.
+ *   Sharing: all calls on a device use the same array and leave their data in
+ *   it; each call writes every byte it later reads, so nothing needs
+ *   clearing, but calls that overlap on the GPU (different streams, or host
+ *   threads sharing a device without ordering) race on it and must be
+ *   serialised by the caller.
+ * Other arguments, rules and errors: as ar_allreduce_fp8. */
+ar_status_t ar_allreduce_fp8_noalloc(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
+                                     ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
+                                     ar_stream_t stream);
+
 /* Static text for a status code. */
 const char *ar_status_string(ar_status_t status);
 
