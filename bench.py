@@ -1,21 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 gradient allreduce.
 
-Default workload (one line of JSON on stdout): the allreduce of one 25 MiB
-fp32 DDP bucket across N = 8 virtual ranks held in one GPU's HBM
-(8 x 6,553,600 fp32, N(0, 1e-3), op = avg), one fused ring-order pass per
-step. Inputs are 200 MiB, larger than L2, so no flush between steps.
+Default line (one JSON line on stdout): the allreduce of one 25 MiB fp32 DDP
+bucket across N = 8 virtual ranks held in one GPU's HBM (8 x 6,553,600 fp32,
+N(0, 1e-3), op = avg), one fused ring-order pass per step. Inputs are
+200 MiB, larger than L2, so no flush between steps.
 
   metric: busbw GB/s = (M / t) * 2(N-1)/N, M = bytes per rank (the ring
           volume factor of the AllReduce glossary's algorithm table), and the
           fraction of the HBM roofline with bytes = 2*N*M per step.
   e2e:    the same metric with the host->device copy of the 8 inputs and the
           device->host copy of the 8 outputs (pinned host memory) inside the
-          timed region, through the same C-ABI call.
+          timed region, through the same C-ABI call; copies in and out run on
+          their own streams with two device buffer sets, so one step's
+          download overlaps the next step's upload.
+  rows:   the other hot-path rows on their own workloads: the GPT-2-small
+          DDP bucket sync (flatten -> allreduce -> unflatten, bf16, 8 ranks)
+          and the FP8-compressed allreduce (16 x 134,217,728 bf16).
   cpu_baseline: the CPU oracle (literal ring simulator, one thread) on the
-          same workload, a bounded number of repetitions.
+          same bucket, a bounded number of repetitions.
 
-`--impl reference` times the oracle alone on this workload (rank 0 only).
+`--workload sweep` prints one line per message size (8 ranks, 4 KiB..1 GiB
+per rank, fp32 sum; ring, tree and fused; warm and cold L2).
+`--impl reference` times the oracle alone on the bucket (rank 0 only).
 Under torchrun each GPU runs its own full workload (weak scaling: the
 virtual ranks already live on one device, so there is no exchange between
 GPUs); a gloo process group supplies the barrier and the max over ranks.
@@ -25,6 +32,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -42,6 +50,8 @@ COUNT = 6_553_600  # 25 MiB of fp32 per rank
 SIGMA = 1e-3
 OP = "avg"
 FALLBACK_HBM_GBS = 6800.0
+CSRC = ROOT / "gradient_allreduce_collective_gb300" / "csrc"
+FUSED_KERNEL_SOURCES = ("ar_internal.h", "ar_device.cuh", "ar_reduce_impl.cuh", "ar_reduce_f32.cu")
 
 
 def busbw_gbs(bytes_per_rank: float, seconds: float, nranks: int = NRANKS) -> float:
@@ -63,7 +73,8 @@ def init_dist(world: int):
         return None
     import torch.distributed as dist
 
-    dist.init_process_group("gloo")
+    if not dist.is_initialized():
+        dist.init_process_group("gloo")
     return dist
 
 
@@ -72,23 +83,14 @@ def barrier(dist):
         dist.barrier()
 
 
-def max_over_ranks(dist, x: float) -> float:
+def reduce_over_ranks(dist, x: float, op: str) -> float:
+    """max or sum of a host scalar over the ranks (identity without a group)."""
     if dist is None:
         return x
     import torch
 
     t = torch.tensor([x], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def sum_over_ranks(dist, x: float) -> float:
-    if dist is None:
-        return x
-    import torch
-
-    t = torch.tensor([x], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -103,7 +105,6 @@ class ClockSampler:
     def __init__(self, device_id: str | None):
         self.device_id = device_id
         self.proc = None
-        self.lines: list[str] = []
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
@@ -142,8 +143,7 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        # samples under load: the upper half of the power readings
-        pmid = statistics.median(power)
+        pmid = statistics.median(power)  # samples under load: the upper half of the power readings
         loaded = [s for s, p in zip(sm, power) if p >= pmid] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm), "power_w_max": max(power)}
@@ -153,8 +153,7 @@ def device_uuid(dev: int) -> str | None:
     import torch
 
     try:
-        u = torch.cuda.get_device_properties(dev).uuid
-        s = str(u)
+        s = str(torch.cuda.get_device_properties(dev).uuid)
         return s if s.startswith("GPU-") else f"GPU-{s}"
     except Exception:
         return None
@@ -173,18 +172,24 @@ def measured_peaks() -> dict:
     return {}
 
 
-def kernel_source_hash() -> str:
+def hbm_peak() -> tuple[float, str]:
+    peaks = measured_peaks()
+    if "hbm_gbs" in peaks:
+        return float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(files=FUSED_KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    csrc = ROOT / "gradient_allreduce_collective_gb300" / "csrc"
-    for p in sorted(csrc.iterdir()):
-        if p.is_file():
-            h.update(p.name.encode())
-            h.update(p.read_bytes())
+    for name in files:
+        p = CSRC / name
+        h.update(name.encode())
+        h.update(p.read_bytes())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(profile_name: str) -> float | None:
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel
+def profiled_traffic(profile_name: str, files=FUSED_KERNEL_SOURCES) -> float | None:
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel's
     sources have not changed since (the summary records their hash)."""
     p = ROOT / "profiles" / profile_name
     if not p.exists():
@@ -192,7 +197,7 @@ def profiled_traffic(profile_name: str) -> float | None:
     text = p.read_text(encoding="utf-8")
     m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(files):
         return None
     return float(m_bytes.group(1))
 
@@ -225,8 +230,17 @@ def oracle_baseline(budget_s: float, nranks: int = NRANKS, count: int = COUNT) -
     t = elapsed / reps
     return {"value": busbw_gbs(n * 4, t, nranks), "unit": "GB/s (busbw)", "cores": 1, "kind": "oracle",
             "sample": f"{nranks} ranks x first {n:,} of {count:,} fp32 (the full bucket when equal), op={OP}, "
-                      f"{reps} repetitions, {t * 1e3:.1f} ms each, single-threaded C ring simulator",
-            "ms_per_step": t * 1e3}
+                      f"{reps} repetitions, {t * 1e3:.1f} ms each, single-threaded C ring simulator"}
+
+
+def workload_config(algo: str) -> dict:
+    return {
+        "workload": f"allreduce of one 25 MiB fp32 DDP bucket: N={NRANKS} virtual ranks x {COUNT:,} fp32 "
+                    f"in one GPU's HBM, op={OP}, {algo} ring-order pass",
+        "nranks": NRANKS, "count_per_rank": COUNT, "bytes_per_rank": COUNT * 4, "op": OP, "algo": algo,
+        "l2": "inputs 200 MiB and outputs 200 MiB exceed the 126 MiB L2; no flush between steps",
+        "parallelism": "virtual ranks on one device; GPUs run independent buckets (weak scaling)",
+    }
 
 
 def run_reference(args):
@@ -267,20 +281,11 @@ def run_reference(args):
     return 0
 
 
-# ----------------------------------------------------------------- GPU arm
-
-
-def workload_config(algo: str) -> dict:
-    return {
-        "workload": f"allreduce of one 25 MiB fp32 DDP bucket: N={NRANKS} virtual ranks x {COUNT:,} fp32 "
-                    f"in one GPU's HBM, op={OP}, {algo} ring-order pass",
-        "nranks": NRANKS, "count_per_rank": COUNT, "bytes_per_rank": COUNT * 4, "op": OP, "algo": algo,
-        "l2": "inputs 200 MiB and outputs 200 MiB exceed the 126 MiB L2; no flush between steps",
-        "parallelism": "virtual ranks on one device; GPUs run independent buckets (weak scaling)",
-    }
+# ----------------------------------------------------------------- GPU helpers
 
 
 def time_steps(fn, steps: int, stream) -> float:
+    """Average ms per call of fn() over `steps` calls, CUDA events on `stream`."""
     import torch
 
     start = torch.cuda.Event(enable_timing=True)
@@ -291,7 +296,118 @@ def time_steps(fn, steps: int, stream) -> float:
         fn()
     end.record(stream)
     end.synchronize()
-    return start.elapsed_time(end) / steps  # ms
+    return start.elapsed_time(end) / steps
+
+
+def to_dev_bf16(a):
+    import torch
+
+    return torch.from_numpy(a).view(torch.int16).view(torch.bfloat16).cuda()
+
+
+def measure_ddp(gar, steps: int, warmup: int) -> dict:
+    """GPT-2-small DDP gradient sync on 8 ranks: per bucket one flatten call
+    for all ranks, one in-place fused allreduce (avg), one unflatten call."""
+    import torch
+    import synthgen
+
+    n = 8
+    shapes = [s for _, s in synthgen.gpt2_small_param_shapes()]
+    counts = [math.prod(s) for s in shapes]
+    total = sum(counts)
+    grads = [to_dev_bf16(g) for g in synthgen.ranks_normal(n, total, 1e-4, base_seed=0, dtype="bf16")]
+    starts, pos = [], 0
+    for c in counts:
+        starts.append(pos)
+        pos += c
+    views = [[g[s:s + c] for s, c in zip(starts, counts)] for g in grads]
+    bucket_of, offset_of, bcounts = gar.ar_bucket_plan(counts, torch.bfloat16, 25 * 1024 * 1024)
+    plan = []
+    for b, bc in enumerate(bcounts):
+        stride = (bc + 127) // 128 * 128  # 256-byte aligned rank slots
+        flat = torch.empty(n * stride, dtype=torch.bfloat16, device="cuda")
+        ids = [t for t in range(len(counts)) if bucket_of[t] == b]
+        tens = [views[r][t] for r in range(n) for t in ids]
+        offs = [r * stride + offset_of[t] for r in range(n) for t in ids]
+        ranks = [flat[r * stride:r * stride + bc] for r in range(n)]
+        plan.append((flat, tens, offs, ranks))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for flat, tens, offs, ranks in plan:
+            gar.ar_bucket_flatten(tens, offs, flat, stream)
+            gar.ar_allreduce(ranks, ranks, "avg", "fused", stream)
+            gar.ar_bucket_unflatten(flat, tens, offs, stream)
+
+    for _ in range(warmup):
+        step()
+    ms_eager = time_steps(step, steps, stream)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        graph.capture_begin()
+        for flat, tens, offs, ranks in plan:
+            gar.ar_bucket_flatten(tens, offs, flat, side)
+            gar.ar_allreduce(ranks, ranks, "avg", "fused", side)
+            gar.ar_bucket_unflatten(flat, tens, offs, side)
+        graph.capture_end()
+    stream.wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    ms_graph = time_steps(graph.replay, steps, stream)
+    peak, _ = hbm_peak()
+    grad_bytes = total * 2
+    moved = 6 * n * grad_bytes  # flatten, allreduce and unflatten each read and write every byte
+    best = min(ms_eager, ms_graph)
+    return {
+        "workload": "DDP gradient sync: GPT-2-small shapes (148 tensors, 124,439,808 bf16 values) x 8 ranks, "
+                    "N(0,1e-4), 9 buckets of <= 25 MiB; per bucket flatten (all ranks) -> fused allreduce avg "
+                    "(binary32 accumulation) -> unflatten",
+        "buckets": len(bcounts), "launches_per_step": 3 * len(bcounts),
+        "ms_per_step_eager": ms_eager, "ms_per_step_cuda_graph": ms_graph,
+        "busbw_gbs": busbw_gbs(grad_bytes, best * 1e-3, n),
+        "hbm_gbs": moved / (best * 1e-3) / 1e9, "frac_hbm": moved / (best * 1e-3) / 1e9 / peak,
+        "algorithmic_bytes_per_step": moved,
+    }
+
+
+def measure_fp8(gar, steps: int, warmup: int) -> dict:
+    """16 ranks x 134,217,728 bf16 with 0.1% outliers x100: quantise to E4M3
+    blocks (workspace) then dequantise + fused ring-order reduce (sum) + 16
+    bf16 replicas."""
+    import torch
+    import synthgen
+
+    n, count = 16, 134_217_728
+    send = [to_dev_bf16(a) for a in synthgen.ranks_normal(n, count, 1e-3, base_seed=0, dtype="bf16",
+                                                          outlier_p=1e-3, outlier_scale=100.0)]
+    recv = [torch.empty_like(s) for s in send]
+    ws = torch.empty(gar.ar_fp8_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gar.ar_allreduce_fp8(send, recv, ws, "sum", "fused", stream)
+
+    for _ in range(warmup):
+        step()
+    ms = time_steps(step, steps, stream)
+    M = count * 2
+    wire = count + 4 * (count // 128)  # E4M3 codes + block scales per rank
+    moved = n * M + n * wire + n * wire + n * M
+    peak, _ = hbm_peak()
+    del send, recv, ws
+    torch.cuda.empty_cache()
+    return {
+        "workload": "FP8-compressed allreduce: 16 ranks x 134,217,728 bf16 (256 MiB), N(0,1e-3), 0.1% outliers "
+                    "x100, E4M3 per-128 block scales, binary32 accumulation, sum, bf16 out, fused",
+        "ms_per_step": ms, "busbw_gbs": busbw_gbs(M, ms * 1e-3, n),
+        "hbm_gbs": moved / (ms * 1e-3) / 1e9, "frac_hbm": moved / (ms * 1e-3) / 1e9 / peak,
+        "algorithmic_bytes_per_step": moved, "launches_per_step": 2,
+    }
+
+
+# ----------------------------------------------------------------- GPU arm: headline
 
 
 def run_ours(args):
@@ -327,48 +443,79 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(dist)
     clk = clocks.stop()
-    ms_max = max_over_ranks(dist, ms)
+    ms_max = reduce_over_ranks(dist, ms, "max")
 
-    # the same workload through the other two orders (not the headline)
-    extra = {}
+    # the same bucket through the other two orders (not the headline)
+    other = {}
     for algo in ("ring", "tree"):
         def f(a=algo):
             gar.ar_allreduce(send, recv, OP, a, stream)
         for _ in range(max(3, args.warmup)):
             f()
-        extra[algo] = time_steps(f, max(10, min(args.steps, 2000)), stream)
+        other[algo] = time_steps(f, max(10, min(args.steps, 2000)), stream)
 
-    # end to end: pinned host inputs -> device -> allreduce -> host outputs
+    # end to end: pinned host inputs -> device -> allreduce -> pinned host outputs
     h_in = [torch.from_numpy(a).pin_memory() for a in send_np]
     h_out = [torch.empty(COUNT, dtype=torch.float32).pin_memory() for _ in range(NRANKS)]
+    d_in = [[torch.empty(COUNT, device="cuda") for _ in range(NRANKS)] for _ in range(2)]
+    d_out = [[torch.empty(COUNT, device="cuda") for _ in range(NRANKS)] for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_red = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    k = [0]
 
     def step_e2e():
-        for d, h in zip(send, h_in):
-            d.copy_(h, non_blocking=True)
-        gar.ar_allreduce(send, recv, OP, "fused", stream)
-        for h, d in zip(h_out, recv):
-            h.copy_(d, non_blocking=True)
+        j = k[0] & 1
+        k[0] += 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_red[j])  # the previous reduction that read this input set is done
+            for d, h in zip(d_in[j], h_in):
+                d.copy_(h, non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])  # the previous download of this output set is done
+        gar.ar_allreduce(d_in[j], d_out[j], OP, "fused", stream)
+        ev_red[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_red[j])
+            for h, d in zip(h_out, d_out[j]):
+                h.copy_(d, non_blocking=True)
+            ev_out[j].record(s_out)
 
+    for e in ev_red + ev_out:
+        e.record(stream)
     for _ in range(3):
         step_e2e()
+    torch.cuda.synchronize()
     e2e_steps = max(5, min(args.steps, 200))
     barrier(dist)
-    ms_e2e = max_over_ranks(dist, time_steps(step_e2e, e2e_steps, stream))
-    torch.cuda.synchronize()
-    ok = all(np.array_equal(h_out[r].numpy(), h_out[0].numpy()) for r in range(1, NRANKS))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(e2e_steps):
+        step_e2e()
+    stream.wait_stream(s_out)
+    end.record(stream)
+    end.synchronize()
+    ms_e2e = reduce_over_ranks(dist, start.elapsed_time(end) / e2e_steps, "max")
+    gar.ar_allreduce(send, recv, OP, "fused", stream)  # recv last held the tree-order result
+    want = recv[0].cpu().numpy()
+    ok = all(np.array_equal(h.numpy(), want) for h in h_out)
 
-    peaks = measured_peaks()
-    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks else "fallback"
+    rows = {}
+    if not args.headline_only:
+        del d_in, d_out
+        rows["ddp_bucket_sync"] = measure_ddp(gar, steps=max(5, min(args.steps, 50)), warmup=3)
+        rows["fp8_allreduce"] = measure_fp8(gar, steps=max(5, min(args.steps, 20)), warmup=3)
+
+    peak, peak_src = hbm_peak()
     alg_bytes = 2 * NRANKS * M
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     traffic = profiled_traffic("ar_fused_f32_avg_n8_25MiB.md")
-
-    value = sum_over_ranks(dist, busbw_gbs(M, ms_max * 1e-3)) if dist else busbw_gbs(M, ms_max * 1e-3)
+    value = reduce_over_ranks(dist, busbw_gbs(M, ms_max * 1e-3), "sum") if dist else busbw_gbs(M, ms_max * 1e-3)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_baseline(args.cpu_budget)
-        cpu.pop("ms_per_step", None)
     if rank != 0:
         return 0
     line = {
@@ -393,13 +540,81 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": alg_bytes, "peak_source": peak_src},
         "e2e": {"value": (world if dist else 1) * busbw_gbs(M, ms_e2e * 1e-3), "unit": "GB/s",
                 "ms_per_step": ms_e2e, "h2d_bytes_per_step": NRANKS * M, "d2h_bytes_per_step": NRANKS * M,
-                "replicas_identical": ok},
+                "pipelined": "copy-in and copy-out streams, two device buffer sets", "replicas_identical": ok},
         "gpu_launches": args.steps,
         "clocks": clk,
-        "other_orders_ms_per_step": {"ring_rs_plus_ag": extra["ring"], "tree_recursive_halving": extra["tree"]},
+        "other_orders_ms_per_step": {"ring_rs_plus_ag": other["ring"], "tree_recursive_halving": other["tree"]},
+        "rows": rows,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm: size sweep
+
+
+def run_sweep(args):
+    import torch
+
+    import gradient_allreduce_collective_gb300 as gar
+    import synthgen
+
+    torch.cuda.set_device(dist_env()[2])
+    gar.build()
+    gar.lib()
+    n = 8
+    max_bytes = args.sweep_max_bytes
+    nmax = max_bytes // 4
+    host = synthgen.ranks_uniform(n, nmax, -1.0, 1.0, base_seed=0)
+    send = [torch.from_numpy(a).cuda() for a in host]
+    del host
+    recv = [torch.empty_like(s) for s in send]
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    peak, _ = hbm_peak()
+    size = 4096
+    while size <= max_bytes:
+        cnt = size // 4
+        s_v = [t[:cnt] for t in send]
+        r_v = [t[:cnt] for t in recv]
+        res = {}
+        for algo in ("fused", "tree", "ring"):
+            def f(a=algo):
+                gar.ar_allreduce(s_v, r_v, "sum", a, stream)
+            for _ in range(5):
+                f()
+            reps = max(5, min(2000, int(2e9 / (2 * n * size))))
+            warm = time_steps(f, reps, stream)
+            # cold: flush L2 before every call, time the call alone
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+            for a, b in ev:
+                flush.fill_(1.0)
+                a.record(stream)
+                f()
+                b.record(stream)
+            torch.cuda.synchronize()
+            cold = statistics.median(a.elapsed_time(b) for a, b in ev)
+            res[algo] = {"warm_us": warm * 1e3, "cold_us": cold * 1e3,
+                         "busbw_gbs_cold": busbw_gbs(size, cold * 1e-3, n),
+                         "hbm_frac_cold": 2 * n * size / (cold * 1e-3) / 1e9 / peak}
+        # small sizes are launch-bound: a CUDA graph of 100 fused calls
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            g.capture_begin()
+            for _ in range(100):
+                gar.ar_allreduce(s_v, r_v, "sum", "fused", side)
+            g.capture_end()
+        stream.wait_stream(side)
+        g.replay()
+        gms = time_steps(g.replay, 5, stream) / 100
+        print(json.dumps({"workload": "size sweep", "nranks": n, "bytes_per_rank": size, "dtype": "f32", "op": "sum",
+                          "in_l2": 2 * n * size <= l2, "fused_graph_us": gms * 1e3, **res}))
+        sys.stdout.flush()
+        size *= 2
     return 0
 
 
@@ -409,13 +624,18 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("bucket", "sweep"), default="bucket")
+    ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true", help="skip the DDP and FP8 rows")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "sweep":
+        return run_sweep(args)
     return run_ours(args)
 
 

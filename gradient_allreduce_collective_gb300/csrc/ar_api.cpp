@@ -3,7 +3,6 @@
 // by-value kernel argument blocks. Everything here runs on the host; nothing
 // allocates device memory or synchronises.
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <string>
@@ -15,21 +14,6 @@
 #include "ar_internal.h"
 
 namespace gar {
-
-int sm_count() {
-  static std::atomic<int> cache[kMaxRanks];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  const bool cacheable = dev >= 0 && dev < kMaxRanks;
-  if (cacheable) {
-    const int v = cache[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-  }
-  int v = 0;
-  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
-  if (cacheable) cache[dev].store(v, std::memory_order_relaxed);
-  return v;
-}
 
 // in ar_reduce_<type>.cu
 cudaError_t launch_reduce_f32(int op, int mode, const ReduceArgs& a, cudaStream_t stream);

@@ -68,13 +68,8 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
 }
 
 template <int U> cudaError_t launch_gather_u(const GatherArgs& a, cudaStream_t stream) {
-  static const int resident = [] {
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_gather<U>, kThreads, 0) != cudaSuccess) b = 1;
-    return b;
-  }();
   const uint64_t items = a.units > a.tail_bytes ? a.units : a.tail_bytes;
-  k_gather<U><<<grid_for(items, resident), kThreads, 0, stream>>>(a);
+  k_gather<U><<<grid_for(items), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -125,15 +120,10 @@ __global__ void __launch_bounds__(kThreads) k_multicopy(const __grid_constant__ 
 }
 
 cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream) {
-  static const int resident = [] {
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_multicopy, kThreads, 0) != cudaSuccess) b = 1;
-    return b;
-  }();
   const uint32_t total = a.tile_start[a.nitems];
   if (total == 0) return cudaSuccess;
-  uint64_t cap = (uint64_t)sm_count() * (uint64_t)(resident > 0 ? resident : 1);
-  const unsigned grid = (unsigned)(total < cap ? total : cap);
+  // one block per tile
+  const unsigned grid = total < 0x7FFFFFFFu ? total : 0x7FFFFFFFu;
   k_multicopy<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }

@@ -117,15 +117,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_scalar(const __grid_cons
   }
 }
 
-template <class K> static int resident_blocks(K kernel) {
-  int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1) b = 1;
-  return b;
-}
-
 template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& a, cudaStream_t stream) {
-  static const int res_v = resident_blocks(k_fp8_quant_vec<DT>);
-  static const int res_s = resident_blocks(k_fp8_quant_scalar<DT>);
   constexpr int GPW = 32 / (kFp8Block / (16 / Fmt<DT>::bytes));
   const uint64_t nblocks = (a.count + kFp8Block - 1) / kFp8Block;
   Fp8QuantArgs b = a;
@@ -133,7 +125,7 @@ template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& 
     const uint64_t nfull = a.count / kFp8Block;
     if (nfull > 0) {
       const uint64_t warps = ((uint64_t)a.nranks * nfull + GPW - 1) / GPW;
-      k_fp8_quant_vec<DT><<<grid_for(warps * 32, res_v), kThreads, 0, stream>>>(a);
+      k_fp8_quant_vec<DT><<<grid_for(warps * 32), kThreads, 0, stream>>>(a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -143,7 +135,7 @@ template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& 
   }
   if (b.first_block < nblocks) {
     const uint64_t warps = (uint64_t)a.nranks * (nblocks - b.first_block);
-    k_fp8_quant_scalar<DT><<<grid_for(warps * 32, res_s), kThreads, 0, stream>>>(b);
+    k_fp8_quant_scalar<DT><<<grid_for(warps * 32), kThreads, 0, stream>>>(b);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -268,9 +260,8 @@ __global__ void __launch_bounds__(kThreads) k_fp8_reduce(const __grid_constant__
 
 template <int ODT, int OP, int MODE, int MAXN>
 cudaError_t launch_fp8_reduce_n(const Fp8ReduceArgs& a, cudaStream_t stream) {
-  static const int resident = resident_blocks(k_fp8_reduce<ODT, OP, MODE, MAXN>);
   const uint64_t items = a.vec ? a.count / (16 / Fmt<ODT>::bytes) : a.count;
-  k_fp8_reduce<ODT, OP, MODE, MAXN><<<grid_for(items, resident), kThreads, 0, stream>>>(a);
+  k_fp8_reduce<ODT, OP, MODE, MAXN><<<grid_for(items > 0 ? items : a.count), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

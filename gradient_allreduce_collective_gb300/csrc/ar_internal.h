@@ -95,15 +95,16 @@ cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream);
 
-// Streaming multiprocessors of the calling thread's current device (cached).
-int sm_count();
-
-// Grid for a grid-stride kernel: enough blocks for `items` (one per thread),
-// at most `resident` blocks per SM on every SM.
-inline unsigned grid_for(uint64_t items, int resident) {
+// Grid for the streaming kernels: one work item per thread. Measured on
+// GB300, short-lived blocks that each move one item per thread keep more
+// loads in flight across the whole kernel (and leave no partial last round of
+// a persistent grid) than a grid of resident blocks looping over the data:
+// the fused 8 x 25 MiB allreduce runs at the speed of a plain device copy of
+// the same bytes this way. The kernels keep their grid-stride loops for
+// counts beyond the largest grid.
+inline unsigned grid_for(uint64_t items) {
   uint64_t need = (items + kThreads - 1) / kThreads;
-  uint64_t cap = (uint64_t)sm_count() * (uint64_t)(resident > 0 ? resident : 1);
-  if (need > cap) need = cap;
+  if (need > 0x7FFFFFFFull) need = 0x7FFFFFFFull;
   return (unsigned)(need > 0 ? need : 1);
 }
 

@@ -2,13 +2,13 @@
 // fused tree), instantiated per element type in ar_reduce_<type>.cu.
 //
 // One thread owns one 16-byte vector position (or one element on the
-// unaligned path) at a time, walks a grid-stride loop over positions, and for
-// each: loads the N ranks' vectors (8 in flight), folds them in the fixed
-// order, finishes (AVG divide, rounding) and stores to the chunk owner
-// (MODE_RS) or to all N outputs (fused modes). Chunk boundaries are multiples
-// of the vector width, so a vector never straddles two chunks and its fold
-// start rank is constant; threads track their chunk incrementally instead of
-// dividing per position. HBM-bound: N*16 bytes read and 16 or N*16 bytes
+// unaligned path): it loads the N ranks' vectors (8 in flight), folds them in
+// the fixed order, finishes (AVG divide, rounding) and stores to the chunk
+// owner (MODE_RS) or to all N outputs (fused modes). The grid has one thread
+// per position; the grid-stride loop only matters beyond the largest grid,
+// and then tracks the chunk incrementally. Chunk boundaries are multiples of
+// the vector width, so a vector never straddles two chunks and its fold start
+// rank is constant. HBM-bound: N*16 bytes read and 16 or N*16 bytes
 // written per vector, ~(N-1)/4 flops per 16 bytes read.
 #pragma once
 
@@ -118,14 +118,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Red
 
 template <int DT, int OP, int MODE, int MAXN>
 cudaError_t launch_reduce_n(const ReduceArgs& a, cudaStream_t stream) {
-  static const int resident = [] {
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_reduce<DT, OP, MODE, MAXN>, kThreads, 0) != cudaSuccess)
-      b = 1;
-    return b;
-  }();
   const uint64_t items = a.vec ? a.count / (16 / Fmt<DT>::bytes) : a.count;
-  k_reduce<DT, OP, MODE, MAXN><<<grid_for(items, resident), kThreads, 0, stream>>>(a);
+  k_reduce<DT, OP, MODE, MAXN><<<grid_for(items > 0 ? items : a.count), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
