@@ -306,8 +306,12 @@ def to_dev_bf16(a):
 
 
 def measure_ddp(gar, steps: int, warmup: int) -> dict:
-    """GPT-2-small DDP gradient sync on 8 ranks: per bucket one flatten call
-    for all ranks, one in-place fused allreduce (avg), one unflatten call."""
+    """GPT-2-small DDP gradient sync on 8 ranks, two ways: (a) per bucket one
+    flatten call for all ranks, one in-place fused allreduce (avg), one
+    unflatten call; (b) per bucket one ar_bucket_allreduce straight from the
+    gradient tensors (bit-identical results, no bucket copies). Then (b) on a
+    communication stream overlapped with a synthetic backward pass (bf16 GEMMs
+    on a compute stream), wall clock."""
     import torch
     import synthgen
 
@@ -322,7 +326,7 @@ def measure_ddp(gar, steps: int, warmup: int) -> dict:
         pos += c
     views = [[g[s:s + c] for s, c in zip(starts, counts)] for g in grads]
     bucket_of, offset_of, bcounts = gar.ar_bucket_plan(counts, torch.bfloat16, 25 * 1024 * 1024)
-    plan = []
+    plan, fused = [], []
     for b, bc in enumerate(bcounts):
         stride = (bc + 127) // 128 * 128  # 256-byte aligned rank slots
         flat = torch.empty(n * stride, dtype=torch.bfloat16, device="cuda")
@@ -331,55 +335,109 @@ def measure_ddp(gar, steps: int, warmup: int) -> dict:
         offs = [r * stride + offset_of[t] for r in range(n) for t in ids]
         ranks = [flat[r * stride:r * stride + bc] for r in range(n)]
         plan.append((flat, tens, offs, ranks))
+        fused.append(([[views[r][t] for t in ids] for r in range(n)], [offset_of[t] for t in ids], bc))
     stream = torch.cuda.current_stream()
 
-    def step():
+    def three_step(st):
         for flat, tens, offs, ranks in plan:
-            gar.ar_bucket_flatten(tens, offs, flat, stream)
-            gar.ar_allreduce(ranks, ranks, "avg", "fused", stream)
-            gar.ar_bucket_unflatten(flat, tens, offs, stream)
+            gar.ar_bucket_flatten(tens, offs, flat, st)
+            gar.ar_allreduce(ranks, ranks, "avg", "fused", st)
+            gar.ar_bucket_unflatten(flat, tens, offs, st)
 
-    for _ in range(warmup):
-        step()
-    ms_eager = time_steps(step, steps, stream)
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        graph.capture_begin()
-        for flat, tens, offs, ranks in plan:
-            gar.ar_bucket_flatten(tens, offs, flat, side)
-            gar.ar_allreduce(ranks, ranks, "avg", "fused", side)
-            gar.ar_bucket_unflatten(flat, tens, offs, side)
-        graph.capture_end()
-    stream.wait_stream(side)
-    for _ in range(3):
-        graph.replay()
-    ms_graph = time_steps(graph.replay, steps, stream)
+    def direct(st):
+        for tens, offs, bc in fused:
+            gar.ar_bucket_allreduce(tens, tens, offs, bc, "avg", "fused", st)
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            g.capture_begin()
+            fn(side)
+            g.capture_end()
+        stream.wait_stream(side)
+        for _ in range(3):
+            g.replay()
+        return g
+
+    res = {}
+    for name, fn in (("three_step", three_step), ("direct", direct)):
+        for _ in range(warmup):
+            fn(stream)
+        eager = time_steps(lambda: fn(stream), steps, stream)
+        g = graph_of(fn)
+        res[name] = (eager, time_steps(g.replay, steps, stream), g)
     peak, _ = hbm_peak()
     grad_bytes = total * 2
-    moved = 6 * n * grad_bytes  # flatten, allreduce and unflatten each read and write every byte
-    best = min(ms_eager, ms_graph)
-    return {
+
+    # overlap: synthetic backward (bf16 GEMMs) on one stream, direct sync on another
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    w = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    o = torch.empty_like(a)
+    g_direct = res["direct"][2]
+
+    def backward():
+        for _ in range(8):
+            torch.matmul(a, w, out=o)
+
+    def timed(run):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(20):
+            run()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / 20 * 1e3
+
+    def both():
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        comp.wait_event(ev)
+        comm.wait_event(ev)
+        with torch.cuda.stream(comp):
+            backward()
+        with torch.cuda.stream(comm):
+            g_direct.replay()
+        stream.wait_stream(comp)
+        stream.wait_stream(comm)
+
+    for _ in range(3):
+        backward()
+        both()
+    t_comp = timed(backward)
+    t_comm = timed(g_direct.replay)
+    t_both = timed(both)
+    out = {
         "workload": "DDP gradient sync: GPT-2-small shapes (148 tensors, 124,439,808 bf16 values) x 8 ranks, "
-                    "N(0,1e-4), 9 buckets of <= 25 MiB; per bucket flatten (all ranks) -> fused allreduce avg "
-                    "(binary32 accumulation) -> unflatten",
-        "buckets": len(bcounts), "launches_per_step": 3 * len(bcounts),
-        "ms_per_step_eager": ms_eager, "ms_per_step_cuda_graph": ms_graph,
-        "busbw_gbs": busbw_gbs(grad_bytes, best * 1e-3, n),
-        "hbm_gbs": moved / (best * 1e-3) / 1e9, "frac_hbm": moved / (best * 1e-3) / 1e9 / peak,
-        "algorithmic_bytes_per_step": moved,
+                    "N(0,1e-4), 9 buckets of <= 25 MiB, avg with binary32 accumulation",
+        "buckets": len(bcounts),
     }
+    for name, (eager, graph, _) in res.items():
+        best = min(eager, graph)
+        moved = (6 if name == "three_step" else 2) * n * grad_bytes
+        out[name] = {"ms_per_step_eager": eager, "ms_per_step_cuda_graph": graph,
+                     "launches_per_step": (3 if name == "three_step" else 1) * len(bcounts),
+                     "busbw_gbs": busbw_gbs(grad_bytes, best * 1e-3, n),
+                     "algorithmic_bytes_per_step": moved, "hbm_gbs": moved / (best * 1e-3) / 1e9,
+                     "frac_hbm": moved / (best * 1e-3) / 1e9 / peak}
+    out["three_step"]["what"] = "per bucket: flatten (all ranks) -> fused allreduce in place -> unflatten"
+    out["direct"]["what"] = "per bucket: ar_bucket_allreduce from the tensors (no bucket copies)"
+    out["overlap"] = {"backward_ms": t_comp, "sync_ms": t_comm, "both_ms": t_both,
+                      "hidden_fraction_of_sync": max(0.0, (t_comp + t_comm - t_both) / t_comm),
+                      "what": "8 bf16 4096^3 GEMMs (torch.matmul) on a compute stream while the direct "
+                              "sync (one CUDA graph) runs on a communication stream; wall clock, 20 reps"}
+    return out
 
 
-def measure_fp8(gar, steps: int, warmup: int) -> dict:
-    """16 ranks x 134,217,728 bf16 with 0.1% outliers x100: quantise to E4M3
+def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728) -> dict:
+    """16 ranks x `count` bf16 with 0.1% outliers x100: quantise to E4M3
     blocks (workspace) then dequantise + fused ring-order reduce (sum) + 16
     bf16 replicas."""
     import torch
     import synthgen
 
-    n, count = 16, 134_217_728
+    n = 16
     send = [to_dev_bf16(a) for a in synthgen.ranks_normal(n, count, 1e-3, base_seed=0, dtype="bf16",
                                                           outlier_p=1e-3, outlier_scale=100.0)]
     recv = [torch.empty_like(s) for s in send]
@@ -399,7 +457,7 @@ def measure_fp8(gar, steps: int, warmup: int) -> dict:
     del send, recv, ws
     torch.cuda.empty_cache()
     return {
-        "workload": "FP8-compressed allreduce: 16 ranks x 134,217,728 bf16 (256 MiB), N(0,1e-3), 0.1% outliers "
+        "workload": f"FP8-compressed allreduce: 16 ranks x {count:,} bf16, N(0,1e-3), 0.1% outliers "
                     "x100, E4M3 per-128 block scales, binary32 accumulation, sum, bf16 out, fused",
         "ms_per_step": ms, "busbw_gbs": busbw_gbs(M, ms * 1e-3, n),
         "hbm_gbs": moved / (ms * 1e-3) / 1e9, "frac_hbm": moved / (ms * 1e-3) / 1e9 / peak,
@@ -624,7 +682,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("bucket", "sweep"), default="bucket")
+    ap.add_argument("--workload", choices=("bucket", "sweep", "fp8"), default="bucket")
+    ap.add_argument("--fp8-count", type=int, default=134_217_728, help="elements per rank for --workload fp8")
     ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -636,6 +695,15 @@ def main(argv=None):
         return run_reference(args)
     if args.workload == "sweep":
         return run_sweep(args)
+    if args.workload == "fp8":
+        import torch
+
+        import gradient_allreduce_collective_gb300 as gar
+        torch.cuda.set_device(dist_env()[2])
+        gar.build()
+        gar.lib()
+        print(json.dumps(measure_fp8(gar, args.steps, args.warmup, args.fp8_count)))
+        return 0
     return run_ours(args)
 
 

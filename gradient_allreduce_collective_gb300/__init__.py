@@ -18,7 +18,7 @@ from ._build import build, lib_path
 
 __all__ = [
     "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_reduce_scatter", "ar_all_gather",
-    "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_fp8_workspace_bytes",
+    "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
     "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_status_string", "ar_last_error", "ar_version",
     "DTYPES", "OPS", "ALGOS",
 ]
@@ -59,13 +59,14 @@ def lib() -> ctypes.CDLL:
     L.ar_bucket_plan.argtypes = [vp, ci, ci, sz, vp, vp, vp, vp]
     L.ar_bucket_flatten.argtypes = [pp, vp, vp, ci, ci, vp, vp]
     L.ar_bucket_unflatten.argtypes = [vp, pp, vp, vp, ci, ci, vp]
+    L.ar_bucket_allreduce.argtypes = [pp, pp, ci, ci, vp, vp, sz, ci, ci, ci, vp]
     L.ar_fp8_workspace_bytes.argtypes = [ci, sz]
     L.ar_fp8_workspace_bytes.restype = sz
     L.ar_quantize_fp8_blocks.argtypes = [vp, ci, sz, vp, vp, vp]
     L.ar_allreduce_fp8.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp, sz, vp]
     L.ar_allreduce_fp8_noalloc.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
-                 "ar_bucket_unflatten", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc"):
+                 "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc"):
         getattr(L, name).restype = ci
     L.ar_status_string.argtypes = [ci]
     L.ar_status_string.restype = ctypes.c_char_p
@@ -174,6 +175,24 @@ def ar_bucket_unflatten(bucket: torch.Tensor, tensors: Sequence[torch.Tensor], o
     offs = (ctypes.c_size_t * max(t, 1))(*offsets)
     _check(lib().ar_bucket_unflatten(bucket.data_ptr(), _ptrs(tensors), counts, offs, t, DTYPES[bucket.dtype],
                                      _stream(stream)))
+
+
+def ar_bucket_allreduce(tensors: Sequence[Sequence[torch.Tensor]], out_tensors: Sequence[Sequence[torch.Tensor]],
+                        offsets: Sequence[int], bucket_count: int, op: str = "avg", algo: str = "fused",
+                        stream=None) -> None:
+    """tensors[r][t] / out_tensors[r][t]: rank r's tensor t; offsets[t]: its
+    element offset in the bucket layout of bucket_count elements."""
+    n = len(tensors)
+    t = len(tensors[0]) if n else 0
+    flat_in = [x for rank in tensors for x in rank]
+    flat_out = [x for rank in out_tensors for x in rank]
+    if len(flat_in) != n * t or len(flat_out) != n * t:
+        raise ValueError("every rank needs the same tensors")
+    dt = flat_in[0].dtype
+    counts = (ctypes.c_size_t * max(t, 1))(*[x.numel() for x in tensors[0]])
+    offs = (ctypes.c_size_t * max(t, 1))(*offsets)
+    _check(lib().ar_bucket_allreduce(_ptrs(flat_in), _ptrs(flat_out), n, t, counts, offs, bucket_count, DTYPES[dt],
+                                     OPS[op], ALGOS[algo], _stream(stream)))
 
 
 def ar_fp8_workspace_bytes(nranks: int, count: int) -> int:

@@ -31,6 +31,22 @@ cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cuda
   }
 }
 
+// in ar_bucket_<type>.cu
+cudaError_t launch_bucket_f32(int op, int mode, const BucketArgs& a, cudaStream_t stream);
+cudaError_t launch_bucket_f16(int op, int mode, const BucketArgs& a, cudaStream_t stream);
+cudaError_t launch_bucket_bf16(int op, int mode, const BucketArgs& a, cudaStream_t stream);
+cudaError_t launch_bucket_i32(int op, int mode, const BucketArgs& a, cudaStream_t stream);
+
+cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream) {
+  switch (dtype) {
+    case DT_F32: return launch_bucket_f32(op, mode, a, stream);
+    case DT_F16: return launch_bucket_f16(op, mode, a, stream);
+    case DT_BF16: return launch_bucket_bf16(op, mode, a, stream);
+    case DT_I32: return launch_bucket_i32(op, mode, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace gar
 
 namespace {
@@ -406,6 +422,101 @@ ar_status_t ar_bucket_unflatten(const void* bucket, void* const* tensors, const 
   if (!bucket && ntensors > 0) return fail(AR_ERR_INVALID_ARGUMENT, "null bucket");
   return bucket_copy(nullptr, tensors, bucket, nullptr, counts, offsets, ntensors, dtype,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+ar_status_t ar_bucket_allreduce(const void* const* tensors, void* const* out_tensors, int nranks, int ntensors,
+                                const size_t* counts, const size_t* offsets, size_t bucket_count, ar_dtype_t dtype,
+                                ar_op_t op, ar_algo_t algo, ar_stream_t stream) {
+  ar_status_t st = common_checks(tensors, out_tensors, nranks, dtype);
+  if (st != AR_SUCCESS) return st;
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if (algo == AR_ALGO_TREE && !pow2(nranks))
+    return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
+  if (ntensors < 0) return fail(AR_ERR_INVALID_ARGUMENT, "ntensors < 0");
+  if (ntensors == 0 || bucket_count == 0) return ok();
+  if (!counts || !offsets) return fail(AR_ERR_INVALID_ARGUMENT, "null counts/offsets");
+  const size_t es = elem_size(dtype);
+  if (bucket_count > SIZE_MAX / es / 4) return fail(AR_ERR_INVALID_ARGUMENT, "bucket too large");
+  const size_t vecw = 16 / es;
+  bool vec = true;
+  std::vector<Span> spans;
+  spans.reserve(2 * (size_t)nranks * (size_t)ntensors);
+  std::vector<int> pair_in;
+  std::vector<uintptr_t> pair_off;
+  for (int t = 0; t < ntensors; ++t) {
+    if (counts[t] == 0) continue;
+    if (offsets[t] > bucket_count || counts[t] > bucket_count - offsets[t])
+      return fail(AR_ERR_INVALID_ARGUMENT, "tensor " + std::to_string(t) + " lies outside the bucket");
+    if (offsets[t] % vecw) vec = false;
+    for (int r = 0; r < nranks; ++r) {
+      const void* in = tensors[(size_t)r * ntensors + t];
+      void* out = out_tensors[(size_t)r * ntensors + t];
+      if (!in || !out) return fail(AR_ERR_INVALID_ARGUMENT, "null tensor pointer");
+      if (!aligned(in, es) || !aligned(out, es))
+        return fail(AR_ERR_INVALID_ARGUMENT, "tensor not aligned to the element size");
+      if (!aligned(in, 16) || !aligned(out, 16)) vec = false;
+      const int id = (int)pair_in.size();
+      const uintptr_t n = counts[t] * es;
+      spans.push_back({addr(in), addr(in) + n, false, id});
+      spans.push_back({addr(out), addr(out) + n, true, id});
+      pair_in.push_back(id);  // in place: out == in for the same rank and tensor
+      pair_off.push_back(0);
+    }
+  }
+  if (!overlap_ok(spans, pair_in, pair_off)) return fail(AR_ERR_ALIAS, "buffers overlap");
+  const size_t L = chunk_len(bucket_count, nranks, vecw);
+  const int mode = algo == AR_ALGO_TREE ? MODE_FUSED_TREE : MODE_FUSED_RING;
+  const int per_launch = std::min(kBucketTensors, kBucketPtrs / nranks);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  BucketArgs a{};
+  a.nranks = nranks;
+  a.L = L;
+  a.vec = vec ? 1 : 0;
+  uint64_t tiles = 0;
+  auto flush = [&]() -> ar_status_t {
+    if (a.nt == 0) return AR_SUCCESS;
+    // pointer slots are rank-major over the tensors of this launch
+    const cudaError_t e = launch_bucket_reduce(dtype, op, mode, a, s);
+    a.nt = 0;
+    tiles = 0;
+    return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "bucket allreduce launch");
+  };
+  std::vector<int> batch;
+  auto pack = [&]() -> ar_status_t {
+    const int nt = (int)batch.size();
+    a.nt = nt;
+    tiles = 0;
+    for (int j = 0; j < nt; ++j) {
+      const int t = batch[j];
+      a.count[j] = counts[t];
+      a.offset[j] = offsets[t];
+      a.tile_start[j] = (uint32_t)tiles;
+      const uint64_t items = vec ? (counts[t] + vecw - 1) / vecw : counts[t];
+      tiles += (items + kThreads - 1) / kThreads;
+      for (int r = 0; r < nranks; ++r) {
+        a.src[r * nt + j] = tensors[(size_t)r * ntensors + t];
+        a.dst[r * nt + j] = out_tensors[(size_t)r * ntensors + t];
+      }
+    }
+    a.tile_start[nt] = (uint32_t)tiles;
+    batch.clear();
+    return flush();
+  };
+  uint64_t batch_tiles = 0;
+  for (int t = 0; t < ntensors; ++t) {
+    if (counts[t] == 0) continue;
+    const uint64_t items = vec ? (counts[t] + vecw - 1) / vecw : counts[t];
+    const uint64_t nt_tiles = (items + kThreads - 1) / kThreads;
+    if ((int)batch.size() == per_launch || batch_tiles + nt_tiles > 0x7FFFFFFFull) {
+      if ((st = pack()) != AR_SUCCESS) return st;
+      batch_tiles = 0;
+    }
+    batch.push_back(t);
+    batch_tiles += nt_tiles;
+  }
+  if (!batch.empty() && (st = pack()) != AR_SUCCESS) return st;
+  return ok();
 }
 
 size_t ar_fp8_workspace_bytes(int nranks, size_t count) {

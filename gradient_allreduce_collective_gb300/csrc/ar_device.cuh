@@ -182,7 +182,9 @@ template <class Ld> struct Fold {
       }
     }
     if constexpr (MAXN > 8) {
-      for (int b0 = 8; b0 < N; b0 += 8) {
+#pragma unroll
+      for (int b0 = 8; b0 < MAXN; b0 += 8) {
+        if (b0 >= N) break;
         Raw raw[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -245,7 +247,7 @@ template <class Ld> struct Fold {
     const int nb = N >> 3;
     Acc part[8][V];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < (MAXN >= 64 ? 8 : MAXN / 8); ++r)
       if (r < nb) tree8(ld, r, nb, 8, part[r]);
     halve(part, nb);
 #pragma unroll

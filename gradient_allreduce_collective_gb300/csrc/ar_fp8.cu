@@ -32,44 +32,70 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
   return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
+// Blocks handled by one lane group per launch row: every lane issues the loads
+// of kQuantUnroll blocks before any arithmetic, so 4 x 16 bytes are in flight.
+constexpr int kQuantUnroll = 4;
+
+// E4M3 codes of (a, b) with a in the low byte: one paired conversion.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// E4M3 codes of x[k] / s for one lane's V values (q = RN_E4M3_sat(RN(x / s)),
+// the IEEE division as the oracle does it), packed little-endian into V/4
+// words; amax == 0 gives all-zero codes. (A division-free bracket with an
+// exact fallback was measured slower: with bf16 inputs x/s sits on or near
+// E4M3 rounding boundaries often enough, and the bracket's checks cost as
+// many instructions as the division they replace.)
+template <int V>
+__device__ __forceinline__ void quantise_lane(const float (&x)[V], float amax, float s, uint32_t (&word)[V / 4]) {
+#pragma unroll
+  for (int k = 0; k < V; k += 4) {
+    uint32_t w = 0;
+    if (amax != 0.0f) {
+      const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[k], s), __fdiv_rn(x[k + 1], s));
+      const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[k + 2], s), __fdiv_rn(x[k + 3], s));
+      w = lo | (hi << 16);
+    }
+    word[k / 4] = w;
+  }
+}
+
+// grid.y = rank; along x, each warp takes kQuantUnroll groups of 32/G blocks
+// (G = 128/V lanes per block: 16 for bf16/fp16, 32 for fp32).
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constant__ Fp8QuantArgs A) {
-  constexpr int B = Fmt<DT>::bytes, V = 16 / B, G = kFp8Block / V, GPW = 32 / G;
+  constexpr int B = Fmt<DT>::bytes, V = 16 / B, G = kFp8Block / V, BPW = 32 / G;
+  const int r = blockIdx.y;
   const uint64_t nfull = A.count / kFp8Block;
-  const uint64_t tasks = (uint64_t)A.nranks * nfull;  // (rank, block) pairs
   const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
-  const uint64_t warp0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-  const uint64_t wtasks = (tasks + GPW - 1) / GPW;
-  for (uint64_t w = warp0; w < wtasks; w += nwarps) {  // uniform across the warp
-    const uint64_t task = w * GPW + g;
-    const bool valid = task < tasks;
-    int r = 0;
-    uint64_t b = 0;
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (valid) {
-      r = (int)(task / nfull);
-      b = task - (uint64_t)r * nfull;
-      raw = __ldcs(reinterpret_cast<const uint4*>(static_cast<const char*>(A.src[r]) +
-                                                  (b * kFp8Block + (uint64_t)gl * V) * B));
-    }
+  const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint64_t b0 = warp * (uint64_t)(kQuantUnroll * BPW);
+  if (b0 >= nfull) return;  // warp-uniform
+  const char* src = static_cast<const char*>(A.src[r]);
+  uint4 raw[kQuantUnroll];
+#pragma unroll
+  for (int u = 0; u < kQuantUnroll; ++u) {
+    const uint64_t b = b0 + (uint64_t)(u * BPW + g);
+    raw[u] = (b < nfull) ? __ldcs(reinterpret_cast<const uint4*>(src + (b * kFp8Block + (uint64_t)gl * V) * B))
+                         : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int u = 0; u < kQuantUnroll; ++u) {
+    const uint64_t b = b0 + (uint64_t)(u * BPW + g);
     float x[V];
     float amax = 0.0f;
 #pragma unroll
     for (int k = 0; k < V; ++k) {
-      x[k] = to_f32<DT>(get_lane<B>(raw, k));
+      x[k] = to_f32<DT>(get_lane<B>(raw[u], k));
       amax = fmaxf(amax, fabsf(x[k]));
     }
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = __fdiv_rn(amax, 448.0f);
-    uint32_t word[(V + 3) / 4] = {};
-#pragma unroll
-    for (int k = 0; k < V; ++k) {
-      const uint32_t q = (amax == 0.0f) ? 0u : f32_to_e4m3(__fdiv_rn(x[k], s));
-      word[k >> 2] |= q << ((k & 3) * 8);
-    }
-    if (valid) {
+    uint32_t word[V / 4];
+    quantise_lane<V>(x, amax, s, word);
+    if (b < nfull) {
       uint8_t* qp = A.q[r] + b * kFp8Block + (uint64_t)gl * V;
       if constexpr (V == 8) __stcs(reinterpret_cast<uint2*>(qp), make_uint2(word[0], word[1]));
       else __stcs(reinterpret_cast<unsigned int*>(qp), word[0]);
@@ -118,14 +144,15 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_scalar(const __grid_cons
 }
 
 template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& a, cudaStream_t stream) {
-  constexpr int GPW = 32 / (kFp8Block / (16 / Fmt<DT>::bytes));
+  constexpr int BPW = 32 / (kFp8Block / (16 / Fmt<DT>::bytes));
   const uint64_t nblocks = (a.count + kFp8Block - 1) / kFp8Block;
   Fp8QuantArgs b = a;
   if (vec) {
     const uint64_t nfull = a.count / kFp8Block;
     if (nfull > 0) {
-      const uint64_t warps = ((uint64_t)a.nranks * nfull + GPW - 1) / GPW;
-      k_fp8_quant_vec<DT><<<grid_for(warps * 32), kThreads, 0, stream>>>(a);
+      const uint64_t warps = (nfull + kQuantUnroll * BPW - 1) / (kQuantUnroll * BPW);
+      const dim3 grid(grid_for(warps * 32), (unsigned)a.nranks);
+      k_fp8_quant_vec<DT><<<grid, kThreads, 0, stream>>>(a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -267,19 +294,19 @@ cudaError_t launch_fp8_reduce_n(const Fp8ReduceArgs& a, cudaStream_t stream) {
 
 template <int ODT, int OP>
 cudaError_t launch_fp8_reduce_op(int mode, const Fp8ReduceArgs& a, cudaStream_t stream) {
-  const bool small = a.nranks <= 8;
+  // compile-time rank bound: 8, 16 (two batches of loads, unrolled) or 64
+  const int tier = a.nranks <= 8 ? 0 : (a.nranks <= 16 ? 1 : 2);
+#define GAR_TIERS(MODEV)                                                                          \
+  return tier == 0 ? launch_fp8_reduce_n<ODT, OP, MODEV, 8>(a, stream)                          \
+       : tier == 1 ? launch_fp8_reduce_n<ODT, OP, MODEV, 16>(a, stream)                         \
+                   : launch_fp8_reduce_n<ODT, OP, MODEV, kMaxRanks>(a, stream);
   switch (mode) {
-    case MODE_RS:
-      return small ? launch_fp8_reduce_n<ODT, OP, MODE_RS, 8>(a, stream)
-                   : launch_fp8_reduce_n<ODT, OP, MODE_RS, kMaxRanks>(a, stream);
-    case MODE_FUSED_RING:
-      return small ? launch_fp8_reduce_n<ODT, OP, MODE_FUSED_RING, 8>(a, stream)
-                   : launch_fp8_reduce_n<ODT, OP, MODE_FUSED_RING, kMaxRanks>(a, stream);
-    case MODE_FUSED_TREE:
-      return small ? launch_fp8_reduce_n<ODT, OP, MODE_FUSED_TREE, 8>(a, stream)
-                   : launch_fp8_reduce_n<ODT, OP, MODE_FUSED_TREE, kMaxRanks>(a, stream);
+    case MODE_RS: GAR_TIERS(MODE_RS)
+    case MODE_FUSED_RING: GAR_TIERS(MODE_FUSED_RING)
+    case MODE_FUSED_TREE: GAR_TIERS(MODE_FUSED_TREE)
     default: return cudaErrorInvalidValue;
   }
+#undef GAR_TIERS
 }
 
 template <int ODT> cudaError_t launch_fp8_reduce_dt(int op, int mode, const Fp8ReduceArgs& a, cudaStream_t s) {

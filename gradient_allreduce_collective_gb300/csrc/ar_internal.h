@@ -88,10 +88,30 @@ struct Fp8ReduceArgs {
   int vec;
 };
 
+// Bucket allreduce straight from the gradient tensors: tensor t of rank r is
+// src[r * nt + t] (counts[t] elements) at element offset[t] of the bucket
+// layout, whose chunk length is L; results go to dst[r * nt + t]. Work is cut
+// into tiles of kThreads items (16-byte vectors, or elements on the
+// element-wise path); tile_start[t] is tensor t's first tile.
+constexpr int kBucketPtrs = 1024;
+constexpr int kBucketTensors = 128;
+struct BucketArgs {
+  const void* src[kBucketPtrs];
+  void* dst[kBucketPtrs];
+  uint64_t count[kBucketTensors];
+  uint64_t offset[kBucketTensors];
+  uint32_t tile_start[kBucketTensors + 1];
+  uint64_t L;
+  int nt;
+  int nranks;
+  int vec;
+};
+
 // Launchers: enqueue on `stream`, return the launch status.
 cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream);
+cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream);
 

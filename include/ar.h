@@ -153,6 +153,29 @@ ar_status_t ar_bucket_flatten(const void *const *tensors, const size_t *counts, 
 ar_status_t ar_bucket_unflatten(const void *bucket, void *const *tensors, const size_t *counts, const size_t *offsets,
                                 int ntensors, ar_dtype_t dtype, ar_stream_t stream);
 
+/* Bucket allreduce from the gradient tensors themselves (no flat bucket).
+ * Same result, bit for bit, as flattening every rank's tensors into a bucket
+ * of bucket_count elements at `offsets`, ar_allreduce on the buckets, and
+ * unflattening ([GL] §パフォーマンスチューニング: bucketing; [AW] §计算-通信
+ * 重叠: a bucket's allreduce starts as soon as its gradients are ready), but
+ * each rank's tensors are read where they live and the result is written to
+ * every rank's output tensors directly: 2*N*B bytes moved instead of 6*N*B.
+ *   tensors[r*ntensors + t]     — rank r's tensor t (device), counts[t]
+ *                                 elements of dtype; host array of
+ *                                 nranks*ntensors pointers, rank-major.
+ *   out_tensors[r*ntensors + t] — where rank r's reduced tensor t goes; may
+ *                                 equal tensors[r*ntensors + t] (in place).
+ *   counts, offsets             — host arrays of ntensors entries: element
+ *                                 count and element offset of tensor t in the
+ *                                 bucket layout (as ar_bucket_plan gives).
+ *   bucket_count                — elements in the bucket (fixes the chunks).
+ * algo: RING and FUSED give the same bits (the ring order, computed in one
+ * pass); TREE is recursive halving (nranks a power of two). Output tensors
+ * must not overlap each other or any input other than their own. */
+ar_status_t ar_bucket_allreduce(const void *const *tensors, void *const *out_tensors, int nranks, int ntensors,
+                                const size_t *counts, const size_t *offsets, size_t bucket_count, ar_dtype_t dtype,
+                                ar_op_t op, ar_algo_t algo, ar_stream_t stream);
+
 /* FP8 gradient compression ([GL] §NCCLにおけるAllReduce: FP8 AllReduce halves
  * the traffic; §勾配圧縮技術: FP8 quantisation; [VL] §data typeと圧縮は品質だけ
  * の問題ではない: quantise, dequantise and a scale exchange are needed and the

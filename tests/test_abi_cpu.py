@@ -152,3 +152,20 @@ def test_bucket_copy_errors(L):
     assert L.ar_bucket_flatten(_arr(t), counts, offs_ok, 2, 2, 0, None) == gar.AR_ERR_INVALID_ARGUMENT
     assert L.ar_bucket_flatten(_arr(t), counts, offs_ok, 0, 2, 0x4000000, None) == gar.AR_SUCCESS
     del torch
+
+
+def test_bucket_allreduce_argument_errors(L):
+    n, nt = 4, 3
+    ins = [0x1000000 * (1 + r * nt + t) for r in range(n) for t in range(nt)]
+    outs = [0x40000000 + 0x1000000 * (r * nt + t) for r in range(n) for t in range(nt)]
+    counts = (ctypes.c_size_t * nt)(100, 200, 300)
+    offs = (ctypes.c_size_t * nt)(0, 104, 304)
+    f = L.ar_bucket_allreduce
+    bad_offs = (ctypes.c_size_t * nt)(0, 104, 400)  # last tensor ends beyond the bucket
+    assert f(_arr(ins), _arr(outs), n, nt, counts, bad_offs, 600, 2, 1, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert "outside the bucket" in gar.ar_last_error()
+    over = list(outs)
+    over[5] = outs[4] + 2  # two outputs overlap
+    assert f(_arr(ins), _arr(over), n, nt, counts, offs, 604, 2, 1, 1, None) == gar.AR_ERR_ALIAS
+    assert f(_arr(ins[:9]), _arr(outs[:9]), 3, nt, counts, offs, 604, 2, 1, 2, None) == gar.AR_ERR_UNSUPPORTED
+    assert f(_arr(ins), _arr(outs), n, 0, counts, offs, 604, 2, 1, 1, None) == gar.AR_SUCCESS

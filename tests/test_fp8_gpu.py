@@ -46,6 +46,49 @@ def test_quantize_matches_oracle(in_dtype):
             assert _same_bits(from_dev(q), wq) and _same_bits(from_dev(s), ws), (count, off)
 
 
+def _e4m3_midpoints():
+    codes = np.arange(0x7F, dtype=np.uint8)
+    v = np.sort(oracle.e4m3_to_f32(codes).astype(np.float64))
+    return (v[1:] + v[:-1]) / 2  # 126 rounding boundaries between magnitudes
+
+
+def test_quantize_rounding_boundaries():
+    # every block: x[0] = amax (so s = amax/448), then values whose x/s fall on
+    # and within a few binary32 ulps of every E4M3 midpoint, both signs
+    mids = _e4m3_midpoints()
+    blocks = []
+    for amax in (1.0, 3.0, 0.7, 1e-3, 123456.0, 1e-36, 2.0**-127, 2.0**-140):
+        a = np.float32(amax)
+        s = np.float32(a / np.float32(448.0))
+        vals = []
+        for m in mids:
+            x = np.float32(m * np.float64(s))
+            for j in range(-3, 4):
+                y = x
+                for _ in range(abs(j)):
+                    y = np.nextafter(y, np.float32(np.inf) if j > 0 else np.float32(0))
+                if abs(y) <= a:
+                    vals.append(y)
+        vals = np.array(vals, dtype=np.float32)
+        vals = np.concatenate([vals, -vals])
+        for i in range(0, len(vals), 127):
+            blk = np.zeros(128, dtype=np.float32)
+            blk[0] = a
+            part = vals[i:i + 127]
+            blk[1:1 + len(part)] = part
+            blocks.append(blk)
+    blocks.append(np.zeros(128, dtype=np.float32))
+    x = np.concatenate(blocks)
+    q = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(x.size // 128, dtype=torch.float32, device="cuda")
+    gar.ar_quantize_fp8_blocks(to_dev(x, "f32"), q, sc)
+    wq, ws = oracle.fp8_quantize(x, "f32")
+    assert _same_bits(from_dev(sc), ws)
+    got = from_dev(q)
+    bad = np.nonzero(got != wq)[0]
+    assert bad.size == 0, (bad[:10], got[bad[:10]], wq[bad[:10]], x[bad[:10]])
+
+
 def test_fp8_block_example():
     g = G.load("fp8_block_example.txt")
     send = [to_dev(synthgen.to_dtype(np.array(G.nums(g[f"rank{r}"]), dtype=np.float32), "bf16"), "bf16")
