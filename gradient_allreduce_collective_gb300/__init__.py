@@ -19,7 +19,8 @@ from ._build import build, lib_path
 __all__ = [
     "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_reduce_scatter", "ar_all_gather",
     "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
-    "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_status_string", "ar_last_error", "ar_version",
+    "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_noalloc",
+    "ar_status_string", "ar_last_error", "ar_version",
     "DTYPES", "OPS", "ALGOS",
 ]
 
@@ -65,8 +66,9 @@ def lib() -> ctypes.CDLL:
     L.ar_quantize_fp8_blocks.argtypes = [vp, ci, sz, vp, vp, vp]
     L.ar_allreduce_fp8.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp, sz, vp]
     L.ar_allreduce_fp8_noalloc.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
+    L.ar_allreduce_fp8_fused.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
-                 "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc"):
+                 "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused"):
         getattr(L, name).restype = ci
     L.ar_status_string.argtypes = [ci]
     L.ar_status_string.restype = ctypes.c_char_p
@@ -211,6 +213,15 @@ def ar_allreduce_fp8(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.
     _check(lib().ar_allreduce_fp8(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], DTYPES[odt],
                                   OPS[op], ALGOS[algo], workspace.data_ptr(),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ar_allreduce_fp8_fused(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], op: str = "sum",
+                           algo: str = "fused", stream=None) -> None:
+    """ar_allreduce_fp8's result with the quantisation fused into the reduction (no workspace)."""
+    dt, n = _same(sendbufs, "sendbufs")
+    odt, _ = _same(recvbufs, "recvbufs")
+    _check(lib().ar_allreduce_fp8_fused(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], DTYPES[odt],
+                                        OPS[op], ALGOS[algo], _stream(stream)))
 
 
 FP8_STATIC_WS_BYTES = 16 * 1024 * 1024

@@ -37,6 +37,24 @@ cudaError_t launch_bucket_f16(int op, int mode, const BucketArgs& a, cudaStream_
 cudaError_t launch_bucket_bf16(int op, int mode, const BucketArgs& a, cudaStream_t stream);
 cudaError_t launch_bucket_i32(int op, int mode, const BucketArgs& a, cudaStream_t stream);
 
+// in ar_fp8_fused_<input type>.cu
+cudaError_t launch_fp8_fused_bf16(int out_dtype, int op, int mode, bool vec, const Fp8FusedArgs& a,
+                                  cudaStream_t stream);
+cudaError_t launch_fp8_fused_f16(int out_dtype, int op, int mode, bool vec, const Fp8FusedArgs& a,
+                                 cudaStream_t stream);
+cudaError_t launch_fp8_fused_f32(int out_dtype, int op, int mode, bool vec, const Fp8FusedArgs& a,
+                                 cudaStream_t stream);
+
+cudaError_t launch_fp8_fused(int in_dtype, int out_dtype, int op, int mode, bool vec, const Fp8FusedArgs& a,
+                             cudaStream_t stream) {
+  switch (in_dtype) {
+    case DT_BF16: return launch_fp8_fused_bf16(out_dtype, op, mode, vec, a, stream);
+    case DT_F16: return launch_fp8_fused_f16(out_dtype, op, mode, vec, a, stream);
+    case DT_F32: return launch_fp8_fused_f32(out_dtype, op, mode, vec, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream) {
   switch (dtype) {
     case DT_F32: return launch_bucket_f32(op, mode, a, stream);
@@ -621,6 +639,71 @@ ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs,
   for (int r = 0; r < nranks; ++r) ra.dst[r] = recvbufs[r];
   e = launch_fp8_reduce(out_dtype, op, algo == AR_ALGO_TREE ? MODE_FUSED_TREE : MODE_FUSED_RING, ra, s);
   return e == cudaSuccess ? ok() : cuda_fail(e, "fp8 allreduce launch");
+}
+
+
+ar_status_t ar_allreduce_fp8_fused(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                                   ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
+                                   ar_stream_t stream) {
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, in_dtype);
+  if (st != AR_SUCCESS) return st;
+  if (in_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating input type");
+  if (elem_size(out_dtype) == 0) return fail(AR_ERR_INVALID_ARGUMENT, "unknown out_dtype");
+  if (out_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating output type");
+  if (elem_size(in_dtype) == 2 && elem_size(out_dtype) == 4)
+    return fail(AR_ERR_UNSUPPORTED, "fused FP8 path: 16-bit inputs need a 16-bit output type");
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (op != AR_SUM && op != AR_AVG) return fail(AR_ERR_UNSUPPORTED, "FP8 path supports SUM and AVG");
+  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if (algo == AR_ALGO_TREE && !pow2(nranks))
+    return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
+  if (count == 0) return ok();
+  const size_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
+  if (count > SIZE_MAX / 8 / (size_t)nranks) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if ((st = check_ptrs(sendbufs, nranks, ies, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, oes, "recvbufs")) != AR_SUCCESS) return st;
+  std::vector<Span> spans;
+  for (int r = 0; r < nranks; ++r) {
+    spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + count * ies, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + count * oes, true, r});
+  }
+  if (!overlap_ok(spans, {}, {})) return fail(AR_ERR_ALIAS, "buffers overlap");
+
+  Fp8FusedArgs a{};
+  a.nranks = nranks;
+  a.count = count;
+  a.L = chunk_len(count, nranks, 16 / oes);
+  for (int r = 0; r < nranks; ++r) {
+    a.src[r] = sendbufs[r];
+    a.dst[r] = recvbufs[r];
+  }
+  const bool vec = all_aligned16(sendbufs, nranks) && all_aligned16(recvbufs, nranks);
+  const uint64_t nfull = count / AR_FP8_BLOCK;
+  const int mode = algo == AR_ALGO_TREE ? MODE_FUSED_TREE : MODE_FUSED_RING;
+  if (!vec) {
+    a.first_block = 0;  // every block on the element-wise kernel
+  } else {
+    a.first_block = nfull;  // the short last block, if any
+    if (mode == MODE_FUSED_RING) {
+      // a warp of the vector kernel covers BPW blocks and needs them in one
+      // chunk; list the blocks of each warp that a chunk boundary cuts
+      const uint64_t bpw = 32 / (AR_FP8_BLOCK * ies / 16);
+      uint64_t last_w = UINT64_MAX;
+      for (int c = 1; c < nranks; ++c) {
+        const uint64_t e = (uint64_t)c * a.L;
+        if (e >= nfull * AR_FP8_BLOCK) break;
+        const uint64_t w = e / AR_FP8_BLOCK / bpw;
+        if (e == w * bpw * AR_FP8_BLOCK || w == last_w) continue;
+        last_w = w;
+        for (uint64_t b = w * bpw; b < (w + 1) * bpw && b < nfull; ++b) {
+          if (a.nlist == kFusedList) return fail(AR_ERR_UNSUPPORTED, "too many chunk boundaries");
+          a.list[a.nlist++] = b;
+        }
+      }
+    }
+  }
+  const cudaError_t e = launch_fp8_fused(in_dtype, out_dtype, op, mode, vec, a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "fused fp8 allreduce launch");
 }
 
 }  // extern "C"

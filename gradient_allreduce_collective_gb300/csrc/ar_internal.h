@@ -107,6 +107,22 @@ struct BucketArgs {
   int vec;
 };
 
+// FP8 allreduce with the quantisation fused into the reduction (no wire
+// buffer). The vector kernel takes every full 128-element block except those
+// listed for the element-wise kernel; the element-wise kernel takes the
+// listed blocks and blocks [first_block, nblocks).
+constexpr int kFusedList = 160;
+struct Fp8FusedArgs {
+  const void* src[kMaxRanks];
+  void* dst[kMaxRanks];
+  uint64_t count;
+  uint64_t L;
+  uint64_t list[kFusedList];  // element-wise kernel: listed blocks first
+  uint64_t first_block;       // then blocks [first_block, nblocks)
+  int nlist;
+  int nranks;
+};
+
 // Launchers: enqueue on `stream`, return the launch status.
 cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream);
@@ -114,6 +130,10 @@ cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream);
+// vec: run the vector kernel over the full blocks; then the element-wise
+// kernel over the listed blocks and [first_block, nblocks) (if any).
+cudaError_t launch_fp8_fused(int in_dtype, int out_dtype, int op, int mode, bool vec, const Fp8FusedArgs& a,
+                             cudaStream_t stream);
 
 // Grid for the streaming kernels: one work item per thread. Measured on
 // GB300, short-lived blocks that each move one item per thread keep more

@@ -209,6 +209,21 @@ ar_status_t ar_allreduce_fp8(const void *const *sendbufs, void *const *recvbufs,
                              ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
                              void *workspace, size_t ws_bytes, ar_stream_t stream);
 
+/* FP8-compressed allreduce with the quantisation fused into the reduction:
+ * the same bits as ar_allreduce_fp8 with the same arguments (every rank's
+ * blocks quantised once, dequantised, reduced in binary32 in the order `algo`
+ * names), but the E4M3 codes and scales stay in registers instead of a wire
+ * buffer, so no workspace is needed and the call moves 2*N*M bytes instead
+ * of 2*N*M + 2*N*(M/2 + M/64). ([GL] §勾配圧縮技術: FP8 quantisation;
+ * [VL] §data typeと圧縮: quantise/dequantise and scale handling cost extra
+ * kernels and bytes — here they are folded into the one pass.)
+ * RING and FUSED give the same bits; TREE is recursive halving. 16-bit
+ * inputs need a 16-bit output type (AR_ERR_UNSUPPORTED otherwise).
+ * recvbufs must not overlap sendbufs or each other. */
+ar_status_t ar_allreduce_fp8_fused(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
+                                   ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
+                                   ar_stream_t stream);
+
 /* Bytes of the FP8 workspace built into the library (16 MiB per device). */
 #define AR_FP8_STATIC_WS_BYTES (16u * 1024u * 1024u)
 

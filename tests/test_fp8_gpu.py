@@ -123,6 +123,51 @@ def test_fp8_allreduce_matches_oracle(in_dtype, out_dtype):
                         assert _same_bits(from_dev(v), want), (n, count, op, algo)
 
 
+FUSED_IO = [("bf16", "bf16"), ("bf16", "f16"), ("f16", "f16"), ("f16", "bf16"), ("f32", "f32"), ("f32", "bf16"),
+            ("f32", "f16")]
+
+
+@pytest.mark.parametrize("in_dtype,out_dtype", FUSED_IO)
+def test_fp8_fused_matches_oracle(in_dtype, out_dtype):
+    # counts put chunk boundaries inside vector-kernel warps (element-wise path),
+    # on warp edges, and leave short last blocks
+    for n in (1, 2, 3, 5, 8, 16):
+        for count in (1, 100, 128 * 97 + 24, 128 * 300, 128 * 1000 + 72):
+            send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=3 * n + count, dtype=in_dtype,
+                                            outlier_p=1e-2, outlier_scale=100.0)
+            send = [to_dev(a, in_dtype) for a in send_np]
+            for op in ("sum", "avg"):
+                algos = ("ring", "fused", "tree") if n & (n - 1) == 0 else ("ring", "fused")
+                for algo in algos:
+                    if algo == "tree":
+                        want = oracle.fp8_tree_allreduce(send_np, in_dtype, out_dtype, op)[0]
+                    else:
+                        want = oracle.fp8_ring_allreduce(send_np, in_dtype, out_dtype, op)[0]
+                    out = Guarded(n, count, out_dtype)
+                    gar.ar_allreduce_fp8_fused(send, out.views, op, algo)
+                    out.check()
+                    for v in out.views:
+                        assert _same_bits(from_dev(v), want), (n, count, op, algo)
+
+
+def test_fp8_fused_unaligned_and_unsupported():
+    n, count = 4, 128 * 20 + 9
+    send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=6, dtype="bf16")
+    want = oracle.fp8_ring_allreduce(send_np, "bf16", "bf16", "sum")[0]
+    gin = Guarded(n, count, "bf16", 2)
+    for v, a in zip(gin.views, send_np):
+        v.copy_(to_dev(a, "bf16"))
+    out = Guarded(n, count, "bf16", 6)
+    gar.ar_allreduce_fp8_fused(gin.views, out.views, "sum", "fused")
+    out.check()
+    for v in out.views:
+        assert _same_bits(from_dev(v), want)
+    f32_out = [torch.empty(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+    with pytest.raises(gar.ArError) as ei:
+        gar.ar_allreduce_fp8_fused(gin.views, f32_out, "sum", "fused")
+    assert ei.value.status == gar.AR_ERR_UNSUPPORTED
+
+
 def test_fp8_unaligned_outputs():
     n, count = 4, 128 * 20 + 9
     send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=5, dtype="bf16")
@@ -149,6 +194,12 @@ def test_config5_full_size_sampled():
     f0 = fused[0].view(torch.int16)
     for r in range(n):
         assert torch.equal(fused[r].view(torch.int16), f0)
+        assert torch.equal(ring[r].view(torch.int16), f0)
+    del ws
+    # the quantisation fused into the reduction gives the same bits
+    gar.ar_allreduce_fp8_fused(send, ring, "sum", "fused")
+    torch.cuda.synchronize()
+    for r in range(n):
         assert torch.equal(ring[r].view(torch.int16), f0)
     del ring
     rng = np.random.default_rng(0)
