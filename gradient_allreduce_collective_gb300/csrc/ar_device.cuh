@@ -147,14 +147,31 @@ template <int BYTES> __device__ __forceinline__ void set_lane(uint4& v, int k, u
 // Loads of up to 8 ranks are issued before any combine so that 8 x 16 bytes
 // per thread are in flight.
 
+// A loader may declare `static constexpr bool kPairAdd = true` when its comb
+// is the binary32 add; pairs of lanes then use the packed add, whose
+// components are rounded exactly as two scalar adds.
+template <class Ld, class = void> struct PairAdd { static constexpr bool value = false; };
+template <class Ld> struct PairAdd<Ld, std::void_t<decltype(Ld::kPairAdd)>> {
+  static constexpr bool value = Ld::kPairAdd;
+};
+
 template <class Ld> struct Fold {
   using Acc = typename Ld::Acc;
   using Raw = typename Ld::Raw;
   static constexpr int V = Ld::V;
 
   __device__ __forceinline__ static void comb_into(Acc (&a)[V], const Acc (&b)[V]) {
+    if constexpr (PairAdd<Ld>::value && V % 2 == 0) {
 #pragma unroll
-    for (int k = 0; k < V; ++k) a[k] = Ld::comb(a[k], b[k]);
+      for (int k = 0; k < V; k += 2) {
+        const float2 p = __fadd2_rn(make_float2(a[k], a[k + 1]), make_float2(b[k], b[k + 1]));
+        a[k] = p.x;
+        a[k + 1] = p.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < V; ++k) a[k] = Ld::comb(a[k], b[k]);
+    }
   }
 
   // ring order starting at rank s (0 <= s < N): acc = x_s (+) x_{s+1} (+) ...

@@ -145,6 +145,7 @@ cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cuda
 
 template <int VV> struct Fp8Ld {
   static constexpr int V = VV;
+  static constexpr bool kPairAdd = true;  // comb is a binary32 add: pairs may use the packed add
   using Acc = float;
   struct Raw {
     uint32_t q[(V + 3) / 4];
@@ -169,8 +170,7 @@ template <int VV> struct Fp8Ld {
     return w;
   }
   __device__ __forceinline__ void unpack(const Raw& w, Acc (&a)[V]) const {
-#pragma unroll
-    for (int k = 0; k < V; ++k) a[k] = __fmul_rn(e4m3_to_f32((w.q[k >> 2] >> ((k & 3) * 8)) & 0xFFu), w.s);
+    dequantise_lane<V>(w.q, w.s, a);
   }
   __device__ __forceinline__ static Acc comb(Acc a, Acc b) { return __fadd_rn(a, b); }
 };

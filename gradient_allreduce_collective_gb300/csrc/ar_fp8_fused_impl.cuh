@@ -35,6 +35,7 @@ template <int IDT> struct Fp8FusedLd {
   static constexpr int B = Fmt<IDT>::bytes;
   static constexpr int V = 16 / B;
   static constexpr int G = kFp8Block / V;
+  static constexpr bool kPairAdd = true;  // comb is a binary32 add: pairs may use the packed add
   using Acc = float;
   using Raw = uint4;
 
@@ -59,8 +60,7 @@ template <int IDT> struct Fp8FusedLd {
     const float s = __fdiv_rn(amax, 448.0f);
     uint32_t word[V / 4];
     quantise_lane<V>(x, amax, s, word);
-#pragma unroll
-    for (int k = 0; k < V; ++k) d[k] = __fmul_rn(e4m3_to_f32((word[k >> 2] >> ((k & 3) * 8)) & 0xFFu), s);
+    dequantise_lane<V>(word, s, d);
   }
   __device__ __forceinline__ static Acc comb(Acc a, Acc b) { return __fadd_rn(a, b); }
 };
@@ -135,8 +135,10 @@ __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_consta
       const float s = __fdiv_rn(amax, 448.0f);
       uint32_t word[1];
       quantise_lane<4>(x, amax, s, word);
+      float t[4];
+      dequantise_lane<4>(word, s, t);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) d[r][k] = __fmul_rn(e4m3_to_f32((word[0] >> (k * 8)) & 0xFFu), s);
+      for (int k = 0; k < 4; ++k) d[r][k] = t[k];
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {

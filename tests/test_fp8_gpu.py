@@ -89,6 +89,54 @@ def test_quantize_rounding_boundaries():
     assert bad.size == 0, (bad[:10], got[bad[:10]], wq[bad[:10]], x[bad[:10]])
 
 
+def _every_bf16_blocks():
+    pats = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    f = oracle.bf16_to_f32(pats)
+    fin = np.isfinite(f) & (f >= 0)
+    pos = pats[fin]
+    posf = f[fin]
+    rng = np.random.default_rng(17)
+    amaxes = [1.0, 448.0, 3.0, 0.0078125, 1e-3, 65504.0, 1e30, 3e38, 1e-24, 1e-26, 1e-30, 2.0**-120,
+              2.0**-133, 5e29, 3.7e-25]
+    amaxes += list(oracle.bf16_to_f32(rng.choice(pos[posf > 0], 25)).astype(float))
+    blocks = []
+    for amax in amaxes:
+        a = synthgen.to_dtype(np.array([amax], dtype=np.float32), "bf16")[0]
+        af = oracle.bf16_to_f32(np.array([a]))[0]
+        vals = pos[posf <= af]
+        vals = np.concatenate([vals, vals | np.uint16(0x8000)])
+        for i in range(0, len(vals), 127):
+            part = vals[i:i + 127]
+            blk = np.full(128, a, dtype=np.uint16)
+            blk[1:1 + len(part)] = part
+            blocks.append(blk)
+    return np.concatenate(blocks)
+
+
+def test_quantize_every_bf16_value():
+    # every finite bf16 x with |x| <= amax, for ~40 block maxima spanning the
+    # reciprocal path and the division fallback (s < 2^-90, s > 2^90)
+    x = _every_bf16_blocks()
+    q = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(x.size // 128, dtype=torch.float32, device="cuda")
+    gar.ar_quantize_fp8_blocks(to_dev(x, "bf16"), q, sc)
+    wq, ws = oracle.fp8_quantize(x, "bf16")
+    assert _same_bits(from_dev(sc), ws)
+    got = from_dev(q)
+    bad = np.nonzero(got != wq)[0]
+    assert bad.size == 0, (bad[:8], got[bad[:8]], wq[bad[:8]], oracle.bf16_to_f32(x[bad[:8]]))
+    # the same values through both allreduce paths (one rank: the dequantised values, rounded to bf16)
+    want = oracle.fp8_ring_allreduce([x], "bf16", "bf16", "sum")[0]
+    xin = [to_dev(x, "bf16")]
+    for fn in ("materialised", "fused"):
+        out = [torch.empty(x.size, dtype=torch.bfloat16, device="cuda")]
+        if fn == "fused":
+            gar.ar_allreduce_fp8_fused(xin, out, "sum", "fused")
+        else:
+            gar.ar_allreduce_fp8(xin, out, _ws(1, x.size), "sum", "fused")
+        assert _same_bits(from_dev(out[0]), want), fn
+
+
 def test_fp8_block_example():
     g = G.load("fp8_block_example.txt")
     send = [to_dev(synthgen.to_dtype(np.array(G.nums(g[f"rank{r}"]), dtype=np.float32), "bf16"), "bf16")
