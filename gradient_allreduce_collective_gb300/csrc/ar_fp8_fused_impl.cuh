@@ -66,7 +66,7 @@ template <int IDT> struct Fp8FusedLd {
 };
 
 template <int IDT, int ODT, int OP, int MODE, int MAXN>
-__global__ void __launch_bounds__(kThreads) k_fp8_fused_vec(const __grid_constant__ Fp8FusedArgs A) {
+__global__ void __launch_bounds__(kThreads, MODE == MODE_FUSED_TREE ? 1 : 4) k_fp8_fused_vec(const __grid_constant__ Fp8FusedArgs A) {
   using Ld = Fp8FusedLd<IDT>;
   constexpr int V = Ld::V, G = Ld::G, BPW = 32 / G, OB = Fmt<ODT>::bytes;
   const int N = A.nranks;
