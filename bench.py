@@ -305,7 +305,22 @@ def to_dev_bf16(a):
     return torch.from_numpy(a).view(torch.int16).view(torch.bfloat16).cuda()
 
 
-def measure_ddp(gar, steps: int, warmup: int) -> dict:
+def oracle_row_timing(fn, max_n: int, budget_s: float = 6.0) -> dict:
+    """Run `fn(n)` (the oracle on the first n elements of every rank, n <=
+    max_n) on a sample sized to fill about budget_s / 4 seconds; returns
+    seconds per element of one rank and the sample used."""
+    n = min(16_384, max_n)
+    while True:
+        t0 = time.perf_counter()
+        fn(n)
+        t = time.perf_counter() - t0
+        if t > budget_s / 4 or n >= max_n:
+            break
+        n = min(max_n, int(n * min(8.0, max(2.0, budget_s / 4 / max(t, 1e-6)))))
+    return {"seconds_per_element_per_rank": t / n, "sample_elements_per_rank": n, "seconds": t}
+
+
+def measure_ddp(gar, steps: int, warmup: int, with_oracle: bool = False) -> dict:
     """GPT-2-small DDP gradient sync on 8 ranks, two ways: (a) per bucket one
     flatten call for all ranks, one in-place fused allreduce (avg), one
     unflatten call; (b) per bucket one ar_bucket_allreduce straight from the
@@ -423,6 +438,17 @@ def measure_ddp(gar, steps: int, warmup: int) -> dict:
                      "frac_hbm": moved / (best * 1e-3) / 1e9 / peak}
     out["three_step"]["what"] = "per bucket: flatten (all ranks) -> fused allreduce in place -> unflatten"
     out["direct"]["what"] = "per bucket: ar_bucket_allreduce from the tensors (no bucket copies)"
+    if with_oracle:
+        import oracle
+        samp = synthgen.ranks_normal(n, 1 << 22, 1e-4, base_seed=0, dtype="bf16")
+        o = oracle_row_timing(lambda k: oracle.ring_allreduce([a[:k] for a in samp], "bf16", "avg"), samp[0].size)
+        t_all = o["seconds_per_element_per_rank"] * total
+        out["cpu_oracle"] = {"kind": "oracle", "cores": 1,
+                             "sample": f"ring allreduce (bf16, avg, 8 ranks) of the first "
+                                       f"{o['sample_elements_per_rank']:,} values of a bucket, "
+                                       f"{o['seconds']:.2f} s; scaled to all {total:,} values",
+                             "ms_per_step_estimate": t_all * 1e3,
+                             "busbw_gbs": busbw_gbs(grad_bytes, t_all, n)}
     out["overlap"] = {"backward_ms": t_comp, "sync_ms": t_comm, "both_ms": t_both,
                       "hidden_fraction_of_sync": max(0.0, (t_comp + t_comm - t_both) / t_comm),
                       "what": "8 bf16 4096^3 GEMMs (torch.matmul) on a compute stream while the direct "
@@ -430,7 +456,7 @@ def measure_ddp(gar, steps: int, warmup: int) -> dict:
     return out
 
 
-def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728) -> dict:
+def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728, with_oracle: bool = False) -> dict:
     """16 ranks x `count` bf16 with 0.1% outliers x100: quantise to E4M3
     blocks (workspace) then dequantise + fused ring-order reduce (sum) + 16
     bf16 replicas."""
@@ -463,7 +489,21 @@ def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728) -> dict:
     peak, _ = hbm_peak()
     del send, recv, ws
     torch.cuda.empty_cache()
+    cpu = None
+    if with_oracle:
+        import oracle
+        samp = synthgen.ranks_normal(n, 1 << 20, 1e-3, base_seed=0, dtype="bf16", outlier_p=1e-3,
+                                     outlier_scale=100.0)
+        o = oracle_row_timing(lambda k: oracle.fp8_ring_allreduce([a[:k] for a in samp], "bf16", "bf16", "sum"),
+                              samp[0].size)
+        t_all = o["seconds_per_element_per_rank"] * count
+        cpu = {"kind": "oracle", "cores": 1,
+               "sample": f"FP8 ring allreduce (16 ranks, bf16 in/out, sum) of the first "
+                         f"{o['sample_elements_per_rank']:,} values per rank, {o['seconds']:.2f} s; "
+                         f"scaled to {count:,}",
+               "ms_per_step_estimate": t_all * 1e3, "busbw_gbs": busbw_gbs(count * 2, t_all, n)}
     return {
+        "cpu_oracle": cpu,
         "workload": f"FP8-compressed allreduce: 16 ranks x {count:,} bf16, N(0,1e-3), 0.1% outliers "
                     "x100, E4M3 per-128 block scales, binary32 accumulation, sum, bf16 out, fused",
         "materialised": {"what": "quantise every rank into the workspace (the wire format), then dequantise + "
@@ -578,8 +618,11 @@ def run_ours(args):
     rows = {}
     if not args.headline_only:
         del d_in, d_out
-        rows["ddp_bucket_sync"] = measure_ddp(gar, steps=max(5, min(args.steps, 50)), warmup=3)
-        rows["fp8_allreduce"] = measure_fp8(gar, steps=max(5, min(args.steps, 20)), warmup=3)
+        timed_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+        rows["ddp_bucket_sync"] = measure_ddp(gar, steps=max(5, min(args.steps, 50)), warmup=3,
+                                              with_oracle=timed_cpu)
+        rows["fp8_allreduce"] = measure_fp8(gar, steps=max(5, min(args.steps, 20)), warmup=3,
+                                            with_oracle=timed_cpu)
 
     peak, peak_src = hbm_peak()
     alg_bytes = 2 * NRANKS * M

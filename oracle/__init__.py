@@ -71,6 +71,8 @@ def _load():
     lib.or_fp8_ring_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
     lib.or_fp8_tree_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
     lib.or_fp8_ring_blocks.argtypes = [vp, vp, vp, sz, sz, ci, ci, ci, ci, vp]
+    lib.or_fp8_hop_ring_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
+    lib.or_fp8_hop_blocks_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
     lib.or_bucket_plan.argtypes = [vp, ci, ci, ctypes.c_uint64, vp, vp, vp, vp]
     lib.or_chunk_len.argtypes = [sz, ci, sz]
     lib.or_chunk_len.restype = sz
@@ -199,6 +201,24 @@ def fp8_tree_allreduce(send, in_dtype: str, out_dtype: str, op: str):
     _check(_load().or_fp8_tree_allreduce(_ptrs(send), _ptrs(recv), len(send), send[0].size, DTYPES[in_dtype],
                                          DTYPES[out_dtype], OPS[op]), "fp8_tree_allreduce")
     return recv
+
+
+def _fp8_hop(fn: str, send, in_dtype: str, out_dtype: str, op: str):
+    send = _contig(send, in_dtype)
+    recv = [np.empty(send[0].size, dtype=NP_STORAGE[out_dtype]) for _ in send]
+    _check(getattr(_load(), fn)(_ptrs(send), _ptrs(recv), len(send), send[0].size, DTYPES[in_dtype],
+                                DTYPES[out_dtype], OPS[op]), fn)
+    return recv
+
+
+def fp8_hop_ring_allreduce(send, in_dtype: str, out_dtype: str, op: str):
+    """FP8 on every ring hop: literal ring simulation with quantised wire buffers."""
+    return _fp8_hop("or_fp8_hop_ring_allreduce", send, in_dtype, out_dtype, op)
+
+
+def fp8_hop_blocks_allreduce(send, in_dtype: str, out_dtype: str, op: str):
+    """The same computation written per block (cross-check)."""
+    return _fp8_hop("or_fp8_hop_blocks_allreduce", send, in_dtype, out_dtype, op)
 
 
 def fp8_ring_blocks(blocks: np.ndarray, first: np.ndarray, blen: np.ndarray, count: int, in_dtype: str,

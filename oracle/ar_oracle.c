@@ -643,6 +643,124 @@ int or_fp8_ring_blocks(const void *blocks, const int64_t *first, const int32_t *
 }
 
 /* ------------------------------------------------------------------------- */
+/* FP8 on every ring hop (reading fp8-hop). A compressed ring sends each      */
+/* partial sum in FP8 ([GL] §NCCLにおけるAllReduce: FP8 AllReduce halves the  */
+/* traffic; [VL] §data typeと圧縮: partial results reduced at low precision   */
+/* change the numerical error). At reduce-scatter step s the sender          */
+/* quantises its partial of the chunk it sends in blocks of 128 elements     */
+/* counted from the chunk's start (s = amax/448, E4M3 nearest-even with      */
+/* saturation, amax = 0 -> 0) and the receiver adds the dequantised values   */
+/* float(q)*s to its own value in binary32 (received first). The owner       */
+/* finishes the chunk (AVG divides by N), quantises it the same way once     */
+/* more for the all-gather, and every rank, the owner included, keeps the    */
+/* dequantised chunk rounded to the output type, so replicas are identical.  */
+/* Parity unpinned as far as the pages go (they fix no block rule); pinned   */
+/* by a hand-computed example, N = 1 against the quantise-once path, a       */
+/* second formulation and error bounds.                                      */
+/* ------------------------------------------------------------------------- */
+
+/* quantise-dequantise in place, blocks of 128 from v[0] */
+static void or_qdq_run(float *v, size_t n)
+{
+    for (size_t lo = 0; lo < n; lo += OR_FP8_BLOCK) {
+        size_t hi = lo + OR_FP8_BLOCK < n ? lo + OR_FP8_BLOCK : n;
+        float amax = 0.0f;
+        for (size_t i = lo; i < hi; ++i) {
+            float a = fabsf(v[i]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / 448.0f;
+        for (size_t i = lo; i < hi; ++i)
+            v[i] = (amax == 0.0f) ? 0.0f : or_fp8_deq(or_f32_to_e4m3(v[i] / s), s);
+    }
+}
+
+int or_fp8_hop_ring_allreduce(const void *const *send, void *const *recv, int N, size_t count,
+                              int in_dt, int out_dt, int op)
+{
+    if (or_fp8_check(N, in_dt, out_dt, op)) return OR_EINVAL;
+    size_t es = or_esize(out_dt), L = or_chunk_len(count, N, 16 / es);
+    or_val **st = or_alloc_state(N, count);
+    float **sb = (float **)calloc((size_t)N, sizeof(float *));
+    int rc = (st && sb) ? OR_OK : OR_ENOMEM;
+    for (int r = 0; rc == OR_OK && r < N; ++r)
+        if (!(sb[r] = (float *)malloc((L ? L : 1) * sizeof(float)))) rc = OR_ENOMEM;
+    if (rc == OR_OK) {
+        for (int r = 0; r < N; ++r)
+            for (size_t i = 0; i < count; ++i) st[r][i] = or_load(in_dt, send[r], i);
+        for (int s = 0; s < N - 1; ++s) {
+            for (int r = 0; r < N; ++r) {                  /* every sender puts its FP8 partial on the wire */
+                size_t lo, hi;
+                or_chunk(count, L, or_mod(r - s - 1, N), &lo, &hi);
+                for (size_t i = lo; i < hi; ++i) sb[r][i - lo] = st[r][i].f;
+                or_qdq_run(sb[r], hi - lo);
+            }
+            for (int r = 0; r < N; ++r) {                  /* receivers add their own value */
+                int dst = (r + 1) % N;
+                size_t lo, hi;
+                or_chunk(count, L, or_mod(r - s - 1, N), &lo, &hi);
+                for (size_t i = lo; i < hi; ++i) st[dst][i].f = sb[r][i - lo] + st[dst][i].f;
+            }
+        }
+        for (int c = 0; c < N; ++c) {                      /* owner finishes, quantises for the all-gather */
+            size_t lo, hi;
+            or_chunk(count, L, c, &lo, &hi);
+            for (size_t i = lo; i < hi; ++i) sb[0][i - lo] = or_finish(OR_F32, op, st[c][i], N).f;
+            or_qdq_run(sb[0], hi - lo);
+            for (size_t i = lo; i < hi; ++i) {
+                or_val v;
+                v.f = sb[0][i - lo];
+                or_store(out_dt, recv[c], i, v);
+            }
+        }
+        rc = or_ring_ag_phase((unsigned char **)recv, N, count, L, es);
+    }
+    if (sb)
+        for (int r = 0; r < N; ++r) free(sb[r]);
+    free(sb);
+    or_free_state(st, N);
+    return rc;
+}
+
+/* The same computation written per block: for every chunk c and each of its
+   128-element blocks, fold the ranks from c+1 onwards, re-quantising the
+   running partial before each addition. */
+int or_fp8_hop_blocks_allreduce(const void *const *send, void *const *recv, int N, size_t count,
+                                int in_dt, int out_dt, int op)
+{
+    if (or_fp8_check(N, in_dt, out_dt, op)) return OR_EINVAL;
+    size_t L = or_chunk_len(count, N, 16 / or_esize(out_dt));
+    float p[OR_FP8_BLOCK];
+    for (int c = 0; c < N; ++c) {
+        size_t clo, chi;
+        or_chunk(count, L, c, &clo, &chi);
+        for (size_t lo = clo; lo < chi; lo += OR_FP8_BLOCK) {
+            size_t n = chi - lo < OR_FP8_BLOCK ? chi - lo : OR_FP8_BLOCK;
+            int r = (c + 1) % N;
+            for (size_t k = 0; k < n; ++k) p[k] = or_load(in_dt, send[r], lo + k).f;
+            for (int j = 1; j < N; ++j) {
+                r = (r + 1) % N;
+                or_qdq_run(p, n);
+                for (size_t k = 0; k < n; ++k) p[k] = p[k] + or_load(in_dt, send[r], lo + k).f;
+            }
+            for (size_t k = 0; k < n; ++k) {
+                or_val v;
+                v.f = p[k];
+                p[k] = or_finish(OR_F32, op, v, N).f;
+            }
+            or_qdq_run(p, n);
+            for (int q = 0; q < N; ++q)
+                for (size_t k = 0; k < n; ++k) {
+                    or_val v;
+                    v.f = p[k];
+                    or_store(out_dt, recv[q], lo + k, v);
+                }
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Gradient bucketing ([GL] §パフォーマンスチューニング: DDP packs many small   */
 /* tensors into one bucket per allreduce, 25 MB by default; [AW] §计算-通信重叠: */
 /* gradients become ready from the output layer backwards). Reading bucket:   */

@@ -338,3 +338,56 @@ def test_empty_inputs():
         assert all(y.size == 0 for y in oracle.ring_allreduce(send, dtype, "sum"))
         assert all(y.size == 0 for y in oracle.tree_allreduce(send, dtype, "sum"))
     assert oracle.bucket_plan([], 2, 1 << 20)[2].size == 0
+
+
+# ------------------------------------------------------------------ FP8 per hop
+
+def test_fp8_hop_example():
+    g = G.load("fp8_hop_example.txt")
+    send = [_as("bf16", G.nums(g[f"rank{r}"])) for r in range(2)]
+    for op in ("sum", "avg"):
+        for fn in (oracle.fp8_hop_ring_allreduce, oracle.fp8_hop_blocks_allreduce):
+            for y in fn(send, "bf16", "bf16", op):
+                assert oracle.bf16_to_f32(y).tolist() == G.nums(g[f"expect_{op}"])
+    once = oracle.fp8_ring_allreduce(send, "bf16", "bf16", "sum")[0]
+    assert oracle.bf16_to_f32(once).tolist() == G.nums(g["expect_once_sum"])
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 16])
+def test_fp8_hop_simulator_equals_block_fold(n):
+    for count in (1, 100, 128 * 9 + 7, 128 * 40):
+        send = synthgen.ranks_normal(n, count, 1e-3, base_seed=n * 7 + count, dtype="bf16", outlier_p=1e-2,
+                                     outlier_scale=100.0)
+        for op in ("sum", "avg"):
+            a = oracle.fp8_hop_ring_allreduce(send, "bf16", "bf16", op)
+            b = oracle.fp8_hop_blocks_allreduce(send, "bf16", "bf16", op)
+            for r in range(n):
+                assert np.array_equal(a[r], a[0]) and np.array_equal(b[r], a[0])
+
+
+def test_fp8_hop_single_rank_equals_quantise_once():
+    x = synthgen.ranks_normal(1, 128 * 50 + 3, 1e-3, base_seed=2, dtype="bf16", outlier_p=1e-2, outlier_scale=100.0)
+    for op in ("sum", "avg"):
+        assert np.array_equal(oracle.fp8_hop_ring_allreduce(x, "bf16", "bf16", op)[0],
+                              oracle.fp8_ring_allreduce(x, "bf16", "bf16", op)[0])
+
+
+def test_fp8_hop_error_bound_and_growth():
+    # each hop's E4M3 rounding is at most u = 2^-4 relative to the block's magnitude
+    # (u/(1+u) for normals) plus half a subnormal step s*2^-10; the bound below sums
+    # those over the N-1 hops and the final quantisation, then the bf16 output rounding
+    n, count = 16, 128 * 200
+    send = synthgen.ranks_normal(n, count, 1e-3, base_seed=0, dtype="bf16", outlier_p=1e-3, outlier_scale=100.0)
+    ystar, S = oracle.reference_f64(send, "bf16", "sum")
+    hop = oracle.bf16_to_f32(oracle.fp8_hop_ring_allreduce(send, "bf16", "bf16", "sum")[0]).astype(np.float64)
+    once = oracle.bf16_to_f32(oracle.fp8_ring_allreduce(send, "bf16", "bf16", "sum")[0]).astype(np.float64)
+    e_hop = np.linalg.norm(hop - ystar) / np.linalg.norm(ystar)
+    e_once = np.linalg.norm(once - ystar) / np.linalg.norm(ystar)
+    # per-element: |partial error| grows at most by 0.0589*|partial| + 2^-10 * blockmax/448 per hop
+    x = np.stack([oracle.bf16_to_f32(a).astype(np.float64) for a in send])
+    blockmax = np.abs(np.cumsum(x, axis=0)).reshape(n, -1, 128).max(axis=2).repeat(128, axis=1)
+    partial = np.abs(np.cumsum(x, axis=0))
+    per = (0.0589 * (partial + S) + blockmax / 448 * 2.0**-10 * 2).sum(axis=0)
+    assert np.all(np.abs(hop - ystar) <= per + 2.0**-8 * (np.abs(ystar) + per))
+    assert e_hop <= 6e-2 * 4 and e_once <= 6e-2
+    assert e_hop > e_once  # re-quantising partials on every hop loses more than quantising inputs once
