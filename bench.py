@@ -463,9 +463,11 @@ def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728, with_ora
     import torch
     import synthgen
 
+    import numpy as np
+
     n = 16
-    send = [to_dev_bf16(a) for a in synthgen.ranks_normal(n, count, 1e-3, base_seed=0, dtype="bf16",
-                                                          outlier_p=1e-3, outlier_scale=100.0)]
+    host = synthgen.ranks_normal(n, count, 1e-3, base_seed=0, dtype="bf16", outlier_p=1e-3, outlier_scale=100.0)
+    send = [to_dev_bf16(a) for a in host]
     recv = [torch.empty_like(s) for s in send]
     ws = torch.empty(gar.ar_fp8_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -483,6 +485,26 @@ def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728, with_ora
     for _ in range(warmup):
         step_fused()
     ms_fused = time_steps(step_fused, steps, stream)
+    # error against the fp64 sum on sampled elements, quantised once vs on every hop
+    idx = np.sort(np.random.default_rng(0).choice(count, min(count, 1 << 20), replace=False))
+    xs = np.stack([(a[idx].astype(np.uint32) << 16).view(np.float32).astype(np.float64) for a in host])
+    ystar = xs.sum(axis=0)
+    idx_t = torch.from_numpy(idx).cuda()
+
+    def sampled_error(out):
+        y = out[0].float()[idx_t].double().cpu().numpy()
+        return float(np.linalg.norm(y - ystar) / np.linalg.norm(ystar))
+
+    err_once = sampled_error(recv)
+
+    def step_hops():
+        gar.ar_allreduce_fp8_hops(send, recv, "sum", stream)
+
+    for _ in range(warmup):
+        step_hops()
+    ms_hops = time_steps(step_hops, max(3, steps // 2), stream)
+    torch.cuda.synchronize()
+    err_hops = sampled_error(recv)
     M = count * 2
     wire = count + 4 * (count // 128)  # E4M3 codes + block scales per rank
     moved = n * M + n * wire + n * wire + n * M
@@ -516,7 +538,15 @@ def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728, with_ora
                                "ms_per_step": ms_fused, "busbw_gbs": busbw_gbs(M, ms_fused * 1e-3, n),
                                "hbm_gbs": 2 * n * M / (ms_fused * 1e-3) / 1e9,
                                "frac_hbm": 2 * n * M / (ms_fused * 1e-3) / 1e9 / peak,
-                               "algorithmic_bytes_per_step": 2 * n * M, "launches_per_step": 1},
+                               "algorithmic_bytes_per_step": 2 * n * M, "launches_per_step": 1,
+                               "normwise_error_vs_fp64": err_once},
+        "per_hop": {"what": "ar_allreduce_fp8_hops: the running partial re-quantised to FP8 on each of the 15 "
+                            "ring hops, the finished chunk once more for the all-gather",
+                    "ms_per_step": ms_hops, "busbw_gbs": busbw_gbs(M, ms_hops * 1e-3, n),
+                    "hbm_gbs": 2 * n * M / (ms_hops * 1e-3) / 1e9,
+                    "frac_hbm": 2 * n * M / (ms_hops * 1e-3) / 1e9 / peak,
+                    "algorithmic_bytes_per_step": 2 * n * M, "launches_per_step": 1,
+                    "normwise_error_vs_fp64": err_hops},
     }
 
 

@@ -19,7 +19,7 @@ from ._build import build, lib_path
 __all__ = [
     "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_reduce_scatter", "ar_all_gather",
     "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
-    "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_noalloc",
+    "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops", "ar_allreduce_fp8_noalloc",
     "ar_status_string", "ar_last_error", "ar_version",
     "DTYPES", "OPS", "ALGOS",
 ]
@@ -67,8 +67,9 @@ def lib() -> ctypes.CDLL:
     L.ar_allreduce_fp8.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp, sz, vp]
     L.ar_allreduce_fp8_noalloc.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_fused.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
+    L.ar_allreduce_fp8_hops.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
     for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
-                 "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused"):
+                 "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops"):
         getattr(L, name).restype = ci
     L.ar_status_string.argtypes = [ci]
     L.ar_status_string.restype = ctypes.c_char_p
@@ -222,6 +223,15 @@ def ar_allreduce_fp8_fused(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[
     odt, _ = _same(recvbufs, "recvbufs")
     _check(lib().ar_allreduce_fp8_fused(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], DTYPES[odt],
                                         OPS[op], ALGOS[algo], _stream(stream)))
+
+
+def ar_allreduce_fp8_hops(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], op: str = "sum",
+                          stream=None) -> None:
+    """FP8 re-quantised on every ring hop (see include/ar.h)."""
+    dt, n = _same(sendbufs, "sendbufs")
+    odt, _ = _same(recvbufs, "recvbufs")
+    _check(lib().ar_allreduce_fp8_hops(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], DTYPES[odt],
+                                       OPS[op], _stream(stream)))
 
 
 FP8_STATIC_WS_BYTES = 16 * 1024 * 1024

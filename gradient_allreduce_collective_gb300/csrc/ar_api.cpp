@@ -55,6 +55,20 @@ cudaError_t launch_fp8_fused(int in_dtype, int out_dtype, int op, int mode, bool
   }
 }
 
+// in ar_fp8_hop_<input type>.cu
+cudaError_t launch_fp8_hop_bf16(int out_dtype, int op, const Fp8HopArgs& a, cudaStream_t stream);
+cudaError_t launch_fp8_hop_f16(int out_dtype, int op, const Fp8HopArgs& a, cudaStream_t stream);
+cudaError_t launch_fp8_hop_f32(int out_dtype, int op, const Fp8HopArgs& a, cudaStream_t stream);
+
+cudaError_t launch_fp8_hop(int in_dtype, int out_dtype, int op, const Fp8HopArgs& a, cudaStream_t stream) {
+  switch (in_dtype) {
+    case DT_BF16: return launch_fp8_hop_bf16(out_dtype, op, a, stream);
+    case DT_F16: return launch_fp8_hop_f16(out_dtype, op, a, stream);
+    case DT_F32: return launch_fp8_hop_f32(out_dtype, op, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream) {
   switch (dtype) {
     case DT_F32: return launch_bucket_f32(op, mode, a, stream);
@@ -641,6 +655,39 @@ ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs,
   return e == cudaSuccess ? ok() : cuda_fail(e, "fp8 allreduce launch");
 }
 
+
+ar_status_t ar_allreduce_fp8_hops(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                                  ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_stream_t stream) {
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, in_dtype);
+  if (st != AR_SUCCESS) return st;
+  if (in_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating input type");
+  if (elem_size(out_dtype) == 0) return fail(AR_ERR_INVALID_ARGUMENT, "unknown out_dtype");
+  if (out_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating output type");
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (op != AR_SUM && op != AR_AVG) return fail(AR_ERR_UNSUPPORTED, "FP8 path supports SUM and AVG");
+  if (count == 0) return ok();
+  const size_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
+  if (count > SIZE_MAX / 8 / (size_t)nranks) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if ((st = check_ptrs(sendbufs, nranks, ies, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, oes, "recvbufs")) != AR_SUCCESS) return st;
+  std::vector<Span> spans;
+  for (int r = 0; r < nranks; ++r) {
+    spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + count * ies, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + count * oes, true, r});
+  }
+  if (!overlap_ok(spans, {}, {})) return fail(AR_ERR_ALIAS, "buffers overlap");
+  Fp8HopArgs a{};
+  a.nranks = nranks;
+  a.count = count;
+  a.L = chunk_len(count, nranks, 16 / oes);
+  a.nbc = (a.L + AR_FP8_BLOCK - 1) / AR_FP8_BLOCK;
+  for (int r = 0; r < nranks; ++r) {
+    a.src[r] = sendbufs[r];
+    a.dst[r] = recvbufs[r];
+  }
+  const cudaError_t e = launch_fp8_hop(in_dtype, out_dtype, op, a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "per-hop fp8 allreduce launch");
+}
 
 ar_status_t ar_allreduce_fp8_fused(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
                                    ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,

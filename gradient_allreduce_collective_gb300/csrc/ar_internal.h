@@ -123,6 +123,17 @@ struct Fp8FusedArgs {
   int nranks;
 };
 
+// FP8 re-quantised on every ring hop: one warp per 128-element block counted
+// from its chunk's start; nbc = blocks per full chunk.
+struct Fp8HopArgs {
+  const void* src[kMaxRanks];
+  void* dst[kMaxRanks];
+  uint64_t count;
+  uint64_t L;
+  uint64_t nbc;
+  int nranks;
+};
+
 // Launchers: enqueue on `stream`, return the launch status.
 cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream);
@@ -130,6 +141,7 @@ cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream);
+cudaError_t launch_fp8_hop(int in_dtype, int out_dtype, int op, const Fp8HopArgs& a, cudaStream_t stream);
 // vec: run the vector kernel over the full blocks; then the element-wise
 // kernel over the listed blocks and [first_block, nblocks) (if any).
 cudaError_t launch_fp8_fused(int in_dtype, int out_dtype, int op, int mode, bool vec, const Fp8FusedArgs& a,

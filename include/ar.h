@@ -224,6 +224,21 @@ ar_status_t ar_allreduce_fp8_fused(const void *const *sendbufs, void *const *rec
                                    ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
                                    ar_stream_t stream);
 
+/* FP8 re-quantised on every ring hop: what a ring that sends FP8 on the wire
+ * computes when partial sums travel compressed ([GL] §NCCLにおけるAllReduce;
+ * [VL] §data typeと圧縮: reducing partial results at low precision changes the
+ * numerical error). Chunk c starts at rank c+1; before each of the N-1
+ * reduce-scatter hops the running partial of every 128-element block (blocks
+ * counted from the chunk's start) is quantised to E4M3 (s = amax/448, nearest
+ * even, saturating) and dequantised, then the next rank's value is added in
+ * binary32; the finished chunk (AVG divides by N) is quantised once more for
+ * the all-gather and every rank stores the same dequantised values in
+ * out_dtype. Ring order only; SUM or AVG; any F32/F16/BF16 in and out types;
+ * element-aligned buffers. recvbufs must not overlap sendbufs or each other.
+ * Compare ar_allreduce_fp8, which quantises each rank's input once. */
+ar_status_t ar_allreduce_fp8_hops(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
+                                  ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_stream_t stream);
+
 /* Bytes of the FP8 workspace built into the library (16 MiB per device). */
 #define AR_FP8_STATIC_WS_BYTES (16u * 1024u * 1024u)
 

@@ -216,6 +216,34 @@ def test_fp8_fused_unaligned_and_unsupported():
     assert ei.value.status == gar.AR_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("in_dtype,out_dtype", [("bf16", "bf16"), ("bf16", "f32"), ("f16", "f16"), ("f32", "f32"),
+                                               ("f32", "bf16")])
+def test_fp8_hops_matches_oracle(in_dtype, out_dtype):
+    for n in (1, 2, 3, 5, 8, 16, 33):
+        for count in (1, 100, 128 * 9 + 7, 128 * 40, 128 * 300 + 72):
+            send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=5 * n + count, dtype=in_dtype,
+                                            outlier_p=1e-2, outlier_scale=100.0)
+            send = [to_dev(a, in_dtype) for a in send_np]
+            for op in ("sum", "avg"):
+                want = oracle.fp8_hop_ring_allreduce(send_np, in_dtype, out_dtype, op)[0]
+                out = Guarded(n, count, out_dtype, ESIZE[out_dtype] if n == 3 else 0)
+                gar.ar_allreduce_fp8_hops(send, out.views, op)
+                out.check()
+                for v in out.views:
+                    assert _same_bits(from_dev(v), want), (n, count, op)
+
+
+def test_fp8_hops_example():
+    g = G.load("fp8_hop_example.txt")
+    send = [to_dev(synthgen.to_dtype(np.array(G.nums(g[f"rank{r}"]), dtype=np.float32), "bf16"), "bf16")
+            for r in range(2)]
+    for op in ("sum", "avg"):
+        recv = [torch.empty(4, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        gar.ar_allreduce_fp8_hops(send, recv, op)
+        for y in recv:
+            assert y.float().cpu().tolist() == G.nums(g[f"expect_{op}"])
+
+
 def test_fp8_unaligned_outputs():
     n, count = 4, 128 * 20 + 9
     send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=5, dtype="bf16")
