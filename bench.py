@@ -720,6 +720,7 @@ def run_sweep(args):
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     peak, _ = hbm_peak()
+    fits: dict[str, list] = {}
     size = 4096
     while size <= max_bytes:
         cnt = size // 4
@@ -745,22 +746,47 @@ def run_sweep(args):
             res[algo] = {"warm_us": warm * 1e3, "cold_us": cold * 1e3,
                          "busbw_gbs_cold": busbw_gbs(size, cold * 1e-3, n),
                          "hbm_frac_cold": 2 * n * size / (cold * 1e-3) / 1e9 / peak}
-        # small sizes are launch-bound: a CUDA graph of 100 fused calls
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            g.capture_begin()
-            for _ in range(100):
-                gar.ar_allreduce(s_v, r_v, "sum", "fused", side)
-            g.capture_end()
-        stream.wait_stream(side)
-        g.replay()
-        gms = time_steps(g.replay, 5, stream) / 100
+        # per-call time inside a CUDA graph (launch overhead of the host gone), every order
+        graph_us = {}
+        reps = 100 if size <= (1 << 22) else 10
+        for algo in ("fused", "tree", "ring", "step_ring", "step_tree"):
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                g.capture_begin()
+                for _ in range(reps):
+                    gar.ar_allreduce(s_v, r_v, "sum", algo, side)
+                g.capture_end()
+            stream.wait_stream(side)
+            g.replay()
+            graph_us[algo] = time_steps(g.replay, 3, stream) / reps * 1e3
+            del g
+        for algo, us in graph_us.items():
+            fits.setdefault(algo, []).append((size, us))
         print(json.dumps({"workload": "size sweep", "nranks": n, "bytes_per_rank": size, "dtype": "f32", "op": "sum",
-                          "in_l2": 2 * n * size <= l2, "fused_graph_us": gms * 1e3, **res}))
+                          "in_l2": 2 * n * size <= l2, "graph_us": graph_us, **res}))
         sys.stdout.flush()
         size *= 2
+    # alpha-beta model per order: t = alpha * launches + bytes / beta, least squares over the
+    # sizes whose traffic exceeds L2 (bandwidth) and all sizes (latency)
+    import numpy as np
+    launches = {"fused": 1, "tree": 1, "ring": 2, "step_ring": 2 * (n - 1), "step_tree": 2 * int(math.log2(n))}
+    traffic = {"fused": 2 * n, "tree": 2 * n, "ring": 2 * n + 1, "step_ring": 5 * (n - 1), "step_tree": 5 * (n - 1)}
+    model = {}
+    for algo, pts in fits.items():
+        a = np.array([[launches[algo], traffic[algo] * m / 1e3] for m, _ in pts])  # us, (bytes/1e3) -> us at GB/s
+        t = np.array([us for _, us in pts])
+        (alpha, inv_beta), *_ = np.linalg.lstsq(a, t, rcond=None)
+        model[algo] = {"alpha_us_per_launch": float(alpha), "beta_gbs": float(1.0 / inv_beta) if inv_beta > 0 else None,
+                       "launches_per_call": launches[algo], "bytes_per_call": f"{traffic[algo]} x M"}
+    best = {}
+    for m in [1 << k for k in range(12, 31)]:
+        pred = {al: v["alpha_us_per_launch"] * v["launches_per_call"] + traffic[al] * m / 1e3 / v["beta_gbs"]
+                for al, v in model.items() if v["beta_gbs"]}
+        best[m] = min(pred, key=pred.get)
+    print(json.dumps({"workload": "alpha-beta fit", "nranks": n, "model": model,
+                      "fastest_by_model": {str(k): v for k, v in best.items()}}))
     return 0
 
 

@@ -29,7 +29,7 @@ AR_SUCCESS, AR_ERR_INVALID_ARGUMENT, AR_ERR_UNSUPPORTED, AR_ERR_ALIAS, AR_ERR_CU
 DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3}
 DTYPE_NAMES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
 OPS = {"sum": 0, "avg": 1, "min": 2, "max": 3}
-ALGOS = {"ring": 0, "fused": 1, "tree": 2}
+ALGOS = {"ring": 0, "fused": 1, "tree": 2, "step_ring": 3, "step_tree": 4, "auto": 5}
 FP8_BLOCK = 128
 
 

@@ -111,6 +111,17 @@ size_t elem_size(int dt) {
 
 bool valid_op(int op) { return op >= AR_SUM && op <= AR_MAX; }
 bool valid_algo(int a) { return a >= AR_ALGO_RING && a <= AR_ALGO_TREE; }
+bool valid_any_algo(int a) { return a >= AR_ALGO_RING && a <= AR_ALGO_AUTO; }
+
+// The one-pass orders for entry points that have no stepwise form: AUTO is
+// the fused order; the stepwise values are refused.
+ar_status_t basic_algo(ar_algo_t* algo) {
+  if (*algo == AR_ALGO_AUTO) *algo = AR_ALGO_FUSED;
+  if (*algo == AR_ALGO_STEP_RING || *algo == AR_ALGO_STEP_TREE)
+    return fail(AR_ERR_UNSUPPORTED, "stepwise orders exist for ar_allreduce only");
+  if (!valid_algo(*algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  return AR_SUCCESS;
+}
 bool pow2(int n) { return n >= 1 && (n & (n - 1)) == 0; }
 uintptr_t addr(const void* p) { return reinterpret_cast<uintptr_t>(p); }
 bool aligned(const void* p, size_t a) { return (addr(p) % a) == 0; }
@@ -203,6 +214,121 @@ ar_status_t ring_gather(void* const* recv, int n, size_t count, size_t L, size_t
   return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "all-gather launch");
 }
 
+// All-gather steps of the stepwise executors: batched copies of N ranges.
+ar_status_t step_copies(const std::vector<CopyItem>& items, cudaStream_t s) {
+  MultiCopyArgs a{};
+  uint64_t tiles = 0;
+  for (const CopyItem& it : items) {
+    if (it.bytes == 0) continue;
+    a.item[a.nitems] = it;
+    a.tile_start[a.nitems] = (uint32_t)tiles;
+    tiles += (it.bytes + kCopyTile - 1) / kCopyTile;
+    a.nitems += 1;
+  }
+  a.tile_start[a.nitems] = (uint32_t)tiles;
+  const cudaError_t e = launch_multicopy(a, s);
+  return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "all-gather step launch");
+}
+
+struct StepTask {
+  const void* a;
+  const void* b;
+  void* dst;
+  uint64_t len;
+};
+
+ar_status_t step_combine(int dtype, int op, int nranks, bool finish, bool vec, const std::vector<StepTask>& tasks,
+                         cudaStream_t s) {
+  StepArgs a{};
+  a.nranks = nranks;
+  a.finish = finish ? 1 : 0;
+  a.vec = vec ? 1 : 0;
+  uint64_t tiles = 0;
+  for (const StepTask& t : tasks) {
+    if (t.len == 0) continue;
+    const int k = a.ntasks++;
+    a.a[k] = t.a;
+    a.b[k] = t.b;
+    a.dst[k] = t.dst;
+    a.len[k] = t.len;
+    a.tile_start[k] = (uint32_t)tiles;
+    const uint64_t items = vec ? (t.len + 3) / 4 : t.len;
+    tiles += (items + kThreads - 1) / kThreads;
+  }
+  a.tile_start[a.ntasks] = (uint32_t)tiles;
+  const cudaError_t e = launch_step_combine(dtype, op, a, s);
+  return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "reduce-scatter step launch");
+}
+
+const char* at(const void* p, uint64_t elems) { return static_cast<const char*>(p) + elems * 4; }
+char* at(void* p, uint64_t elems) { return static_cast<char*>(p) + elems * 4; }
+
+// Ring, literally: step s, rank r sends its partial of chunk (r-s-1) mod N to
+// r+1, which adds it to its own values of that chunk (the sender's partial is
+// its input at step 0); then N-1 forwarding steps. 4-byte elements.
+ar_status_t step_ring(const void* const* send, void* const* recv, int n, size_t count, int dtype, int op,
+                      bool vec, cudaStream_t s) {
+  const size_t L = chunk_len(count, n, 4);
+  auto lo_of = [&](int c) { return std::min((size_t)c * L, count); };
+  auto hi_of = [&](int c) { return std::min((size_t)(c + 1) * L, count); };
+  for (int st = 0; st < n - 1; ++st) {
+    std::vector<StepTask> tasks;
+    for (int r = 0; r < n; ++r) {
+      const int c = ((r - st - 1) % n + n) % n, d = (r + 1) % n;
+      const size_t lo = lo_of(c), hi = hi_of(c);
+      tasks.push_back({at(st == 0 ? send[r] : (const void*)recv[r], lo), at(send[d], lo), at(recv[d], lo), hi - lo});
+    }
+    if (ar_status_t e = step_combine(dtype, op, n, st == n - 2, vec, tasks, s); e != AR_SUCCESS) return e;
+  }
+  for (int st = 0; st < n - 1; ++st) {
+    std::vector<CopyItem> items;
+    for (int r = 0; r < n; ++r) {
+      const int c = ((r - st) % n + n) % n, d = (r + 1) % n;
+      const size_t lo = lo_of(c), hi = hi_of(c);
+      items.push_back({at(recv[r], lo), at(recv[d], lo), (hi - lo) * 4});
+    }
+    if (ar_status_t e = step_copies(items, s); e != AR_SUCCESS) return e;
+  }
+  return AR_SUCCESS;
+}
+
+// Recursive halving reduce-scatter then recursive doubling all-gather: at
+// distance d = N/2, N/4, ..., 1 partners r and r^d split their common segment
+// (first half rounded up to 16 bytes) and each combines the half it keeps.
+ar_status_t step_tree(const void* const* send, void* const* recv, int n, size_t count, int dtype, int op,
+                      bool vec, cudaStream_t s) {
+  int levels = 0;
+  while ((1 << levels) < n) ++levels;
+  std::vector<std::vector<std::pair<size_t, size_t>>> seg(levels + 1,
+                                                          std::vector<std::pair<size_t, size_t>>(n));
+  for (int r = 0; r < n; ++r) seg[0][r] = {0, count};
+  for (int i = 0; i < levels; ++i) {
+    const int d = n >> (i + 1);
+    std::vector<StepTask> tasks;
+    for (int r = 0; r < n; ++r) {
+      const size_t lo = seg[i][r].first, hi = seg[i][r].second;
+      const size_t half = ((hi - lo + 1) / 2 + 3) / 4 * 4;
+      const size_t mid = std::min(lo + half, hi);
+      seg[i + 1][r] = (r & d) ? std::make_pair(mid, hi) : std::make_pair(lo, mid);
+      const int p = r ^ d;
+      const size_t klo = seg[i + 1][r].first, khi = seg[i + 1][r].second;
+      tasks.push_back({at(i == 0 ? send[r] : (const void*)recv[r], klo), at(i == 0 ? send[p] : (const void*)recv[p], klo),
+                       at(recv[r], klo), khi - klo});
+    }
+    if (ar_status_t e = step_combine(dtype, op, n, i == levels - 1, vec, tasks, s); e != AR_SUCCESS) return e;
+  }
+  for (int i = levels - 1; i >= 0; --i) {
+    const int d = n >> (i + 1);
+    std::vector<CopyItem> items;
+    for (int r = 0; r < n; ++r) {
+      const size_t lo = seg[i + 1][r].first, hi = seg[i + 1][r].second;
+      items.push_back({at(recv[r], lo), at(recv[r ^ d], lo), (hi - lo) * 4});
+    }
+    if (ar_status_t e = step_copies(items, s); e != AR_SUCCESS) return e;
+  }
+  return AR_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,11 +355,15 @@ ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
   if (st != AR_SUCCESS) return st;
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
-  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
-  if (algo == AR_ALGO_TREE && !pow2(nranks))
+  if (!valid_any_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if (algo == AR_ALGO_AUTO) algo = AR_ALGO_FUSED;  // fastest one-pass order at every size on one device
+  if ((algo == AR_ALGO_TREE || algo == AR_ALGO_STEP_TREE) && !pow2(nranks))
     return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
-  if (count == 0) return ok();
   const size_t es = elem_size(dtype);
+  const bool stepwise = algo == AR_ALGO_STEP_RING || algo == AR_ALGO_STEP_TREE;
+  if (stepwise && es != 4)
+    return fail(AR_ERR_UNSUPPORTED, "stepwise orders keep partials in the element type: F32 or I32 only");
+  if (count == 0) return ok();
   if (count > SIZE_MAX / es / 2) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
   if ((st = check_ptrs(sendbufs, nranks, es, "sendbufs")) != AR_SUCCESS) return st;
   if ((st = check_ptrs(recvbufs, nranks, es, "recvbufs")) != AR_SUCCESS) return st;
@@ -258,6 +388,11 @@ ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int
   a.vec = vec ? 1 : 0;
   for (int r = 0; r < nranks; ++r) a.src[r] = sendbufs[r];
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (stepwise && nranks > 1) {
+    st = algo == AR_ALGO_STEP_RING ? step_ring(sendbufs, recvbufs, nranks, count, dtype, op, vec, s)
+                                   : step_tree(sendbufs, recvbufs, nranks, count, dtype, op, vec, s);
+    return st == AR_SUCCESS ? ok() : st;
+  }
   if (algo == AR_ALGO_RING) {
     for (int c = 0; c < nranks; ++c)
       a.dst[c] = static_cast<char*>(recvbufs[c]) + ((size_t)c * L < count ? (size_t)c * L * es : 0);
@@ -462,7 +597,7 @@ ar_status_t ar_bucket_allreduce(const void* const* tensors, void* const* out_ten
   ar_status_t st = common_checks(tensors, out_tensors, nranks, dtype);
   if (st != AR_SUCCESS) return st;
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
-  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if ((st = basic_algo(&algo)) != AR_SUCCESS) return st;
   if (algo == AR_ALGO_TREE && !pow2(nranks))
     return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
   if (ntensors < 0) return fail(AR_ERR_INVALID_ARGUMENT, "ntensors < 0");
@@ -595,7 +730,7 @@ ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs,
   if (out_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating output type");
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
   if (op != AR_SUM && op != AR_AVG) return fail(AR_ERR_UNSUPPORTED, "FP8 path supports SUM and AVG");
-  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if ((st = basic_algo(&algo)) != AR_SUCCESS) return st;
   if (algo == AR_ALGO_TREE && !pow2(nranks))
     return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
   if (count == 0) return ok();
@@ -701,7 +836,7 @@ ar_status_t ar_allreduce_fp8_fused(const void* const* sendbufs, void* const* rec
     return fail(AR_ERR_UNSUPPORTED, "fused FP8 path: 16-bit inputs need a 16-bit output type");
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
   if (op != AR_SUM && op != AR_AVG) return fail(AR_ERR_UNSUPPORTED, "FP8 path supports SUM and AVG");
-  if (!valid_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  if ((st = basic_algo(&algo)) != AR_SUCCESS) return st;
   if (algo == AR_ALGO_TREE && !pow2(nranks))
     return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
   if (count == 0) return ok();

@@ -134,10 +134,26 @@ struct Fp8HopArgs {
   int nranks;
 };
 
+// One step of a stepwise ring or recursive-halving reduce-scatter: for each
+// task t, dst[t][i] = a[t][i] (+) b[t][i] for i < len[t], finished (AVG
+// divide, canonical NaN) when `finish` is set. Tasks never overlap.
+struct StepArgs {
+  const void* a[kMaxRanks];
+  const void* b[kMaxRanks];
+  void* dst[kMaxRanks];
+  uint64_t len[kMaxRanks];
+  uint32_t tile_start[kMaxRanks + 1];  // tiles of kThreads items per task
+  int ntasks;
+  int nranks;  // divisor for AVG
+  int finish;
+  int vec;     // all pointers 16-byte aligned: items are 16-byte vectors
+};
+
 // Launchers: enqueue on `stream`, return the launch status.
 cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream);
+cudaError_t launch_step_combine(int dtype, int op, const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream);

@@ -86,8 +86,29 @@ typedef enum { AR_SUM = 0, AR_AVG = 1, AR_MIN = 2, AR_MAX = 3 } ar_op_t;
  * [c*L, min((c+1)*L, count)), L = ceil(count/N) rounded up to a multiple of
  * 16 bytes / element size (trailing chunks may be short or empty). Chunk c is
  * folded starting at rank c+1: x_{c+1}, x_{c+2}, ..., x_{c+N} (mod N), and
- * rank c ends holding it. */
-typedef enum { AR_ALGO_RING = 0, AR_ALGO_FUSED = 1, AR_ALGO_TREE = 2 } ar_algo_t;
+ * rank c ends holding it.
+ *   AR_ALGO_STEP_RING — the ring executed literally, one launch per step:
+ *                   N-1 reduce-scatter steps (every rank adds the partial it
+ *                   receives from rank r-1 to its own chunk) and N-1 all-gather
+ *                   steps (every rank forwards a finished chunk to r+1).
+ *                   Same bits as RING; moves 5(N-1)*M bytes in 2(N-1) launches.
+ *   AR_ALGO_STEP_TREE — recursive halving reduce-scatter (partners at
+ *                   distance N/2, N/4, ..., 1 exchange halves of their
+ *                   segment) then recursive doubling all-gather ([AW] table,
+ *                   Rabenseifner). Same bits as TREE; 5(N-1)*M bytes in
+ *                   2*log2(N) launches.
+ *   The stepwise orders keep partial sums in the output buffers, so they
+ *   take 4-byte element types (F32, I32) only; AR_ERR_UNSUPPORTED otherwise.
+ *   AR_ALGO_AUTO      — chosen by the library: the one-pass FUSED kernel, which
+ *                   measured fastest at every message size on one device. */
+typedef enum {
+    AR_ALGO_RING = 0,
+    AR_ALGO_FUSED = 1,
+    AR_ALGO_TREE = 2,
+    AR_ALGO_STEP_RING = 3,
+    AR_ALGO_STEP_TREE = 4,
+    AR_ALGO_AUTO = 5
+} ar_algo_t;
 
 #define AR_MAX_RANKS 64
 #define AR_FP8_BLOCK 128

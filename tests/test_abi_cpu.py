@@ -64,7 +64,11 @@ def test_allreduce_argument_errors(L):
     assert L.ar_allreduce(_arr(s * 9), _arr(d * 9), 65, 16, 0, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
     assert _ar(L, s, d, 8, 16, dt=7) == gar.AR_ERR_INVALID_ARGUMENT
     assert _ar(L, s, d, 8, 16, op=9) == gar.AR_ERR_INVALID_ARGUMENT
-    assert _ar(L, s, d, 8, 16, algo=5) == gar.AR_ERR_INVALID_ARGUMENT
+    assert _ar(L, s, d, 8, 16, algo=9) == gar.AR_ERR_INVALID_ARGUMENT
+    # stepwise orders keep partials in the element type: 4-byte types only; tree needs 2^k ranks
+    assert _ar(L, s, d, 8, 16, dt=2, algo=3) == gar.AR_ERR_UNSUPPORTED
+    assert _ar(L, s[:3], d[:3], 3, 16, algo=4) == gar.AR_ERR_UNSUPPORTED
+    assert _ar(L, s[:3], d[:3], 3, 0, algo=5) == gar.AR_SUCCESS
     assert _ar(L, s[:3], d[:3], 3, 16, algo=2) == gar.AR_ERR_UNSUPPORTED
     assert "power of two" in gar.ar_last_error()
     assert _ar(L, s[:3], d[:3], 3, 0, algo=1) == gar.AR_SUCCESS  # count 0: no-op
@@ -119,6 +123,7 @@ def test_fp8_argument_errors(L):
     assert f(_arr(s), _arr(d), n, count, 2, 2, 0, 1, ws + 8, need, None) == gar.AR_ERR_INVALID_ARGUMENT
     assert f(_arr(s[:3]), _arr(d[:3]), 3, count, 2, 2, 0, 2, ws, need, None) == gar.AR_ERR_UNSUPPORTED
     assert f(_arr(s), _arr(d), n, count, 2, 2, 0, 1, d[1] + 64, need, None) == gar.AR_ERR_ALIAS
+    assert f(_arr(s), _arr(d), n, count, 2, 2, 0, 3, ws, need, None) == gar.AR_ERR_UNSUPPORTED  # stepwise
     assert gar.ar_fp8_workspace_bytes(0, 10) == 0
 
 

@@ -46,7 +46,7 @@ def _gpu_allreduce(send_np, dtype, op, algo, offset=0, in_offset=0):
 
 
 def _expect(send_np, dtype, op, algo):
-    if algo == "tree":
+    if algo in ("tree", "step_tree"):
         return oracle.tree_allreduce(send_np, dtype, op)[0]
     return oracle.ring_allreduce(send_np, dtype, op)[0]
 
@@ -55,8 +55,13 @@ def _same_bits(a, b):
     return np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
 
-def _algos(n):
-    return ("ring", "fused", "tree") if n & (n - 1) == 0 else ("ring", "fused")
+def _algos(n, dtype="f32"):
+    """Orders to check: the one-pass ones, AUTO, and (4-byte types) the stepwise executors."""
+    pow2 = n & (n - 1) == 0
+    algos = ["ring", "fused", "auto"] + (["tree"] if pow2 else [])
+    if dtype in ("f32", "i32"):
+        algos += ["step_ring"] + (["step_tree"] if pow2 else [])
+    return tuple(algos)
 
 
 def test_worked_example_every_algo():
@@ -102,7 +107,7 @@ def test_tiny_brute_force(dtype, op):
     for n in (1, 2, 3, 4, 5, 6, 7, 8, 16):
         for count in counts:
             send = _rand(dtype, n, count, seed=1000 * n + count)
-            for algo in _algos(n):
+            for algo in _algos(n, dtype):
                 want = _expect(send, dtype, op, algo)
                 for y in _gpu_allreduce(send, dtype, op, algo):
                     assert _same_bits(y, want), (n, count, algo)
@@ -113,7 +118,7 @@ def test_tiny_brute_force(dtype, op):
 def test_multi_tile_ragged(dtype, op):
     n, count = 8, 3 * (1 << 20) + 12345
     send = _rand(dtype, n, count, seed=7)
-    for algo in ("ring", "fused", "tree"):
+    for algo in _algos(n, dtype):
         want = _expect(send, dtype, op, algo)
         ys = _gpu_allreduce(send, dtype, op, algo)
         for y in ys:
@@ -125,7 +130,7 @@ def test_many_ranks(n):
     count = 50_003
     for dtype in ("f32", "bf16"):
         send = _rand(dtype, n, count, seed=n)
-        for algo in _algos(n):
+        for algo in _algos(n, dtype):
             want = _expect(send, dtype, "sum", algo)
             for y in _gpu_allreduce(send, dtype, "sum", algo):
                 assert _same_bits(y, want), (n, dtype, algo)
@@ -187,7 +192,7 @@ def test_in_place_forms():
     n, count = 8, 100_000
     for dtype in ("f32", "bf16", "i32"):
         send_np = _rand(dtype, n, count, seed=3)
-        for algo in ("ring", "fused", "tree"):
+        for algo in _algos(n, dtype):
             bufs = [to_dev(a, dtype) for a in send_np]
             gar.ar_allreduce(bufs, bufs, "sum", algo)
             want = _expect(send_np, dtype, "sum", algo)
@@ -211,7 +216,7 @@ def test_unaligned_buffers_take_the_element_path():
     for dtype in ("f32", "bf16", "f16", "i32"):
         send = _rand(dtype, n, count, seed=9)
         es = ESIZE[dtype]
-        for algo in _algos(n):
+        for algo in _algos(n, dtype):
             want = _expect(send, dtype, "avg", algo)
             for y in _gpu_allreduce(send, dtype, "avg", algo, offset=es, in_offset=3 * es):
                 assert _same_bits(y, want)
