@@ -588,6 +588,18 @@ def run_ours(args):
     clk = clocks.stop()
     ms_max = reduce_over_ranks(dist, ms, "max")
 
+    # per-call durations (the vasteelab metrics list: average, p95, p99 per call site)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
+    for a, b in evs:
+        a.record(stream)
+        step_fused()
+        b.record(stream)
+    torch.cuda.synchronize()
+    per_call = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    pct = {"p50": per_call[len(per_call) // 2], "p95": per_call[int(len(per_call) * 0.95)],
+           "p99": per_call[int(len(per_call) * 0.99)], "mean": sum(per_call) / len(per_call),
+           "what": "200 fused calls, each between its own CUDA events (includes event overhead)"}
+
     # the same bucket through the other two orders (not the headline)
     other = {}
     for algo in ("ring", "tree"):
@@ -689,6 +701,7 @@ def run_ours(args):
                 "pipelined": "copy-in and copy-out streams, two device buffer sets", "replicas_identical": ok},
         "gpu_launches": args.steps,
         "clocks": clk,
+        "per_call_us": pct,
         "other_orders_ms_per_step": {"ring_rs_plus_ag": other["ring"], "tree_recursive_halving": other["tree"]},
         "rows": rows,
         "cpu_baseline": cpu,

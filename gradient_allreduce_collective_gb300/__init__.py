@@ -21,7 +21,7 @@ __all__ = [
     "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
     "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops", "ar_allreduce_fp8_noalloc",
     "ar_status_string", "ar_last_error", "ar_version",
-    "DTYPES", "OPS", "ALGOS",
+    "DTYPES", "OPS", "ALGOS", "Comm", "CallRecord",
 ]
 
 AR_SUCCESS, AR_ERR_INVALID_ARGUMENT, AR_ERR_UNSUPPORTED, AR_ERR_ALIAS, AR_ERR_CUDA, AR_ERR_TIMEOUT, \
@@ -38,6 +38,14 @@ class ArError(RuntimeError):
         self.status = status
         self.detail = detail
         super().__init__(f"{_status_text(status)} ({status}): {detail}")
+
+
+class CallRecord(ctypes.Structure):
+    """ar_call_record_t: what a rank last did on a communicator."""
+    _fields_ = [("comm_id", ctypes.c_uint64), ("seq", ctypes.c_uint64), ("collective", ctypes.c_int),
+                ("count", ctypes.c_size_t), ("dtype", ctypes.c_int), ("op", ctypes.c_int), ("algo", ctypes.c_int),
+                ("status", ctypes.c_int), ("arrived_mask", ctypes.c_uint64), ("mismatch_mask", ctypes.c_uint64),
+                ("arrival_skew_ms", ctypes.c_double)]
 
 
 _lib = None
@@ -70,6 +78,12 @@ def lib() -> ctypes.CDLL:
     L.ar_allreduce_fp8_hops.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
     for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
                  "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops"):
+        getattr(L, name).restype = ci
+    L.ar_comm_create.argtypes = [ci, ci, ctypes.POINTER(ctypes.c_void_p)]
+    L.ar_comm_destroy.argtypes = [vp]
+    L.ar_comm_allreduce.argtypes = [vp, ci, vp, vp, sz, ci, ci, ci, vp]
+    L.ar_comm_last_record.argtypes = [vp, ci, ctypes.POINTER(CallRecord)]
+    for name in ("ar_comm_create", "ar_comm_destroy", "ar_comm_allreduce", "ar_comm_last_record"):
         getattr(L, name).restype = ci
     L.ar_status_string.argtypes = [ci]
     L.ar_status_string.restype = ctypes.c_char_p
@@ -246,3 +260,42 @@ def ar_allreduce_fp8_noalloc(sendbufs: Sequence[torch.Tensor], recvbufs: Sequenc
     odt, _ = _same(recvbufs, "recvbufs")
     _check(lib().ar_allreduce_fp8_noalloc(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt],
                                           DTYPES[odt], OPS[op], ALGOS[algo], _stream(stream)))
+
+
+class Comm:
+    """ar_comm_t: host-side communicator of `nranks` virtual ranks (one host thread per rank)."""
+
+    def __init__(self, nranks: int, timeout_ms: int):
+        h = ctypes.c_void_p()
+        _check(lib().ar_comm_create(nranks, timeout_ms, ctypes.byref(h)))
+        self.handle = h
+        self.nranks = nranks
+
+    def allreduce(self, rank: int, sendbuf, recvbuf, count: int | None = None, dtype=None, op: str = "sum",
+                  algo: str = "fused", stream=None) -> int:
+        """Rank `rank`'s half of an allreduce; returns the status (0 = success). Tensors or raw addresses."""
+        if count is None:
+            count = sendbuf.numel()
+        if dtype is None:
+            dtype = sendbuf.dtype
+        sp = sendbuf if isinstance(sendbuf, int) else sendbuf.data_ptr()
+        rp = recvbuf if isinstance(recvbuf, int) else recvbuf.data_ptr()
+        dt = DTYPES[dtype] if not isinstance(dtype, int) else dtype
+        st = stream if isinstance(stream, int) else (0 if stream is None else stream.cuda_stream)
+        return int(lib().ar_comm_allreduce(self.handle, rank, sp, rp, count, dt, OPS[op], ALGOS[algo], st))
+
+    def last_record(self, rank: int) -> CallRecord:
+        rec = CallRecord()
+        _check(lib().ar_comm_last_record(self.handle, rank, ctypes.byref(rec)))
+        return rec
+
+    def close(self) -> None:
+        if self.handle:
+            lib().ar_comm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -289,6 +289,45 @@ ar_status_t ar_allreduce_fp8_noalloc(const void *const *sendbufs, void *const *r
                                      ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
                                      ar_stream_t stream);
 
+/* Host-side communicator for virtual ranks driven by host threads
+ * ([VL] §rankとcommunicator: every rank calls the matching collective with the
+ * same count and type; §hangをtimeoutだけで再起動しない: hangs come from ranks
+ * that skip a call, differ in count or type, call in a different order, or
+ * failed earlier; record each rank's last collective, sequence number, shape,
+ * type, communicator id and earlier error). Each thread calls
+ * ar_comm_allreduce with its rank's buffers; the call blocks until every rank
+ * of the communicator has entered its call with the same sequence number,
+ * and the last arrival enqueues the one ar_allreduce on `stream`.
+ *   AR_ERR_MISMATCH — a rank's count, dtype, op, algo or stream differs from
+ *                     the first arrival's (also a different call order):
+ *                     nothing is launched, every rank of the call gets it.
+ *   AR_ERR_TIMEOUT  — not every rank arrived within timeout_ms: nothing is
+ *                     launched; waiting ranks return after the timeout.
+ * After either error the communicator is poisoned: every later call returns
+ * the same status at once (isolate the group and rebuild it). Waits are on
+ * the host only; no kernel waits on another rank. Thread-safe; one thread per
+ * rank at a time. */
+typedef struct ar_comm ar_comm_t;
+
+/* What a rank last did on a communicator. */
+typedef struct {
+    uint64_t comm_id;        /* process-unique communicator id */
+    uint64_t seq;            /* collectives this rank has entered (1-based) */
+    int collective;          /* 1 = allreduce */
+    size_t count;            /* elements */
+    int dtype, op, algo;     /* as passed */
+    int status;              /* outcome (ar_status_t) */
+    uint64_t arrived_mask;   /* ranks that had arrived for this call */
+    uint64_t mismatch_mask;  /* ranks whose arguments differed */
+    double arrival_skew_ms;  /* last arrival minus first arrival so far */
+} ar_call_record_t;
+
+ar_status_t ar_comm_create(int nranks, int timeout_ms, ar_comm_t **comm);
+ar_status_t ar_comm_destroy(ar_comm_t *comm);
+ar_status_t ar_comm_allreduce(ar_comm_t *comm, int rank, const void *sendbuf, void *recvbuf, size_t count,
+                              ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, ar_stream_t stream);
+ar_status_t ar_comm_last_record(ar_comm_t *comm, int rank, ar_call_record_t *out);
+
 /* Static text for a status code. */
 const char *ar_status_string(ar_status_t status);
 

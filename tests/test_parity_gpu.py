@@ -280,3 +280,31 @@ def test_cuda_graph_capture_and_side_stream():
     torch.cuda.synchronize()
     for r in recv:
         assert _same_bits(from_dev(r), want)
+
+
+def test_communicator_threads_launch_one_allreduce():
+    import threading
+    n, count = 8, 1 << 20
+    send_np = _rand("f32", n, count, seed=33)
+    send = [to_dev(a, "f32") for a in send_np]
+    recv = [torch.empty_like(x) for x in send]
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    comm = gar.Comm(n, 10_000)
+    st = [None] * n
+
+    def go(r):
+        st[r] = comm.allreduce(r, send[r], recv[r], op="avg", algo="fused", stream=stream)
+
+    ts = [threading.Thread(target=go, args=(r,)) for r in range(n)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join(timeout=60)
+    assert st == [0] * n
+    stream.synchronize()
+    want = oracle.ring_allreduce(send_np, "f32", "avg")[0]
+    for r in range(n):
+        assert _same_bits(from_dev(recv[r]), want)
+    rec = comm.last_record(0)
+    assert rec.seq == 1 and rec.arrived_mask == (1 << n) - 1
