@@ -71,6 +71,8 @@ def _load():
     lib.or_fp8_ring_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
     lib.or_fp8_tree_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
     lib.or_fp8_ring_blocks.argtypes = [vp, vp, vp, sz, sz, ci, ci, ci, ci, vp]
+    lib.or_topk_compress.argtypes = [vp, vp, sz, sz, vp, vp]
+    lib.or_sparse_to_dense.argtypes = [vp, vp, sz, sz, vp]
     lib.or_fp8_hop_ring_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
     lib.or_fp8_hop_blocks_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci]
     lib.or_bucket_plan.argtypes = [vp, ci, ci, ctypes.c_uint64, vp, vp, vp, vp]
@@ -233,6 +235,33 @@ def fp8_ring_blocks(blocks: np.ndarray, first: np.ndarray, blen: np.ndarray, cou
                                       count, blocks.shape[1], DTYPES[in_dtype], DTYPES[out_dtype], OPS[op],
                                       out.ctypes.data), "fp8_ring_blocks")
     return out
+
+
+def topk_compress(grad, residual, k: int):
+    """(idx, val, new_residual): a = grad + residual; the k largest |a| (ties: lower
+    index first) as ascending (index, value) pairs; residual = a with those zeroed."""
+    g = np.ascontiguousarray(grad, dtype=np.float32)
+    e = np.array(residual, dtype=np.float32, copy=True)
+    idx = np.empty(max(k, 1), dtype=np.uint32)
+    val = np.empty(max(k, 1), dtype=np.float32)
+    _check(_load().or_topk_compress(g.ctypes.data, e.ctypes.data, g.size, k, idx.ctypes.data, val.ctypes.data),
+           "topk_compress")
+    return idx[:k].copy(), val[:k].copy(), e
+
+
+def sparse_to_dense(idx, val, count: int):
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    val = np.ascontiguousarray(val, dtype=np.float32)
+    out = np.empty(count, dtype=np.float32)
+    _check(_load().or_sparse_to_dense(idx.ctypes.data, val.ctypes.data, idx.size, count, out.ctypes.data),
+           "sparse_to_dense")
+    return out
+
+
+def sparse_ring_allreduce(idx_list, val_list, count: int, op: str):
+    """Allreduce of sparse vectors: the ring allreduce of their dense forms."""
+    dense = [sparse_to_dense(i, v, count) for i, v in zip(idx_list, val_list)]
+    return ring_allreduce(dense, "f32", op)
 
 
 def bucket_plan(counts, esize: int, cap_bytes: int):

@@ -391,3 +391,65 @@ def test_fp8_hop_error_bound_and_growth():
     assert np.all(np.abs(hop - ystar) <= per + 2.0**-8 * (np.abs(ystar) + per))
     assert e_hop <= 6e-2 * 4 and e_once <= 6e-2
     assert e_hop > e_once  # re-quantising partials on every hop loses more than quantising inputs once
+
+
+# ------------------------------------------------------------- Top-K sparsification
+
+def test_topk_hand_ties():
+    g = G.load("topk_ties.txt")
+    grad = np.array(G.nums(g["grad"]), dtype=np.float32)
+    res = np.array(G.nums(g["residual"]), dtype=np.float32)
+    idx, val, e = oracle.topk_compress(grad, res, 3)
+    assert idx.tolist() == G.nums(g["k3_idx"], int) and val.tolist() == G.nums(g["k3_val"])
+    idx, val, e = oracle.topk_compress(grad, res, 2)
+    assert idx.tolist() == G.nums(g["k2_idx"], int) and val.tolist() == G.nums(g["k2_val"])
+    assert e.tolist() == G.nums(g["k2_residual"])
+
+
+def test_topk_extremes_partition_and_brute_force():
+    rng = np.random.default_rng(4)
+    for count in (1, 7, 300, 5000):
+        grad = synthgen.normal_f32(count, seed=count, sigma=1e-3)
+        res = synthgen.normal_f32(count, seed=count + 1, sigma=1e-4)
+        # ties on purpose: repeat some magnitudes
+        grad[rng.integers(0, count, size=count // 10)] = np.float32(2e-3)
+        a = (grad + res).astype(np.float32)
+        for k in sorted({0, 1, count // 3, count}):
+            idx, val, e = oracle.topk_compress(grad, res, k)
+            assert idx.size == k and np.all(np.diff(idx.astype(np.int64)) > 0)
+            dense = oracle.sparse_to_dense(idx, val, count)
+            assert np.array_equal((dense + e).view(np.uint32), a.view(np.uint32))  # a = s + e, bitwise
+            assert np.all(dense[e != 0] == 0)
+            # brute force: the kept set is the k smallest (-|a|, index) pairs
+            order = sorted(range(count), key=lambda i: (-abs(float(a[i])), i))[:k]
+            assert sorted(order) == idx.tolist()
+
+
+def test_sparse_allreduce_is_dense_allreduce_of_sparse_vectors():
+    n, count, k = 8, 20_000, 2_000
+    grads = synthgen.ranks_normal(n, count, 1e-3, base_seed=2)
+    res = [np.zeros(count, dtype=np.float32) for _ in range(n)]
+    sp = [oracle.topk_compress(g, e, k) for g, e in zip(grads, res)]
+    y = oracle.sparse_ring_allreduce([s[0] for s in sp], [s[1] for s in sp], count, "avg")[0]
+    dense = [oracle.sparse_to_dense(s[0], s[1], count) for s in sp]
+    assert np.array_equal(y, oracle.ring_allreduce(dense, "f32", "avg")[0])
+    # every kept value appears in the sum (at most n contributions per element)
+    support = np.zeros(count, dtype=bool)
+    for s in sp:
+        support[s[0]] = True
+    assert np.all(y[~support] == 0)
+
+
+def test_error_feedback_conserves_the_gradient_mass():
+    # over T steps, sent + final residual = sum of gradients (up to the rounding of g + e)
+    count, k, T = 4000, 200, 6
+    e = np.zeros(count, dtype=np.float32)
+    sent = np.zeros(count, dtype=np.float64)
+    total = np.zeros(count, dtype=np.float64)
+    for t in range(T):
+        g = synthgen.normal_f32(count, seed=100 + t, sigma=1e-3)
+        idx, val, e = oracle.topk_compress(g, e, k)
+        sent[idx] += val
+        total += g
+    err = np.abs(sent + e - total)
+    assert np.all(err <= T * 2.0**-23 * (np.abs(total) + np.abs(sent) + 1e-3))
