@@ -20,6 +20,7 @@ __all__ = [
     "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_reduce_scatter", "ar_all_gather",
     "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
     "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops", "ar_allreduce_fp8_noalloc",
+    "ar_topk_workspace_bytes", "ar_topk_compress", "ar_sparse_allreduce",
     "ar_status_string", "ar_last_error", "ar_version",
     "DTYPES", "OPS", "ALGOS", "Comm", "CallRecord",
 ]
@@ -76,8 +77,13 @@ def lib() -> ctypes.CDLL:
     L.ar_allreduce_fp8_noalloc.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_fused.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_hops.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
+    L.ar_topk_workspace_bytes.argtypes = [sz]
+    L.ar_topk_workspace_bytes.restype = sz
+    L.ar_topk_compress.argtypes = [vp, vp, sz, sz, vp, vp, vp, sz, vp]
+    L.ar_sparse_allreduce.argtypes = [pp, pp, vp, ci, sz, ci, ci, pp, vp]
     for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
-                 "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops"):
+                 "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops",
+                 "ar_topk_compress", "ar_sparse_allreduce"):
         getattr(L, name).restype = ci
     L.ar_comm_create.argtypes = [ci, ci, ctypes.POINTER(ctypes.c_void_p)]
     L.ar_comm_destroy.argtypes = [vp]
@@ -260,6 +266,50 @@ def ar_allreduce_fp8_noalloc(sendbufs: Sequence[torch.Tensor], recvbufs: Sequenc
     odt, _ = _same(recvbufs, "recvbufs")
     _check(lib().ar_allreduce_fp8_noalloc(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt],
                                           DTYPES[odt], OPS[op], ALGOS[algo], _stream(stream)))
+
+
+def ar_topk_workspace_bytes(count: int) -> int:
+    return int(lib().ar_topk_workspace_bytes(count))
+
+
+def _idx_ok(t: torch.Tensor, what: str) -> None:
+    if t.dtype not in (torch.int32, torch.uint32) or not t.is_contiguous():
+        raise ValueError(f"{what}: contiguous 32-bit index tensor expected")
+
+
+def ar_topk_compress(grad: torch.Tensor, residual: torch.Tensor, k: int, idx: torch.Tensor, val: torch.Tensor,
+                     workspace: torch.Tensor, stream=None) -> None:
+    """One rank's Top-K step with error feedback (see include/ar.h): residual
+    becomes grad + residual with the kept entries zeroed; idx[:k] / val[:k] the
+    kept (index, value) pairs in ascending index order."""
+    for t, what in ((grad, "grad"), (residual, "residual"), (val, "val")):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{what}: contiguous float32 tensor expected")
+    _idx_ok(idx, "idx")
+    if residual.numel() != grad.numel() or idx.numel() < k or val.numel() < k:
+        raise ValueError("residual must match grad; idx and val need k entries")
+    _check(lib().ar_topk_compress(grad.data_ptr(), residual.data_ptr(), grad.numel(), k, idx.data_ptr(),
+                                  val.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+
+
+def ar_sparse_allreduce(idx: Sequence[torch.Tensor], val: Sequence[torch.Tensor], nnz: Sequence[int],
+                        recvbufs: Sequence[torch.Tensor], op: str = "sum", algo: str = "fused", stream=None) -> None:
+    """Allreduce of each rank's sparse vector (idx[r][:nnz[r]], val[r][:nnz[r]])
+    into the dense float32 recvbufs (see include/ar.h)."""
+    n = len(recvbufs)
+    if len(idx) != n or len(val) != n or len(nnz) != n:
+        raise ValueError("one idx, val, nnz and output per rank")
+    _, count = _same(recvbufs, "recvbufs")
+    for r in range(n):
+        _idx_ok(idx[r], "idx")
+        if recvbufs[r].dtype != torch.float32 or val[r].dtype != torch.float32:
+            raise ValueError("values and outputs are float32")
+        if idx[r].numel() < nnz[r] or val[r].numel() < nnz[r]:
+            raise ValueError("idx and val need nnz entries")
+    counts = (ctypes.c_size_t * n)(*nnz)
+    _check(lib().ar_sparse_allreduce(_ptrs(idx), _ptrs(val), counts, n, count, OPS[op], ALGOS[algo],
+                                     _ptrs(recvbufs), _stream(stream)))
 
 
 class Comm:

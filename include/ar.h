@@ -289,6 +289,53 @@ ar_status_t ar_allreduce_fp8_noalloc(const void *const *sendbufs, void *const *r
                                      ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
                                      ar_stream_t stream);
 
+/* Top-K gradient sparsification with error feedback ([GL] §勾配圧縮技術: only
+ * the largest K% of the gradient is communicated and error feedback makes up
+ * for what is dropped; [WP] §优化技术: top-k sends the indices as well). The
+ * pages fix no formula or tie rule; this library's reading, per rank:
+ *   a = grad + residual            (binary32 add, round to nearest even)
+ *   keep the k entries of largest |a|; among equal |a| the lower index first
+ *   idx[0..k), val[0..k) = the kept (index, a[index]) in ascending index order
+ *   residual = a with the kept entries set to +0
+ * so the dense form of (idx, val) plus the new residual equals a exactly.
+ * |a| is compared through its bit pattern with the sign cleared (so -0 ties
+ * +0, and a NaN ranks above every number).
+ *
+ * Workspace bytes for ar_topk_compress over `count` values (a multiple of
+ * 256; about count / 1024 words plus 8 KiB); 0 if count >= 2^32. */
+size_t ar_topk_workspace_bytes(size_t count);
+
+/* One rank's Top-K step on `stream`: reads grad[count], updates
+ * residual[count] in place and writes idx[k] (uint32 indices) and val[k].
+ *   grad, residual: F32 device buffers, 4-byte aligned (16-byte aligned ones
+ *     take the vector path; results are identical either way).
+ *   workspace: device memory of at least ar_topk_workspace_bytes(count),
+ *     16-byte aligned, owned by the caller; its contents need no
+ *     initialisation and are meaningless afterwards.
+ *   Errors: AR_ERR_INVALID_ARGUMENT for k > count, count >= 2^32, a null or
+ *   misaligned pointer or a short workspace; AR_ERR_ALIAS if grad, residual,
+ *   idx, val or the workspace overlap. k == 0 only folds grad into residual;
+ *   count == 0 is a no-op. */
+ar_status_t ar_topk_compress(const float *grad, float *residual, size_t count, size_t k, uint32_t *idx, float *val,
+                             void *workspace, size_t ws_bytes, ar_stream_t stream);
+
+/* Allreduce of sparse vectors ([GL] §勾配圧縮技術): rank r contributes the
+ * dense vector of length `count` that is zero except at idx[r][j] where it
+ * holds val[r][j] (j < nnz[r]); every recvbufs[r] receives the allreduce of
+ * those dense vectors, computed exactly as ar_allreduce of F32 buffers with
+ * the same op and algo (bit-identical to it). The outputs are zeroed, the
+ * pairs scattered into them, and the allreduce run in place.
+ *   idx[r], val[r]: device arrays of nnz[r] entries; indices must be < count
+ *     and distinct within a rank (ar_topk_compress output is both). An index
+ *     >= count is dropped; which of two equal indices wins is unspecified.
+ *   recvbufs[r]: F32 device buffers of `count`, 4-byte aligned, disjoint from
+ *     each other and from every idx/val array.
+ *   Errors: as ar_allreduce, plus AR_ERR_INVALID_ARGUMENT for nnz[r] > count
+ *   or count >= 2^32. */
+ar_status_t ar_sparse_allreduce(const uint32_t *const *idx, const float *const *val, const size_t *nnz, int nranks,
+                                size_t count, ar_op_t op, ar_algo_t algo, float *const *recvbufs,
+                                ar_stream_t stream);
+
 /* Host-side communicator for virtual ranks driven by host threads
  * ([VL] §rankとcommunicator: every rank calls the matching collective with the
  * same count and type; §hangをtimeoutだけで再起動しない: hangs come from ranks

@@ -174,3 +174,45 @@ def test_bucket_allreduce_argument_errors(L):
     assert f(_arr(ins), _arr(over), n, nt, counts, offs, 604, 2, 1, 1, None) == gar.AR_ERR_ALIAS
     assert f(_arr(ins[:9]), _arr(outs[:9]), 3, nt, counts, offs, 604, 2, 1, 2, None) == gar.AR_ERR_UNSUPPORTED
     assert f(_arr(ins), _arr(outs), n, 0, counts, offs, 604, 2, 1, 1, None) == gar.AR_SUCCESS
+
+
+def test_topk_workspace_and_argument_errors(L):
+    count = 100_000
+    need = gar.ar_topk_workspace_bytes(count)
+    nb = math.ceil(count / 4096)
+    assert need == math.ceil((2048 + 16 + 4 * nb) * 4 / 256) * 256
+    assert gar.ar_topk_workspace_bytes(1 << 32) == 0
+    g, e, i, v, ws = 0x1000000, 0x2000000, 0x3000000, 0x4000000, 0x5000000
+    f = L.ar_topk_compress
+    assert f(g, e, count, count + 1, i, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT  # k > count
+    assert f(g, e, 1 << 32, 10, i, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(g, e, count, 10, i, v, ws, need - 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(g, e, count, 10, i, v, ws + 8, need, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(g, e + 2, count, 10, i, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(g, e, count, 10, None, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(g, g + 4 * 50, count, 10, i, v, ws, need, None) == gar.AR_ERR_ALIAS       # residual inside grad
+    assert f(g, e, count, 10, i, i + 8, ws, need, None) == gar.AR_ERR_ALIAS            # idx and val overlap
+    assert f(g, e, count, 10, i, v, e + 64, need, None) == gar.AR_ERR_ALIAS            # workspace inside residual
+    assert f(g, e, 0, 0, None, None, None, 0, None) == gar.AR_SUCCESS                  # empty
+
+
+def test_sparse_allreduce_argument_errors(L):
+    n, count = 4, 1000
+    idx = [0x1000000 * (r + 1) for r in range(n)]
+    val = [0x10000000 + 0x1000000 * r for r in range(n)]
+    out = [0x20000000 + 0x1000000 * r for r in range(n)]
+    nnz = (ctypes.c_size_t * n)(10, 0, 1000, 5)
+    f = L.ar_sparse_allreduce
+    assert f(_arr(idx), _arr(val), (ctypes.c_size_t * n)(10, 0, 1001, 5), n, count, 0, 1, _arr(out), None) \
+        == gar.AR_ERR_INVALID_ARGUMENT  # nnz > count
+    assert f(_arr(idx), _arr(val), nnz, 3, count, 0, 2, _arr(out[:3]), None) == gar.AR_ERR_UNSUPPORTED  # tree, N=3
+    assert f(_arr(idx), _arr(val), nnz, n, count, 7, 1, _arr(out), None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(_arr(idx), _arr(val), nnz, n, count, 0, 9, _arr(out), None) == gar.AR_ERR_INVALID_ARGUMENT
+    over = list(out)
+    over[2] = out[1] + 400
+    assert f(_arr(idx), _arr(val), nnz, n, count, 0, 1, _arr(over), None) == gar.AR_ERR_ALIAS
+    bad = list(idx)
+    bad[3] = out[0] + 8  # an index array inside an output
+    assert f(_arr(bad), _arr(val), nnz, n, count, 0, 1, _arr(out), None) == gar.AR_ERR_ALIAS
+    assert f(_arr(idx), _arr(val), nnz, n, 1 << 32, 0, 1, _arr(out), None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(_arr(idx), _arr(val), nnz, n, 0, 0, 1, _arr(out), None) == gar.AR_SUCCESS

@@ -1,0 +1,210 @@
+"""GPU parity of Top-K sparsification with error feedback and of the sparse
+allreduce, against the oracle: bit-exact indices, values and residuals on
+seeded inputs (ragged sizes, heavy ties, signed zeros, k = 0 and k = count,
+unaligned buffers, several steps of error feedback), and in full at the size
+of one 25 MiB f32 gradient per rank on 8 ranks."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_allreduce_collective_gb300 as gar
+import oracle
+import synthgen
+from tests._dev import from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gar.build()
+    gar.lib()
+
+
+def _bits(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+def _dev_f32(a: np.ndarray, offset: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """(base, view): a device copy of `a` starting `offset` elements into its allocation."""
+    base = torch.empty(a.size + offset + 1, dtype=torch.float32, device="cuda")
+    base.fill_(float("nan"))
+    v = base[offset: offset + a.size]
+    v.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return base, v
+
+
+def _gpu_topk(g: np.ndarray, e: np.ndarray, k: int, offset: int = 0):
+    count = g.size
+    gb, gd = _dev_f32(g, offset)
+    eb, ed = _dev_f32(e, offset)
+    idx = torch.full((k + 8,), -1, dtype=torch.int32, device="cuda")
+    val = torch.full((k + 8,), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(gar.ar_topk_workspace_bytes(count), dtype=torch.uint8, device="cuda")
+    ws.fill_(0x5A)  # the workspace needs no initialisation
+    gar.ar_topk_compress(gd, ed, k, idx, val, ws)
+    torch.cuda.synchronize()
+    i = from_dev(idx).view(np.uint32)
+    v = from_dev(val)
+    # nothing beyond k written, grad untouched, nothing outside the residual written
+    assert np.all(i[k:] == 0xFFFFFFFF) and np.all(v[k:] == 7.0)
+    assert np.array_equal(_bits(from_dev(gd)), _bits(g))
+    eb_host = from_dev(eb)
+    assert np.all(np.isnan(eb_host[:offset])) and np.all(np.isnan(eb_host[offset + count:]))
+    return i[:k].copy(), v[:k].copy(), from_dev(ed).copy()
+
+
+def _check_against_oracle(g, e, k, offset=0):
+    gi, gv, ge = _gpu_topk(g, e, k, offset)
+    oi, ov, oe = oracle.topk_compress(g, e, k)
+    assert np.array_equal(gi, oi), "indices differ"
+    assert np.array_equal(_bits(gv), _bits(ov)), "values differ"
+    assert np.array_equal(_bits(ge), _bits(oe)), "residuals differ"
+
+
+@pytest.mark.parametrize("count", [0, 1, 7, 4095, 4096, 4097, 100_003, (1 << 20) + 13])
+def test_topk_matches_oracle_ragged(count):
+    g = synthgen.normal_f32(count, 11, 1e-3)
+    e = synthgen.normal_f32(count, 12, 1e-4)
+    for k in sorted({0, 1, max(1, count // 100), count // 2, count}):
+        _check_against_oracle(g, e, k)
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_topk_unaligned_buffers_take_the_element_path(offset):
+    count = 50_001
+    g = synthgen.normal_f32(count, 21, 1.0)
+    e = synthgen.normal_f32(count, 22, 0.1)
+    for k in (1, 500, 25_000):
+        _check_against_oracle(g, e, k, offset)
+
+
+def test_topk_heavy_ties_and_signed_zeros():
+    # magnitudes from {0, 1, 2, 3}, both signs, both zeros: every threshold is
+    # a tie that the lower indices win
+    count = 30_011
+    ints = synthgen.uniform_i32(count, 31, -3, 3)
+    g = ints.astype(np.float32)
+    g[ints == 0] = np.where(np.arange(count)[ints == 0] % 2 == 0, 0.0, -0.0).astype(np.float32)
+    e = np.zeros(count, dtype=np.float32)
+    e[::7] = -0.0
+    nz3 = int(np.sum(np.abs(g) == 3))
+    for k in (1, nz3 - 1, nz3, nz3 + 1, count // 2, count - 1, count):
+        _check_against_oracle(g, e, k)
+
+
+def test_topk_special_values():
+    count = 9000
+    g = synthgen.normal_f32(count, 41, 1.0)
+    g[5] = np.inf
+    g[17] = -np.inf
+    g[100:200] = np.float32(1e-45)  # subnormals
+    g[300] = np.finfo(np.float32).max
+    e = np.zeros(count, dtype=np.float32)
+    e[300] = np.finfo(np.float32).max  # overflows to +inf in a = g + e
+    for k in (1, 2, 3, 4, 50, 8950, count):
+        _check_against_oracle(g, e, k)
+
+
+def test_error_feedback_over_several_steps():
+    count, k = 200_000, 2_000
+    e_host = np.zeros(count, dtype=np.float32)
+    ed = torch.zeros(count, dtype=torch.float32, device="cuda")
+    idx = torch.empty(k, dtype=torch.int32, device="cuda")
+    val = torch.empty(k, dtype=torch.float32, device="cuda")
+    ws = torch.empty(gar.ar_topk_workspace_bytes(count), dtype=torch.uint8, device="cuda")
+    for step in range(4):
+        g = synthgen.normal_f32(count, 100 + step, 1e-3)
+        gar.ar_topk_compress(to_dev(g, "f32"), ed, k, idx, val, ws)
+        oi, ov, e_host = oracle.topk_compress(g, e_host, k)
+        torch.cuda.synchronize()
+        assert np.array_equal(from_dev(idx).view(np.uint32), oi)
+        assert np.array_equal(_bits(from_dev(val)), _bits(ov))
+        assert np.array_equal(_bits(from_dev(ed)), _bits(e_host))
+
+
+def _algos(n):
+    pow2 = n & (n - 1) == 0
+    return ["ring", "fused", "auto", "step_ring"] + (["tree", "step_tree"] if pow2 else [])
+
+
+@pytest.mark.parametrize("n", [1, 3, 4, 8])
+def test_sparse_allreduce_matches_oracle(n):
+    count = 40_009
+    idx_np, val_np = [], []
+    for r in range(n):
+        g = synthgen.normal_f32(count, 200 + r, 1.0)
+        k = [count // 100, 0, count, 517, 3, 1, 4000, count // 2][r % 8]
+        i, v, _ = oracle.topk_compress(g, np.zeros(count, dtype=np.float32), k)
+        idx_np.append(i)
+        val_np.append(v)
+    idx = [torch.from_numpy(i.view(np.int32)).cuda() if i.size else torch.empty(0, dtype=torch.int32, device="cuda")
+           for i in idx_np]
+    val = [to_dev(v, "f32") if v.size else torch.empty(0, dtype=torch.float32, device="cuda") for v in val_np]
+    nnz = [i.size for i in idx_np]
+    for op in ("sum", "avg", "max"):
+        for algo in _algos(n):
+            out = [torch.full((count,), float("nan"), device="cuda") for _ in range(n)]
+            gar.ar_sparse_allreduce(idx, val, nnz, out, op, algo)
+            torch.cuda.synchronize()
+            dense = [oracle.sparse_to_dense(i, v, count) for i, v in zip(idx_np, val_np)]
+            if algo in ("tree", "step_tree"):
+                want = oracle.tree_allreduce(dense, "f32", op)[0]
+            else:
+                want = oracle.sparse_ring_allreduce(idx_np, val_np, count, op)[0]
+            for r in range(n):
+                assert np.array_equal(_bits(from_dev(out[r])), _bits(want)), (op, algo, r)
+
+
+def test_sparse_allreduce_drops_out_of_range_indices():
+    count = 1000
+    idx = torch.tensor([0, 999, 1000, 5000], dtype=torch.int32, device="cuda")
+    val = torch.tensor([1.0, 2.0, 3.0, 4.0], device="cuda")
+    out = [torch.full((count + 64,), 9.0, device="cuda")]
+    gar.ar_sparse_allreduce([idx], [val], [4], [out[0][:count]])
+    torch.cuda.synchronize()
+    h = from_dev(out[0])
+    assert h[0] == 1.0 and h[999] == 2.0 and np.all(h[1:999] == 0.0) and np.all(h[count:] == 9.0)
+
+
+def test_topk_full_size_eight_ranks():
+    """8 ranks x 6,553,600 f32 (25 MiB each), k = 1%: every rank's indices,
+    values and residual against the oracle in full, the defining properties
+    checked on the device, and the sparse allreduce of the oracle's pairs on
+    sampled elements against the oracle's ring-order fold."""
+    n, count = 8, 6_553_600
+    k = count // 100
+    g_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=300)
+    e_np = synthgen.ranks_normal(n, count, 1e-4, base_seed=400)
+    grads = [to_dev(x, "f32") for x in g_np]
+    res = [to_dev(x, "f32") for x in e_np]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    ws = torch.empty(gar.ar_topk_workspace_bytes(count), dtype=torch.uint8, device="cuda")
+    for r in range(n):
+        gar.ar_topk_compress(grads[r], res[r], k, idx[r], val[r], ws)
+    torch.cuda.synchronize()
+    o_idx, o_val = [], []
+    for r in range(n):
+        oi, ov, oe = oracle.topk_compress(g_np[r], e_np[r], k)
+        assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), r
+        assert np.array_equal(_bits(from_dev(val[r])), _bits(ov)), r
+        assert np.array_equal(_bits(from_dev(res[r])), _bits(oe)), r
+        o_idx.append(oi)
+        o_val.append(ov)
+        # the defining properties: ascending indices, kept magnitudes never below dropped ones
+        i = idx[r].long()
+        assert bool((i[1:] > i[:-1]).all())
+        assert float(res[r].abs().max()) <= float(val[r].abs().min())
+    # sparse allreduce of the oracle's pairs
+    d_idx = [torch.from_numpy(i.view(np.int32)).cuda() for i in o_idx]
+    d_val = [to_dev(v, "f32") for v in o_val]
+    out = [torch.empty(count, device="cuda") for _ in range(n)]
+    gar.ar_sparse_allreduce(d_idx, d_val, [k] * n, out, "avg", "fused")
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    sample = np.unique(np.concatenate([rng.integers(0, count, 4000)] + [i[:64].astype(np.int64) for i in o_idx]))
+    vals = np.stack([oracle.sparse_to_dense(i, v, count)[sample] for i, v in zip(o_idx, o_val)], axis=1)
+    want = oracle.fold_points(vals, sample, count, "f32", "avg")
+    for r in range(n):
+        assert np.array_equal(_bits(from_dev(out[r])[sample]), _bits(want)), r
