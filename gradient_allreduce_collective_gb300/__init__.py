@@ -77,9 +77,9 @@ def lib() -> ctypes.CDLL:
     L.ar_allreduce_fp8_noalloc.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_fused.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_hops.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
-    L.ar_topk_workspace_bytes.argtypes = [sz]
+    L.ar_topk_workspace_bytes.argtypes = [ci, sz]
     L.ar_topk_workspace_bytes.restype = sz
-    L.ar_topk_compress.argtypes = [vp, vp, sz, sz, vp, vp, vp, sz, vp]
+    L.ar_topk_compress.argtypes = [pp, pp, ci, sz, sz, pp, pp, vp, sz, vp]
     L.ar_sparse_allreduce.argtypes = [pp, pp, vp, ci, sz, ci, ci, pp, vp]
     for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
                  "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops",
@@ -268,8 +268,8 @@ def ar_allreduce_fp8_noalloc(sendbufs: Sequence[torch.Tensor], recvbufs: Sequenc
                                           DTYPES[odt], OPS[op], ALGOS[algo], _stream(stream)))
 
 
-def ar_topk_workspace_bytes(count: int) -> int:
-    return int(lib().ar_topk_workspace_bytes(count))
+def ar_topk_workspace_bytes(nranks: int, count: int) -> int:
+    return int(lib().ar_topk_workspace_bytes(nranks, count))
 
 
 def _idx_ok(t: torch.Tensor, what: str) -> None:
@@ -277,19 +277,27 @@ def _idx_ok(t: torch.Tensor, what: str) -> None:
         raise ValueError(f"{what}: contiguous 32-bit index tensor expected")
 
 
-def ar_topk_compress(grad: torch.Tensor, residual: torch.Tensor, k: int, idx: torch.Tensor, val: torch.Tensor,
-                     workspace: torch.Tensor, stream=None) -> None:
-    """One rank's Top-K step with error feedback (see include/ar.h): residual
-    becomes grad + residual with the kept entries zeroed; idx[:k] / val[:k] the
-    kept (index, value) pairs in ascending index order."""
-    for t, what in ((grad, "grad"), (residual, "residual"), (val, "val")):
-        if t.dtype != torch.float32 or not t.is_contiguous():
-            raise ValueError(f"{what}: contiguous float32 tensor expected")
-    _idx_ok(idx, "idx")
-    if residual.numel() != grad.numel() or idx.numel() < k or val.numel() < k:
-        raise ValueError("residual must match grad; idx and val need k entries")
-    _check(lib().ar_topk_compress(grad.data_ptr(), residual.data_ptr(), grad.numel(), k, idx.data_ptr(),
-                                  val.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+def ar_topk_compress(grads: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor], k: int,
+                     idx: Sequence[torch.Tensor], val: Sequence[torch.Tensor], workspace: torch.Tensor,
+                     stream=None) -> None:
+    """Every rank's Top-K step with error feedback (see include/ar.h):
+    residuals[r] becomes grads[r] + residuals[r] with the kept entries zeroed;
+    idx[r][:k] / val[r][:k] the kept (index, value) pairs in ascending index order."""
+    n = len(grads)
+    if len(residuals) != n or len(idx) != n or len(val) != n:
+        raise ValueError("one grad, residual, idx and val per rank")
+    dt, count = _same(grads, "grads")
+    rdt, rcount = _same(residuals, "residuals")
+    if dt != torch.float32 or rdt != torch.float32 or rcount != count:
+        raise ValueError("grads and residuals: float32 tensors of one size")
+    for r in range(n):
+        _idx_ok(idx[r], "idx")
+        if val[r].dtype != torch.float32 or not val[r].is_contiguous():
+            raise ValueError("val: contiguous float32 tensor expected")
+        if idx[r].numel() < k or val[r].numel() < k:
+            raise ValueError("idx and val need k entries")
+    _check(lib().ar_topk_compress(_ptrs(grads), _ptrs(residuals), n, count, k, _ptrs(idx), _ptrs(val),
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                   _stream(stream)))
 
 

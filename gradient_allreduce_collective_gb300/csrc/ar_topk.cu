@@ -12,11 +12,15 @@
 // Exact selection without sorting: the key T of the k-th largest magnitude
 // comes from a three-pass radix select over the 31 magnitude bits — a
 // histogram of bits 30..20 (fused with a = g + e), then of bits 19..10 and
-// 9..0 among the keys that match the prefix found so far; after each
-// histogram a one-thread kernel picks the digit, so the state never leaves
-// the device. Keys above T are all kept; of the keys equal to T, the first
-// (k - #above) in index order are kept: per-block counts, a one-block scan
-// over the blocks, and block-wide scans give every kept element its slot.
+// 9..0 among the keys that match the prefix found so far. The block of each
+// pass that finishes last picks the digit (a block-wide scan of the
+// histogram from the top), so the state never leaves the device and no
+// launch is spent on it. Keys above T are all kept; of the keys equal to T,
+// the first (k - #above) in index order are kept: per-block counts, scanned
+// by the count pass's last block, and block-wide scans in the emit pass give
+// every kept element its slot. All ranks of a call share each launch
+// (grid.y = rank): six launches per call whatever the number of ranks.
+#include <algorithm>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -30,129 +34,30 @@ void set_last_error(const std::string& msg);
 
 namespace {
 
-constexpr int kTopkElems = 16;                     // elements per thread in count / emit
-constexpr int kTopkBlock = kThreads * kTopkElems;  // elements per block in count / emit
 constexpr int kHistBlocksPerSm = 8;
 constexpr int kSms = 152;
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
 
-// kTopkElems consecutive values starting at `base` (zero past the end)
-template <bool VEC>
-__device__ __forceinline__ void load_run(const float* __restrict__ a, uint64_t base, uint64_t count,
-                                         float (&v)[kTopkElems]) {
-  if (VEC && base + kTopkElems <= count) {
-    const float4* p = reinterpret_cast<const float4*>(a + base);
-#pragma unroll
-    for (int q = 0; q < kTopkElems / 4; ++q) {
-      const float4 x = p[q];
-      v[4 * q] = x.x;
-      v[4 * q + 1] = x.y;
-      v[4 * q + 2] = x.z;
-      v[4 * q + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kTopkElems; ++j) v[j] = base + j < count ? a[base + j] : 0.0f;
-  }
-}
+struct RankWs {
+  uint32_t* hist;
+  TopkState* st;
+  uint32_t* n_gt;
+  uint32_t* n_eq;
+  uint32_t* eq_before;
+  uint32_t* out_off;
+};
 
-// a = g + e into e, and the histogram of bits 30..20 of |a| (pass 1)
-template <bool VEC>
-__global__ void __launch_bounds__(kThreads) k_topk_add_hist(const float* __restrict__ g, float* __restrict__ e,
-                                                            uint64_t count, uint32_t* __restrict__ hist) {
-  __shared__ uint32_t sh[2048];
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x) sh[i] = 0;
-  __syncthreads();
-  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  uint64_t done = 0;
-  if (VEC) {
-    const uint64_t n4 = count / 4;
-    const float4* g4 = reinterpret_cast<const float4*>(g);
-    float4* e4 = reinterpret_cast<float4*>(e);
-    for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4; q += stride) {
-      const float4 x = __ldcs(g4 + q);
-      const float4 y = e4[q];
-      float4 s;
-      s.x = __fadd_rn(x.x, y.x);
-      s.y = __fadd_rn(x.y, y.y);
-      s.z = __fadd_rn(x.z, y.z);
-      s.w = __fadd_rn(x.w, y.w);
-      e4[q] = s;
-      atomicAdd(&sh[mag_key(s.x) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s.y) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s.z) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s.w) >> 20], 1u);
-    }
-    done = n4 * 4;
-  }
-  for (uint64_t i = done + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
-    const float s = __fadd_rn(g[i], e[i]);
-    e[i] = s;
-    atomicAdd(&sh[mag_key(s) >> 20], 1u);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
-    if (sh[i]) atomicAdd(&hist[i], sh[i]);
-}
-
-// histogram of the 10-bit digit at `shift` among keys whose fixed bits match
-template <bool VEC>
-__global__ void __launch_bounds__(kThreads) k_topk_hist(const float* __restrict__ a, uint64_t count,
-                                                        const TopkState* __restrict__ st, int shift,
-                                                        uint32_t* __restrict__ hist) {
-  __shared__ uint32_t sh[1024];
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
-  __syncthreads();
-  const uint32_t mask = st->mask, prefix = st->prefix;
-  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  uint64_t done = 0;
-  if (VEC) {
-    const uint64_t n4 = count / 4;
-    const float4* a4 = reinterpret_cast<const float4*>(a);
-    for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4; q += stride) {
-      const float4 x = a4[q];
-      const uint32_t k0 = mag_key(x.x), k1 = mag_key(x.y), k2 = mag_key(x.z), k3 = mag_key(x.w);
-      if ((k0 & mask) == prefix) atomicAdd(&sh[(k0 >> shift) & 1023u], 1u);
-      if ((k1 & mask) == prefix) atomicAdd(&sh[(k1 >> shift) & 1023u], 1u);
-      if ((k2 & mask) == prefix) atomicAdd(&sh[(k2 >> shift) & 1023u], 1u);
-      if ((k3 & mask) == prefix) atomicAdd(&sh[(k3 >> shift) & 1023u], 1u);
-    }
-    done = n4 * 4;
-  }
-  for (uint64_t i = done + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
-    const uint32_t key = mag_key(a[i]);
-    if ((key & mask) == prefix) atomicAdd(&sh[(key >> shift) & 1023u], 1u);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
-    if (sh[i]) atomicAdd(&hist[i], sh[i]);
-}
-
-// One thread: the highest digit whose count from the top reaches `need`;
-// fold it into the prefix and clear the histogram for the next pass.
-__global__ void k_topk_find(uint32_t* __restrict__ hist, int bins, int shift, TopkState* __restrict__ st) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  uint64_t above = 0;
-  int b = bins - 1;
-  for (; b > 0; --b) {
-    if (above + hist[b] >= st->need) break;
-    above += hist[b];
-  }
-  st->prefix |= (uint32_t)b << shift;
-  st->mask |= (uint32_t)(bins - 1) << shift;
-  st->need -= (uint32_t)above;
-  st->gt += (uint32_t)above;
-  for (int i = 0; i < bins; ++i) hist[i] = 0;
-}
-
-__global__ void k_topk_init(TopkState* st, uint32_t k) {
-  if (threadIdx.x == 0 && blockIdx.x == 0) {
-    st->prefix = 0;
-    st->mask = 0;
-    st->need = k;
-    st->gt = 0;
-  }
+__device__ __forceinline__ RankWs rank_ws(const TopkArgs& A, int r) {
+  uint32_t* base = A.ws + (uint64_t)r * A.ws_words;
+  RankWs w;
+  w.hist = base;
+  w.st = reinterpret_cast<TopkState*>(base + kTopkHistWords);
+  w.n_gt = base + kTopkHistWords + kTopkStateWords;
+  w.n_eq = w.n_gt + A.nb;
+  w.eq_before = w.n_eq + A.nb;
+  w.out_off = w.eq_before + A.nb;
+  return w;
 }
 
 // exclusive scan over the block of one value per thread; *total = block sum
@@ -183,15 +88,202 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
   return before;
 }
 
-// per block of kTopkBlock elements: keys above T and keys equal to T
+// Called by every thread of a block after its global writes for this pass:
+// true in the block that finishes last among the gridDim.x blocks of its
+// rank. No block waits for another.
+__device__ __forceinline__ bool last_block(uint32_t* ticket) {
+  __shared__ bool s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (s_last) __threadfence();
+  return s_last;
+}
+
+// The last block of a radix pass: the highest digit whose count from the top
+// reaches `need` (a block-wide scan over BINS bins, highest first); fold it
+// into the prefix and clear the bins for the next pass.
+template <int BINS>
+__device__ void find_digit(uint32_t* hist, int shift, TopkState* st) {
+  constexpr int R = BINS / kThreads;
+  const int top = BINS - threadIdx.x * R;  // this thread: bins [top - R, top)
+  const uint32_t need = st->need;
+  uint32_t h[R];
+  uint32_t local = 0;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    h[j] = __ldcg(hist + top - 1 - j);
+    local += h[j];
+  }
+  const uint32_t above0 = block_exclusive_scan(local, nullptr);
+  if (above0 < need && above0 + local >= need) {  // exactly one thread
+    uint32_t above = above0;
+    int pick = top - R;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (above + h[j] >= need) {
+        pick = top - 1 - j;
+        break;
+      }
+      above += h[j];
+    }
+    st->prefix |= (uint32_t)pick << shift;
+    st->mask |= (uint32_t)(BINS - 1) << shift;
+    st->need = need - above;
+    st->gt += above;
+  }
+#pragma unroll
+  for (int j = 0; j < R; ++j) hist[top - 1 - j] = 0;
+}
+
+__global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ TopkArgs A) {
+  const RankWs w = rank_ws(A, blockIdx.y);
+  for (int i = threadIdx.x; i < kTopkHistWords; i += blockDim.x) w.hist[i] = 0;
+  if (threadIdx.x == 0) {
+    w.st->prefix = 0;
+    w.st->mask = 0;
+    w.st->need = A.k;
+    w.st->gt = 0;
+    for (int p = 0; p < 4; ++p) w.st->ticket[p] = 0;
+  }
+}
+
+__device__ __forceinline__ float4 add4(float4 x, float4 y) {
+  return make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z), __fadd_rn(x.w, y.w));
+}
+
+// Pass 1: a = g + e into e, histogram of bits 30..20 of |a|, then (last
+// block, if k > 0) the first digit.
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads) k_topk_count(const float* __restrict__ a, uint64_t count,
-                                                         const TopkState* __restrict__ st, uint32_t* __restrict__ n_gt,
-                                                         uint32_t* __restrict__ n_eq) {
-  const uint32_t T = st->prefix;
-  const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)threadIdx.x * kTopkElems;
-  float v[kTopkElems];
-  load_run<VEC>(a, base, count, v);
+__global__ void __launch_bounds__(kThreads) k_topk_pass1(const __grid_constant__ TopkArgs A) {
+  __shared__ uint32_t sh[2048];
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  const float* __restrict__ g = A.g[r];
+  float* __restrict__ e = A.e[r];
+  const uint64_t count = A.count;
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint64_t done = 0;
+  if (VEC) {
+    const uint64_t n4 = count / 4;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    float4* e4 = reinterpret_cast<float4*>(e);
+    uint64_t q = t0;
+    for (; q + stride < n4; q += 2 * stride) {
+      const float4 x0 = __ldcs(g4 + q), x1 = __ldcs(g4 + q + stride);
+      const float4 y0 = e4[q], y1 = e4[q + stride];
+      const float4 s0 = add4(x0, y0), s1 = add4(x1, y1);
+      e4[q] = s0;
+      e4[q + stride] = s1;
+      atomicAdd(&sh[mag_key(s0.x) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s0.y) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s0.z) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s0.w) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s1.x) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s1.y) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s1.z) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s1.w) >> 20], 1u);
+    }
+    if (q < n4) {
+      const float4 s = add4(__ldcs(g4 + q), e4[q]);
+      e4[q] = s;
+      atomicAdd(&sh[mag_key(s.x) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s.y) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s.z) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s.w) >> 20], 1u);
+    }
+    done = n4 * 4;
+  }
+  for (uint64_t i = done + t0; i < count; i += stride) {
+    const float s = __fadd_rn(g[i], e[i]);
+    e[i] = s;
+    atomicAdd(&sh[mag_key(s) >> 20], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
+    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
+  if (A.k == 0) return;  // nothing to select
+  if (last_block(&w.st->ticket[0])) find_digit<2048>(w.hist, 20, w.st);
+}
+
+// Passes 2 and 3: histogram of the 10-bit digit at `shift` among keys whose
+// fixed bits match, then (last block) that digit.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) k_topk_pass(const __grid_constant__ TopkArgs A, int shift, int pass) {
+  __shared__ uint32_t sh[1024];
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  const float* __restrict__ a = A.e[r];
+  const uint64_t count = A.count;
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  const uint32_t mask = w.st->mask, prefix = w.st->prefix;
+  auto add = [&](float v) {
+    const uint32_t key = mag_key(v);
+    if ((key & mask) == prefix) atomicAdd(&sh[(key >> shift) & 1023u], 1u);
+  };
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint64_t done = 0;
+  if (VEC) {
+    const uint64_t n4 = count / 4;
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    uint64_t q = t0;
+    for (; q + 3 * stride < n4; q += 4 * stride) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = a4[q + u * stride];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        add(x[u].x);
+        add(x[u].y);
+        add(x[u].z);
+        add(x[u].w);
+      }
+    }
+    for (; q < n4; q += stride) {
+      const float4 x = a4[q];
+      add(x.x);
+      add(x.y);
+      add(x.z);
+      add(x.w);
+    }
+    done = n4 * 4;
+  }
+  for (uint64_t i = done + t0; i < count; i += stride) add(a[i]);
+  __syncthreads();
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
+  if (last_block(&w.st->ticket[pass])) find_digit<1024>(w.hist, shift, w.st);
+}
+
+// kTopkElems consecutive values starting at `base` (zero past the end)
+template <bool VEC>
+__device__ __forceinline__ void load_run(const float* __restrict__ a, uint64_t base, uint64_t count,
+                                         float (&v)[kTopkElems]) {
+  if (VEC && base + kTopkElems <= count) {
+    const float4* p = reinterpret_cast<const float4*>(a + base);
+#pragma unroll
+    for (int q = 0; q < kTopkElems / 4; ++q) {
+      const float4 x = p[q];
+      v[4 * q] = x.x;
+      v[4 * q + 1] = x.y;
+      v[4 * q + 2] = x.z;
+      v[4 * q + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kTopkElems; ++j) v[j] = base + j < count ? a[base + j] : 0.0f;
+  }
+}
+
+// keys above T (low 16 bits) and equal to T (high 16 bits) in a run
+__device__ __forceinline__ uint32_t run_counts(const float (&v)[kTopkElems], uint64_t base, uint64_t count,
+                                               uint32_t T) {
   uint32_t gt = 0, eq = 0;
 #pragma unroll
   for (int j = 0; j < kTopkElems; ++j) {
@@ -201,75 +293,85 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const float* __restrict
       eq += key == T;
     }
   }
-  // gt and eq fit 16 bits each (at most kTopkBlock per block): one scan
-  uint32_t tot;
-  block_exclusive_scan(gt | (eq << 16), &tot);
-  if (threadIdx.x == 0) {
-    n_gt[blockIdx.x] = tot & 0xFFFFu;
-    n_eq[blockIdx.x] = tot >> 16;
+  return gt | (eq << 16);
+}
+
+// The count pass's last block: eq_before[b] = keys equal to T in earlier
+// blocks; out_off[b] = kept elements in earlier blocks, where block b keeps
+// all its keys above T and min(n_eq[b], max(0, need - eq_before[b])) of its
+// keys equal to T. Each thread scans a contiguous run of blocks.
+__device__ void scan_blocks(const RankWs& w, uint64_t nb) {
+  const uint32_t need = w.st->need;
+  const uint64_t m = (nb + kThreads - 1) / kThreads;
+  const uint64_t lo = (uint64_t)threadIdx.x * m < nb ? (uint64_t)threadIdx.x * m : nb;
+  const uint64_t hi = lo + m < nb ? lo + m : nb;
+  uint32_t se = 0;
+  for (uint64_t b = lo; b < hi; ++b) se += __ldcg(w.n_eq + b);
+  const uint32_t eq0 = block_exclusive_scan(se, nullptr);
+  auto take_of = [&](uint64_t b, uint32_t eqb) {
+    const uint32_t e = __ldcg(w.n_eq + b);
+    const uint32_t rest = need > eqb ? need - eqb : 0u;
+    return __ldcg(w.n_gt + b) + (e < rest ? e : rest);
+  };
+  uint32_t st = 0;
+  uint32_t eqb = eq0;
+  for (uint64_t b = lo; b < hi; ++b) {
+    st += take_of(b, eqb);
+    eqb += __ldcg(w.n_eq + b);
+  }
+  uint32_t off = block_exclusive_scan(st, nullptr);
+  eqb = eq0;
+  for (uint64_t b = lo; b < hi; ++b) {
+    const uint32_t t = take_of(b, eqb);
+    w.eq_before[b] = eqb;
+    w.out_off[b] = off;
+    off += t;
+    eqb += __ldcg(w.n_eq + b);
   }
 }
 
-// One block: eq_before[b] = keys equal to T in earlier blocks; out_off[b] =
-// kept elements in earlier blocks, where block b keeps all its keys above T
-// and min(n_eq[b], max(0, need - eq_before[b])) of its keys equal to T.
-__global__ void __launch_bounds__(kThreads) k_topk_scan(const uint32_t* __restrict__ n_gt,
-                                                        const uint32_t* __restrict__ n_eq, uint32_t nb,
-                                                        const TopkState* __restrict__ st,
-                                                        uint32_t* __restrict__ eq_before,
-                                                        uint32_t* __restrict__ out_off) {
-  const uint32_t need = st->need;
-  uint32_t carry_eq = 0, carry_out = 0;
-  for (uint32_t start = 0; start < nb; start += kThreads) {
-    const uint32_t b = start + threadIdx.x;
-    const uint32_t e = b < nb ? n_eq[b] : 0;
-    uint32_t tot_e;
-    const uint32_t ex_e = block_exclusive_scan(e, &tot_e) + carry_eq;
-    uint32_t take = 0;
-    if (b < nb) {
-      const uint32_t rest = need > ex_e ? need - ex_e : 0;
-      take = n_gt[b] + (e < rest ? e : rest);
-      eq_before[b] = ex_e;
-    }
-    uint32_t tot_o;
-    const uint32_t ex_o = block_exclusive_scan(take, &tot_o) + carry_out;
-    if (b < nb) out_off[b] = ex_o;
-    carry_eq += tot_e;
-    carry_out += tot_o;
+// per kTopkBlock-element block: keys above T and equal to T; the last block
+// scans the counts of all blocks
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  const uint32_t T = w.st->prefix;
+  const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)threadIdx.x * kTopkElems;
+  float v[kTopkElems];
+  load_run<VEC>(A.e[r], base, A.count, v);
+  uint32_t tot;
+  block_exclusive_scan(run_counts(v, base, A.count, T), &tot);  // no field overflows: <= 4096 each
+  if (threadIdx.x == 0) {
+    w.n_gt[blockIdx.x] = tot & 0xFFFFu;
+    w.n_eq[blockIdx.x] = tot >> 16;
   }
+  if (last_block(&w.st->ticket[3])) scan_blocks(w, A.nb);
 }
 
 // Kept elements to (index, value) in index order; zero their residual.
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads) k_topk_emit(float* __restrict__ a, uint64_t count,
-                                                        const TopkState* __restrict__ st,
-                                                        const uint32_t* __restrict__ eq_before,
-                                                        const uint32_t* __restrict__ out_off,
-                                                        uint32_t* __restrict__ idx, float* __restrict__ val) {
-  const uint32_t T = st->prefix, need = st->need;
+__global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  float* __restrict__ a = A.e[r];
+  uint32_t* __restrict__ idx = A.idx[r];
+  float* __restrict__ val = A.val[r];
+  const uint64_t count = A.count;
+  const uint32_t T = w.st->prefix, need = w.st->need;
   const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)threadIdx.x * kTopkElems;
   float v[kTopkElems];
   load_run<VEC>(a, base, count, v);
-  uint32_t gt = 0, eq = 0;
-#pragma unroll
-  for (int j = 0; j < kTopkElems; ++j) {
-    if (base + j < count) {
-      const uint32_t key = mag_key(v[j]);
-      gt += key > T;
-      eq += key == T;
-    }
-  }
-  // the block's keys above T and equal to T before this thread's run
-  const uint32_t ex = block_exclusive_scan(gt | (eq << 16), nullptr);
-  uint32_t eq_rank = eq_before[blockIdx.x] + (ex >> 16);
-  const uint32_t eq_in_block_before = ex >> 16;
-  const uint32_t eq_block_before = eq_before[blockIdx.x];
-  // kept before this thread in the block: all keys above T, plus the keys
-  // equal to T whose rank among all equal keys is below `need`
-  const uint32_t eq_kept_before =
-      need > eq_block_before ? min(eq_in_block_before, need - eq_block_before) : 0u;
-  uint32_t pos = out_off[blockIdx.x] + (ex & 0xFFFFu) + eq_kept_before;
-  if (gt == 0 && eq == 0) return;
+  const uint32_t mine = run_counts(v, base, count, T);
+  const uint32_t ex = block_exclusive_scan(mine, nullptr);
+  if (mine == 0) return;
+  // kept before this run: every key above T in earlier runs of the block, and
+  // the keys equal to T whose rank among all equal keys is below `need`
+  const uint32_t eq_block = w.eq_before[blockIdx.x];
+  const uint32_t eq_in_block = ex >> 16;
+  const uint32_t eq_kept = need > eq_block ? min(eq_in_block, need - eq_block) : 0u;
+  uint32_t pos = w.out_off[blockIdx.x] + (ex & 0xFFFFu) + eq_kept;
+  uint32_t eq_rank = eq_block + eq_in_block;
 #pragma unroll
   for (int j = 0; j < kTopkElems; ++j) {
     const uint64_t i = base + j;
@@ -307,47 +409,31 @@ __global__ void __launch_bounds__(kThreads) k_sparse_scatter(const __grid_consta
   }
 }
 
-}  // namespace
-
-size_t topk_workspace_bytes(uint64_t count) {
-  const uint64_t nb = (count + kTopkBlock - 1) / kTopkBlock;
-  const uint64_t words = 2048 + 16 + 4 * nb;
-  return (size_t)((words * 4 + 255) / 256 * 256);
+template <bool VEC>
+cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
+  const dim3 one(1, a.nranks);
+  k_topk_init<<<one, kThreads, 0, s>>>(a);
+  // histogram passes: a resident grid looping over the data, so that each
+  // block flushes its shared histogram once
+  const uint64_t items = VEC ? (a.count + 3) / 4 : a.count;
+  unsigned per_rank = (unsigned)(kSms * kHistBlocksPerSm / a.nranks);
+  if (per_rank < 1) per_rank = 1;
+  const unsigned hx = grid_for(items) < per_rank ? grid_for(items) : per_rank;
+  const dim3 hgrid(hx, a.nranks);
+  k_topk_pass1<VEC><<<hgrid, kThreads, 0, s>>>(a);
+  if (a.k == 0) return cudaGetLastError();  // nothing kept: e = a
+  k_topk_pass<VEC><<<hgrid, kThreads, 0, s>>>(a, 10, 1);
+  k_topk_pass<VEC><<<hgrid, kThreads, 0, s>>>(a, 0, 2);
+  const dim3 bgrid((unsigned)a.nb, a.nranks);
+  k_topk_count<VEC><<<bgrid, kThreads, 0, s>>>(a);
+  k_topk_emit<VEC><<<bgrid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* grad, float* residual, uint64_t count, uint64_t k, uint32_t* idx, float* val,
-                        void* ws, cudaStream_t s) {
-  uint32_t* hist = static_cast<uint32_t*>(ws);
-  TopkState* st = reinterpret_cast<TopkState*>(hist + 2048);
-  const uint64_t nb = (count + kTopkBlock - 1) / kTopkBlock;
-  uint32_t* n_gt = hist + 2048 + 16;
-  uint32_t* n_eq = n_gt + nb;
-  uint32_t* eq_before = n_eq + nb;
-  uint32_t* out_off = eq_before + nb;
-  const bool vec = (reinterpret_cast<uintptr_t>(grad) % 16 == 0) && (reinterpret_cast<uintptr_t>(residual) % 16 == 0);
-  // histogram kernels: a resident grid looping over the data, so that each
-  // block's shared histogram is flushed once
-  const uint64_t items = vec ? (count + 3) / 4 : count;
-  const unsigned cap = kSms * kHistBlocksPerSm;
-  const unsigned hgrid = grid_for(items) < cap ? grid_for(items) : cap;
-  cudaError_t e = cudaMemsetAsync(hist, 0, 2048 * sizeof(uint32_t), s);
-  if (e != cudaSuccess) return e;
-  k_topk_init<<<1, 32, 0, s>>>(st, (uint32_t)k);
-  if (vec) k_topk_add_hist<true><<<hgrid, kThreads, 0, s>>>(grad, residual, count, hist);
-  else k_topk_add_hist<false><<<hgrid, kThreads, 0, s>>>(grad, residual, count, hist);
-  if (k == 0) return cudaGetLastError();  // nothing kept: e = a
-  k_topk_find<<<1, 32, 0, s>>>(hist, 2048, 20, st);
-  for (int shift = 10; shift >= 0; shift -= 10) {
-    if (vec) k_topk_hist<true><<<hgrid, kThreads, 0, s>>>(residual, count, st, shift, hist);
-    else k_topk_hist<false><<<hgrid, kThreads, 0, s>>>(residual, count, st, shift, hist);
-    k_topk_find<<<1, 32, 0, s>>>(hist, 1024, shift, st);
-  }
-  if (vec) k_topk_count<true><<<(unsigned)nb, kThreads, 0, s>>>(residual, count, st, n_gt, n_eq);
-  else k_topk_count<false><<<(unsigned)nb, kThreads, 0, s>>>(residual, count, st, n_gt, n_eq);
-  k_topk_scan<<<1, kThreads, 0, s>>>(n_gt, n_eq, (uint32_t)nb, st, eq_before, out_off);
-  if (vec) k_topk_emit<true><<<(unsigned)nb, kThreads, 0, s>>>(residual, count, st, eq_before, out_off, idx, val);
-  else k_topk_emit<false><<<(unsigned)nb, kThreads, 0, s>>>(residual, count, st, eq_before, out_off, idx, val);
-  return cudaGetLastError();
+}  // namespace
+
+cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream) {
+  return vec ? launch_topk_t<true>(a, stream) : launch_topk_t<false>(a, stream);
 }
 
 cudaError_t launch_sparse_scatter(const ScatterArgs& a, cudaStream_t stream) {
@@ -373,42 +459,74 @@ ar_status_t tk_ok() {
   return AR_SUCCESS;
 }
 uintptr_t tk_addr(const void* p) { return reinterpret_cast<uintptr_t>(p); }
-bool tk_overlap(const void* a, size_t na, const void* b, size_t nb) {
-  return na && nb && tk_addr(a) < tk_addr(b) + nb && tk_addr(b) < tk_addr(a) + na;
+
+struct Rng {
+  uintptr_t lo, hi;
+};
+// true if any two of the ranges overlap
+bool any_overlap(std::vector<Rng> v) {
+  std::vector<Rng> s;
+  for (const Rng& x : v)
+    if (x.hi > x.lo) s.push_back(x);
+  std::sort(s.begin(), s.end(), [](const Rng& a, const Rng& b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < s.size(); ++i)
+    if (s[i].lo < s[i - 1].hi) return true;
+  return false;
 }
 
 }  // namespace
 
 extern "C" {
 
-size_t ar_topk_workspace_bytes(size_t count) {
-  if (count > 0xFFFFFFFFull) return 0;
-  return gar::topk_workspace_bytes(count);
+size_t ar_topk_workspace_bytes(int nranks, size_t count) {
+  if (nranks < 1 || nranks > AR_MAX_RANKS || count > 0xFFFFFFFFull) return 0;
+  return (size_t)nranks * gar::topk_rank_words(count) * 4;
 }
 
-ar_status_t ar_topk_compress(const float* grad, float* residual, size_t count, size_t k, uint32_t* idx, float* val,
-                             void* workspace, size_t ws_bytes, ar_stream_t stream) {
+ar_status_t ar_topk_compress(const float* const* grads, float* const* residuals, int nranks, size_t count, size_t k,
+                             uint32_t* const* idx, float* const* val, void* workspace, size_t ws_bytes,
+                             ar_stream_t stream) {
+  if (!grads || !residuals || !idx || !val) return tk_fail(AR_ERR_INVALID_ARGUMENT, "null buffer array");
+  if (nranks < 1 || nranks > AR_MAX_RANKS) return tk_fail(AR_ERR_INVALID_ARGUMENT, "nranks must be in 1..64");
   if (count > 0xFFFFFFFFull) return tk_fail(AR_ERR_INVALID_ARGUMENT, "count must fit 32-bit indices");
   if (k > count) return tk_fail(AR_ERR_INVALID_ARGUMENT, "k exceeds count");
   if (count == 0) return tk_ok();
-  if (!grad || !residual || !workspace || (k > 0 && (!idx || !val)))
-    return tk_fail(AR_ERR_INVALID_ARGUMENT, "null pointer");
-  if (tk_addr(grad) % 4 || tk_addr(residual) % 4 || tk_addr(idx) % 4 || tk_addr(val) % 4)
-    return tk_fail(AR_ERR_INVALID_ARGUMENT, "buffer not aligned to its element size");
+  const size_t need = ar_topk_workspace_bytes(nranks, count);
+  if (!workspace) return tk_fail(AR_ERR_INVALID_ARGUMENT, "null workspace");
   if (tk_addr(workspace) % 16) return tk_fail(AR_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
-  const size_t need = gar::topk_workspace_bytes(count);
   if (ws_bytes < need) return tk_fail(AR_ERR_INVALID_ARGUMENT, "workspace too small");
   const size_t b = count * 4, kb = k * 4;
-  // grad is read only; residual, idx, val and the workspace are written
-  const void* outs[4] = {residual, idx, val, workspace};
-  const size_t out_bytes[4] = {b, kb, kb, need};
-  for (int i = 0; i < 4; ++i) {
-    if (tk_overlap(grad, b, outs[i], out_bytes[i])) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
-    for (int j = i + 1; j < 4; ++j)
-      if (tk_overlap(outs[i], out_bytes[i], outs[j], out_bytes[j])) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
+  std::vector<Rng> outs = {{tk_addr(workspace), tk_addr(workspace) + need}};
+  gar::TopkArgs a{};
+  bool vec = true;
+  for (int r = 0; r < nranks; ++r) {
+    if (!grads[r] || !residuals[r] || (k > 0 && (!idx[r] || !val[r])))
+      return tk_fail(AR_ERR_INVALID_ARGUMENT, "null buffer of rank " + std::to_string(r));
+    if (tk_addr(grads[r]) % 4 || tk_addr(residuals[r]) % 4 || tk_addr(idx[r]) % 4 || tk_addr(val[r]) % 4)
+      return tk_fail(AR_ERR_INVALID_ARGUMENT, "buffer not aligned to its element size");
+    vec = vec && tk_addr(grads[r]) % 16 == 0 && tk_addr(residuals[r]) % 16 == 0;
+    outs.push_back({tk_addr(residuals[r]), tk_addr(residuals[r]) + b});
+    outs.push_back({tk_addr(idx[r]), tk_addr(idx[r]) + kb});
+    outs.push_back({tk_addr(val[r]), tk_addr(val[r]) + kb});
+    a.g[r] = grads[r];
+    a.e[r] = residuals[r];
+    a.idx[r] = idx[r];
+    a.val[r] = val[r];
   }
-  const cudaError_t e = gar::launch_topk(grad, residual, count, k, idx, val, workspace,
-                                         reinterpret_cast<cudaStream_t>(stream));
+  // outputs are disjoint from each other and from every input (inputs may overlap each other)
+  if (any_overlap(outs)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
+  for (int r = 0; r < nranks; ++r) {
+    std::vector<Rng> v = outs;
+    v.push_back({tk_addr(grads[r]), tk_addr(grads[r]) + b});
+    if (any_overlap(v)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
+  }
+  a.ws = static_cast<uint32_t*>(workspace);
+  a.ws_words = gar::topk_rank_words(count);
+  a.count = count;
+  a.nb = gar::topk_blocks(count);
+  a.k = (uint32_t)k;
+  a.nranks = nranks;
+  const cudaError_t e = gar::launch_topk(a, vec, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("top-k launch: ") + cudaGetErrorString(e));
   return tk_ok();
 }
@@ -428,17 +546,14 @@ ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* 
   gar::ScatterArgs a{};
   a.nranks = nranks;
   a.count = count;
+  std::vector<Rng> outs;
   for (int r = 0; r < nranks; ++r) {
     if (nnz[r] > count) return tk_fail(AR_ERR_INVALID_ARGUMENT, "nnz exceeds count");
     if (!recvbufs[r] || (nnz[r] > 0 && (!idx[r] || !val[r])))
       return tk_fail(AR_ERR_INVALID_ARGUMENT, "null buffer of rank " + std::to_string(r));
     if (tk_addr(recvbufs[r]) % 4 || tk_addr(idx[r]) % 4 || tk_addr(val[r]) % 4)
       return tk_fail(AR_ERR_INVALID_ARGUMENT, "buffer not aligned to its element size");
-    for (int q = 0; q < nranks; ++q) {
-      if (q != r && tk_overlap(recvbufs[r], b, recvbufs[q], b)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
-      if (tk_overlap(recvbufs[r], b, idx[q], nnz[q] * 4) || tk_overlap(recvbufs[r], b, val[q], nnz[q] * 4))
-        return tk_fail(AR_ERR_ALIAS, "buffers overlap");
-    }
+    outs.push_back({tk_addr(recvbufs[r]), tk_addr(recvbufs[r]) + b});
     a.idx[r] = idx[r];
     a.val[r] = val[r];
     a.dst[r] = recvbufs[r];
@@ -447,6 +562,14 @@ ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* 
     tiles += (nnz[r] + gar::kThreads - 1) / gar::kThreads;
   }
   a.tile_start[nranks] = (uint32_t)tiles;
+  if (any_overlap(outs)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
+  for (int r = 0; r < nranks; ++r) {
+    std::vector<Rng> v = outs;
+    v.push_back({tk_addr(idx[r]), tk_addr(idx[r]) + nnz[r] * 4});
+    if (any_overlap(v)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
+    v.back() = {tk_addr(val[r]), tk_addr(val[r]) + nnz[r] * 4};
+    if (any_overlap(v)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   for (int r = 0; r < nranks; ++r) {
     const cudaError_t e = cudaMemsetAsync(recvbufs[r], 0, b, s);

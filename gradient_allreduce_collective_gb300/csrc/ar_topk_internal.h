@@ -10,18 +10,51 @@
 
 namespace gar {
 
-// Radix-select state, kept on the device between the passes. The key of a
-// value is the bit pattern of its magnitude (sign bit cleared), which orders
-// like the magnitude for every non-NaN binary32 value.
+// Elements per block of the count and emit kernels.
+constexpr int kTopkElems = 16;                     // per thread
+constexpr int kTopkBlock = kThreads * kTopkElems;  // per block
+
+// Per-rank workspace, in 32-bit words (a multiple of 64 words, 256 bytes):
+//   [0, 2048)        histogram of the current radix pass
+//   [2048, 2064)     TopkState
+//   then nb words each of n_gt, n_eq, eq_before, out_off (nb = count blocks)
+constexpr int kTopkHistWords = 2048;
+constexpr int kTopkStateWords = 16;
+inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
+inline uint64_t topk_rank_words(uint64_t count) {
+  return (kTopkHistWords + kTopkStateWords + 4 * topk_blocks(count) + 63) / 64 * 64;
+}
+
+// Radix-select state of one rank, kept on the device between the passes. The
+// key of a value is the bit pattern of its magnitude (sign bit cleared),
+// which orders like the magnitude for every non-NaN binary32 value.
 //   prefix/mask: the key bits fixed so far (after the last pass: the key T of
 //                the k-th largest magnitude)
 //   need:        how many keys equal to the prefix still have to be kept
 //   gt:          keys strictly above the prefix (all kept)
+//   ticket[p]:   blocks of pass p that have finished (the last one to finish
+//                carries out the pass's single-block step)
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
   uint32_t need;
   uint32_t gt;
+  uint32_t ticket[4];
+};
+
+// Every rank's buffers for one Top-K call; rank r's workspace starts at
+// ws + r * ws_words.
+struct TopkArgs {
+  const float* g[kMaxRanks];
+  float* e[kMaxRanks];
+  uint32_t* idx[kMaxRanks];
+  float* val[kMaxRanks];
+  uint32_t* ws;
+  uint64_t ws_words;
+  uint64_t count;
+  uint64_t nb;
+  uint32_t k;
+  int nranks;
 };
 
 // Scatter of every rank's (index, value) pairs into its zeroed dense buffer;
@@ -36,12 +69,10 @@ struct ScatterArgs {
   int nranks;
 };
 
-// Workspace bytes for launch_topk over `count` values (a multiple of 256).
-size_t topk_workspace_bytes(uint64_t count);
-// a = grad + residual into residual; (idx, val) = the k largest |a| in index
-// order (ties: lower index first); residual = a with those entries zeroed.
-cudaError_t launch_topk(const float* grad, float* residual, uint64_t count, uint64_t k, uint32_t* idx, float* val,
-                        void* ws, cudaStream_t stream);
+// For every rank: a = g + e into e; (idx, val) = the k largest |a| in index
+// order (ties: lower index first); e = a with those entries zeroed. `vec`:
+// every g and e is 16-byte aligned.
+cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream);
 cudaError_t launch_sparse_scatter(const ScatterArgs& a, cudaStream_t stream);
 
 }  // namespace gar

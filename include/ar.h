@@ -292,32 +292,37 @@ ar_status_t ar_allreduce_fp8_noalloc(const void *const *sendbufs, void *const *r
 /* Top-K gradient sparsification with error feedback ([GL] §勾配圧縮技術: only
  * the largest K% of the gradient is communicated and error feedback makes up
  * for what is dropped; [WP] §优化技术: top-k sends the indices as well). The
- * pages fix no formula or tie rule; this library's reading, per rank:
- *   a = grad + residual            (binary32 add, round to nearest even)
+ * pages fix no formula or tie rule; this library's reading, per rank r:
+ *   a = grads[r] + residuals[r]    (binary32 add, round to nearest even)
  *   keep the k entries of largest |a|; among equal |a| the lower index first
- *   idx[0..k), val[0..k) = the kept (index, a[index]) in ascending index order
- *   residual = a with the kept entries set to +0
+ *   idx[r][0..k), val[r][0..k) = the kept (index, a[index]) in ascending
+ *                                 index order
+ *   residuals[r] = a with the kept entries set to +0
  * so the dense form of (idx, val) plus the new residual equals a exactly.
  * |a| is compared through its bit pattern with the sign cleared (so -0 ties
  * +0, and a NaN ranks above every number).
  *
- * Workspace bytes for ar_topk_compress over `count` values (a multiple of
- * 256; about count / 1024 words plus 8 KiB); 0 if count >= 2^32. */
-size_t ar_topk_workspace_bytes(size_t count);
+ * Workspace bytes for ar_topk_compress over nranks x `count` values (per
+ * rank about count / 1024 words plus 8 KiB, a multiple of 256 bytes); 0 if
+ * nranks is outside 1..AR_MAX_RANKS or count >= 2^32. */
+size_t ar_topk_workspace_bytes(int nranks, size_t count);
 
-/* One rank's Top-K step on `stream`: reads grad[count], updates
- * residual[count] in place and writes idx[k] (uint32 indices) and val[k].
- *   grad, residual: F32 device buffers, 4-byte aligned (16-byte aligned ones
- *     take the vector path; results are identical either way).
- *   workspace: device memory of at least ar_topk_workspace_bytes(count),
- *     16-byte aligned, owned by the caller; its contents need no
+/* Every rank's Top-K step in one call on `stream` (six kernel launches
+ * whatever nranks is): reads grads[r][count], updates residuals[r][count] in
+ * place and writes idx[r][k] (uint32 indices) and val[r][k].
+ *   grads[r], residuals[r]: F32 device buffers, 4-byte aligned (when all are
+ *     16-byte aligned the vector path runs; results are identical either way).
+ *   workspace: device memory of at least ar_topk_workspace_bytes(nranks,
+ *     count), 16-byte aligned, owned by the caller; its contents need no
  *     initialisation and are meaningless afterwards.
  *   Errors: AR_ERR_INVALID_ARGUMENT for k > count, count >= 2^32, a null or
- *   misaligned pointer or a short workspace; AR_ERR_ALIAS if grad, residual,
- *   idx, val or the workspace overlap. k == 0 only folds grad into residual;
+ *   misaligned pointer or a short workspace; AR_ERR_ALIAS if an output
+ *   (residual, idx, val, workspace) overlaps another output or an input
+ *   (inputs may overlap each other). k == 0 only folds grads into residuals;
  *   count == 0 is a no-op. */
-ar_status_t ar_topk_compress(const float *grad, float *residual, size_t count, size_t k, uint32_t *idx, float *val,
-                             void *workspace, size_t ws_bytes, ar_stream_t stream);
+ar_status_t ar_topk_compress(const float *const *grads, float *const *residuals, int nranks, size_t count,
+                             size_t k, uint32_t *const *idx, float *const *val, void *workspace, size_t ws_bytes,
+                             ar_stream_t stream);
 
 /* Allreduce of sparse vectors ([GL] §勾配圧縮技術): rank r contributes the
  * dense vector of length `count` that is zero except at idx[r][j] where it

@@ -177,23 +177,31 @@ def test_bucket_allreduce_argument_errors(L):
 
 
 def test_topk_workspace_and_argument_errors(L):
-    count = 100_000
-    need = gar.ar_topk_workspace_bytes(count)
+    n, count = 3, 100_000
+    need = gar.ar_topk_workspace_bytes(n, count)
     nb = math.ceil(count / 4096)
-    assert need == math.ceil((2048 + 16 + 4 * nb) * 4 / 256) * 256
-    assert gar.ar_topk_workspace_bytes(1 << 32) == 0
-    g, e, i, v, ws = 0x1000000, 0x2000000, 0x3000000, 0x4000000, 0x5000000
-    f = L.ar_topk_compress
-    assert f(g, e, count, count + 1, i, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT  # k > count
-    assert f(g, e, 1 << 32, 10, i, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT
-    assert f(g, e, count, 10, i, v, ws, need - 1, None) == gar.AR_ERR_INVALID_ARGUMENT
-    assert f(g, e, count, 10, i, v, ws + 8, need, None) == gar.AR_ERR_INVALID_ARGUMENT
-    assert f(g, e + 2, count, 10, i, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT
-    assert f(g, e, count, 10, None, v, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT
-    assert f(g, g + 4 * 50, count, 10, i, v, ws, need, None) == gar.AR_ERR_ALIAS       # residual inside grad
-    assert f(g, e, count, 10, i, i + 8, ws, need, None) == gar.AR_ERR_ALIAS            # idx and val overlap
-    assert f(g, e, count, 10, i, v, e + 64, need, None) == gar.AR_ERR_ALIAS            # workspace inside residual
-    assert f(g, e, 0, 0, None, None, None, 0, None) == gar.AR_SUCCESS                  # empty
+    assert need == n * math.ceil((2048 + 16 + 4 * nb) / 64) * 64 * 4
+    assert gar.ar_topk_workspace_bytes(1, 1 << 32) == 0 and gar.ar_topk_workspace_bytes(0, 10) == 0
+    g = [0x1000000 * (r + 1) for r in range(n)]
+    e = [0x10000000 + 0x1000000 * r for r in range(n)]
+    i = [0x20000000 + 0x1000000 * r for r in range(n)]
+    v = [0x30000000 + 0x1000000 * r for r in range(n)]
+    ws = 0x40000000
+
+    def f(g=g, e=e, count=count, k=10, i=i, v=v, ws=ws, wsb=need, n=n):
+        return L.ar_topk_compress(_arr(g), _arr(e), n, count, k, _arr(i), _arr(v), ws, wsb, None)
+
+    assert f(k=count + 1) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(count=1 << 32) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(wsb=need - 1) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(ws=ws + 8) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(e=[e[0] + 2] + e[1:]) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(i=[None] + i[1:]) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(n=0) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(e=[g[1] + 200] + e[1:]) == gar.AR_ERR_ALIAS          # a residual inside another rank's grad
+    assert f(v=[i[0] + 8] + v[1:]) == gar.AR_ERR_ALIAS            # idx and val overlap
+    assert f(ws=e[2] + 64) == gar.AR_ERR_ALIAS                    # workspace inside a residual
+    assert f(count=0, k=0, ws=None, wsb=0) == gar.AR_SUCCESS      # empty
 
 
 def test_sparse_allreduce_argument_errors(L):

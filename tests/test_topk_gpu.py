@@ -40,9 +40,9 @@ def _gpu_topk(g: np.ndarray, e: np.ndarray, k: int, offset: int = 0):
     eb, ed = _dev_f32(e, offset)
     idx = torch.full((k + 8,), -1, dtype=torch.int32, device="cuda")
     val = torch.full((k + 8,), 7.0, dtype=torch.float32, device="cuda")
-    ws = torch.empty(gar.ar_topk_workspace_bytes(count), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(gar.ar_topk_workspace_bytes(1, count), 1), dtype=torch.uint8, device="cuda")
     ws.fill_(0x5A)  # the workspace needs no initialisation
-    gar.ar_topk_compress(gd, ed, k, idx, val, ws)
+    gar.ar_topk_compress([gd], [ed], k, [idx], [val], ws)
     torch.cuda.synchronize()
     i = from_dev(idx).view(np.uint32)
     v = from_dev(val)
@@ -66,7 +66,7 @@ def _check_against_oracle(g, e, k, offset=0):
 def test_topk_matches_oracle_ragged(count):
     g = synthgen.normal_f32(count, 11, 1e-3)
     e = synthgen.normal_f32(count, 12, 1e-4)
-    for k in sorted({0, 1, max(1, count // 100), count // 2, count}):
+    for k in sorted({0, min(1, count), max(min(1, count), count // 100), count // 2, count}):
         _check_against_oracle(g, e, k)
 
 
@@ -77,6 +77,34 @@ def test_topk_unaligned_buffers_take_the_element_path(offset):
     e = synthgen.normal_f32(count, 22, 0.1)
     for k in (1, 500, 25_000):
         _check_against_oracle(g, e, k, offset)
+
+
+@pytest.mark.parametrize("unaligned_rank", [None, 3])
+def test_topk_many_ranks_in_one_call(unaligned_rank):
+    # 5 ranks with different data, scales and residuals; one unaligned rank
+    # sends the whole call down the element path
+    n, count, k = 5, 70_001, 700
+    g_np = [synthgen.normal_f32(count, 500 + r, 10.0 ** -r) for r in range(n)]
+    e_np = [synthgen.normal_f32(count, 600 + r, 10.0 ** (-r - 1)) for r in range(n)]
+    keep = []
+    grads, res = [], []
+    for r in range(n):
+        off = 1 if r == unaligned_rank else 0
+        gb, gd = _dev_f32(g_np[r], off)
+        eb, ed = _dev_f32(e_np[r], off)
+        keep += [gb, eb]
+        grads.append(gd)
+        res.append(ed)
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    ws = torch.full((gar.ar_topk_workspace_bytes(n, count),), 0xC3, dtype=torch.uint8, device="cuda")
+    gar.ar_topk_compress(grads, res, k, idx, val, ws)
+    torch.cuda.synchronize()
+    for r in range(n):
+        oi, ov, oe = oracle.topk_compress(g_np[r], e_np[r], k)
+        assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), r
+        assert np.array_equal(_bits(from_dev(val[r])), _bits(ov)), r
+        assert np.array_equal(_bits(from_dev(res[r])), _bits(oe)), r
 
 
 def test_topk_heavy_ties_and_signed_zeros():
@@ -112,10 +140,10 @@ def test_error_feedback_over_several_steps():
     ed = torch.zeros(count, dtype=torch.float32, device="cuda")
     idx = torch.empty(k, dtype=torch.int32, device="cuda")
     val = torch.empty(k, dtype=torch.float32, device="cuda")
-    ws = torch.empty(gar.ar_topk_workspace_bytes(count), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(gar.ar_topk_workspace_bytes(1, count), dtype=torch.uint8, device="cuda")
     for step in range(4):
         g = synthgen.normal_f32(count, 100 + step, 1e-3)
-        gar.ar_topk_compress(to_dev(g, "f32"), ed, k, idx, val, ws)
+        gar.ar_topk_compress([to_dev(g, "f32")], [ed], k, [idx], [val], ws)
         oi, ov, e_host = oracle.topk_compress(g, e_host, k)
         torch.cuda.synchronize()
         assert np.array_equal(from_dev(idx).view(np.uint32), oi)
@@ -180,9 +208,8 @@ def test_topk_full_size_eight_ranks():
     res = [to_dev(x, "f32") for x in e_np]
     idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
     val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
-    ws = torch.empty(gar.ar_topk_workspace_bytes(count), dtype=torch.uint8, device="cuda")
-    for r in range(n):
-        gar.ar_topk_compress(grads[r], res[r], k, idx[r], val[r], ws)
+    ws = torch.empty(gar.ar_topk_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    gar.ar_topk_compress(grads, res, k, idx, val, ws)
     torch.cuda.synchronize()
     o_idx, o_val = [], []
     for r in range(n):
