@@ -46,6 +46,7 @@ struct RankWs {
   uint32_t* n_eq;
   uint32_t* eq_before;
   uint32_t* out_off;
+  uint32_t* masks;
 };
 
 __device__ __forceinline__ RankWs rank_ws(const TopkArgs& A, int r) {
@@ -57,6 +58,7 @@ __device__ __forceinline__ RankWs rank_ws(const TopkArgs& A, int r) {
   w.n_eq = w.n_gt + A.nb;
   w.eq_before = w.n_eq + A.nb;
   w.out_off = w.eq_before + A.nb;
+  w.masks = w.out_off + A.nb;
   return w;
 }
 
@@ -281,19 +283,25 @@ __device__ __forceinline__ void load_run(const float* __restrict__ a, uint64_t b
   }
 }
 
-// keys above T (low 16 bits) and equal to T (high 16 bits) in a run
-__device__ __forceinline__ uint32_t run_counts(const float (&v)[kTopkElems], uint64_t base, uint64_t count,
-                                               uint32_t T) {
-  uint32_t gt = 0, eq = 0;
+// run mask: bit j set if value j's key is above T, bit 16 + j if it equals T
+__device__ __forceinline__ uint32_t run_mask(const float (&v)[kTopkElems], uint64_t base, uint64_t count,
+                                             uint32_t T) {
+  static_assert(kTopkElems == 16, "one 32-bit mask word per run");
+  uint32_t m = 0;
 #pragma unroll
   for (int j = 0; j < kTopkElems; ++j) {
     if (base + j < count) {
       const uint32_t key = mag_key(v[j]);
-      gt += key > T;
-      eq += key == T;
+      m |= (key > T ? 1u : 0u) << j;
+      m |= (key == T ? 1u : 0u) << (16 + j);
     }
   }
-  return gt | (eq << 16);
+  return m;
+}
+
+// keys above T (low 16 bits) and equal to T (high 16 bits) of a run mask
+__device__ __forceinline__ uint32_t mask_counts(uint32_t m) {
+  return (uint32_t)__popc(m & 0xFFFFu) | ((uint32_t)__popc(m >> 16) << 16);
 }
 
 // The count pass's last block: eq_before[b] = keys equal to T in earlier
@@ -330,8 +338,8 @@ __device__ void scan_blocks(const RankWs& w, uint64_t nb) {
   }
 }
 
-// per kTopkBlock-element block: keys above T and equal to T; the last block
-// scans the counts of all blocks
+// per kTopkBlock-element block: the run masks, and the keys above T and
+// equal to T; the last block scans the counts of all blocks
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
   const int r = blockIdx.y;
@@ -340,8 +348,10 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__
   const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)threadIdx.x * kTopkElems;
   float v[kTopkElems];
   load_run<VEC>(A.e[r], base, A.count, v);
+  const uint32_t m = run_mask(v, base, A.count, T);
+  w.masks[(uint64_t)blockIdx.x * kThreads + threadIdx.x] = m;
   uint32_t tot;
-  block_exclusive_scan(run_counts(v, base, A.count, T), &tot);  // no field overflows: <= 4096 each
+  block_exclusive_scan(mask_counts(m), &tot);  // no field overflows: <= 4096 each
   if (threadIdx.x == 0) {
     w.n_gt[blockIdx.x] = tot & 0xFFFFu;
     w.n_eq[blockIdx.x] = tot >> 16;
@@ -349,22 +359,19 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__
   if (last_block(&w.st->ticket[3])) scan_blocks(w, A.nb);
 }
 
-// Kept elements to (index, value) in index order; zero their residual.
-template <bool VEC>
+// Kept elements to (index, value) in index order; zero their residual. Only
+// the run masks are read in full; values are read where a key is kept.
 __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
+  const uint32_t m = w.masks[(uint64_t)blockIdx.x * kThreads + threadIdx.x];
+  const uint32_t ex = block_exclusive_scan(mask_counts(m), nullptr);
+  if (m == 0) return;
   float* __restrict__ a = A.e[r];
   uint32_t* __restrict__ idx = A.idx[r];
   float* __restrict__ val = A.val[r];
-  const uint64_t count = A.count;
-  const uint32_t T = w.st->prefix, need = w.st->need;
+  const uint32_t need = w.st->need;
   const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)threadIdx.x * kTopkElems;
-  float v[kTopkElems];
-  load_run<VEC>(a, base, count, v);
-  const uint32_t mine = run_counts(v, base, count, T);
-  const uint32_t ex = block_exclusive_scan(mine, nullptr);
-  if (mine == 0) return;
   // kept before this run: every key above T in earlier runs of the block, and
   // the keys equal to T whose rank among all equal keys is below `need`
   const uint32_t eq_block = w.eq_before[blockIdx.x];
@@ -374,17 +381,15 @@ __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ 
   uint32_t eq_rank = eq_block + eq_in_block;
 #pragma unroll
   for (int j = 0; j < kTopkElems; ++j) {
-    const uint64_t i = base + j;
-    if (i >= count) continue;
-    const uint32_t key = mag_key(v[j]);
-    bool keep = key > T;
-    if (key == T) {
+    bool keep = (m >> j) & 1u;
+    if ((m >> (16 + j)) & 1u) {
       keep = eq_rank < need;
       ++eq_rank;
     }
     if (keep) {
+      const uint64_t i = base + j;
       idx[pos] = (uint32_t)i;
-      val[pos] = v[j];
+      val[pos] = a[i];
       a[i] = 0.0f;
       ++pos;
     }
@@ -426,7 +431,7 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   k_topk_pass<VEC><<<hgrid, kThreads, 0, s>>>(a, 0, 2);
   const dim3 bgrid((unsigned)a.nb, a.nranks);
   k_topk_count<VEC><<<bgrid, kThreads, 0, s>>>(a);
-  k_topk_emit<VEC><<<bgrid, kThreads, 0, s>>>(a);
+  k_topk_emit<<<bgrid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -303,7 +303,7 @@ ar_status_t ar_allreduce_fp8_noalloc(const void *const *sendbufs, void *const *r
  * +0, and a NaN ranks above every number).
  *
  * Workspace bytes for ar_topk_compress over nranks x `count` values (per
- * rank about count / 1024 words plus 8 KiB, a multiple of 256 bytes); 0 if
+ * rank about count / 4 bytes plus 8 KiB, a multiple of 256 bytes); 0 if
  * nranks is outside 1..AR_MAX_RANKS or count >= 2^32. */
 size_t ar_topk_workspace_bytes(int nranks, size_t count);
 
