@@ -15,13 +15,16 @@ N(0, 1e-3), op = avg), one fused ring-order pass per step. Inputs are
           their own streams with two device buffer sets, so one step's
           download overlaps the next step's upload.
   rows:   the other hot-path rows on their own workloads: the GPT-2-small
-          DDP bucket sync (flatten -> allreduce -> unflatten, bf16, 8 ranks)
-          and the FP8-compressed allreduce (16 x 134,217,728 bf16).
+          DDP bucket sync (flatten -> allreduce -> unflatten, bf16, 8 ranks),
+          the FP8-compressed allreduce (16 x 134,217,728 bf16) and Top-K
+          sparsification with error feedback + the sparse allreduce (the
+          bucket's 8 x 6,553,600 f32, k = 1%).
   cpu_baseline: the CPU oracle (literal ring simulator, one thread) on the
           same bucket, a bounded number of repetitions.
 
 `--workload sweep` prints one line per message size (8 ranks, 4 KiB..1 GiB
 per rank, fp32 sum; ring, tree and fused; warm and cold L2).
+`--workload fp8` and `--workload topk` print only that row.
 `--impl reference` times the oracle alone on the bucket (rank 0 only).
 Under torchrun each GPU runs its own full workload (weak scaling: the
 virtual ranks already live on one device, so there is no exchange between
@@ -550,6 +553,81 @@ def measure_fp8(gar, steps: int, warmup: int, count: int = 134_217_728, with_ora
     }
 
 
+def measure_topk(gar, steps: int, warmup: int, count: int = COUNT, frac: float = 0.01,
+                 with_oracle: bool = False) -> dict:
+    """Top-K sparsification with error feedback on 8 ranks x `count` f32
+    (k = frac * count per rank, the residual carried from step to step), then
+    the allreduce (avg) of the sparse vectors."""
+    import torch
+    import synthgen
+
+    n = NRANKS
+    k = int(count * frac)
+    grads = [torch.from_numpy(a).cuda() for a in synthgen.ranks_normal(n, count, 1e-3, base_seed=0)]
+    res = [torch.zeros(count, device="cuda") for _ in range(n)]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    out = [torch.empty(count, device="cuda") for _ in range(n)]
+    ws = torch.empty(gar.ar_topk_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def compress():
+        gar.ar_topk_compress(grads, res, k, idx, val, ws, stream)
+
+    def sparse_ar():
+        gar.ar_sparse_allreduce(idx, val, [k] * n, out, "avg", "fused", stream)
+
+    def step():
+        compress()
+        sparse_ar()
+
+    for _ in range(warmup):
+        step()
+    ms = time_steps(step, steps, stream)
+    ms_c = time_steps(compress, steps, stream)
+    ms_s = time_steps(sparse_ar, steps, stream)
+    M = count * 4
+    min_c = n * 3 * M + n * k * 8          # read g and e, write e; the pairs
+    struct_c = n * (3 * M + 3 * M + M // 4 + M // 4) + n * k * 8  # + passes 2, 3, count; masks out and in
+    sparse_b = n * M + 2 * n * M + n * k * 8  # zero outputs, fused allreduce in place, the pairs
+    peak, _ = hbm_peak()
+    del grads, res, idx, val, out, ws
+    torch.cuda.empty_cache()
+    cpu = None
+    if with_oracle:
+        import numpy as np
+        import oracle
+        samp_g = synthgen.ranks_normal(n, 1 << 20, 1e-3, base_seed=0)
+        zero = np.zeros(1 << 20, dtype=np.float32)
+
+        def oracle_step(m):
+            pairs = [oracle.topk_compress(g[:m], zero[:m], max(1, int(m * frac)))[:2] for g in samp_g]
+            oracle.sparse_ring_allreduce([p[0] for p in pairs], [p[1] for p in pairs], m, "avg")
+
+        o = oracle_row_timing(oracle_step, 1 << 20)
+        t_all = o["seconds_per_element_per_rank"] * count
+        cpu = {"kind": "oracle", "cores": 1,
+               "sample": f"Top-K (1%) of 8 ranks then the ring allreduce of the sparse vectors, first "
+                         f"{o['sample_elements_per_rank']:,} values per rank, {o['seconds']:.2f} s; scaled to "
+                         f"{count:,}",
+               "ms_per_step_estimate": t_all * 1e3}
+    return {
+        "cpu_oracle": cpu,
+        "workload": f"Top-K sparsification with error feedback: {n} ranks x {count:,} f32 N(0,1e-3), "
+                    f"k = {k:,} ({frac:.0%}) per rank, residual carried across steps; then the allreduce (avg, "
+                    "fused ring order) of the sparse vectors",
+        "ms_per_step": ms,
+        "compress": {"ms": ms_c, "launches": 6, "min_bytes": min_c, "structure_bytes": struct_c,
+                     "hbm_gbs_min_bytes": min_c / (ms_c * 1e-3) / 1e9,
+                     "hbm_gbs_structure": struct_c / (ms_c * 1e-3) / 1e9,
+                     "frac_hbm_structure": struct_c / (ms_c * 1e-3) / 1e9 / peak},
+        "sparse_allreduce": {"ms": ms_s, "launches": n + 2, "bytes": sparse_b,
+                             "hbm_gbs": sparse_b / (ms_s * 1e-3) / 1e9,
+                             "frac_hbm": sparse_b / (ms_s * 1e-3) / 1e9 / peak},
+        "wire_bytes_per_rank": {"dense_f32": M, "sparse_pairs": k * 8, "ratio": M / (k * 8)},
+    }
+
+
 # ----------------------------------------------------------------- GPU arm: headline
 
 
@@ -665,6 +743,8 @@ def run_ours(args):
                                               with_oracle=timed_cpu)
         rows["fp8_allreduce"] = measure_fp8(gar, steps=max(5, min(args.steps, 20)), warmup=3,
                                             with_oracle=timed_cpu)
+        rows["topk_sparse_allreduce"] = measure_topk(gar, steps=max(5, min(args.steps, 50)), warmup=3,
+                                                     with_oracle=timed_cpu)
 
     peak, peak_src = hbm_peak()
     alg_bytes = 2 * NRANKS * M
@@ -809,12 +889,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("bucket", "sweep", "fp8"), default="bucket")
+    ap.add_argument("--workload", choices=("bucket", "sweep", "fp8", "topk"), default="bucket")
     ap.add_argument("--fp8-count", type=int, default=134_217_728, help="elements per rank for --workload fp8")
     ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--headline-only", action="store_true", help="skip the DDP and FP8 rows")
+    ap.add_argument("--headline-only", action="store_true", help="skip the DDP, FP8 and Top-K rows")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -830,6 +910,15 @@ def main(argv=None):
         gar.build()
         gar.lib()
         print(json.dumps(measure_fp8(gar, args.steps, args.warmup, args.fp8_count)))
+        return 0
+    if args.workload == "topk":
+        import torch
+
+        import gradient_allreduce_collective_gb300 as gar
+        torch.cuda.set_device(dist_env()[2])
+        gar.build()
+        gar.lib()
+        print(json.dumps(measure_topk(gar, args.steps, args.warmup, with_oracle=not args.no_cpu_baseline)))
         return 0
     return run_ours(args)
 

@@ -338,20 +338,27 @@ __device__ void scan_blocks(const RankWs& w, uint64_t nb) {
   }
 }
 
-// per kTopkBlock-element block: the run masks, and the keys above T and
-// equal to T; the last block scans the counts of all blocks
+// per tile: the run masks, and the keys above T and equal to T; the last
+// block scans the counts of all tiles
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   const uint32_t T = w.st->prefix;
-  const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)threadIdx.x * kTopkElems;
-  float v[kTopkElems];
-  load_run<VEC>(A.e[r], base, A.count, v);
-  const uint32_t m = run_mask(v, base, A.count, T);
-  w.masks[(uint64_t)blockIdx.x * kThreads + threadIdx.x] = m;
+  const uint64_t tile = (uint64_t)blockIdx.x * kTopkBlock;
+  float v[kTopkRuns][kTopkElems];
+#pragma unroll
+  for (int u = 0; u < kTopkRuns; ++u)
+    load_run<VEC>(A.e[r], tile + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems, A.count, v[u]);
+  uint32_t c = 0;
+#pragma unroll
+  for (int u = 0; u < kTopkRuns; ++u) {
+    const uint32_t m = run_mask(v[u], tile + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems, A.count, T);
+    w.masks[(uint64_t)blockIdx.x * kThreads * kTopkRuns + u * kThreads + threadIdx.x] = m;
+    c += mask_counts(m);
+  }
   uint32_t tot;
-  block_exclusive_scan(mask_counts(m), &tot);  // no field overflows: <= 4096 each
+  block_exclusive_scan(c, &tot);  // no field overflows: at most kTopkBlock = 16384 each
   if (threadIdx.x == 0) {
     w.n_gt[blockIdx.x] = tot & 0xFFFFu;
     w.n_eq[blockIdx.x] = tot >> 16;
@@ -364,34 +371,58 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__
 __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
-  const uint32_t m = w.masks[(uint64_t)blockIdx.x * kThreads + threadIdx.x];
-  const uint32_t ex = block_exclusive_scan(mask_counts(m), nullptr);
-  if (m == 0) return;
+  uint32_t m[kTopkRuns];
+#pragma unroll
+  for (int u = 0; u < kTopkRuns; ++u)
+    m[u] = w.masks[(uint64_t)blockIdx.x * kThreads * kTopkRuns + u * kThreads + threadIdx.x];
+  const uint32_t need = w.st->need;
+  const uint32_t eq_block = w.eq_before[blockIdx.x];
+  const uint32_t off_block = w.out_off[blockIdx.x];
+  // runs in index order: all of u = 0, then u = 1, ...; ex[u] = the counts of
+  // the tile's runs before run (u, this thread)
+  uint32_t ex[kTopkRuns];
+  uint32_t carry = 0, any = 0;
+#pragma unroll
+  for (int u = 0; u < kTopkRuns; ++u) {
+    uint32_t tot;
+    ex[u] = carry + block_exclusive_scan(mask_counts(m[u]), &tot);
+    carry += tot;
+    any |= m[u];
+  }
+  if (any == 0) return;
   float* __restrict__ a = A.e[r];
   uint32_t* __restrict__ idx = A.idx[r];
   float* __restrict__ val = A.val[r];
-  const uint32_t need = w.st->need;
-  const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)threadIdx.x * kTopkElems;
-  // kept before this run: every key above T in earlier runs of the block, and
-  // the keys equal to T whose rank among all equal keys is below `need`
-  const uint32_t eq_block = w.eq_before[blockIdx.x];
-  const uint32_t eq_in_block = ex >> 16;
-  const uint32_t eq_kept = need > eq_block ? min(eq_in_block, need - eq_block) : 0u;
-  uint32_t pos = w.out_off[blockIdx.x] + (ex & 0xFFFFu) + eq_kept;
-  uint32_t eq_rank = eq_block + eq_in_block;
 #pragma unroll
-  for (int j = 0; j < kTopkElems; ++j) {
-    bool keep = (m >> j) & 1u;
-    if ((m >> (16 + j)) & 1u) {
-      keep = eq_rank < need;
-      ++eq_rank;
+  for (int u = 0; u < kTopkRuns; ++u) {
+    if (m[u] == 0) continue;
+    // kept before this run: every key above T in earlier runs of the tile,
+    // and the keys equal to T whose rank among all equal keys is below `need`
+    const uint32_t eq_in_tile = ex[u] >> 16;
+    const uint32_t eq_kept = need > eq_block ? min(eq_in_tile, need - eq_block) : 0u;
+    uint32_t pos = off_block + (ex[u] & 0xFFFFu) + eq_kept;
+    uint32_t eq_rank = eq_block + eq_in_tile;
+    uint32_t keep = m[u] & 0xFFFFu;
+#pragma unroll
+    for (int j = 0; j < kTopkElems; ++j) {
+      if ((m[u] >> (16 + j)) & 1u) {
+        if (eq_rank < need) keep |= 1u << j;
+        ++eq_rank;
+      }
     }
-    if (keep) {
-      const uint64_t i = base + j;
-      idx[pos] = (uint32_t)i;
-      val[pos] = a[i];
-      a[i] = 0.0f;
-      ++pos;
+    const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems;
+    float x[kTopkElems];
+#pragma unroll
+    for (int j = 0; j < kTopkElems; ++j)
+      if ((keep >> j) & 1u) x[j] = a[base + j];
+#pragma unroll
+    for (int j = 0; j < kTopkElems; ++j) {
+      if ((keep >> j) & 1u) {
+        idx[pos] = (uint32_t)(base + j);
+        val[pos] = x[j];
+        a[base + j] = 0.0f;
+        ++pos;
+      }
     }
   }
 }

@@ -10,22 +10,25 @@
 
 namespace gar {
 
-// Elements per block of the count and emit kernels.
-constexpr int kTopkElems = 16;                     // per thread
-constexpr int kTopkBlock = kThreads * kTopkElems;  // per block
+// Tiles of the count and emit kernels: each thread takes kTopkRuns runs of
+// kTopkElems consecutive values; run u * kThreads + t of a tile belongs to
+// thread t, so every load of a warp is contiguous.
+constexpr int kTopkElems = 16;                                 // values per run
+constexpr int kTopkRuns = 4;                                   // runs per thread
+constexpr int kTopkBlock = kThreads * kTopkRuns * kTopkElems;  // values per tile
 
 // Per-rank workspace, in 32-bit words (a multiple of 64 words, 256 bytes):
 //   [0, 2048)        histogram of the current radix pass
 //   [2048, 2064)     TopkState
-//   then nb words each of n_gt, n_eq, eq_before, out_off (nb = count blocks)
-//   then nb * kThreads words of run masks: for the kTopkElems values of one
-//   thread of the count pass, bit j (j < 16) set if value j's key is above
-//   T, bit 16 + j if it equals T
+//   then nb words each of n_gt, n_eq, eq_before, out_off (nb = tiles)
+//   then nb * kThreads * kTopkRuns words of run masks: for the kTopkElems
+//   values of a run, bit j (j < 16) set if value j's key is above T, bit
+//   16 + j if it equals T
 constexpr int kTopkHistWords = 2048;
 constexpr int kTopkStateWords = 16;
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
 inline uint64_t topk_rank_words(uint64_t count) {
-  return (kTopkHistWords + kTopkStateWords + (4 + (uint64_t)kThreads) * topk_blocks(count) + 63) / 64 * 64;
+  return (kTopkHistWords + kTopkStateWords + (4 + (uint64_t)kThreads * kTopkRuns) * topk_blocks(count) + 63) / 64 * 64;
 }
 
 // Radix-select state of one rank, kept on the device between the passes. The

@@ -179,8 +179,8 @@ def test_bucket_allreduce_argument_errors(L):
 def test_topk_workspace_and_argument_errors(L):
     n, count = 3, 100_000
     need = gar.ar_topk_workspace_bytes(n, count)
-    nb = math.ceil(count / 4096)
-    assert need == n * math.ceil((2048 + 16 + (4 + 256) * nb) / 64) * 64 * 4
+    nb = math.ceil(count / 16384)
+    assert need == n * math.ceil((2048 + 16 + (4 + 1024) * nb) / 64) * 64 * 4
     assert gar.ar_topk_workspace_bytes(1, 1 << 32) == 0 and gar.ar_topk_workspace_bytes(0, 10) == 0
     g = [0x1000000 * (r + 1) for r in range(n)]
     e = [0x10000000 + 0x1000000 * r for r in range(n)]
