@@ -77,7 +77,7 @@ def lib() -> ctypes.CDLL:
     L.ar_allreduce_fp8_noalloc.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_fused.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_hops.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
-    L.ar_topk_workspace_bytes.argtypes = [ci, sz]
+    L.ar_topk_workspace_bytes.argtypes = [ci, sz, sz]
     L.ar_topk_workspace_bytes.restype = sz
     L.ar_topk_compress.argtypes = [pp, pp, ci, sz, sz, pp, pp, vp, sz, vp]
     L.ar_sparse_allreduce.argtypes = [pp, pp, vp, ci, sz, ci, ci, pp, vp]
@@ -268,8 +268,8 @@ def ar_allreduce_fp8_noalloc(sendbufs: Sequence[torch.Tensor], recvbufs: Sequenc
                                           DTYPES[odt], OPS[op], ALGOS[algo], _stream(stream)))
 
 
-def ar_topk_workspace_bytes(nranks: int, count: int) -> int:
-    return int(lib().ar_topk_workspace_bytes(nranks, count))
+def ar_topk_workspace_bytes(nranks: int, count: int, k: int) -> int:
+    return int(lib().ar_topk_workspace_bytes(nranks, count, k))
 
 
 def _idx_ok(t: torch.Tensor, what: str) -> None:

@@ -46,7 +46,10 @@ struct RankWs {
   uint32_t* n_eq;
   uint32_t* eq_before;
   uint32_t* out_off;
+  uint32_t* n_a;
+  uint32_t* n_c;
   uint32_t* masks;
+  uint32_t* slots;
 };
 
 __device__ __forceinline__ RankWs rank_ws(const TopkArgs& A, int r) {
@@ -58,8 +61,23 @@ __device__ __forceinline__ RankWs rank_ws(const TopkArgs& A, int r) {
   w.n_eq = w.n_gt + A.nb;
   w.eq_before = w.n_eq + A.nb;
   w.out_off = w.eq_before + A.nb;
-  w.masks = w.out_off + A.nb;
+  w.n_a = w.out_off + A.nb;
+  w.n_c = w.n_a + A.nb;
+  w.masks = w.n_c + A.nb;
+  w.slots = w.masks + A.nb * kThreads * kTopkRuns;
   return w;
+}
+
+// the slots of one tile: class A indices, values, class C indices, values
+struct TileSlots {
+  uint32_t* a_idx;
+  float* a_val;
+  uint32_t* c_idx;
+  float* c_val;
+};
+__device__ __forceinline__ TileSlots tile_slots(const RankWs& w, uint64_t tile, uint32_t S) {
+  uint32_t* b = w.slots + tile * 4ull * S;
+  return {b, reinterpret_cast<float*>(b + S), b + 2 * S, reinterpret_cast<float*>(b + 3 * S)};
 }
 
 // exclusive scan over the block of one value per thread; *total = block sum
@@ -148,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ 
     w.st->need = A.k;
     w.st->gt = 0;
     for (int p = 0; p < 4; ++p) w.st->ticket[p] = 0;
+    w.st->overflow = 0;
   }
 }
 
@@ -212,57 +231,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass1(const __grid_constant__
   if (last_block(&w.st->ticket[0])) find_digit<2048>(w.hist, 20, w.st);
 }
 
-// Passes 2 and 3: histogram of the 10-bit digit at `shift` among keys whose
-// fixed bits match, then (last block) that digit.
-template <bool VEC>
-__global__ void __launch_bounds__(kThreads) k_topk_pass(const __grid_constant__ TopkArgs A, int shift, int pass) {
-  __shared__ uint32_t sh[1024];
-  const int r = blockIdx.y;
-  const RankWs w = rank_ws(A, r);
-  const float* __restrict__ a = A.e[r];
-  const uint64_t count = A.count;
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
-  __syncthreads();
-  const uint32_t mask = w.st->mask, prefix = w.st->prefix;
-  auto add = [&](float v) {
-    const uint32_t key = mag_key(v);
-    if ((key & mask) == prefix) atomicAdd(&sh[(key >> shift) & 1023u], 1u);
-  };
-  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  uint64_t done = 0;
-  if (VEC) {
-    const uint64_t n4 = count / 4;
-    const float4* a4 = reinterpret_cast<const float4*>(a);
-    uint64_t q = t0;
-    for (; q + 3 * stride < n4; q += 4 * stride) {
-      float4 x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) x[u] = a4[q + u * stride];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        add(x[u].x);
-        add(x[u].y);
-        add(x[u].z);
-        add(x[u].w);
-      }
-    }
-    for (; q < n4; q += stride) {
-      const float4 x = a4[q];
-      add(x.x);
-      add(x.y);
-      add(x.z);
-      add(x.w);
-    }
-    done = n4 * 4;
-  }
-  for (uint64_t i = done + t0; i < count; i += stride) add(a[i]);
-  __syncthreads();
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
-    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
-  if (last_block(&w.st->ticket[pass])) find_digit<1024>(w.hist, shift, w.st);
-}
-
 // kTopkElems consecutive values starting at `base` (zero past the end)
 template <bool VEC>
 __device__ __forceinline__ void load_run(const float* __restrict__ a, uint64_t base, uint64_t count,
@@ -281,6 +249,134 @@ __device__ __forceinline__ void load_run(const float* __restrict__ a, uint64_t b
 #pragma unroll
     for (int j = 0; j < kTopkElems; ++j) v[j] = base + j < count ? a[base + j] : 0.0f;
   }
+}
+
+__device__ __forceinline__ uint64_t run_base(uint64_t tile, int u) {
+  return tile * kTopkBlock + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems;
+}
+
+// Pass 2, one tile per block: the histogram of bits 19..10 of the keys in
+// the first digit's bin, and the order-preserving compaction of the tile's
+// class-A keys (bin above it: all kept) and class-C keys (in it: the
+// candidates) into the tile's slots; then (last block) the second digit.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__ TopkArgs A) {
+  __shared__ uint32_t sh[1024];
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  const uint64_t tile = blockIdx.x;
+  const uint64_t count = A.count;
+  const uint32_t S = A.slots;
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
+  const uint32_t d1 = w.st->prefix >> 20;
+  float v[kTopkRuns][kTopkElems];
+#pragma unroll
+  for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(A.e[r], run_base(tile, u), count, v[u]);
+  __syncthreads();
+  uint32_t am[kTopkRuns], cm[kTopkRuns];
+#pragma unroll
+  for (int u = 0; u < kTopkRuns; ++u) {
+    am[u] = 0;
+    cm[u] = 0;
+    const uint64_t base = run_base(tile, u);
+#pragma unroll
+    for (int j = 0; j < kTopkElems; ++j) {
+      if (base + j < count) {
+        const uint32_t key = mag_key(v[u][j]);
+        const uint32_t bin = key >> 20;
+        am[u] |= (bin > d1 ? 1u : 0u) << j;
+        if (bin == d1) {
+          cm[u] |= 1u << j;
+          atomicAdd(&sh[(key >> 10) & 1023u], 1u);
+        }
+      }
+    }
+  }
+  // slot positions in index order: all runs of u = 0, then u = 1, ...
+  const TileSlots ts = tile_slots(w, tile, S);
+  uint32_t carry = 0;
+#pragma unroll
+  for (int u = 0; u < kTopkRuns; ++u) {
+    uint32_t tot;
+    const uint32_t ex = carry + block_exclusive_scan((uint32_t)__popc(am[u]) | ((uint32_t)__popc(cm[u]) << 16),
+                                                     &tot);
+    carry += tot;
+    uint32_t pa = ex & 0xFFFFu, pc = ex >> 16;
+    const uint64_t base = run_base(tile, u);
+#pragma unroll
+    for (int j = 0; j < kTopkElems; ++j) {
+      if ((am[u] >> j) & 1u) {
+        if (pa < S) {
+          ts.a_idx[pa] = (uint32_t)(base + j);
+          ts.a_val[pa] = v[u][j];
+        }
+        ++pa;
+      }
+      if ((cm[u] >> j) & 1u) {
+        if (pc < S) {
+          ts.c_idx[pc] = (uint32_t)(base + j);
+          ts.c_val[pc] = v[u][j];
+        }
+        ++pc;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    const uint32_t na = carry & 0xFFFFu, nc = carry >> 16;  // at most kTopkBlock = 16384 each
+    w.n_a[tile] = na;
+    w.n_c[tile] = nc;
+    if (na > S || nc > S) atomicOr(&w.st->overflow, 1u);
+  }
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
+  if (last_block(&w.st->ticket[1])) find_digit<1024>(w.hist, 10, w.st);
+}
+
+// Pass 3: histogram of bits 9..0 among the keys that match the prefix, read
+// from the candidate slots (or, after an overflow, from the data); then
+// (last block) the last digit, which completes T.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__ TopkArgs A) {
+  __shared__ uint32_t sh[1024];
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  const uint32_t mask = w.st->mask, prefix = w.st->prefix;
+  auto add = [&](float x) {
+    const uint32_t key = mag_key(x);
+    if ((key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
+  };
+  if (!w.st->overflow) {
+    for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
+      const TileSlots ts = tile_slots(w, tile, A.slots);
+      const uint32_t nc = w.n_c[tile];
+      for (uint32_t c = threadIdx.x; c < nc; c += blockDim.x) add(ts.c_val[c]);
+    }
+  } else {
+    const float* __restrict__ a = A.e[r];
+    const uint64_t count = A.count;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint64_t done = 0;
+    if (VEC) {
+      const uint64_t n4 = count / 4;
+      const float4* a4 = reinterpret_cast<const float4*>(a);
+      for (uint64_t q = t0; q < n4; q += stride) {
+        const float4 x = a4[q];
+        add(x.x);
+        add(x.y);
+        add(x.z);
+        add(x.w);
+      }
+      done = n4 * 4;
+    }
+    for (uint64_t i = done + t0; i < count; i += stride) add(a[i]);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
+  if (last_block(&w.st->ticket[2])) find_digit<1024>(w.hist, 0, w.st);
 }
 
 // run mask: bit j set if value j's key is above T, bit 16 + j if it equals T
@@ -305,9 +401,9 @@ __device__ __forceinline__ uint32_t mask_counts(uint32_t m) {
 }
 
 // The count pass's last block: eq_before[b] = keys equal to T in earlier
-// blocks; out_off[b] = kept elements in earlier blocks, where block b keeps
-// all its keys above T and min(n_eq[b], max(0, need - eq_before[b])) of its
-// keys equal to T. Each thread scans a contiguous run of blocks.
+// tiles; out_off[b] = kept elements in earlier tiles, where tile b keeps all
+// its keys above T and min(n_eq[b], max(0, need - eq_before[b])) of its keys
+// equal to T. Each thread scans a contiguous run of tiles.
 __device__ void scan_blocks(const RankWs& w, uint64_t nb) {
   const uint32_t need = w.st->need;
   const uint64_t m = (nb + kThreads - 1) / kThreads;
@@ -338,46 +434,123 @@ __device__ void scan_blocks(const RankWs& w, uint64_t nb) {
   }
 }
 
-// per tile: the run masks, and the keys above T and equal to T; the last
-// block scans the counts of all tiles
+// Per tile: keys above T and equal to T — from the slots (class A is above T;
+// class C is compared), or after an overflow from the data, writing the run
+// masks. The last block scans the counts of all tiles.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   const uint32_t T = w.st->prefix;
-  const uint64_t tile = (uint64_t)blockIdx.x * kTopkBlock;
-  float v[kTopkRuns][kTopkElems];
-#pragma unroll
-  for (int u = 0; u < kTopkRuns; ++u)
-    load_run<VEC>(A.e[r], tile + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems, A.count, v[u]);
+  const uint64_t tile = blockIdx.x;
   uint32_t c = 0;
+  if (!w.st->overflow) {
+    const TileSlots ts = tile_slots(w, tile, A.slots);
+    const uint32_t nc = w.n_c[tile];
+    for (uint32_t q = threadIdx.x; q < nc; q += blockDim.x) {
+      const uint32_t key = mag_key(ts.c_val[q]);
+      c += (key > T ? 1u : 0u) | ((key == T ? 1u : 0u) << 16);
+    }
+    if (threadIdx.x == 0) c += w.n_a[tile];
+  } else {
+    float v[kTopkRuns][kTopkElems];
 #pragma unroll
-  for (int u = 0; u < kTopkRuns; ++u) {
-    const uint32_t m = run_mask(v[u], tile + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems, A.count, T);
-    w.masks[(uint64_t)blockIdx.x * kThreads * kTopkRuns + u * kThreads + threadIdx.x] = m;
-    c += mask_counts(m);
+    for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(A.e[r], run_base(tile, u), A.count, v[u]);
+#pragma unroll
+    for (int u = 0; u < kTopkRuns; ++u) {
+      const uint32_t m = run_mask(v[u], run_base(tile, u), A.count, T);
+      w.masks[tile * kThreads * kTopkRuns + u * kThreads + threadIdx.x] = m;
+      c += mask_counts(m);
+    }
   }
   uint32_t tot;
   block_exclusive_scan(c, &tot);  // no field overflows: at most kTopkBlock = 16384 each
   if (threadIdx.x == 0) {
-    w.n_gt[blockIdx.x] = tot & 0xFFFFu;
-    w.n_eq[blockIdx.x] = tot >> 16;
+    w.n_gt[tile] = tot & 0xFFFFu;
+    w.n_eq[tile] = tot >> 16;
   }
   if (last_block(&w.st->ticket[3])) scan_blocks(w, A.nb);
 }
 
-// Kept elements to (index, value) in index order; zero their residual. Only
-// the run masks are read in full; values are read where a key is kept.
-__global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
-  const int r = blockIdx.y;
-  const RankWs w = rank_ws(A, r);
+// number of entries of the ascending list l[0..n) below x
+__device__ __forceinline__ uint32_t lower_bound(const uint32_t* l, uint32_t n, uint32_t x) {
+  uint32_t lo = 0, hi = n;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (l[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Emission from the slots: the tile's class-A keys and its kept class-C keys
+// merged in index order (each finds its place by a binary search in the
+// other list, held in shared memory). Dynamic shared memory: 3 * S words.
+__device__ void emit_slots(const TopkArgs& A, const RankWs& w, int r, uint64_t tile) {
+  extern __shared__ uint32_t dyn[];
+  const uint32_t S = A.slots;
+  uint32_t* s_a = dyn;           // class A indices
+  uint32_t* s_c = dyn + S;       // class C indices
+  uint32_t* s_kc = dyn + 2 * S;  // kept class-C entries before each class-C entry
+  const TileSlots ts = tile_slots(w, tile, S);
+  const uint32_t na = w.n_a[tile], nc = w.n_c[tile];
+  const uint32_t T = w.st->prefix, need = w.st->need;
+  const uint32_t eq_tile = w.eq_before[tile], off = w.out_off[tile];
+  for (uint32_t q = threadIdx.x; q < na; q += blockDim.x) s_a[q] = ts.a_idx[q];
+  // keep flags of the candidates in index order: ties kept while their rank
+  // among all keys equal to T is below `need`
+  uint32_t carry_eq = 0, carry_keep = 0;
+  for (uint32_t b = 0; b < nc; b += blockDim.x) {
+    const uint32_t q = b + threadIdx.x;
+    uint32_t key = 0;
+    if (q < nc) {
+      key = mag_key(ts.c_val[q]);
+      s_c[q] = ts.c_idx[q];
+    }
+    const bool eq = q < nc && key == T;
+    uint32_t tot_eq;
+    const uint32_t eq_rank = eq_tile + carry_eq + block_exclusive_scan(eq ? 1u : 0u, &tot_eq);
+    const bool keep = q < nc && (key > T || (eq && eq_rank < need));
+    uint32_t tot_keep;
+    const uint32_t kb = carry_keep + block_exclusive_scan(keep ? 1u : 0u, &tot_keep);
+    if (q < nc) s_kc[q] = kb | (keep ? 0x80000000u : 0u);
+    carry_eq += tot_eq;
+    carry_keep += tot_keep;
+  }
+  __syncthreads();
+  float* __restrict__ e = A.e[r];
+  uint32_t* __restrict__ idx = A.idx[r];
+  float* __restrict__ val = A.val[r];
+  const uint32_t kept_c = carry_keep;
+  for (uint32_t q = threadIdx.x; q < na; q += blockDim.x) {
+    const uint32_t i = s_a[q];
+    const uint32_t lb = lower_bound(s_c, nc, i);
+    const uint32_t kc = lb < nc ? (s_kc[lb] & 0x7FFFFFFFu) : kept_c;
+    const uint32_t pos = off + q + kc;
+    idx[pos] = i;
+    val[pos] = ts.a_val[q];
+    e[i] = 0.0f;
+  }
+  for (uint32_t q = threadIdx.x; q < nc; q += blockDim.x) {
+    const uint32_t kq = s_kc[q];
+    if (!(kq & 0x80000000u)) continue;
+    const uint32_t i = s_c[q];
+    const uint32_t pos = off + (kq & 0x7FFFFFFFu) + lower_bound(s_a, na, i);
+    idx[pos] = i;
+    val[pos] = ts.c_val[q];
+    e[i] = 0.0f;
+  }
+}
+
+// Emission from the run masks (after an overflow): values are read where a
+// key is kept.
+__device__ void emit_masks(const TopkArgs& A, const RankWs& w, int r, uint64_t tile) {
   uint32_t m[kTopkRuns];
 #pragma unroll
-  for (int u = 0; u < kTopkRuns; ++u)
-    m[u] = w.masks[(uint64_t)blockIdx.x * kThreads * kTopkRuns + u * kThreads + threadIdx.x];
+  for (int u = 0; u < kTopkRuns; ++u) m[u] = w.masks[tile * kThreads * kTopkRuns + u * kThreads + threadIdx.x];
   const uint32_t need = w.st->need;
-  const uint32_t eq_block = w.eq_before[blockIdx.x];
-  const uint32_t off_block = w.out_off[blockIdx.x];
+  const uint32_t eq_block = w.eq_before[tile];
+  const uint32_t off_block = w.out_off[tile];
   // runs in index order: all of u = 0, then u = 1, ...; ex[u] = the counts of
   // the tile's runs before run (u, this thread)
   uint32_t ex[kTopkRuns];
@@ -410,7 +583,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ 
         ++eq_rank;
       }
     }
-    const uint64_t base = (uint64_t)blockIdx.x * kTopkBlock + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems;
+    const uint64_t base = run_base(tile, u);
     float x[kTopkElems];
 #pragma unroll
     for (int j = 0; j < kTopkElems; ++j)
@@ -425,6 +598,14 @@ __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ 
       }
     }
   }
+}
+
+// Kept elements to (index, value) in index order; zero their residual.
+__global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  if (!w.st->overflow) emit_slots(A, w, r, blockIdx.x);
+  else emit_masks(A, w, r, blockIdx.x);
 }
 
 // recv[r][idx_r[j]] = val_r[j] for every rank (outputs already zeroed)
@@ -449,8 +630,8 @@ template <bool VEC>
 cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 one(1, a.nranks);
   k_topk_init<<<one, kThreads, 0, s>>>(a);
-  // histogram passes: a resident grid looping over the data, so that each
-  // block flushes its shared histogram once
+  // histogram passes over the data: a resident grid looping over it, so that
+  // each block flushes its shared histogram once
   const uint64_t items = VEC ? (a.count + 3) / 4 : a.count;
   unsigned per_rank = (unsigned)(kSms * kHistBlocksPerSm / a.nranks);
   if (per_rank < 1) per_rank = 1;
@@ -458,11 +639,11 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 hgrid(hx, a.nranks);
   k_topk_pass1<VEC><<<hgrid, kThreads, 0, s>>>(a);
   if (a.k == 0) return cudaGetLastError();  // nothing kept: e = a
-  k_topk_pass<VEC><<<hgrid, kThreads, 0, s>>>(a, 10, 1);
-  k_topk_pass<VEC><<<hgrid, kThreads, 0, s>>>(a, 0, 2);
-  const dim3 bgrid((unsigned)a.nb, a.nranks);
-  k_topk_count<VEC><<<bgrid, kThreads, 0, s>>>(a);
-  k_topk_emit<<<bgrid, kThreads, 0, s>>>(a);
+  const dim3 tgrid((unsigned)a.nb, a.nranks);
+  k_topk_split<VEC><<<tgrid, kThreads, 0, s>>>(a);
+  k_topk_pass3<VEC><<<hgrid, kThreads, 0, s>>>(a);
+  k_topk_count<VEC><<<tgrid, kThreads, 0, s>>>(a);
+  k_topk_emit<<<tgrid, kThreads, 3 * a.slots * sizeof(uint32_t), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -514,9 +695,9 @@ bool any_overlap(std::vector<Rng> v) {
 
 extern "C" {
 
-size_t ar_topk_workspace_bytes(int nranks, size_t count) {
-  if (nranks < 1 || nranks > AR_MAX_RANKS || count > 0xFFFFFFFFull) return 0;
-  return (size_t)nranks * gar::topk_rank_words(count) * 4;
+size_t ar_topk_workspace_bytes(int nranks, size_t count, size_t k) {
+  if (nranks < 1 || nranks > AR_MAX_RANKS || count > 0xFFFFFFFFull || k > count) return 0;
+  return (size_t)nranks * gar::topk_rank_words(count, k) * 4;
 }
 
 ar_status_t ar_topk_compress(const float* const* grads, float* const* residuals, int nranks, size_t count, size_t k,
@@ -527,7 +708,7 @@ ar_status_t ar_topk_compress(const float* const* grads, float* const* residuals,
   if (count > 0xFFFFFFFFull) return tk_fail(AR_ERR_INVALID_ARGUMENT, "count must fit 32-bit indices");
   if (k > count) return tk_fail(AR_ERR_INVALID_ARGUMENT, "k exceeds count");
   if (count == 0) return tk_ok();
-  const size_t need = ar_topk_workspace_bytes(nranks, count);
+  const size_t need = ar_topk_workspace_bytes(nranks, count, k);
   if (!workspace) return tk_fail(AR_ERR_INVALID_ARGUMENT, "null workspace");
   if (tk_addr(workspace) % 16) return tk_fail(AR_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
   if (ws_bytes < need) return tk_fail(AR_ERR_INVALID_ARGUMENT, "workspace too small");
@@ -557,7 +738,8 @@ ar_status_t ar_topk_compress(const float* const* grads, float* const* residuals,
     if (any_overlap(v)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
   }
   a.ws = static_cast<uint32_t*>(workspace);
-  a.ws_words = gar::topk_rank_words(count);
+  a.ws_words = gar::topk_rank_words(count, k);
+  a.slots = gar::topk_slots(count, k);
   a.count = count;
   a.nb = gar::topk_blocks(count);
   a.k = (uint32_t)k;

@@ -10,25 +10,45 @@
 
 namespace gar {
 
-// Tiles of the count and emit kernels: each thread takes kTopkRuns runs of
+// Tiles of the tile-shaped passes: each thread takes kTopkRuns runs of
 // kTopkElems consecutive values; run u * kThreads + t of a tile belongs to
 // thread t, so every load of a warp is contiguous.
 constexpr int kTopkElems = 16;                                 // values per run
 constexpr int kTopkRuns = 4;                                   // runs per thread
 constexpr int kTopkBlock = kThreads * kTopkRuns * kTopkElems;  // values per tile
+constexpr uint32_t kTopkMaxSlots = 4032;  // slot cap per tile and class (3 * 4032 words of shared memory fit 48 KiB)
 
 // Per-rank workspace, in 32-bit words (a multiple of 64 words, 256 bytes):
 //   [0, 2048)        histogram of the current radix pass
 //   [2048, 2064)     TopkState
-//   then nb words each of n_gt, n_eq, eq_before, out_off (nb = tiles)
-//   then nb * kThreads * kTopkRuns words of run masks: for the kTopkElems
-//   values of a run, bit j (j < 16) set if value j's key is above T, bit
-//   16 + j if it equals T
+//   then nb words each of n_gt, n_eq, eq_before, out_off, n_a, n_c (nb = tiles)
+//   then nb * kThreads * kTopkRuns words of run masks (used only when a
+//   tile's slots overflow): for the kTopkElems values of a run, bit j (j < 16)
+//   set if value j's key is above T, bit 16 + j if it equals T
+//   then per tile 4 * S words of slots: S indices and S values of the tile's
+//   keys above the first digit's bin (class A, all kept), then S indices and
+//   S values of the keys inside that bin (class C, the candidates), each in
+//   index order
 constexpr int kTopkHistWords = 2048;
 constexpr int kTopkStateWords = 16;
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
-inline uint64_t topk_rank_words(uint64_t count) {
-  return (kTopkHistWords + kTopkStateWords + (4 + (uint64_t)kThreads * kTopkRuns) * topk_blocks(count) + 63) / 64 * 64;
+
+// Slot capacity per tile and class: four times the tile's share of k plus a
+// margin, a multiple of 32, at most kTopkMaxSlots and at most a tile.
+inline uint32_t topk_slots(uint64_t count, uint64_t k) {
+  if (count == 0) return 32;
+  const uint64_t share = (k * kTopkBlock + count - 1) / count;
+  uint64_t s = (4 * share + 256 + 31) / 32 * 32;
+  const uint64_t tile = count < (uint64_t)kTopkBlock ? (count + 31) / 32 * 32 : (uint64_t)kTopkBlock;
+  if (s > tile) s = tile;
+  if (s > kTopkMaxSlots) s = kTopkMaxSlots;
+  return (uint32_t)s;
+}
+
+inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
+  const uint64_t nb = topk_blocks(count);
+  return (kTopkHistWords + kTopkStateWords + (6 + (uint64_t)kThreads * kTopkRuns) * nb +
+          4ull * topk_slots(count, k) * nb + 63) / 64 * 64;
 }
 
 // Radix-select state of one rank, kept on the device between the passes. The
@@ -40,13 +60,18 @@ inline uint64_t topk_rank_words(uint64_t count) {
 //   gt:          keys strictly above the prefix (all kept)
 //   ticket[p]:   blocks of pass p that have finished (the last one to finish
 //                carries out the pass's single-block step)
+//   overflow:    nonzero if some tile had more class-A or class-C keys than
+//                its slots hold; the later passes then read the data instead
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
   uint32_t need;
   uint32_t gt;
   uint32_t ticket[4];
+  uint32_t overflow;
+  uint32_t pad[7];
 };
+static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 
 // Every rank's buffers for one Top-K call; rank r's workspace starts at
 // ws + r * ws_words.
@@ -60,6 +85,7 @@ struct TopkArgs {
   uint64_t count;
   uint64_t nb;
   uint32_t k;
+  uint32_t slots;  // S, slot capacity per tile and class
   int nranks;
 };
 

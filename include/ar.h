@@ -302,10 +302,11 @@ ar_status_t ar_allreduce_fp8_noalloc(const void *const *sendbufs, void *const *r
  * |a| is compared through its bit pattern with the sign cleared (so -0 ties
  * +0, and a NaN ranks above every number).
  *
- * Workspace bytes for ar_topk_compress over nranks x `count` values (per
- * rank about count / 4 bytes plus 8 KiB, a multiple of 256 bytes); 0 if
- * nranks is outside 1..AR_MAX_RANKS or count >= 2^32. */
-size_t ar_topk_workspace_bytes(int nranks, size_t count);
+ * Workspace bytes for ar_topk_compress over nranks x `count` values keeping
+ * k per rank (per rank about count / 4 bytes plus 32 * max(k, count / 256)
+ * bytes, at most 4.25 bytes per value, plus 8 KiB; a multiple of 256 bytes);
+ * 0 if nranks is outside 1..AR_MAX_RANKS, count >= 2^32 or k > count. */
+size_t ar_topk_workspace_bytes(int nranks, size_t count, size_t k);
 
 /* Every rank's Top-K step in one call on `stream` (six kernel launches
  * whatever nranks is): reads grads[r][count], updates residuals[r][count] in
@@ -313,7 +314,7 @@ size_t ar_topk_workspace_bytes(int nranks, size_t count);
  *   grads[r], residuals[r]: F32 device buffers, 4-byte aligned (when all are
  *     16-byte aligned the vector path runs; results are identical either way).
  *   workspace: device memory of at least ar_topk_workspace_bytes(nranks,
- *     count), 16-byte aligned, owned by the caller; its contents need no
+ *     count, k), 16-byte aligned, owned by the caller; its contents need no
  *     initialisation and are meaningless afterwards.
  *   Errors: AR_ERR_INVALID_ARGUMENT for k > count, count >= 2^32, a null or
  *   misaligned pointer or a short workspace; AR_ERR_ALIAS if an output

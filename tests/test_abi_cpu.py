@@ -177,16 +177,23 @@ def test_bucket_allreduce_argument_errors(L):
 
 
 def test_topk_workspace_and_argument_errors(L):
-    n, count = 3, 100_000
-    need = gar.ar_topk_workspace_bytes(n, count)
+    n, count, k10 = 3, 100_000, 1000
+    need = gar.ar_topk_workspace_bytes(n, count, k10)
     nb = math.ceil(count / 16384)
-    assert need == n * math.ceil((2048 + 16 + (4 + 1024) * nb) / 64) * 64 * 4
-    assert gar.ar_topk_workspace_bytes(1, 1 << 32) == 0 and gar.ar_topk_workspace_bytes(0, 10) == 0
+    share = math.ceil(k10 * 16384 / count)
+    slots = min(16384, 4032, math.ceil((4 * share + 256) / 32) * 32)
+    assert need == n * math.ceil((2048 + 16 + (6 + 1024) * nb + 4 * slots * nb) / 64) * 64 * 4
+    assert gar.ar_topk_workspace_bytes(1, 1 << 32, 1) == 0 and gar.ar_topk_workspace_bytes(0, 10, 1) == 0
+    assert gar.ar_topk_workspace_bytes(1, 10, 11) == 0
+    # at most about 4.25 bytes per value plus the fixed part, whatever k is
+    assert gar.ar_topk_workspace_bytes(1, count, count) <= 4.25 * count + 3 * 16384 * 4 + 9 * 1024
     g = [0x1000000 * (r + 1) for r in range(n)]
     e = [0x10000000 + 0x1000000 * r for r in range(n)]
     i = [0x20000000 + 0x1000000 * r for r in range(n)]
     v = [0x30000000 + 0x1000000 * r for r in range(n)]
     ws = 0x40000000
+
+    need = gar.ar_topk_workspace_bytes(n, count, 10)
 
     def f(g=g, e=e, count=count, k=10, i=i, v=v, ws=ws, wsb=need, n=n):
         return L.ar_topk_compress(_arr(g), _arr(e), n, count, k, _arr(i), _arr(v), ws, wsb, None)

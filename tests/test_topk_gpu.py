@@ -40,7 +40,7 @@ def _gpu_topk(g: np.ndarray, e: np.ndarray, k: int, offset: int = 0):
     eb, ed = _dev_f32(e, offset)
     idx = torch.full((k + 8,), -1, dtype=torch.int32, device="cuda")
     val = torch.full((k + 8,), 7.0, dtype=torch.float32, device="cuda")
-    ws = torch.empty(max(gar.ar_topk_workspace_bytes(1, count), 1), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(gar.ar_topk_workspace_bytes(1, count, k), 1), dtype=torch.uint8, device="cuda")
     ws.fill_(0x5A)  # the workspace needs no initialisation
     gar.ar_topk_compress([gd], [ed], k, [idx], [val], ws)
     torch.cuda.synchronize()
@@ -97,7 +97,7 @@ def test_topk_many_ranks_in_one_call(unaligned_rank):
         res.append(ed)
     idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
     val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
-    ws = torch.full((gar.ar_topk_workspace_bytes(n, count),), 0xC3, dtype=torch.uint8, device="cuda")
+    ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0xC3, dtype=torch.uint8, device="cuda")
     gar.ar_topk_compress(grads, res, k, idx, val, ws)
     torch.cuda.synchronize()
     for r in range(n):
@@ -107,9 +107,11 @@ def test_topk_many_ranks_in_one_call(unaligned_rank):
         assert np.array_equal(_bits(from_dev(res[r])), _bits(oe)), r
 
 
-def test_topk_heavy_ties_and_signed_zeros():
+@pytest.mark.parametrize("offset", [0, 1])
+def test_topk_heavy_ties_and_signed_zeros(offset):
     # magnitudes from {0, 1, 2, 3}, both signs, both zeros: every threshold is
-    # a tie that the lower indices win
+    # a tie that the lower indices win; the candidate slots overflow, so the
+    # passes after the second read the data
     count = 30_011
     ints = synthgen.uniform_i32(count, 31, -3, 3)
     g = ints.astype(np.float32)
@@ -118,6 +120,17 @@ def test_topk_heavy_ties_and_signed_zeros():
     e[::7] = -0.0
     nz3 = int(np.sum(np.abs(g) == 3))
     for k in (1, nz3 - 1, nz3, nz3 + 1, count // 2, count - 1, count):
+        _check_against_oracle(g, e, k, offset)
+
+
+def test_topk_one_overflowing_tile():
+    # a block of equal magnitudes inside one tile holds the threshold: that
+    # tile's candidates overflow their slots while every other tile's fit
+    count = 200_000
+    g = synthgen.normal_f32(count, 51, 1e-3)
+    g[40_000:46_000] = np.where(np.arange(6_000) % 3 == 0, -0.5, 0.5).astype(np.float32)
+    e = np.zeros(count, dtype=np.float32)
+    for k in (100, 3_000, 6_000, 6_001, 8_000):
         _check_against_oracle(g, e, k)
 
 
@@ -140,7 +153,7 @@ def test_error_feedback_over_several_steps():
     ed = torch.zeros(count, dtype=torch.float32, device="cuda")
     idx = torch.empty(k, dtype=torch.int32, device="cuda")
     val = torch.empty(k, dtype=torch.float32, device="cuda")
-    ws = torch.empty(gar.ar_topk_workspace_bytes(1, count), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(gar.ar_topk_workspace_bytes(1, count, k), dtype=torch.uint8, device="cuda")
     for step in range(4):
         g = synthgen.normal_f32(count, 100 + step, 1e-3)
         gar.ar_topk_compress([to_dev(g, "f32")], [ed], k, [idx], [val], ws)
@@ -208,7 +221,7 @@ def test_topk_full_size_eight_ranks():
     res = [to_dev(x, "f32") for x in e_np]
     idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
     val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
-    ws = torch.empty(gar.ar_topk_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(gar.ar_topk_workspace_bytes(n, count, k), dtype=torch.uint8, device="cuda")
     gar.ar_topk_compress(grads, res, k, idx, val, ws)
     torch.cuda.synchronize()
     o_idx, o_val = [], []
