@@ -39,6 +39,8 @@ constexpr int kSms = 152;
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
 
+constexpr int kWarps = kThreads / 32;  // tiles per block in the slot-reading passes
+
 struct RankWs {
   uint32_t* hist;
   TopkState* st;
@@ -46,8 +48,7 @@ struct RankWs {
   uint32_t* n_eq;
   uint32_t* eq_before;
   uint32_t* out_off;
-  uint32_t* n_a;
-  uint32_t* n_c;
+  uint32_t* n_s;
   uint32_t* masks;
   uint32_t* slots;
 };
@@ -61,23 +62,18 @@ __device__ __forceinline__ RankWs rank_ws(const TopkArgs& A, int r) {
   w.n_eq = w.n_gt + A.nb;
   w.eq_before = w.n_eq + A.nb;
   w.out_off = w.eq_before + A.nb;
-  w.n_a = w.out_off + A.nb;
-  w.n_c = w.n_a + A.nb;
-  w.masks = w.n_c + A.nb;
+  w.n_s = w.out_off + A.nb;
+  w.masks = w.n_s + A.nb;
   w.slots = w.masks + A.nb * kThreads * kTopkRuns;
   return w;
 }
 
-// the slots of one tile: class A indices, values, class C indices, values
-struct TileSlots {
-  uint32_t* a_idx;
-  float* a_val;
-  uint32_t* c_idx;
-  float* c_val;
-};
-__device__ __forceinline__ TileSlots tile_slots(const RankWs& w, uint64_t tile, uint32_t S) {
-  uint32_t* b = w.slots + tile * 4ull * S;
-  return {b, reinterpret_cast<float*>(b + S), b + 2 * S, reinterpret_cast<float*>(b + 3 * S)};
+// slot indices and values of one tile
+__device__ __forceinline__ uint32_t* slot_idx(const RankWs& w, uint64_t tile, uint32_t S) {
+  return w.slots + tile * 2ull * S;
+}
+__device__ __forceinline__ float* slot_val(const RankWs& w, uint64_t tile, uint32_t S) {
+  return reinterpret_cast<float*>(w.slots + tile * 2ull * S + S);
 }
 
 // exclusive scan over the block of one value per thread; *total = block sum
@@ -255,10 +251,22 @@ __device__ __forceinline__ uint64_t run_base(uint64_t tile, int u) {
   return tile * kTopkBlock + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems;
 }
 
-// Pass 2, one tile per block: the histogram of bits 19..10 of the keys in
-// the first digit's bin, and the order-preserving compaction of the tile's
-// class-A keys (bin above it: all kept) and class-C keys (in it: the
-// candidates) into the tile's slots; then (last block) the second digit.
+// bit j set if value j of the run (inside the data) has a key >= lo
+__device__ __forceinline__ uint32_t ge_mask(const float (&v)[kTopkElems], uint64_t base, uint64_t count,
+                                            uint32_t lo) {
+  uint32_t m = 0;
+  const bool full = base + kTopkElems <= count;
+#pragma unroll
+  for (int j = 0; j < kTopkElems; ++j)
+    if (mag_key(v[j]) >= lo && (full || base + j < count)) m |= 1u << j;
+  return m;
+}
+
+// Pass 2, one tile per block: the tile's keys at or above the first digit's
+// bin (every key that can still be kept) compacted in index order into the
+// tile's slots, and the histogram of bits 19..10 of the keys inside that
+// bin; then (last block) the second digit. The sparse work runs over the set
+// bits of each run's mask, re-reading those few values from the cache.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__ TopkArgs A) {
   __shared__ uint32_t sh[1024];
@@ -266,75 +274,64 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   const RankWs w = rank_ws(A, r);
   const uint64_t tile = blockIdx.x;
   const uint64_t count = A.count;
+  const float* __restrict__ a = A.e[r];
   const uint32_t S = A.slots;
   for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
   const uint32_t d1 = w.st->prefix >> 20;
-  float v[kTopkRuns][kTopkElems];
+  const uint32_t lo = d1 << 20;
+  uint32_t m[kTopkRuns];
+  {
+    float v[kTopkRuns][kTopkElems];
 #pragma unroll
-  for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(A.e[r], run_base(tile, u), count, v[u]);
-  __syncthreads();
-  uint32_t am[kTopkRuns], cm[kTopkRuns];
+    for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(a, run_base(tile, u), count, v[u]);
 #pragma unroll
-  for (int u = 0; u < kTopkRuns; ++u) {
-    am[u] = 0;
-    cm[u] = 0;
-    const uint64_t base = run_base(tile, u);
-#pragma unroll
-    for (int j = 0; j < kTopkElems; ++j) {
-      if (base + j < count) {
-        const uint32_t key = mag_key(v[u][j]);
-        const uint32_t bin = key >> 20;
-        am[u] |= (bin > d1 ? 1u : 0u) << j;
-        if (bin == d1) {
-          cm[u] |= 1u << j;
-          atomicAdd(&sh[(key >> 10) & 1023u], 1u);
-        }
-      }
-    }
+    for (int u = 0; u < kTopkRuns; ++u) m[u] = ge_mask(v[u], run_base(tile, u), count, lo);
   }
-  // slot positions in index order: all runs of u = 0, then u = 1, ...
-  const TileSlots ts = tile_slots(w, tile, S);
-  uint32_t carry = 0;
+  // slot positions in index order (all runs of u = 0, then u = 1, ...):
+  // runs 0 and 1, and runs 2 and 3, share one scan of two 16-bit counts
+  uint32_t t01, t23;
+  const uint32_t e01 = block_exclusive_scan((uint32_t)__popc(m[0]) | ((uint32_t)__popc(m[1]) << 16), &t01);
+  const uint32_t e23 = block_exclusive_scan((uint32_t)__popc(m[2]) | ((uint32_t)__popc(m[3]) << 16), &t23);
+  const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
+  uint32_t pos[kTopkRuns];
+  pos[0] = e01 & 0xFFFFu;
+  pos[1] = tot0 + (e01 >> 16);
+  pos[2] = tot0 + tot1 + (e23 & 0xFFFFu);
+  pos[3] = tot0 + tot1 + tot2 + (e23 >> 16);
+  uint32_t* __restrict__ si = slot_idx(w, tile, S);
+  float* __restrict__ sv = slot_val(w, tile, S);
 #pragma unroll
   for (int u = 0; u < kTopkRuns; ++u) {
-    uint32_t tot;
-    const uint32_t ex = carry + block_exclusive_scan((uint32_t)__popc(am[u]) | ((uint32_t)__popc(cm[u]) << 16),
-                                                     &tot);
-    carry += tot;
-    uint32_t pa = ex & 0xFFFFu, pc = ex >> 16;
     const uint64_t base = run_base(tile, u);
-#pragma unroll
-    for (int j = 0; j < kTopkElems; ++j) {
-      if ((am[u] >> j) & 1u) {
-        if (pa < S) {
-          ts.a_idx[pa] = (uint32_t)(base + j);
-          ts.a_val[pa] = v[u][j];
-        }
-        ++pa;
+    uint32_t bits = m[u];
+    uint32_t p = pos[u];
+    while (bits) {
+      const int j = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const float x = a[base + j];
+      const uint32_t key = mag_key(x);
+      if ((key >> 20) == d1) atomicAdd(&sh[(key >> 10) & 1023u], 1u);
+      if (p < S) {
+        si[p] = (uint32_t)(base + j);
+        sv[p] = x;
       }
-      if ((cm[u] >> j) & 1u) {
-        if (pc < S) {
-          ts.c_idx[pc] = (uint32_t)(base + j);
-          ts.c_val[pc] = v[u][j];
-        }
-        ++pc;
-      }
+      ++p;
     }
   }
   if (threadIdx.x == 0) {
-    const uint32_t na = carry & 0xFFFFu, nc = carry >> 16;  // at most kTopkBlock = 16384 each
-    w.n_a[tile] = na;
-    w.n_c[tile] = nc;
-    if (na > S || nc > S) atomicOr(&w.st->overflow, 1u);
+    const uint32_t n = tot0 + tot1 + tot2 + tot3;
+    w.n_s[tile] = n;
+    if (n > S) atomicOr(&w.st->overflow, 1u);
   }
+  __syncthreads();
   for (int i = threadIdx.x; i < 1024; i += blockDim.x)
     if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
   if (last_block(&w.st->ticket[1])) find_digit<1024>(w.hist, 10, w.st);
 }
 
 // Pass 3: histogram of bits 9..0 among the keys that match the prefix, read
-// from the candidate slots (or, after an overflow, from the data); then
-// (last block) the last digit, which completes T.
+// from the slots (or, after an overflow, from the data); then (last block)
+// the last digit, which completes T.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__ TopkArgs A) {
   __shared__ uint32_t sh[1024];
@@ -349,9 +346,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
   };
   if (!w.st->overflow) {
     for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
-      const TileSlots ts = tile_slots(w, tile, A.slots);
-      const uint32_t nc = w.n_c[tile];
-      for (uint32_t c = threadIdx.x; c < nc; c += blockDim.x) add(ts.c_val[c]);
+      const float* sv = slot_val(w, tile, A.slots);
+      const uint32_t n = w.n_s[tile];
+      for (uint32_t c = threadIdx.x; c < n; c += blockDim.x) add(sv[c]);
     }
   } else {
     const float* __restrict__ a = A.e[r];
@@ -434,116 +431,103 @@ __device__ void scan_blocks(const RankWs& w, uint64_t nb) {
   }
 }
 
-// Per tile: keys above T and equal to T — from the slots (class A is above T;
-// class C is compared), or after an overflow from the data, writing the run
-// masks. The last block scans the counts of all tiles.
+// Keys above T and equal to T per tile. From the slots: one warp per tile.
+// After an overflow: the block takes its kWarps tiles one after another from
+// the data, writing the run masks. The last block scans all tiles' counts.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   const uint32_t T = w.st->prefix;
-  const uint64_t tile = blockIdx.x;
-  uint32_t c = 0;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (!w.st->overflow) {
-    const TileSlots ts = tile_slots(w, tile, A.slots);
-    const uint32_t nc = w.n_c[tile];
-    for (uint32_t q = threadIdx.x; q < nc; q += blockDim.x) {
-      const uint32_t key = mag_key(ts.c_val[q]);
-      c += (key > T ? 1u : 0u) | ((key == T ? 1u : 0u) << 16);
+    const uint64_t tile = (uint64_t)blockIdx.x * kWarps + wid;
+    if (tile < A.nb) {
+      const float* sv = slot_val(w, tile, A.slots);
+      const uint32_t n = w.n_s[tile];
+      uint32_t gt = 0, eq = 0;
+      for (uint32_t c = lane; c < n; c += 32) {
+        const uint32_t key = mag_key(sv[c]);
+        gt += key > T;
+        eq += key == T;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        gt += __shfl_xor_sync(0xffffffffu, gt, o);
+        eq += __shfl_xor_sync(0xffffffffu, eq, o);
+      }
+      if (lane == 0) {
+        w.n_gt[tile] = gt;
+        w.n_eq[tile] = eq;
+      }
     }
-    if (threadIdx.x == 0) c += w.n_a[tile];
   } else {
-    float v[kTopkRuns][kTopkElems];
+    for (int t = 0; t < kWarps; ++t) {
+      const uint64_t tile = (uint64_t)blockIdx.x * kWarps + t;
+      if (tile >= A.nb) break;  // uniform across the block
+      float v[kTopkRuns][kTopkElems];
 #pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(A.e[r], run_base(tile, u), A.count, v[u]);
+      for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(A.e[r], run_base(tile, u), A.count, v[u]);
+      uint32_t c = 0;
 #pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) {
-      const uint32_t m = run_mask(v[u], run_base(tile, u), A.count, T);
-      w.masks[tile * kThreads * kTopkRuns + u * kThreads + threadIdx.x] = m;
-      c += mask_counts(m);
+      for (int u = 0; u < kTopkRuns; ++u) {
+        const uint32_t m = run_mask(v[u], run_base(tile, u), A.count, T);
+        w.masks[tile * kThreads * kTopkRuns + u * kThreads + threadIdx.x] = m;
+        c += mask_counts(m);
+      }
+      uint32_t tot;
+      block_exclusive_scan(c, &tot);  // no field overflows: at most kTopkBlock = 16384 each
+      if (threadIdx.x == 0) {
+        w.n_gt[tile] = tot & 0xFFFFu;
+        w.n_eq[tile] = tot >> 16;
+      }
     }
-  }
-  uint32_t tot;
-  block_exclusive_scan(c, &tot);  // no field overflows: at most kTopkBlock = 16384 each
-  if (threadIdx.x == 0) {
-    w.n_gt[tile] = tot & 0xFFFFu;
-    w.n_eq[tile] = tot >> 16;
   }
   if (last_block(&w.st->ticket[3])) scan_blocks(w, A.nb);
 }
 
-// number of entries of the ascending list l[0..n) below x
-__device__ __forceinline__ uint32_t lower_bound(const uint32_t* l, uint32_t n, uint32_t x) {
-  uint32_t lo = 0, hi = n;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (l[mid] < x) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
-// Emission from the slots: the tile's class-A keys and its kept class-C keys
-// merged in index order (each finds its place by a binary search in the
-// other list, held in shared memory). Dynamic shared memory: 3 * S words.
-__device__ void emit_slots(const TopkArgs& A, const RankWs& w, int r, uint64_t tile) {
-  extern __shared__ uint32_t dyn[];
-  const uint32_t S = A.slots;
-  uint32_t* s_a = dyn;           // class A indices
-  uint32_t* s_c = dyn + S;       // class C indices
-  uint32_t* s_kc = dyn + 2 * S;  // kept class-C entries before each class-C entry
-  const TileSlots ts = tile_slots(w, tile, S);
-  const uint32_t na = w.n_a[tile], nc = w.n_c[tile];
+// Emission from the slots, one warp per tile: the slots are in index order,
+// so the kept ones (above T, or equal to T while their rank among all keys
+// equal to T is below `need`) are written in order with warp ballots.
+__device__ void emit_slots(const TopkArgs& A, const RankWs& w, int r) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t tile = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (tile >= A.nb) return;
   const uint32_t T = w.st->prefix, need = w.st->need;
-  const uint32_t eq_tile = w.eq_before[tile], off = w.out_off[tile];
-  for (uint32_t q = threadIdx.x; q < na; q += blockDim.x) s_a[q] = ts.a_idx[q];
-  // keep flags of the candidates in index order: ties kept while their rank
-  // among all keys equal to T is below `need`
-  uint32_t carry_eq = 0, carry_keep = 0;
-  for (uint32_t b = 0; b < nc; b += blockDim.x) {
-    const uint32_t q = b + threadIdx.x;
-    uint32_t key = 0;
-    if (q < nc) {
-      key = mag_key(ts.c_val[q]);
-      s_c[q] = ts.c_idx[q];
-    }
-    const bool eq = q < nc && key == T;
-    uint32_t tot_eq;
-    const uint32_t eq_rank = eq_tile + carry_eq + block_exclusive_scan(eq ? 1u : 0u, &tot_eq);
-    const bool keep = q < nc && (key > T || (eq && eq_rank < need));
-    uint32_t tot_keep;
-    const uint32_t kb = carry_keep + block_exclusive_scan(keep ? 1u : 0u, &tot_keep);
-    if (q < nc) s_kc[q] = kb | (keep ? 0x80000000u : 0u);
-    carry_eq += tot_eq;
-    carry_keep += tot_keep;
-  }
-  __syncthreads();
+  const uint32_t* si = slot_idx(w, tile, A.slots);
+  const float* sv = slot_val(w, tile, A.slots);
+  const uint32_t n = w.n_s[tile];
+  uint32_t eq_run = w.eq_before[tile], pos_run = w.out_off[tile];
   float* __restrict__ e = A.e[r];
   uint32_t* __restrict__ idx = A.idx[r];
   float* __restrict__ val = A.val[r];
-  const uint32_t kept_c = carry_keep;
-  for (uint32_t q = threadIdx.x; q < na; q += blockDim.x) {
-    const uint32_t i = s_a[q];
-    const uint32_t lb = lower_bound(s_c, nc, i);
-    const uint32_t kc = lb < nc ? (s_kc[lb] & 0x7FFFFFFFu) : kept_c;
-    const uint32_t pos = off + q + kc;
-    idx[pos] = i;
-    val[pos] = ts.a_val[q];
-    e[i] = 0.0f;
-  }
-  for (uint32_t q = threadIdx.x; q < nc; q += blockDim.x) {
-    const uint32_t kq = s_kc[q];
-    if (!(kq & 0x80000000u)) continue;
-    const uint32_t i = s_c[q];
-    const uint32_t pos = off + (kq & 0x7FFFFFFFu) + lower_bound(s_a, na, i);
-    idx[pos] = i;
-    val[pos] = ts.c_val[q];
-    e[i] = 0.0f;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (uint32_t c0 = 0; c0 < n; c0 += 32) {
+    const uint32_t c = c0 + lane;
+    uint32_t key = 0, i = 0;
+    float x = 0.0f;
+    if (c < n) {
+      x = sv[c];
+      i = si[c];
+      key = mag_key(x);
+    }
+    const bool eq = c < n && key == T;
+    const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
+    const bool keep = c < n && (key > T || (eq && eq_run + (uint32_t)__popc(eq_bal & lt) < need));
+    const uint32_t keep_bal = __ballot_sync(0xffffffffu, keep);
+    const uint32_t p = pos_run + (uint32_t)__popc(keep_bal & lt);
+    if (keep && p < A.k) {  // p < k always holds; the test keeps every write inside idx and val
+      idx[p] = i;
+      val[p] = x;
+      e[i] = 0.0f;
+    }
+    eq_run += (uint32_t)__popc(eq_bal);
+    pos_run += (uint32_t)__popc(keep_bal);
   }
 }
 
-// Emission from the run masks (after an overflow): values are read where a
-// key is kept.
+// Emission from the run masks (after an overflow), one tile: values are
+// read where a key is kept. Called by the whole block.
 __device__ void emit_masks(const TopkArgs& A, const RankWs& w, int r, uint64_t tile) {
   uint32_t m[kTopkRuns];
 #pragma unroll
@@ -554,15 +538,13 @@ __device__ void emit_masks(const TopkArgs& A, const RankWs& w, int r, uint64_t t
   // runs in index order: all of u = 0, then u = 1, ...; ex[u] = the counts of
   // the tile's runs before run (u, this thread)
   uint32_t ex[kTopkRuns];
-  uint32_t carry = 0, any = 0;
+  uint32_t carry = 0;
 #pragma unroll
   for (int u = 0; u < kTopkRuns; ++u) {
     uint32_t tot;
     ex[u] = carry + block_exclusive_scan(mask_counts(m[u]), &tot);
     carry += tot;
-    any |= m[u];
   }
-  if (any == 0) return;
   float* __restrict__ a = A.e[r];
   uint32_t* __restrict__ idx = A.idx[r];
   float* __restrict__ val = A.val[r];
@@ -584,28 +566,32 @@ __device__ void emit_masks(const TopkArgs& A, const RankWs& w, int r, uint64_t t
       }
     }
     const uint64_t base = run_base(tile, u);
-    float x[kTopkElems];
-#pragma unroll
-    for (int j = 0; j < kTopkElems; ++j)
-      if ((keep >> j) & 1u) x[j] = a[base + j];
-#pragma unroll
-    for (int j = 0; j < kTopkElems; ++j) {
-      if ((keep >> j) & 1u) {
-        idx[pos] = (uint32_t)(base + j);
-        val[pos] = x[j];
-        a[base + j] = 0.0f;
-        ++pos;
-      }
+    while (keep) {
+      const int j = __ffs(keep) - 1;
+      keep &= keep - 1;
+      if (pos >= A.k) break;  // never taken; keeps every write inside idx and val
+      idx[pos] = (uint32_t)(base + j);
+      val[pos] = a[base + j];
+      a[base + j] = 0.0f;
+      ++pos;
     }
   }
 }
 
-// Kept elements to (index, value) in index order; zero their residual.
+// Kept elements to (index, value) in index order; zero their residual. Each
+// block covers kWarps tiles.
 __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
-  if (!w.st->overflow) emit_slots(A, w, r, blockIdx.x);
-  else emit_masks(A, w, r, blockIdx.x);
+  if (!w.st->overflow) {
+    emit_slots(A, w, r);
+  } else {
+    for (int t = 0; t < kWarps; ++t) {
+      const uint64_t tile = (uint64_t)blockIdx.x * kWarps + t;
+      if (tile >= A.nb) break;  // uniform across the block
+      emit_masks(A, w, r, tile);
+    }
+  }
 }
 
 // recv[r][idx_r[j]] = val_r[j] for every rank (outputs already zeroed)
@@ -639,11 +625,11 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 hgrid(hx, a.nranks);
   k_topk_pass1<VEC><<<hgrid, kThreads, 0, s>>>(a);
   if (a.k == 0) return cudaGetLastError();  // nothing kept: e = a
-  const dim3 tgrid((unsigned)a.nb, a.nranks);
-  k_topk_split<VEC><<<tgrid, kThreads, 0, s>>>(a);
+  k_topk_split<VEC><<<dim3((unsigned)a.nb, a.nranks), kThreads, 0, s>>>(a);
   k_topk_pass3<VEC><<<hgrid, kThreads, 0, s>>>(a);
-  k_topk_count<VEC><<<tgrid, kThreads, 0, s>>>(a);
-  k_topk_emit<<<tgrid, kThreads, 3 * a.slots * sizeof(uint32_t), s>>>(a);
+  const dim3 wgrid((unsigned)((a.nb + kWarps - 1) / kWarps), a.nranks);
+  k_topk_count<VEC><<<wgrid, kThreads, 0, s>>>(a);
+  k_topk_emit<<<wgrid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -16,29 +16,28 @@ namespace gar {
 constexpr int kTopkElems = 16;                                 // values per run
 constexpr int kTopkRuns = 4;                                   // runs per thread
 constexpr int kTopkBlock = kThreads * kTopkRuns * kTopkElems;  // values per tile
-constexpr uint32_t kTopkMaxSlots = 4032;  // slot cap per tile and class (3 * 4032 words of shared memory fit 48 KiB)
+constexpr uint32_t kTopkMaxSlots = 8192;                       // slot cap per tile
 
 // Per-rank workspace, in 32-bit words (a multiple of 64 words, 256 bytes):
 //   [0, 2048)        histogram of the current radix pass
 //   [2048, 2064)     TopkState
-//   then nb words each of n_gt, n_eq, eq_before, out_off, n_a, n_c (nb = tiles)
+//   then nb words each of n_gt, n_eq, eq_before, out_off, n_s (nb = tiles)
 //   then nb * kThreads * kTopkRuns words of run masks (used only when a
 //   tile's slots overflow): for the kTopkElems values of a run, bit j (j < 16)
 //   set if value j's key is above T, bit 16 + j if it equals T
-//   then per tile 4 * S words of slots: S indices and S values of the tile's
-//   keys above the first digit's bin (class A, all kept), then S indices and
-//   S values of the keys inside that bin (class C, the candidates), each in
-//   index order
+//   then per tile 2 * S words of slots: the indices, then the values, of the
+//   tile's keys at or above the first digit's bin (every key that can be
+//   kept), in index order; n_s[tile] of them
 constexpr int kTopkHistWords = 2048;
 constexpr int kTopkStateWords = 16;
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
 
-// Slot capacity per tile and class: four times the tile's share of k plus a
-// margin, a multiple of 32, at most kTopkMaxSlots and at most a tile.
+// Slot capacity per tile: eight times the tile's share of k plus a margin, a
+// multiple of 32, at most kTopkMaxSlots and at most a tile.
 inline uint32_t topk_slots(uint64_t count, uint64_t k) {
   if (count == 0) return 32;
   const uint64_t share = (k * kTopkBlock + count - 1) / count;
-  uint64_t s = (4 * share + 256 + 31) / 32 * 32;
+  uint64_t s = (8 * share + 512 + 31) / 32 * 32;
   const uint64_t tile = count < (uint64_t)kTopkBlock ? (count + 31) / 32 * 32 : (uint64_t)kTopkBlock;
   if (s > tile) s = tile;
   if (s > kTopkMaxSlots) s = kTopkMaxSlots;
@@ -47,8 +46,8 @@ inline uint32_t topk_slots(uint64_t count, uint64_t k) {
 
 inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
   const uint64_t nb = topk_blocks(count);
-  return (kTopkHistWords + kTopkStateWords + (6 + (uint64_t)kThreads * kTopkRuns) * nb +
-          4ull * topk_slots(count, k) * nb + 63) / 64 * 64;
+  return (kTopkHistWords + kTopkStateWords + (5 + (uint64_t)kThreads * kTopkRuns) * nb +
+          2ull * topk_slots(count, k) * nb + 63) / 64 * 64;
 }
 
 // Radix-select state of one rank, kept on the device between the passes. The
@@ -60,8 +59,9 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //   gt:          keys strictly above the prefix (all kept)
 //   ticket[p]:   blocks of pass p that have finished (the last one to finish
 //                carries out the pass's single-block step)
-//   overflow:    nonzero if some tile had more class-A or class-C keys than
-//                its slots hold; the later passes then read the data instead
+//   overflow:    nonzero if some tile had more keys at or above the first
+//                digit's bin than its slots hold; the later passes then read
+//                the data instead
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -85,7 +85,7 @@ struct TopkArgs {
   uint64_t count;
   uint64_t nb;
   uint32_t k;
-  uint32_t slots;  // S, slot capacity per tile and class
+  uint32_t slots;  // S, slot capacity per tile
   int nranks;
 };
 
