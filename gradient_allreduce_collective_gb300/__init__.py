@@ -20,7 +20,7 @@ __all__ = [
     "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_reduce_scatter", "ar_all_gather",
     "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
     "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops", "ar_allreduce_fp8_noalloc",
-    "ar_topk_workspace_bytes", "ar_topk_compress", "ar_sparse_allreduce",
+    "ar_topk_workspace_bytes", "ar_topk_compress", "ar_sparse_workspace_bytes", "ar_sparse_allreduce",
     "ar_status_string", "ar_last_error", "ar_version",
     "DTYPES", "OPS", "ALGOS", "Comm", "CallRecord",
 ]
@@ -80,7 +80,9 @@ def lib() -> ctypes.CDLL:
     L.ar_topk_workspace_bytes.argtypes = [ci, sz, sz]
     L.ar_topk_workspace_bytes.restype = sz
     L.ar_topk_compress.argtypes = [pp, pp, ci, sz, sz, pp, pp, vp, sz, vp]
-    L.ar_sparse_allreduce.argtypes = [pp, pp, vp, ci, sz, ci, ci, pp, vp]
+    L.ar_sparse_workspace_bytes.argtypes = [ci, sz]
+    L.ar_sparse_workspace_bytes.restype = sz
+    L.ar_sparse_allreduce.argtypes = [pp, pp, vp, ci, sz, ci, ci, pp, vp, sz, vp]
     for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
                  "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops",
                  "ar_topk_compress", "ar_sparse_allreduce"):
@@ -301,10 +303,17 @@ def ar_topk_compress(grads: Sequence[torch.Tensor], residuals: Sequence[torch.Te
                                   _stream(stream)))
 
 
+def ar_sparse_workspace_bytes(nranks: int, count: int) -> int:
+    return int(lib().ar_sparse_workspace_bytes(nranks, count))
+
+
 def ar_sparse_allreduce(idx: Sequence[torch.Tensor], val: Sequence[torch.Tensor], nnz: Sequence[int],
-                        recvbufs: Sequence[torch.Tensor], op: str = "sum", algo: str = "fused", stream=None) -> None:
+                        recvbufs: Sequence[torch.Tensor], op: str = "sum", algo: str = "fused",
+                        workspace: torch.Tensor | None = None, stream=None) -> None:
     """Allreduce of each rank's sparse vector (idx[r][:nnz[r]], val[r][:nnz[r]])
-    into the dense float32 recvbufs (see include/ar.h)."""
+    into the dense float32 recvbufs (see include/ar.h); SUM and AVG need a
+    workspace of ar_sparse_workspace_bytes(nranks, count) bytes and ascending
+    indices."""
     n = len(recvbufs)
     if len(idx) != n or len(val) != n or len(nnz) != n:
         raise ValueError("one idx, val, nnz and output per rank")
@@ -316,8 +325,10 @@ def ar_sparse_allreduce(idx: Sequence[torch.Tensor], val: Sequence[torch.Tensor]
         if idx[r].numel() < nnz[r] or val[r].numel() < nnz[r]:
             raise ValueError("idx and val need nnz entries")
     counts = (ctypes.c_size_t * n)(*nnz)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().ar_sparse_allreduce(_ptrs(idx), _ptrs(val), counts, n, count, OPS[op], ALGOS[algo],
-                                     _ptrs(recvbufs), _stream(stream)))
+                                     _ptrs(recvbufs), ws_ptr, ws_len, _stream(stream)))
 
 
 class Comm:

@@ -612,6 +612,92 @@ __global__ void __launch_bounds__(kThreads) k_sparse_scatter(const __grid_consta
   }
 }
 
+// Tile starts of the sparse fold: thread j of rank r (0 <= j <= nnz) writes
+// starts[t] = j for the tiles t after the tile of pair j - 1 up to the tile
+// of pair j (pairs with an index >= count, and j = nnz, count as tile
+// ntiles). With ascending indices every entry is written once; otherwise the
+// fold clamps what it reads.
+__global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constant__ SparseArgs A) {
+  const int r = blockIdx.y;
+  const uint64_t nnz = A.nnz[r];
+  const uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j > nnz) return;
+  const uint32_t* __restrict__ ix = A.idx[r];
+  auto tile_of = [&](uint64_t p) -> int64_t {
+    if (p >= nnz) return A.ntiles;
+    const uint32_t i = ix[p];
+    return i < A.count ? (int64_t)(i / A.tile) : (int64_t)A.ntiles;
+  };
+  const int64_t prev = j == 0 ? -1 : tile_of(j - 1);
+  const int64_t cur = tile_of(j);
+  uint32_t* st = A.starts + (uint64_t)r * (A.ntiles + 1);
+  for (int64_t t = prev + 1; t <= cur; ++t) st[t] = (uint32_t)j;
+}
+
+// One tile per block: every rank's pairs of the tile scattered into shared
+// memory (zeros elsewhere), folded per element in the ring order of its
+// chunk (or recursive halving), divided by N for AVG, and stored to all N
+// outputs. The dense allreduce of the densified vectors gives the same bits.
+__global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant__ SparseArgs A) {
+  extern __shared__ float sm[];  // nranks x tile
+  const int N = A.nranks;
+  const uint32_t T = A.tile;
+  const uint64_t t = blockIdx.x;
+  const uint64_t i0 = t * T;
+  const uint32_t len = (uint32_t)(A.count - i0 < T ? A.count - i0 : T);
+  float4* sm4 = reinterpret_cast<float4*>(sm);
+  for (uint32_t q = threadIdx.x; q < (uint32_t)N * T / 4; q += blockDim.x) sm4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  for (int r = 0; r < N; ++r) {
+    const uint32_t* st = A.starts + (uint64_t)r * (A.ntiles + 1);
+    const uint64_t nnz = A.nnz[r];
+    const uint64_t s = st[t] < nnz ? st[t] : nnz;
+    const uint64_t e = st[t + 1] < nnz ? (st[t + 1] > s ? st[t + 1] : s) : nnz;
+    const uint32_t* __restrict__ ix = A.idx[r];
+    const float* __restrict__ vx = A.val[r];
+    for (uint64_t p = s + threadIdx.x; p < e; p += blockDim.x) {
+      const uint64_t d = (uint64_t)ix[p] - i0;
+      if (d < len) sm[(uint32_t)r * T + (uint32_t)d] = vx[p];
+    }
+  }
+  __syncthreads();
+  // four consecutive elements per thread: one chunk (L is a multiple of 4)
+  for (uint32_t q = threadIdx.x * 4; q < len; q += blockDim.x * 4) {
+    const uint64_t i = i0 + q;
+    float acc[4];
+    if (A.tree) {
+      for (int d = N >> 1; d >= 1; d >>= 1)
+        for (int r = 0; r < d; ++r)
+#pragma unroll
+          for (int l = 0; l < 4; ++l)
+            sm[(uint32_t)r * T + q + l] = __fadd_rn(sm[(uint32_t)r * T + q + l], sm[(uint32_t)(r + d) * T + q + l]);
+#pragma unroll
+      for (int l = 0; l < 4; ++l) acc[l] = sm[q + l];
+    } else {
+      const int c = (int)(i / A.L);
+      int r = c + 1 >= N ? c + 1 - N : c + 1;
+#pragma unroll
+      for (int l = 0; l < 4; ++l) acc[l] = sm[(uint32_t)r * T + q + l];
+      for (int j = 1; j < N; ++j) {
+        r = r + 1 == N ? 0 : r + 1;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) acc[l] = __fadd_rn(acc[l], sm[(uint32_t)r * T + q + l]);
+      }
+    }
+    if (A.avg) {
+#pragma unroll
+      for (int l = 0; l < 4; ++l) acc[l] = __fdiv_rn(acc[l], (float)N);
+    }
+    if (A.vec && q + 4 <= len) {
+      const float4 o = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      for (int r = 0; r < N; ++r) __stcs(reinterpret_cast<float4*>(A.dst[r] + i), o);
+    } else {
+      for (int r = 0; r < N; ++r)
+        for (int l = 0; l < 4 && q + l < len; ++l) A.dst[r][i + l] = acc[l];
+    }
+  }
+}
+
 template <bool VEC>
 cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 one(1, a.nranks);
@@ -637,6 +723,12 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
 
 cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream) {
   return vec ? launch_topk_t<true>(a, stream) : launch_topk_t<false>(a, stream);
+}
+
+cudaError_t launch_sparse_fold(const SparseArgs& a, uint64_t max_nnz, cudaStream_t stream) {
+  k_sparse_bounds<<<dim3(grid_for(max_nnz + 1), a.nranks), kThreads, 0, stream>>>(a);
+  k_sparse_fold<<<a.ntiles, kThreads, (size_t)a.nranks * a.tile * sizeof(float), stream>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_sparse_scatter(const ScatterArgs& a, cudaStream_t stream) {
@@ -735,8 +827,14 @@ ar_status_t ar_topk_compress(const float* const* grads, float* const* residuals,
   return tk_ok();
 }
 
+size_t ar_sparse_workspace_bytes(int nranks, size_t count) {
+  if (nranks < 1 || nranks > AR_MAX_RANKS || count > 0xFFFFFFFFull) return 0;
+  return ((size_t)nranks * (gar::sparse_ntiles(count, nranks) + 1) * 4 + 255) / 256 * 256;
+}
+
 ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* val, const size_t* nnz, int nranks,
-                                size_t count, ar_op_t op, ar_algo_t algo, float* const* recvbufs, ar_stream_t stream) {
+                                size_t count, ar_op_t op, ar_algo_t algo, float* const* recvbufs, void* workspace,
+                                size_t ws_bytes, ar_stream_t stream) {
   if (!idx || !val || !nnz || !recvbufs) return tk_fail(AR_ERR_INVALID_ARGUMENT, "null array");
   if (nranks < 1 || nranks > AR_MAX_RANKS) return tk_fail(AR_ERR_INVALID_ARGUMENT, "nranks must be in 1..64");
   if (op < AR_SUM || op > AR_MAX) return tk_fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
@@ -745,12 +843,21 @@ ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* 
     return tk_fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
   if (count > 0xFFFFFFFFull) return tk_fail(AR_ERR_INVALID_ARGUMENT, "count must fit 32-bit indices");
   if (count == 0) return tk_ok();
+  const bool fold = op == AR_SUM || op == AR_AVG;
+  const size_t need = ar_sparse_workspace_bytes(nranks, count);
+  if (fold) {
+    if (!workspace) return tk_fail(AR_ERR_INVALID_ARGUMENT, "null workspace");
+    if (tk_addr(workspace) % 16) return tk_fail(AR_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+    if (ws_bytes < need) return tk_fail(AR_ERR_INVALID_ARGUMENT, "workspace too small");
+  }
   const size_t b = count * 4;
-  uint64_t tiles = 0;
+  uint64_t tiles = 0, max_nnz = 0;
   gar::ScatterArgs a{};
-  a.nranks = nranks;
-  a.count = count;
+  gar::SparseArgs f{};
+  a.nranks = f.nranks = nranks;
+  a.count = f.count = count;
   std::vector<Rng> outs;
+  if (fold) outs.push_back({tk_addr(workspace), tk_addr(workspace) + need});
   for (int r = 0; r < nranks; ++r) {
     if (nnz[r] > count) return tk_fail(AR_ERR_INVALID_ARGUMENT, "nnz exceeds count");
     if (!recvbufs[r] || (nnz[r] > 0 && (!idx[r] || !val[r])))
@@ -758,12 +865,13 @@ ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* 
     if (tk_addr(recvbufs[r]) % 4 || tk_addr(idx[r]) % 4 || tk_addr(val[r]) % 4)
       return tk_fail(AR_ERR_INVALID_ARGUMENT, "buffer not aligned to its element size");
     outs.push_back({tk_addr(recvbufs[r]), tk_addr(recvbufs[r]) + b});
-    a.idx[r] = idx[r];
-    a.val[r] = val[r];
-    a.dst[r] = recvbufs[r];
-    a.nnz[r] = nnz[r];
+    a.idx[r] = f.idx[r] = idx[r];
+    a.val[r] = f.val[r] = val[r];
+    a.dst[r] = f.dst[r] = recvbufs[r];
+    a.nnz[r] = f.nnz[r] = nnz[r];
     a.tile_start[r] = (uint32_t)tiles;
     tiles += (nnz[r] + gar::kThreads - 1) / gar::kThreads;
+    if (nnz[r] > max_nnz) max_nnz = nnz[r];
   }
   a.tile_start[nranks] = (uint32_t)tiles;
   if (any_overlap(outs)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
@@ -775,13 +883,27 @@ ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* 
     if (any_overlap(v)) return tk_fail(AR_ERR_ALIAS, "buffers overlap");
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fold) {
+    // one pass: densify each tile in shared memory, fold, store N replicas
+    f.starts = static_cast<uint32_t*>(workspace);
+    f.tile = gar::sparse_tile(nranks);
+    f.ntiles = (uint32_t)gar::sparse_ntiles(count, nranks);
+    f.L = (count / (size_t)nranks + (count % (size_t)nranks != 0) + 3) / 4 * 4;  // ar_allreduce's F32 chunk
+    f.avg = op == AR_AVG;
+    f.tree = algo == AR_ALGO_TREE || algo == AR_ALGO_STEP_TREE;
+    f.vec = 1;
+    for (int r = 0; r < nranks; ++r) f.vec = f.vec && tk_addr(recvbufs[r]) % 16 == 0;
+    const cudaError_t e = gar::launch_sparse_fold(f, max_nnz, s);
+    if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("sparse fold launch: ") + cudaGetErrorString(e));
+    return tk_ok();
+  }
+  // MIN / MAX: the dense forms in the outputs, then the dense allreduce in place
   for (int r = 0; r < nranks; ++r) {
     const cudaError_t e = cudaMemsetAsync(recvbufs[r], 0, b, s);
     if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("zeroing the outputs: ") + cudaGetErrorString(e));
   }
   const cudaError_t e = gar::launch_sparse_scatter(a, s);
   if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("sparse scatter launch: ") + cudaGetErrorString(e));
-  // the dense forms now sit in the outputs: allreduce them in place
   std::vector<const void*> in(recvbufs, recvbufs + nranks);
   std::vector<void*> out(recvbufs, recvbufs + nranks);
   return ar_allreduce(in.data(), out.data(), nranks, count, AR_F32, op, algo, stream);

@@ -101,10 +101,46 @@ struct ScatterArgs {
   int nranks;
 };
 
+// Allreduce (SUM or AVG) of sparse vectors without dense copies: the output
+// is cut into tiles of `tile` elements; starts[r * (ntiles + 1) + t] is the
+// first pair of rank r whose index lies in tile t or later (rank r's pairs
+// in ascending index order). Each block densifies every rank's pairs of one
+// tile in shared memory (absent entries +0) and folds them in the ring order
+// of chunk length L (or the recursive-halving order when `tree`).
+struct SparseArgs {
+  const uint32_t* idx[kMaxRanks];
+  const float* val[kMaxRanks];
+  float* dst[kMaxRanks];
+  uint64_t nnz[kMaxRanks];
+  uint32_t* starts;
+  uint64_t count;
+  uint64_t L;
+  uint32_t tile;
+  uint32_t ntiles;
+  int nranks;
+  int avg;
+  int tree;
+  int vec;  // every dst 16-byte aligned
+};
+
+// Tile length of the sparse fold for N ranks: N * tile floats of shared
+// memory stay at 32 KiB (a multiple of 128 elements, 128..4096).
+inline uint32_t sparse_tile(int nranks) {
+  uint32_t t = 8192u / (uint32_t)nranks / 128u * 128u;
+  if (t < 128) t = 128;
+  if (t > 4096) t = 4096;
+  return t;
+}
+inline uint64_t sparse_ntiles(uint64_t count, int nranks) {
+  return (count + sparse_tile(nranks) - 1) / sparse_tile(nranks);
+}
+
 // For every rank: a = g + e into e; (idx, val) = the k largest |a| in index
 // order (ties: lower index first); e = a with those entries zeroed. `vec`:
 // every g and e is 16-byte aligned.
 cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream);
 cudaError_t launch_sparse_scatter(const ScatterArgs& a, cudaStream_t stream);
+// max_nnz: the largest nnz over the ranks
+cudaError_t launch_sparse_fold(const SparseArgs& a, uint64_t max_nnz, cudaStream_t stream);
 
 }  // namespace gar

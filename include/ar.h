@@ -325,22 +325,37 @@ ar_status_t ar_topk_compress(const float *const *grads, float *const *residuals,
                              size_t k, uint32_t *const *idx, float *const *val, void *workspace, size_t ws_bytes,
                              ar_stream_t stream);
 
+/* Workspace bytes for ar_sparse_allreduce with SUM or AVG (a multiple of
+ * 256; about nranks * count / 2048 bytes); 0 if nranks is outside
+ * 1..AR_MAX_RANKS or count >= 2^32. */
+size_t ar_sparse_workspace_bytes(int nranks, size_t count);
+
 /* Allreduce of sparse vectors ([GL] §勾配圧縮技術): rank r contributes the
  * dense vector of length `count` that is zero except at idx[r][j] where it
  * holds val[r][j] (j < nnz[r]); every recvbufs[r] receives the allreduce of
- * those dense vectors, computed exactly as ar_allreduce of F32 buffers with
- * the same op and algo (bit-identical to it). The outputs are zeroed, the
- * pairs scattered into them, and the allreduce run in place.
+ * those dense vectors, bit-identical to ar_allreduce of F32 buffers holding
+ * them (+0 where absent) with the same op and algo.
+ *   SUM, AVG: one pass without dense copies — each tile of the output is
+ *     densified in shared memory from every rank's pairs and folded in the
+ *     order of `algo`; the output buffers are only written. Needs a device
+ *     workspace of ar_sparse_workspace_bytes(nranks, count), 16-byte aligned
+ *     (contents need no initialisation), and each rank's indices in strictly
+ *     ascending order (ar_topk_compress writes them so). Indices out of
+ *     order leave the result unspecified; every access stays inside the
+ *     buffers.
+ *   MIN, MAX: the outputs are zeroed, the pairs scattered into them and the
+ *     dense allreduce run in place; `workspace` is not used (may be null)
+ *     and any index order works.
  *   idx[r], val[r]: device arrays of nnz[r] entries; indices must be < count
- *     and distinct within a rank (ar_topk_compress output is both). An index
- *     >= count is dropped; which of two equal indices wins is unspecified.
+ *     and distinct within a rank. An index >= count is dropped; which of two
+ *     equal indices wins is unspecified.
  *   recvbufs[r]: F32 device buffers of `count`, 4-byte aligned, disjoint from
- *     each other and from every idx/val array.
- *   Errors: as ar_allreduce, plus AR_ERR_INVALID_ARGUMENT for nnz[r] > count
- *   or count >= 2^32. */
+ *     each other, from the workspace and from every idx/val array.
+ *   Errors: as ar_allreduce, plus AR_ERR_INVALID_ARGUMENT for nnz[r] > count,
+ *   count >= 2^32, or (SUM, AVG) a missing, misaligned or short workspace. */
 ar_status_t ar_sparse_allreduce(const uint32_t *const *idx, const float *const *val, const size_t *nnz, int nranks,
-                                size_t count, ar_op_t op, ar_algo_t algo, float *const *recvbufs,
-                                ar_stream_t stream);
+                                size_t count, ar_op_t op, ar_algo_t algo, float *const *recvbufs, void *workspace,
+                                size_t ws_bytes, ar_stream_t stream);
 
 /* Host-side communicator for virtual ranks driven by host threads
  * ([VL] §rankとcommunicator: every rank calls the matching collective with the

@@ -216,18 +216,25 @@ def test_sparse_allreduce_argument_errors(L):
     idx = [0x1000000 * (r + 1) for r in range(n)]
     val = [0x10000000 + 0x1000000 * r for r in range(n)]
     out = [0x20000000 + 0x1000000 * r for r in range(n)]
+    ws = 0x30000000
+    need = gar.ar_sparse_workspace_bytes(n, count)
+    tile = max(128, min(4096, 8192 // n // 128 * 128))
+    assert need == math.ceil(n * (math.ceil(count / tile) + 1) * 4 / 256) * 256
+    assert gar.ar_sparse_workspace_bytes(0, 10) == 0 and gar.ar_sparse_workspace_bytes(1, 1 << 32) == 0
     nnz = (ctypes.c_size_t * n)(10, 0, 1000, 5)
-    f = L.ar_sparse_allreduce
-    assert f(_arr(idx), _arr(val), (ctypes.c_size_t * n)(10, 0, 1001, 5), n, count, 0, 1, _arr(out), None) \
-        == gar.AR_ERR_INVALID_ARGUMENT  # nnz > count
-    assert f(_arr(idx), _arr(val), nnz, 3, count, 0, 2, _arr(out[:3]), None) == gar.AR_ERR_UNSUPPORTED  # tree, N=3
-    assert f(_arr(idx), _arr(val), nnz, n, count, 7, 1, _arr(out), None) == gar.AR_ERR_INVALID_ARGUMENT
-    assert f(_arr(idx), _arr(val), nnz, n, count, 0, 9, _arr(out), None) == gar.AR_ERR_INVALID_ARGUMENT
-    over = list(out)
-    over[2] = out[1] + 400
-    assert f(_arr(idx), _arr(val), nnz, n, count, 0, 1, _arr(over), None) == gar.AR_ERR_ALIAS
-    bad = list(idx)
-    bad[3] = out[0] + 8  # an index array inside an output
-    assert f(_arr(bad), _arr(val), nnz, n, count, 0, 1, _arr(out), None) == gar.AR_ERR_ALIAS
-    assert f(_arr(idx), _arr(val), nnz, n, 1 << 32, 0, 1, _arr(out), None) == gar.AR_ERR_INVALID_ARGUMENT
-    assert f(_arr(idx), _arr(val), nnz, n, 0, 0, 1, _arr(out), None) == gar.AR_SUCCESS
+
+    def f(idx=idx, val=val, nnz=nnz, n=n, count=count, op=0, algo=1, out=out, ws=ws, wsb=need):
+        return L.ar_sparse_allreduce(_arr(idx), _arr(val), nnz, n, count, op, algo, _arr(out), ws, wsb, None)
+
+    assert f(nnz=(ctypes.c_size_t * n)(10, 0, 1001, 5)) == gar.AR_ERR_INVALID_ARGUMENT  # nnz > count
+    assert f(n=3, algo=2, out=out[:3]) == gar.AR_ERR_UNSUPPORTED                        # tree, N=3
+    assert f(op=7) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(algo=9) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(ws=None) == gar.AR_ERR_INVALID_ARGUMENT                                    # SUM needs a workspace
+    assert f(wsb=need - 1) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(ws=ws + 4) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(ws=out[1] + 64) == gar.AR_ERR_ALIAS                                        # workspace inside an output
+    assert f(out=[out[0], out[0] + 400, out[2], out[3]]) == gar.AR_ERR_ALIAS
+    assert f(idx=idx[:3] + [out[0] + 8]) == gar.AR_ERR_ALIAS                            # an index array inside an output
+    assert f(count=1 << 32) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(count=0) == gar.AR_SUCCESS

@@ -186,7 +186,9 @@ def test_sparse_allreduce_matches_oracle(n):
     for op in ("sum", "avg", "max"):
         for algo in _algos(n):
             out = [torch.full((count,), float("nan"), device="cuda") for _ in range(n)]
-            gar.ar_sparse_allreduce(idx, val, nnz, out, op, algo)
+            ws = torch.empty(gar.ar_sparse_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+            ws.fill_(0x77)  # needs no initialisation
+            gar.ar_sparse_allreduce(idx, val, nnz, out, op, algo, ws)
             torch.cuda.synchronize()
             dense = [oracle.sparse_to_dense(i, v, count) for i, v in zip(idx_np, val_np)]
             if algo in ("tree", "step_tree"):
@@ -202,7 +204,8 @@ def test_sparse_allreduce_drops_out_of_range_indices():
     idx = torch.tensor([0, 999, 1000, 5000], dtype=torch.int32, device="cuda")
     val = torch.tensor([1.0, 2.0, 3.0, 4.0], device="cuda")
     out = [torch.full((count + 64,), 9.0, device="cuda")]
-    gar.ar_sparse_allreduce([idx], [val], [4], [out[0][:count]])
+    ws = torch.empty(gar.ar_sparse_workspace_bytes(1, count), dtype=torch.uint8, device="cuda")
+    gar.ar_sparse_allreduce([idx], [val], [4], [out[0][:count]], "sum", "fused", ws)
     torch.cuda.synchronize()
     h = from_dev(out[0])
     assert h[0] == 1.0 and h[999] == 2.0 and np.all(h[1:999] == 0.0) and np.all(h[count:] == 9.0)
@@ -240,7 +243,8 @@ def test_topk_full_size_eight_ranks():
     d_idx = [torch.from_numpy(i.view(np.int32)).cuda() for i in o_idx]
     d_val = [to_dev(v, "f32") for v in o_val]
     out = [torch.empty(count, device="cuda") for _ in range(n)]
-    gar.ar_sparse_allreduce(d_idx, d_val, [k] * n, out, "avg", "fused")
+    sws = torch.empty(gar.ar_sparse_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    gar.ar_sparse_allreduce(d_idx, d_val, [k] * n, out, "avg", "fused", sws)
     torch.cuda.synchronize()
     rng = np.random.default_rng(5)
     sample = np.unique(np.concatenate([rng.integers(0, count, 4000)] + [i[:64].astype(np.int64) for i in o_idx]))
@@ -248,3 +252,30 @@ def test_topk_full_size_eight_ranks():
     want = oracle.fold_points(vals, sample, count, "f32", "avg")
     for r in range(n):
         assert np.array_equal(_bits(from_dev(out[r])[sample]), _bits(want)), r
+
+
+def test_sparse_allreduce_unsorted_indices_stay_in_bounds():
+    # out-of-order indices give an unspecified sum but never an access outside
+    # the buffers: the canaries around every output stay intact
+    from tests._dev import Guarded
+    n, count, k = 4, 30_011, 3_000
+    rng = np.random.default_rng(7)
+    idx, val = [], []
+    for r in range(n):
+        i = rng.permutation(count)[:k].astype(np.int32)
+        idx.append(torch.from_numpy(i).cuda())
+        val.append(torch.from_numpy(rng.standard_normal(k).astype(np.float32)).cuda())
+    out = Guarded(n, count, "f32")
+    ws = torch.empty(gar.ar_sparse_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    gar.ar_sparse_allreduce(idx, val, [k] * n, out.views, "sum", "fused", ws)
+    out.check()
+    # sorted, the same pairs give the oracle's bits
+    order = [torch.argsort(i) for i in idx]
+    idx_s = [i[o].contiguous() for i, o in zip(idx, order)]
+    val_s = [v[o].contiguous() for v, o in zip(val, order)]
+    gar.ar_sparse_allreduce(idx_s, val_s, [k] * n, out.views, "sum", "fused", ws)
+    out.check()
+    want = oracle.sparse_ring_allreduce([from_dev(i).view(np.uint32) for i in idx_s], [from_dev(v) for v in val_s],
+                                        count, "sum")[0]
+    for r in range(n):
+        assert np.array_equal(_bits(from_dev(out.views[r])), _bits(want))
