@@ -648,14 +648,16 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
   float4* sm4 = reinterpret_cast<float4*>(sm);
   for (uint32_t q = threadIdx.x; q < (uint32_t)N * T / 4; q += blockDim.x) sm4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
-  for (int r = 0; r < N; ++r) {
+  // one warp per rank, so that the ranks' short lists are read concurrently
+  const int lane = threadIdx.x & 31;
+  for (int r = threadIdx.x >> 5; r < N; r += kWarps) {
     const uint32_t* st = A.starts + (uint64_t)r * (A.ntiles + 1);
     const uint64_t nnz = A.nnz[r];
     const uint64_t s = st[t] < nnz ? st[t] : nnz;
     const uint64_t e = st[t + 1] < nnz ? (st[t + 1] > s ? st[t + 1] : s) : nnz;
     const uint32_t* __restrict__ ix = A.idx[r];
     const float* __restrict__ vx = A.val[r];
-    for (uint64_t p = s + threadIdx.x; p < e; p += blockDim.x) {
+    for (uint64_t p = s + lane; p < e; p += 32) {
       const uint64_t d = (uint64_t)ix[p] - i0;
       if (d < len) sm[(uint32_t)r * T + (uint32_t)d] = vx[p];
     }
