@@ -280,7 +280,27 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   const uint32_t d1 = w.st->prefix >> 20;
   const uint32_t lo = d1 << 20;
   uint32_t m[kTopkRuns];
-  {
+  if (VEC && (tile + 1) * kTopkBlock <= count) {
+    // a whole tile: no bounds checks (the same for every thread of the block)
+    const float4* p = reinterpret_cast<const float4*>(a + tile * kTopkBlock);
+    float4 x[kTopkRuns][kTopkElems / 4];
+#pragma unroll
+    for (int u = 0; u < kTopkRuns; ++u)
+#pragma unroll
+      for (int q = 0; q < kTopkElems / 4; ++q) x[u][q] = p[(u * kThreads + threadIdx.x) * (kTopkElems / 4) + q];
+#pragma unroll
+    for (int u = 0; u < kTopkRuns; ++u) {
+      uint32_t b = 0;
+#pragma unroll
+      for (int q = 0; q < kTopkElems / 4; ++q) {
+        if (mag_key(x[u][q].x) >= lo) b |= 1u << (4 * q);
+        if (mag_key(x[u][q].y) >= lo) b |= 2u << (4 * q);
+        if (mag_key(x[u][q].z) >= lo) b |= 4u << (4 * q);
+        if (mag_key(x[u][q].w) >= lo) b |= 8u << (4 * q);
+      }
+      m[u] = b;
+    }
+  } else {
     float v[kTopkRuns][kTopkElems];
 #pragma unroll
     for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(a, run_base(tile, u), count, v[u]);
@@ -664,38 +684,40 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
   }
   __syncthreads();
   // four consecutive elements per thread: one chunk (L is a multiple of 4)
-  for (uint32_t q = threadIdx.x * 4; q < len; q += blockDim.x * 4) {
-    const uint64_t i = i0 + q;
-    float acc[4];
+  const float4* s4 = reinterpret_cast<const float4*>(sm);
+  float4* w4 = reinterpret_cast<float4*>(sm);
+  const uint32_t T4 = T / 4;
+  for (uint32_t q = threadIdx.x; q * 4 < len; q += blockDim.x) {
+    const uint64_t i = i0 + 4ull * q;
+    float4 acc;
     if (A.tree) {
       for (int d = N >> 1; d >= 1; d >>= 1)
-        for (int r = 0; r < d; ++r)
-#pragma unroll
-          for (int l = 0; l < 4; ++l)
-            sm[(uint32_t)r * T + q + l] = __fadd_rn(sm[(uint32_t)r * T + q + l], sm[(uint32_t)(r + d) * T + q + l]);
-#pragma unroll
-      for (int l = 0; l < 4; ++l) acc[l] = sm[q + l];
+        for (int r = 0; r < d; ++r) {
+          const float4 x = s4[(uint32_t)r * T4 + q], y = s4[(uint32_t)(r + d) * T4 + q];
+          w4[(uint32_t)r * T4 + q] =
+              make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z), __fadd_rn(x.w, y.w));
+        }
+      acc = s4[q];
     } else {
-      const int c = (int)(i / A.L);
-      int r = c + 1 >= N ? c + 1 - N : c + 1;
-#pragma unroll
-      for (int l = 0; l < 4; ++l) acc[l] = sm[(uint32_t)r * T + q + l];
+      const uint32_t c = (uint32_t)i / (uint32_t)A.L;  // indices fit 32 bits
+      int r = (int)c + 1 >= N ? (int)c + 1 - N : (int)c + 1;
+      acc = s4[(uint32_t)r * T4 + q];
       for (int j = 1; j < N; ++j) {
         r = r + 1 == N ? 0 : r + 1;
-#pragma unroll
-        for (int l = 0; l < 4; ++l) acc[l] = __fadd_rn(acc[l], sm[(uint32_t)r * T + q + l]);
+        const float4 y = s4[(uint32_t)r * T4 + q];
+        acc = make_float4(__fadd_rn(acc.x, y.x), __fadd_rn(acc.y, y.y), __fadd_rn(acc.z, y.z), __fadd_rn(acc.w, y.w));
       }
     }
     if (A.avg) {
-#pragma unroll
-      for (int l = 0; l < 4; ++l) acc[l] = __fdiv_rn(acc[l], (float)N);
+      const float n = (float)N;
+      acc = make_float4(__fdiv_rn(acc.x, n), __fdiv_rn(acc.y, n), __fdiv_rn(acc.z, n), __fdiv_rn(acc.w, n));
     }
-    if (A.vec && q + 4 <= len) {
-      const float4 o = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      for (int r = 0; r < N; ++r) __stcs(reinterpret_cast<float4*>(A.dst[r] + i), o);
+    if (A.vec && 4 * q + 4 <= len) {
+      for (int r = 0; r < N; ++r) __stcs(reinterpret_cast<float4*>(A.dst[r] + i), acc);
     } else {
+      const float o[4] = {acc.x, acc.y, acc.z, acc.w};
       for (int r = 0; r < N; ++r)
-        for (int l = 0; l < 4 && q + l < len; ++l) A.dst[r][i + l] = acc[l];
+        for (uint32_t l = 0; l < 4 && 4 * q + l < len; ++l) A.dst[r][i + l] = o[l];
     }
   }
 }
