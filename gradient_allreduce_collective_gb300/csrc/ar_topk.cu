@@ -35,6 +35,7 @@ void set_last_error(const std::string& msg);
 namespace {
 
 constexpr int kHistBlocksPerSm = 8;
+constexpr int kSplitBlocksPerSm = 3;  // the register budget of k_topk_split
 constexpr int kSms = 152;
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
@@ -106,14 +107,18 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
 
 // Called by every thread of a block after its global writes for this pass:
 // true in the block that finishes last among the gridDim.x blocks of its
-// rank. No block waits for another.
+// rank. The barrier orders the block's writes before thread 0's fence and
+// ticket (the fence is cumulative over what the barrier made visible to it).
+// No block waits for another.
 __device__ __forceinline__ bool last_block(uint32_t* ticket) {
   __shared__ bool s_last;
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    if (s_last) __threadfence();
+  }
   __syncthreads();
-  if (s_last) __threadfence();
   return s_last;
 }
 
@@ -262,86 +267,89 @@ __device__ __forceinline__ uint32_t ge_mask(const float (&v)[kTopkElems], uint64
   return m;
 }
 
-// Pass 2, one tile per block: the tile's keys at or above the first digit's
-// bin (every key that can still be kept) compacted in index order into the
-// tile's slots, and the histogram of bits 19..10 of the keys inside that
-// bin; then (last block) the second digit. The sparse work runs over the set
-// bits of each run's mask, re-reading those few values from the cache.
+// Pass 2, a resident grid looping over the tiles: each tile's keys at or
+// above the first digit's bin (every key that can still be kept) compacted in
+// index order into the tile's slots, and the histogram of bits 19..10 of the
+// keys inside that bin; then (last block) the second digit. The sparse work
+// runs over the set bits of each run's mask, re-reading those few values
+// from the cache.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__ TopkArgs A) {
   __shared__ uint32_t sh[1024];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
-  const uint64_t tile = blockIdx.x;
   const uint64_t count = A.count;
   const float* __restrict__ a = A.e[r];
   const uint32_t S = A.slots;
   for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
   const uint32_t d1 = w.st->prefix >> 20;
   const uint32_t lo = d1 << 20;
-  uint32_t m[kTopkRuns];
-  if (VEC && (tile + 1) * kTopkBlock <= count) {
-    // a whole tile: no bounds checks (the same for every thread of the block)
-    const float4* p = reinterpret_cast<const float4*>(a + tile * kTopkBlock);
-    float4 x[kTopkRuns][kTopkElems / 4];
+  __syncthreads();
+  for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
+    uint32_t m[kTopkRuns];
+    if (VEC && (tile + 1) * kTopkBlock <= count) {
+      // a whole tile: no bounds checks (the same for every thread of the block)
+      const float4* p = reinterpret_cast<const float4*>(a + tile * kTopkBlock);
+      float4 x[kTopkRuns][kTopkElems / 4];
 #pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u)
+      for (int u = 0; u < kTopkRuns; ++u)
 #pragma unroll
-      for (int q = 0; q < kTopkElems / 4; ++q) x[u][q] = p[(u * kThreads + threadIdx.x) * (kTopkElems / 4) + q];
+        for (int q = 0; q < kTopkElems / 4; ++q) x[u][q] = p[(u * kThreads + threadIdx.x) * (kTopkElems / 4) + q];
+#pragma unroll
+      for (int u = 0; u < kTopkRuns; ++u) {
+        uint32_t b = 0;
+#pragma unroll
+        for (int q = 0; q < kTopkElems / 4; ++q) {
+          if (mag_key(x[u][q].x) >= lo) b |= 1u << (4 * q);
+          if (mag_key(x[u][q].y) >= lo) b |= 2u << (4 * q);
+          if (mag_key(x[u][q].z) >= lo) b |= 4u << (4 * q);
+          if (mag_key(x[u][q].w) >= lo) b |= 8u << (4 * q);
+        }
+        m[u] = b;
+      }
+    } else {
+      float v[kTopkRuns][kTopkElems];
+#pragma unroll
+      for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(a, run_base(tile, u), count, v[u]);
+#pragma unroll
+      for (int u = 0; u < kTopkRuns; ++u) m[u] = ge_mask(v[u], run_base(tile, u), count, lo);
+    }
+    // slot positions in index order (all runs of u = 0, then u = 1, ...):
+    // runs 0 and 1, and runs 2 and 3, share one scan of two 16-bit counts
+    uint32_t t01, t23;
+    const uint32_t e01 = block_exclusive_scan((uint32_t)__popc(m[0]) | ((uint32_t)__popc(m[1]) << 16), &t01);
+    const uint32_t e23 = block_exclusive_scan((uint32_t)__popc(m[2]) | ((uint32_t)__popc(m[3]) << 16), &t23);
+    const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
+    uint32_t pos[kTopkRuns];
+    pos[0] = e01 & 0xFFFFu;
+    pos[1] = tot0 + (e01 >> 16);
+    pos[2] = tot0 + tot1 + (e23 & 0xFFFFu);
+    pos[3] = tot0 + tot1 + tot2 + (e23 >> 16);
+    uint32_t* __restrict__ si = slot_idx(w, tile, S);
+    float* __restrict__ sv = slot_val(w, tile, S);
 #pragma unroll
     for (int u = 0; u < kTopkRuns; ++u) {
-      uint32_t b = 0;
-#pragma unroll
-      for (int q = 0; q < kTopkElems / 4; ++q) {
-        if (mag_key(x[u][q].x) >= lo) b |= 1u << (4 * q);
-        if (mag_key(x[u][q].y) >= lo) b |= 2u << (4 * q);
-        if (mag_key(x[u][q].z) >= lo) b |= 4u << (4 * q);
-        if (mag_key(x[u][q].w) >= lo) b |= 8u << (4 * q);
+      const uint64_t base = run_base(tile, u);
+      uint32_t bits = m[u];
+      uint32_t p = pos[u];
+      while (bits) {
+        const int j = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const float x = a[base + j];
+        const uint32_t key = mag_key(x);
+        if ((key >> 20) == d1) atomicAdd(&sh[(key >> 10) & 1023u], 1u);
+        if (p < S) {
+          si[p] = (uint32_t)(base + j);
+          sv[p] = x;
+        }
+        ++p;
       }
-      m[u] = b;
     }
-  } else {
-    float v[kTopkRuns][kTopkElems];
-#pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(a, run_base(tile, u), count, v[u]);
-#pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) m[u] = ge_mask(v[u], run_base(tile, u), count, lo);
-  }
-  // slot positions in index order (all runs of u = 0, then u = 1, ...):
-  // runs 0 and 1, and runs 2 and 3, share one scan of two 16-bit counts
-  uint32_t t01, t23;
-  const uint32_t e01 = block_exclusive_scan((uint32_t)__popc(m[0]) | ((uint32_t)__popc(m[1]) << 16), &t01);
-  const uint32_t e23 = block_exclusive_scan((uint32_t)__popc(m[2]) | ((uint32_t)__popc(m[3]) << 16), &t23);
-  const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
-  uint32_t pos[kTopkRuns];
-  pos[0] = e01 & 0xFFFFu;
-  pos[1] = tot0 + (e01 >> 16);
-  pos[2] = tot0 + tot1 + (e23 & 0xFFFFu);
-  pos[3] = tot0 + tot1 + tot2 + (e23 >> 16);
-  uint32_t* __restrict__ si = slot_idx(w, tile, S);
-  float* __restrict__ sv = slot_val(w, tile, S);
-#pragma unroll
-  for (int u = 0; u < kTopkRuns; ++u) {
-    const uint64_t base = run_base(tile, u);
-    uint32_t bits = m[u];
-    uint32_t p = pos[u];
-    while (bits) {
-      const int j = __ffs(bits) - 1;
-      bits &= bits - 1;
-      const float x = a[base + j];
-      const uint32_t key = mag_key(x);
-      if ((key >> 20) == d1) atomicAdd(&sh[(key >> 10) & 1023u], 1u);
-      if (p < S) {
-        si[p] = (uint32_t)(base + j);
-        sv[p] = x;
-      }
-      ++p;
+    if (threadIdx.x == 0) {
+      const uint32_t n = tot0 + tot1 + tot2 + tot3;
+      w.n_s[tile] = n;
+      if (n > S) atomicOr(&w.st->overflow, 1u);
     }
-  }
-  if (threadIdx.x == 0) {
-    const uint32_t n = tot0 + tot1 + tot2 + tot3;
-    w.n_s[tile] = n;
-    if (n > S) atomicOr(&w.st->overflow, 1u);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 1024; i += blockDim.x)
@@ -368,6 +376,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
       const float* sv = slot_val(w, tile, A.slots);
       const uint32_t n = w.n_s[tile];
+#pragma unroll 4
       for (uint32_t c = threadIdx.x; c < n; c += blockDim.x) add(sv[c]);
     }
   } else {
@@ -466,6 +475,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__
       const float* sv = slot_val(w, tile, A.slots);
       const uint32_t n = w.n_s[tile];
       uint32_t gt = 0, eq = 0;
+#pragma unroll 4
       for (uint32_t c = lane; c < n; c += 32) {
         const uint32_t key = mag_key(sv[c]);
         gt += key > T;
@@ -522,27 +532,33 @@ __device__ void emit_slots(const TopkArgs& A, const RankWs& w, int r) {
   uint32_t* __restrict__ idx = A.idx[r];
   float* __restrict__ val = A.val[r];
   const uint32_t lt = (1u << lane) - 1u;
-  for (uint32_t c0 = 0; c0 < n; c0 += 32) {
-    const uint32_t c = c0 + lane;
-    uint32_t key = 0, i = 0;
-    float x = 0.0f;
-    if (c < n) {
-      x = sv[c];
-      i = si[c];
-      key = mag_key(x);
+  constexpr int U = 4;  // rounds of 32 slots whose loads are issued together
+  for (uint32_t c0 = 0; c0 < n; c0 += 32 * U) {
+    float x[U];
+    uint32_t ii[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t c = c0 + 32 * u + lane;
+      x[u] = c < n ? sv[c] : 0.0f;
+      ii[u] = c < n ? si[c] : 0u;
     }
-    const bool eq = c < n && key == T;
-    const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
-    const bool keep = c < n && (key > T || (eq && eq_run + (uint32_t)__popc(eq_bal & lt) < need));
-    const uint32_t keep_bal = __ballot_sync(0xffffffffu, keep);
-    const uint32_t p = pos_run + (uint32_t)__popc(keep_bal & lt);
-    if (keep && p < A.k) {  // p < k always holds; the test keeps every write inside idx and val
-      idx[p] = i;
-      val[p] = x;
-      e[i] = 0.0f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t c = c0 + 32 * u + lane;
+      const uint32_t key = mag_key(x[u]);
+      const bool eq = c < n && key == T;
+      const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
+      const bool keep = c < n && (key > T || (eq && eq_run + (uint32_t)__popc(eq_bal & lt) < need));
+      const uint32_t keep_bal = __ballot_sync(0xffffffffu, keep);
+      const uint32_t p = pos_run + (uint32_t)__popc(keep_bal & lt);
+      if (keep && p < A.k) {  // p < k always holds; the test keeps every write inside idx and val
+        idx[p] = ii[u];
+        val[p] = x[u];
+        e[ii[u]] = 0.0f;
+      }
+      eq_run += (uint32_t)__popc(eq_bal);
+      pos_run += (uint32_t)__popc(keep_bal);
     }
-    eq_run += (uint32_t)__popc(eq_bal);
-    pos_run += (uint32_t)__popc(keep_bal);
   }
 }
 
@@ -735,7 +751,10 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 hgrid(hx, a.nranks);
   k_topk_pass1<VEC><<<hgrid, kThreads, 0, s>>>(a);
   if (a.k == 0) return cudaGetLastError();  // nothing kept: e = a
-  k_topk_split<VEC><<<dim3((unsigned)a.nb, a.nranks), kThreads, 0, s>>>(a);
+  unsigned sx = (unsigned)(kSms * kSplitBlocksPerSm / a.nranks);
+  if (sx < 1) sx = 1;
+  if (sx > a.nb) sx = (unsigned)a.nb;
+  k_topk_split<VEC><<<dim3(sx, a.nranks), kThreads, 0, s>>>(a);
   k_topk_pass3<VEC><<<hgrid, kThreads, 0, s>>>(a);
   const dim3 wgrid((unsigned)((a.nb + kWarps - 1) / kWarps), a.nranks);
   k_topk_count<VEC><<<wgrid, kThreads, 0, s>>>(a);
