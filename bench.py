@@ -587,12 +587,25 @@ def measure_topk(gar, steps: int, warmup: int, count: int = COUNT, frac: float =
     ms = time_steps(step, steps, stream)
     ms_c = time_steps(compress, steps, stream)
     ms_s = time_steps(sparse_ar, steps, stream)
+    # the same step as one CUDA graph (host launch cost removed)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        g.capture_begin()
+        gar.ar_topk_compress(grads, res, k, idx, val, ws, side)
+        gar.ar_sparse_allreduce(idx, val, [k] * n, out, "avg", "fused", sws, side)
+        g.capture_end()
+    stream.wait_stream(side)
+    for _ in range(3):
+        g.replay()
+    ms_graph = time_steps(g.replay, steps, stream)
     M = count * 4
     min_c = n * 3 * M + n * k * 8          # read g and e, write e; the pairs
     struct_c = n * (3 * M + M) + 3 * n * k * 8  # + pass 2; the pairs into the slots, out of them, out
     sparse_b = n * M + n * k * 8  # the N outputs written once, the pairs read
     peak, _ = hbm_peak()
-    del grads, res, idx, val, out, ws, sws
+    del grads, res, idx, val, out, ws, sws, g
     torch.cuda.empty_cache()
     cpu = None
     if with_oracle:
@@ -618,6 +631,7 @@ def measure_topk(gar, steps: int, warmup: int, count: int = COUNT, frac: float =
                     f"k = {k:,} ({frac:.0%}) per rank, residual carried across steps; then the allreduce (avg, "
                     "fused ring order) of the sparse vectors",
         "ms_per_step": ms,
+        "ms_per_step_graph": ms_graph,
         "compress": {"ms": ms_c, "launches": 6, "min_bytes": min_c, "structure_bytes": struct_c,
                      "full_data_passes": 2,
                      "hbm_gbs_min_bytes": min_c / (ms_c * 1e-3) / 1e9,

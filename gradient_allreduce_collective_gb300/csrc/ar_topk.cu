@@ -36,6 +36,7 @@ namespace {
 
 constexpr int kHistBlocksPerSm = 8;
 constexpr int kSplitBlocksPerSm = 3;  // the register budget of k_topk_split
+constexpr int kPass1BlocksPerSm = 5;  // k_topk_pass1 keeps 8 float4 loads in flight per thread
 constexpr int kSms = 152;
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
@@ -178,7 +179,7 @@ __device__ __forceinline__ float4 add4(float4 x, float4 y) {
 // Pass 1: a = g + e into e, histogram of bits 30..20 of |a|, then (last
 // block, if k > 0) the first digit.
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads) k_topk_pass1(const __grid_constant__ TopkArgs A) {
+__global__ void __launch_bounds__(kThreads, kPass1BlocksPerSm) k_topk_pass1(const __grid_constant__ TopkArgs A) {
   __shared__ uint32_t sh[2048];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
@@ -195,28 +196,31 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass1(const __grid_constant__
     const float4* g4 = reinterpret_cast<const float4*>(g);
     float4* e4 = reinterpret_cast<float4*>(e);
     uint64_t q = t0;
-    for (; q + stride < n4; q += 2 * stride) {
-      const float4 x0 = __ldcs(g4 + q), x1 = __ldcs(g4 + q + stride);
-      const float4 y0 = e4[q], y1 = e4[q + stride];
-      const float4 s0 = add4(x0, y0), s1 = add4(x1, y1);
-      e4[q] = s0;
-      e4[q + stride] = s1;
-      atomicAdd(&sh[mag_key(s0.x) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s0.y) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s0.z) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s0.w) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s1.x) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s1.y) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s1.z) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s1.w) >> 20], 1u);
+    // four float4 of g and of e in flight per thread (128 bytes)
+    for (; q + 3 * stride < n4; q += 4 * stride) {
+      float4 x[4], y[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        x[u] = __ldcs(g4 + q + u * stride);
+        y[u] = e4[q + u * stride];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 s4 = add4(x[u], y[u]);
+        e4[q + u * stride] = s4;
+        atomicAdd(&sh[mag_key(s4.x) >> 20], 1u);
+        atomicAdd(&sh[mag_key(s4.y) >> 20], 1u);
+        atomicAdd(&sh[mag_key(s4.z) >> 20], 1u);
+        atomicAdd(&sh[mag_key(s4.w) >> 20], 1u);
+      }
     }
-    if (q < n4) {
-      const float4 s = add4(__ldcs(g4 + q), e4[q]);
-      e4[q] = s;
-      atomicAdd(&sh[mag_key(s.x) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s.y) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s.z) >> 20], 1u);
-      atomicAdd(&sh[mag_key(s.w) >> 20], 1u);
+    for (; q < n4; q += stride) {
+      const float4 s4 = add4(__ldcs(g4 + q), e4[q]);
+      e4[q] = s4;
+      atomicAdd(&sh[mag_key(s4.x) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s4.y) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s4.z) >> 20], 1u);
+      atomicAdd(&sh[mag_key(s4.w) >> 20], 1u);
     }
     done = n4 * 4;
   }
@@ -749,7 +753,10 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   if (per_rank < 1) per_rank = 1;
   const unsigned hx = grid_for(items) < per_rank ? grid_for(items) : per_rank;
   const dim3 hgrid(hx, a.nranks);
-  k_topk_pass1<VEC><<<hgrid, kThreads, 0, s>>>(a);
+  unsigned p1 = (unsigned)(kSms * kPass1BlocksPerSm / a.nranks);
+  if (p1 < 1) p1 = 1;
+  const unsigned p1x = grid_for(items) < p1 ? grid_for(items) : p1;
+  k_topk_pass1<VEC><<<dim3(p1x, a.nranks), kThreads, 0, s>>>(a);
   if (a.k == 0) return cudaGetLastError();  // nothing kept: e = a
   unsigned sx = (unsigned)(kSms * kSplitBlocksPerSm / a.nranks);
   if (sx < 1) sx = 1;
