@@ -41,6 +41,31 @@ constexpr int kSms = 152;
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
 
+// Programmatic dependent launch: every kernel here is launched so that it may
+// be scheduled while the previous kernel on the stream drains; it waits for
+// that kernel's completion (and its memory) before touching global memory,
+// then lets its own dependents be scheduled.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+// Launch with programmatic stream serialization allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kWarps = kThreads / 32;  // tiles per block in the slot-reading passes
 
 struct RankWs {
@@ -160,6 +185,7 @@ __device__ void find_digit(uint32_t* hist, int shift, TopkState* st) {
 }
 
 __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ TopkArgs A) {
+  pdl_enter();
   const RankWs w = rank_ws(A, blockIdx.y);
   for (int i = threadIdx.x; i < kTopkHistWords; i += blockDim.x) w.hist[i] = 0;
   if (threadIdx.x == 0) {
@@ -180,6 +206,7 @@ __device__ __forceinline__ float4 add4(float4 x, float4 y) {
 // block, if k > 0) the first digit.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads, kPass1BlocksPerSm) k_topk_pass1(const __grid_constant__ TopkArgs A) {
+  pdl_enter();
   __shared__ uint32_t sh[2048];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
@@ -279,6 +306,7 @@ __device__ __forceinline__ uint32_t ge_mask(const float (&v)[kTopkElems], uint64
 // from the cache.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__ TopkArgs A) {
+  pdl_enter();
   __shared__ uint32_t sh[1024];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
@@ -366,6 +394,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
 // the last digit, which completes T.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__ TopkArgs A) {
+  pdl_enter();
   __shared__ uint32_t sh[1024];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
@@ -469,6 +498,7 @@ __device__ void scan_blocks(const RankWs& w, uint64_t nb) {
 // the data, writing the run masks. The last block scans all tiles' counts.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
+  pdl_enter();
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   const uint32_t T = w.st->prefix;
@@ -621,6 +651,7 @@ __device__ void emit_masks(const TopkArgs& A, const RankWs& w, int r, uint64_t t
 // Kept elements to (index, value) in index order; zero their residual. Each
 // block covers kWarps tiles.
 __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
+  pdl_enter();
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   if (!w.st->overflow) {
@@ -636,6 +667,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ 
 
 // recv[r][idx_r[j]] = val_r[j] for every rank (outputs already zeroed)
 __global__ void __launch_bounds__(kThreads) k_sparse_scatter(const __grid_constant__ ScatterArgs A) {
+  pdl_enter();
   const uint32_t total = A.tile_start[A.nranks];
   for (uint32_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
     int lo = 0, hi = A.nranks - 1;
@@ -658,6 +690,7 @@ __global__ void __launch_bounds__(kThreads) k_sparse_scatter(const __grid_consta
 // ntiles). With ascending indices every entry is written once; otherwise the
 // fold clamps what it reads.
 __global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constant__ SparseArgs A) {
+  pdl_enter();
   const int r = blockIdx.y;
   const uint64_t nnz = A.nnz[r];
   const uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -679,6 +712,7 @@ __global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constan
 // chunk (or recursive halving), divided by N for AVG, and stored to all N
 // outputs. The dense allreduce of the densified vectors gives the same bits.
 __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant__ SparseArgs A) {
+  pdl_enter();
   extern __shared__ float sm[];  // nranks x tile
   const int N = A.nranks;
   const uint32_t T = A.tile;
@@ -745,7 +779,8 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
 template <bool VEC>
 cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 one(1, a.nranks);
-  k_topk_init<<<one, kThreads, 0, s>>>(a);
+  cudaError_t err = pdl_launch(k_topk_init, one, 0, s, a);
+  if (err != cudaSuccess) return err;
   // histogram passes over the data: a resident grid looping over it, so that
   // each block flushes its shared histogram once
   const uint64_t items = VEC ? (a.count + 3) / 4 : a.count;
@@ -756,17 +791,17 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   unsigned p1 = (unsigned)(kSms * kPass1BlocksPerSm / a.nranks);
   if (p1 < 1) p1 = 1;
   const unsigned p1x = grid_for(items) < p1 ? grid_for(items) : p1;
-  k_topk_pass1<VEC><<<dim3(p1x, a.nranks), kThreads, 0, s>>>(a);
-  if (a.k == 0) return cudaGetLastError();  // nothing kept: e = a
+  err = pdl_launch(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);
+  if (err != cudaSuccess) return err;
+  if (a.k == 0) return cudaSuccess;  // nothing kept: e = a
   unsigned sx = (unsigned)(kSms * kSplitBlocksPerSm / a.nranks);
   if (sx < 1) sx = 1;
   if (sx > a.nb) sx = (unsigned)a.nb;
-  k_topk_split<VEC><<<dim3(sx, a.nranks), kThreads, 0, s>>>(a);
-  k_topk_pass3<VEC><<<hgrid, kThreads, 0, s>>>(a);
+  if ((err = pdl_launch(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) return err;
+  if ((err = pdl_launch(k_topk_pass3<VEC>, hgrid, 0, s, a)) != cudaSuccess) return err;
   const dim3 wgrid((unsigned)((a.nb + kWarps - 1) / kWarps), a.nranks);
-  k_topk_count<VEC><<<wgrid, kThreads, 0, s>>>(a);
-  k_topk_emit<<<wgrid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if ((err = pdl_launch(k_topk_count<VEC>, wgrid, 0, s, a)) != cudaSuccess) return err;
+  return pdl_launch(k_topk_emit, wgrid, 0, s, a);
 }
 
 }  // namespace
@@ -776,9 +811,9 @@ cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream) {
 }
 
 cudaError_t launch_sparse_fold(const SparseArgs& a, uint64_t max_nnz, cudaStream_t stream) {
-  k_sparse_bounds<<<dim3(grid_for(max_nnz + 1), a.nranks), kThreads, 0, stream>>>(a);
-  k_sparse_fold<<<a.ntiles, kThreads, (size_t)a.nranks * a.tile * sizeof(float), stream>>>(a);
-  return cudaGetLastError();
+  const cudaError_t err = pdl_launch(k_sparse_bounds, dim3(grid_for(max_nnz + 1), a.nranks), 0, stream, a);
+  if (err != cudaSuccess) return err;
+  return pdl_launch(k_sparse_fold, dim3(a.ntiles), (size_t)a.nranks * a.tile * sizeof(float), stream, a);
 }
 
 cudaError_t launch_sparse_scatter(const ScatterArgs& a, cudaStream_t stream) {
