@@ -58,9 +58,7 @@ template <int IDT> struct Fp8FusedLd {
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = __fdiv_rn(amax, 448.0f);
-    uint32_t word[V / 4];
-    quantise_lane<V>(x, amax, s, word);
-    dequantise_lane<V>(word, s, d);
+    qdq_lane<V>(x, amax, s, d);
   }
   __device__ __forceinline__ static Acc comb(Acc a, Acc b) { return __fadd_rn(a, b); }
 };
@@ -133,10 +131,8 @@ __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_consta
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const float s = __fdiv_rn(amax, 448.0f);
-      uint32_t word[1];
-      quantise_lane<4>(x, amax, s, word);
       float t[4];
-      dequantise_lane<4>(word, s, t);
+      qdq_lane<4>(x, amax, s, t);
 #pragma unroll
       for (int k = 0; k < 4; ++k) d[r][k] = t[k];
     }

@@ -29,9 +29,8 @@ __device__ __forceinline__ void qdq_block(float (&p)[4]) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float s = __fdiv_rn(amax, 448.0f);
-  uint32_t word[1];
-  quantise_lane<4>(p, amax, s, word);
-  dequantise_lane<4>(word, s, p);
+  const float x[4] = {p[0], p[1], p[2], p[3]};
+  qdq_lane<4>(x, amax, s, p);
 }
 
 template <int DT> __device__ __forceinline__ float load_elem(const void* base, uint64_t e) {
