@@ -287,6 +287,17 @@ __device__ __forceinline__ uint64_t run_base(uint64_t tile, int u) {
   return tile * kTopkBlock + (uint64_t)(u * kThreads + threadIdx.x) * kTopkElems;
 }
 
+// bit j set if value j of the run (inside the data) has a key >= lo
+__device__ __forceinline__ uint32_t ge_mask(const float (&v)[kTopkElems], uint64_t base, uint64_t count,
+                                            uint32_t lo) {
+  uint32_t m = 0;
+  const bool full = base + kTopkElems <= count;
+#pragma unroll
+  for (int j = 0; j < kTopkElems; ++j)
+    if (mag_key(v[j]) >= lo && (full || base + j < count)) m |= 1u << j;
+  return m;
+}
+
 // Pass 2, a resident grid looping over the tiles: each tile's keys at or
 // above the first digit's bin (every key that can still be kept) compacted in
 // index order into the tile's slots, and the histogram of bits 19..10 of the
@@ -306,56 +317,35 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   const uint32_t d1 = w.st->prefix >> 20;
   const uint32_t lo = d1 << 20;
   __syncthreads();
-  // Software-pipelined: once a tile's masks are taken, the next tile's loads
-  // are issued, so they are in flight during this tile's scans and slot
-  // writes (the values are not needed again: the set bits are re-read from
-  // the cache). One register set holds a tile; a whole tile of aligned data
-  // is read in float4, anything else element by element with zeros past the
-  // end (masked off below).
-  float4 x[kTopkRuns][kTopkElems / 4];
-  auto load_tile = [&](uint64_t t) {
-    if (VEC && (t + 1) * kTopkBlock <= count) {
-      const float4* p = reinterpret_cast<const float4*>(a + t * kTopkBlock);
+  for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
+    uint32_t m[kTopkRuns];
+    if (VEC && (tile + 1) * kTopkBlock <= count) {
+      // a whole tile: no bounds checks (the same for every thread of the block)
+      const float4* p = reinterpret_cast<const float4*>(a + tile * kTopkBlock);
+      float4 x[kTopkRuns][kTopkElems / 4];
 #pragma unroll
       for (int u = 0; u < kTopkRuns; ++u)
 #pragma unroll
         for (int q = 0; q < kTopkElems / 4; ++q) x[u][q] = p[(u * kThreads + threadIdx.x) * (kTopkElems / 4) + q];
-    } else {
 #pragma unroll
       for (int u = 0; u < kTopkRuns; ++u) {
-        const uint64_t base = run_base(t, u);
+        uint32_t b = 0;
 #pragma unroll
         for (int q = 0; q < kTopkElems / 4; ++q) {
-          const uint64_t i = base + 4 * q;
-          x[u][q].x = i < count ? a[i] : 0.0f;
-          x[u][q].y = i + 1 < count ? a[i + 1] : 0.0f;
-          x[u][q].z = i + 2 < count ? a[i + 2] : 0.0f;
-          x[u][q].w = i + 3 < count ? a[i + 3] : 0.0f;
+          if (mag_key(x[u][q].x) >= lo) b |= 1u << (4 * q);
+          if (mag_key(x[u][q].y) >= lo) b |= 2u << (4 * q);
+          if (mag_key(x[u][q].z) >= lo) b |= 4u << (4 * q);
+          if (mag_key(x[u][q].w) >= lo) b |= 8u << (4 * q);
         }
+        m[u] = b;
       }
-    }
-  };
-  if (blockIdx.x < A.nb) load_tile(blockIdx.x);
-  for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
-    uint32_t m[kTopkRuns];
+    } else {
+      float v[kTopkRuns][kTopkElems];
 #pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) {
-      uint32_t b = 0;
+      for (int u = 0; u < kTopkRuns; ++u) load_run<VEC>(a, run_base(tile, u), count, v[u]);
 #pragma unroll
-      for (int q = 0; q < kTopkElems / 4; ++q) {
-        if (mag_key(x[u][q].x) >= lo) b |= 1u << (4 * q);
-        if (mag_key(x[u][q].y) >= lo) b |= 2u << (4 * q);
-        if (mag_key(x[u][q].z) >= lo) b |= 4u << (4 * q);
-        if (mag_key(x[u][q].w) >= lo) b |= 8u << (4 * q);
-      }
-      const uint64_t base = run_base(tile, u);
-      const uint64_t left = base < count ? count - base : 0;  // values of this run inside the data
-      if (left < (uint64_t)kTopkElems) b &= (1u << left) - 1u;
-      m[u] = b;
+      for (int u = 0; u < kTopkRuns; ++u) m[u] = ge_mask(v[u], run_base(tile, u), count, lo);
     }
-    // keep the next tile's loads after the masks: one set of registers
-    asm volatile("" ::: "memory");
-    if (tile + gridDim.x < A.nb) load_tile(tile + gridDim.x);
     // slot positions in index order (all runs of u = 0, then u = 1, ...):
     // runs 0 and 1, and runs 2 and 3, share one scan of two 16-bit counts
     uint32_t t01, t23;
