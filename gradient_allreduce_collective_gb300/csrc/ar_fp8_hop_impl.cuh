@@ -10,9 +10,11 @@
 // in binary32; the finished chunk is quantised once more for the all-gather
 // and every rank stores the same dequantised values in the output type.
 //
-// One warp per block: lane l holds elements l, l+32, l+64, l+96; the block
-// amax of each hop is a warp-wide xor reduction; the ranks' values are loaded
-// in batches of eight ranks before they are folded.
+// One warp per block: lane l holds elements 4l..4l+3 of a whole block when
+// every buffer is aligned for 4-element vectors (one load and one store per
+// rank and lane), otherwise elements l, l+32, l+64, l+96; the block amax of
+// each hop is a warp-wide xor reduction; the ranks' values are loaded in
+// batches of eight ranks before they are folded.
 #pragma once
 
 #include <cstdint>
@@ -33,13 +35,39 @@ __device__ __forceinline__ void qdq_block(float (&p)[4]) {
   qdq_lane<4>(x, amax, s, p);
 }
 
+// four consecutive elements starting at e (e a multiple of 4, base aligned)
+template <int DT> __device__ __forceinline__ void load4(const void* base, uint64_t e, float (&x)[4]) {
+  if constexpr (Fmt<DT>::bytes == 4) {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(base) + e));
+    x[0] = to_f32<DT>(v.x);
+    x[1] = to_f32<DT>(v.y);
+    x[2] = to_f32<DT>(v.z);
+    x[3] = to_f32<DT>(v.w);
+  } else {
+    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + e));
+    x[0] = to_f32<DT>(v.x & 0xFFFFu);
+    x[1] = to_f32<DT>(v.x >> 16);
+    x[2] = to_f32<DT>(v.y & 0xFFFFu);
+    x[3] = to_f32<DT>(v.y >> 16);
+  }
+}
+
+template <int DT> __device__ __forceinline__ void store4(void* base, uint64_t e, const uint32_t (&b)[4]) {
+  if constexpr (Fmt<DT>::bytes == 4) {
+    __stcs(reinterpret_cast<uint4*>(static_cast<uint32_t*>(base) + e), make_uint4(b[0], b[1], b[2], b[3]));
+  } else {
+    __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + e),
+           make_uint2((b[0] & 0xFFFFu) | (b[1] << 16), (b[2] & 0xFFFFu) | (b[3] << 16)));
+  }
+}
+
 template <int DT> __device__ __forceinline__ float load_elem(const void* base, uint64_t e) {
   if constexpr (Fmt<DT>::bytes == 4) return to_f32<DT>(*(static_cast<const uint32_t*>(base) + e));
   else return to_f32<DT>(*(static_cast<const uint16_t*>(base) + e));
 }
 
-template <int IDT, int ODT, int OP, int MAXN>
-__global__ void __launch_bounds__(kThreads) k_fp8_hop(const __grid_constant__ Fp8HopArgs A) {
+template <int IDT, int ODT, int OP, int MAXN, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4) k_fp8_hop(const __grid_constant__ Fp8HopArgs A) {
   const int N = A.nranks;
   const int lane = threadIdx.x & 31;
   const uint64_t tasks = (uint64_t)N * A.nbc;
@@ -53,9 +81,10 @@ __global__ void __launch_bounds__(kThreads) k_fp8_hop(const __grid_constant__ Fp
     const uint64_t lo = clo + j * kFp8Block;
     if (clo >= A.count || lo >= chi) continue;
     const uint64_t hi = (lo + kFp8Block < chi) ? lo + kFp8Block : chi;
+    const bool full = VEC && hi - lo == kFp8Block;  // warp-uniform
     bool valid[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) valid[k] = lo + lane + 32 * k < hi;
+    for (int k = 0; k < 4; ++k) valid[k] = full || lo + lane + 32 * k < hi;
     const int s0 = (c + 1 == N) ? 0 : c + 1;
     float p[4];
 #pragma unroll
@@ -67,8 +96,12 @@ __global__ void __launch_bounds__(kThreads) k_fp8_hop(const __grid_constant__ Fp
         if (b0 + m < N) {
           int r = s0 + b0 + m;
           r = (r >= N) ? r - N : r;
+          if (full) {
+            load4<IDT>(A.src[r], lo + 4 * lane, x[m]);
+          } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) x[m][k] = valid[k] ? load_elem<IDT>(A.src[r], lo + lane + 32 * k) : 0.0f;
+            for (int k = 0; k < 4; ++k) x[m][k] = valid[k] ? load_elem<IDT>(A.src[r], lo + lane + 32 * k) : 0.0f;
+          }
         }
       }
 #pragma unroll
@@ -90,6 +123,13 @@ __global__ void __launch_bounds__(kThreads) k_fp8_hop(const __grid_constant__ Fp
       for (int k = 0; k < 4; ++k) p[k] = __fdiv_rn(p[k], (float)N);
     }
     qdq_block(p);  // the finished chunk, as the all-gather sends it
+    if (full) {
+      uint32_t bits[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) bits[k] = from_f32<ODT>(p[k]);
+      for (int r = 0; r < N; ++r) store4<ODT>(A.dst[r], lo + 4 * lane, bits);
+      continue;
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       if (!valid[k]) continue;
@@ -108,9 +148,24 @@ cudaError_t launch_hop_op(const Fp8HopArgs& a, cudaStream_t s) {
   const uint64_t tasks = (uint64_t)a.nranks * a.nbc;
   if (tasks == 0) return cudaSuccess;
   const unsigned grid = grid_for(tasks * 32);
-  if (a.nranks <= 8) k_fp8_hop<IDT, ODT, OP, 8><<<grid, kThreads, 0, s>>>(a);
-  else if (a.nranks <= 16) k_fp8_hop<IDT, ODT, OP, 16><<<grid, kThreads, 0, s>>>(a);
-  else k_fp8_hop<IDT, ODT, OP, kMaxRanks><<<grid, kThreads, 0, s>>>(a);
+  // 4-element vectors when every buffer allows them (block starts are
+  // multiples of 4 elements: chunk lengths are multiples of 16 bytes of the
+  // output type)
+  bool vec = true;
+  for (int r = 0; r < a.nranks; ++r)
+    vec = vec && reinterpret_cast<uintptr_t>(a.src[r]) % (4 * Fmt<IDT>::bytes) == 0 &&
+          reinterpret_cast<uintptr_t>(a.dst[r]) % (4 * Fmt<ODT>::bytes) == 0;
+#define GAR_HOP(MAXNV)                                                        \
+  if (vec) k_fp8_hop<IDT, ODT, OP, MAXNV, true><<<grid, kThreads, 0, s>>>(a); \
+  else k_fp8_hop<IDT, ODT, OP, MAXNV, false><<<grid, kThreads, 0, s>>>(a);
+  if (a.nranks <= 8) {
+    GAR_HOP(8)
+  } else if (a.nranks <= 16) {
+    GAR_HOP(16)
+  } else {
+    GAR_HOP(kMaxRanks)
+  }
+#undef GAR_HOP
   return cudaGetLastError();
 }
 
