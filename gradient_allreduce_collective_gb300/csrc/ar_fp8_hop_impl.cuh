@@ -98,6 +98,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_fp8_hop(const __grid_constant__
           r = (r >= N) ? r - N : r;
           if (full) {
             load4<IDT>(A.src[r], lo + 4 * lane, x[m]);
+            if (b0 + 8 + m < N) {  // the same lane's vector of the rank eight places later, into L2
+              int r2 = r + 8;
+              r2 = (r2 >= N) ? r2 - N : r2;
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(A.src[r2]) +
+                                                              (lo + 4 * lane) * Fmt<IDT>::bytes));
+            }
           } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) x[m][k] = valid[k] ? load_elem<IDT>(A.src[r], lo + lane + 32 * k) : 0.0f;
