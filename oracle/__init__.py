@@ -64,6 +64,7 @@ def _load():
     lib.or_ring_reduce_scatter.argtypes = [pp, pp, ci, sz, ci, ci]
     lib.or_ring_all_gather.argtypes = [pp, pp, ci, sz, ci]
     lib.or_fold_points.argtypes = [vp, vp, sz, sz, ci, ci, ci, vp]
+    lib.or_fold_allreduce_range.argtypes = [pp, pp, ci, sz, sz, sz, ci, ci]
     lib.or_tree_points.argtypes = [vp, sz, ci, ci, ci, vp]
     lib.or_reference_f64.argtypes = [pp, ci, sz, ci, ci, vp, vp]
     lib.or_fp8_quantize.argtypes = [vp, ci, sz, vp, vp]
@@ -126,6 +127,28 @@ def ring_allreduce(send, dtype: str, op: str):
 def fold_allreduce(send, dtype: str, op: str):
     """Per-element fold in the ring order (cross-check of the simulator)."""
     return _allreduce("or_fold_allreduce", send, dtype, op)
+
+
+def fold_allreduce_threads(send, dtype: str, op: str, threads: int):
+    """The per-element fold over `threads` disjoint element ranges run on
+    host threads at once (the C code releases the interpreter lock); the
+    chunk plan is the whole problem's, so the result equals fold_allreduce."""
+    from concurrent.futures import ThreadPoolExecutor
+    send = _contig(send, dtype)
+    recv = [np.empty_like(send[0]) for _ in send]
+    count = send[0].size
+    sp, rp = _ptrs(send), _ptrs(recv)
+    lib = _load()
+    bounds = [count * k // threads for k in range(threads + 1)]
+
+    def run(k):
+        return lib.or_fold_allreduce_range(sp, rp, len(send), count, bounds[k], bounds[k + 1], DTYPES[dtype],
+                                           OPS[op])
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for rc in ex.map(run, range(threads)):
+            _check(rc, "or_fold_allreduce_range")
+    return recv
 
 
 def tree_allreduce(send, dtype: str, op: str):

@@ -440,6 +440,23 @@ int or_fold_allreduce(const void *const *send, void *const *recv, int N, size_t 
     return OR_OK;
 }
 
+/* The same fold for the elements [lo, hi) of a problem of `count` elements
+   per rank (the chunk plan is that of the whole problem), so that disjoint
+   ranges can run on separate threads. */
+int or_fold_allreduce_range(const void *const *send, void *const *recv, int N, size_t count, size_t lo, size_t hi,
+                            int dt, int op)
+{
+    if (or_check(N, dt, op) || lo > hi || hi > count) return OR_EINVAL;
+    size_t L = or_chunk_len(count, N, 16 / or_esize(dt));
+    or_val x[64];
+    for (size_t i = lo; i < hi; ++i) {
+        for (int r = 0; r < N; ++r) x[r] = or_load(dt, send[r], i);
+        or_val y = or_fold_one(x, N, (int)(i / L), dt, op);
+        for (int r = 0; r < N; ++r) or_store(dt, recv[r], i, y);
+    }
+    return OR_OK;
+}
+
 /* vals: n rows of N values (dtype dt, row-major); gidx[j]: the element's index
    in a problem of `count` elements per rank; out[j]: the result (dtype dt). */
 int or_fold_points(const void *vals, const int64_t *gidx, size_t n, size_t count, int N, int dt, int op, void *out)

@@ -453,3 +453,15 @@ def test_error_feedback_conserves_the_gradient_mass():
         total += g
     err = np.abs(sent + e - total)
     assert np.all(err <= T * 2.0**-23 * (np.abs(total) + np.abs(sent) + 1e-3))
+
+
+@pytest.mark.parametrize("threads", [1, 3, 8])
+def test_threaded_fold_equals_the_ring_simulator(threads):
+    # disjoint element ranges on host threads keep the whole problem's chunk plan
+    for dtype in ("f32", "bf16", "i32"):
+        for n, count in ((8, 100_003), (5, 4_099), (3, 7)):
+            send = _rand(dtype, n, count, seed=31 * n)
+            want = oracle.ring_allreduce(send, dtype, "sum")
+            got = oracle.fold_allreduce_threads(send, dtype, "sum", threads)
+            for g, w in zip(got, want):
+                assert np.array_equal(np.asarray(g).view(np.uint8), np.asarray(w).view(np.uint8))
