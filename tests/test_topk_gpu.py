@@ -279,3 +279,36 @@ def test_sparse_allreduce_unsorted_indices_stay_in_bounds():
                                         count, "sum")[0]
     for r in range(n):
         assert np.array_equal(_bits(from_dev(out.views[r])), _bits(want))
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_topk_guess_carried_in_the_workspace(offset):
+    # The workspace keeps the previous call's first digit; pass 1 then fills
+    # the slots speculatively. Scales that hold still (the guess holds), jump
+    # up (the slots overflow) and drop (the new digit falls below the guess)
+    # must all give the oracle's bits; unaligned buffers take the element path.
+    n, count, k = 3, 300_007, 3_000
+    ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
+    e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
+    keep = []
+    res = []
+    for r in range(n):
+        eb, ed = _dev_f32(e_np[r], offset)
+        keep.append(eb)
+        res.append(ed)
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    for step, scale in enumerate([1.0, 1.0, 1.05, 1e3, 1e3, 1e-3, 1.0, 1.0]):
+        g_np = [synthgen.normal_f32(count, 800 + 10 * step + r, 1e-3 * scale) for r in range(n)]
+        grads = []
+        for r in range(n):
+            gb, gd = _dev_f32(g_np[r], offset)
+            keep.append(gb)
+            grads.append(gd)
+        gar.ar_topk_compress(grads, res, k, idx, val, ws)
+        torch.cuda.synchronize()
+        for r in range(n):
+            oi, ov, e_np[r] = oracle.topk_compress(g_np[r], e_np[r], k)
+            assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), (step, r)
+            assert np.array_equal(_bits(from_dev(val[r])), _bits(ov)), (step, r)
+            assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
