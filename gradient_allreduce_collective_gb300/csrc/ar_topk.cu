@@ -37,7 +37,6 @@ namespace {
 constexpr int kHistBlocksPerSm = 8;
 constexpr int kSplitBlocksPerSm = 3;  // the register budget of k_topk_split
 constexpr int kPass1BlocksPerSm = 5;  // k_topk_pass1 keeps 8 float4 loads in flight per thread
-constexpr int kPass1sBlocksPerSm = 4;  // the register budget of k_topk_pass1s
 constexpr int kSms = 152;
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
@@ -196,8 +195,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ 
     w.st->gt = 0;
     for (int p = 0; p < 4; ++p) w.st->ticket[p] = 0;
     w.st->overflow = 0;
-    w.st->spec = 0;
-    w.st->spec_over = 0;  // guess: kept from the previous call
   }
 }
 
@@ -301,155 +298,6 @@ __device__ __forceinline__ uint32_t ge_mask(const float (&v)[kTopkElems], uint64
   return m;
 }
 
-// Pass 1 with speculative compaction, a resident grid looping over the
-// tiles: a = g + e into e and the histogram of bits 30..20 of |a|, as in
-// k_topk_pass1; and, when the workspace holds the previous call's first digit
-// (the error feedback keeps the magnitudes of a from one step to the next
-// close), every key at or above the bin one below that digit is compacted in
-// index order into the tile's slots. The last block takes the first digit and
-// keeps the speculation only if no tile overflowed and the new digit is not
-// below the guessed bin: then the slots hold every key that can still be kept
-// and pass 2 reads them instead of the data. The guess decides the work done,
-// never the result.
-template <bool VEC>
-__global__ void __launch_bounds__(kThreads, kPass1sBlocksPerSm) k_topk_pass1s(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
-  __shared__ uint32_t sh[2048];
-  const int r = blockIdx.y;
-  const RankWs w = rank_ws(A, r);
-  const float* __restrict__ g = A.g[r];
-  float* __restrict__ e = A.e[r];
-  const uint64_t count = A.count;
-  const uint32_t S = A.slots;
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x) sh[i] = 0;
-  const uint32_t gb = w.st->guess;
-  const uint32_t lo_bin = (gb >= 1 && gb < 2048) ? gb - 1 : 2048u;  // 2048: no speculation
-  const bool spec = lo_bin < 2048;                                    // the same for every block
-  const uint32_t lo = spec ? lo_bin << 20 : 0xFFFFFFFFu;
-  __syncthreads();
-  for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
-    const bool full = VEC && (tile + 1) * kTopkBlock <= count;  // the same for every thread of the block
-    uint32_t m[kTopkRuns];
-#pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) {
-      const uint64_t base = run_base(tile, u);
-      float v[kTopkElems];
-      if (full) {
-        const float4* g4 = reinterpret_cast<const float4*>(g + base);
-        float4* e4 = reinterpret_cast<float4*>(e + base);
-        float4 x[kTopkElems / 4], y[kTopkElems / 4];
-#pragma unroll
-        for (int q = 0; q < kTopkElems / 4; ++q) {
-          x[q] = __ldcs(g4 + q);
-          y[q] = e4[q];
-        }
-#pragma unroll
-        for (int q = 0; q < kTopkElems / 4; ++q) {
-          const float4 s4 = add4(x[q], y[q]);
-          e4[q] = s4;
-          v[4 * q] = s4.x;
-          v[4 * q + 1] = s4.y;
-          v[4 * q + 2] = s4.z;
-          v[4 * q + 3] = s4.w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < kTopkElems; ++j) {
-          v[j] = 0.0f;
-          if (base + j < count) {
-            v[j] = __fadd_rn(g[base + j], e[base + j]);
-            e[base + j] = v[j];
-          }
-        }
-      }
-      const uint64_t left = base < count ? count - base : 0;  // values of this run inside the data
-      uint32_t b = 0;
-#pragma unroll
-      for (int j = 0; j < kTopkElems; ++j) {
-        if (full || (uint64_t)j < left) {
-          const uint32_t key = mag_key(v[j]);
-          atomicAdd(&sh[key >> 20], 1u);
-          if (key >= lo) b |= 1u << j;
-        }
-      }
-      m[u] = b;
-    }
-    if (spec) {
-      uint32_t t01, t23;
-      const uint32_t e01 = block_exclusive_scan((uint32_t)__popc(m[0]) | ((uint32_t)__popc(m[1]) << 16), &t01);
-      const uint32_t e23 = block_exclusive_scan((uint32_t)__popc(m[2]) | ((uint32_t)__popc(m[3]) << 16), &t23);
-      const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
-      uint32_t pos[kTopkRuns];
-      pos[0] = e01 & 0xFFFFu;
-      pos[1] = tot0 + (e01 >> 16);
-      pos[2] = tot0 + tot1 + (e23 & 0xFFFFu);
-      pos[3] = tot0 + tot1 + tot2 + (e23 >> 16);
-      uint32_t* __restrict__ si = slot_idx(w, tile, S);
-      float* __restrict__ sv = slot_val(w, tile, S);
-#pragma unroll
-      for (int u = 0; u < kTopkRuns; ++u) {
-        const uint64_t base = run_base(tile, u);
-        uint32_t bits = m[u];
-        uint32_t p = pos[u];
-        while (bits) {
-          const int j = __ffs(bits) - 1;
-          bits &= bits - 1;
-          if (p < S) {
-            si[p] = (uint32_t)(base + j);
-            sv[p] = e[base + j];  // this thread's own store of a, above
-          }
-          ++p;
-        }
-      }
-      if (threadIdx.x == 0) {
-        const uint32_t n = tot0 + tot1 + tot2 + tot3;
-        w.n_s[tile] = n;
-        if (n > S) atomicOr(&w.st->spec_over, 1u);
-      }
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
-    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
-  if (A.k == 0) return;  // nothing to select
-  if (last_block(&w.st->ticket[0])) {
-    find_digit<2048>(w.hist, 20, w.st);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t d1 = w.st->prefix >> 20;
-      w.st->spec = (spec && w.st->spec_over == 0 && d1 >= lo_bin) ? 1u : 0u;
-      w.st->guess = d1;
-    }
-  }
-}
-
-// Pass 2 from the speculative slots: the histogram of bits 19..10 of the slot
-// keys inside the first digit's bin, then (last block) the second digit.
-// Does nothing when the speculation did not hold (k_topk_split then runs).
-__global__ void __launch_bounds__(kThreads) k_topk_slot2(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
-  __shared__ uint32_t sh[1024];
-  const int r = blockIdx.y;
-  const RankWs w = rank_ws(A, r);
-  if (!w.st->spec) return;  // the same for every block
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
-  __syncthreads();
-  const uint32_t d1 = w.st->prefix >> 20;
-  for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
-    const float* sv = slot_val(w, tile, A.slots);
-    const uint32_t n = w.n_s[tile];
-#pragma unroll 4
-    for (uint32_t c = threadIdx.x; c < n; c += blockDim.x) {
-      const uint32_t key = mag_key(sv[c]);
-      if ((key >> 20) == d1) atomicAdd(&sh[(key >> 10) & 1023u], 1u);
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
-    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
-  if (last_block(&w.st->ticket[1])) find_digit<1024>(w.hist, 10, w.st);
-}
-
 // Pass 2, a resident grid looping over the tiles: each tile's keys at or
 // above the first digit's bin (every key that can still be kept) compacted in
 // index order into the tile's slots, and the histogram of bits 19..10 of the
@@ -465,7 +313,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   const uint64_t count = A.count;
   const float* __restrict__ a = A.e[r];
   const uint32_t S = A.slots;
-  if (w.st->spec) return;  // pass 1 filled the slots; k_topk_slot2 takes pass 2
   for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
   const uint32_t d1 = w.st->prefix >> 20;
   const uint32_t lo = d1 << 20;
@@ -956,16 +803,13 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   unsigned p1 = (unsigned)(kSms * kPass1BlocksPerSm / a.nranks);
   if (p1 < 1) p1 = 1;
   const unsigned p1x = grid_for(items) < p1 ? grid_for(items) : p1;
-  if (a.k == 0) return pdl_launch(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);  // nothing kept: e = a
-  unsigned sx1 = (unsigned)(kSms * kPass1sBlocksPerSm / a.nranks);
-  if (sx1 < 1) sx1 = 1;
-  if (sx1 > a.nb) sx1 = (unsigned)a.nb;
-  if ((err = pdl_launch(k_topk_pass1s<VEC>, dim3(sx1, a.nranks), 0, s, a)) != cudaSuccess) return err;
+  err = pdl_launch(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);
+  if (err != cudaSuccess) return err;
+  if (a.k == 0) return cudaSuccess;  // nothing kept: e = a
   unsigned sx = (unsigned)(kSms * kSplitBlocksPerSm / a.nranks);
   if (sx < 1) sx = 1;
   if (sx > a.nb) sx = (unsigned)a.nb;
   if ((err = pdl_launch(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) return err;
-  if ((err = pdl_launch(k_topk_slot2, hgrid, 0, s, a)) != cudaSuccess) return err;
   if ((err = pdl_launch(k_topk_pass3<VEC>, hgrid, 0, s, a)) != cudaSuccess) return err;
   const dim3 wgrid((unsigned)((a.nb + kWarps - 1) / kWarps), a.nranks);
   if ((err = pdl_launch(k_topk_count<VEC>, wgrid, 0, s, a)) != cudaSuccess) return err;

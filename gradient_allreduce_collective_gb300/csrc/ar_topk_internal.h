@@ -62,12 +62,6 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //   overflow:    nonzero if some tile had more keys at or above the first
 //                digit's bin than its slots hold; the later passes then read
 //                the data instead
-//   guess:       the first digit of the previous call on this workspace (kept
-//                across calls; any value, including uninitialised memory, is
-//                safe: it only decides whether pass 1 tries to fill the slots)
-//   spec:        1 if pass 1 filled the slots with every key that can still
-//                be kept (pass 2 then reads the slots, not the data)
-//   spec_over:   nonzero if a tile's speculative slots overflowed
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -75,10 +69,7 @@ struct TopkState {
   uint32_t gt;
   uint32_t ticket[4];
   uint32_t overflow;
-  uint32_t guess;
-  uint32_t spec;
-  uint32_t spec_over;
-  uint32_t pad[4];
+  uint32_t pad[7];
 };
 static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 

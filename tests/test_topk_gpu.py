@@ -282,11 +282,10 @@ def test_sparse_allreduce_unsorted_indices_stay_in_bounds():
 
 
 @pytest.mark.parametrize("offset", [0, 1])
-def test_topk_guess_carried_in_the_workspace(offset):
-    # The workspace keeps the previous call's first digit; pass 1 then fills
-    # the slots speculatively. Scales that hold still (the guess holds), jump
-    # up (the slots overflow) and drop (the new digit falls below the guess)
-    # must all give the oracle's bits; unaligned buffers take the element path.
+def test_topk_workspace_reused_across_steps(offset):
+    # One workspace for eight steps of error feedback while the gradient scale
+    # holds still, jumps up by 1e3 and drops by 1e6: the oracle's bits every
+    # step; unaligned buffers take the element path.
     n, count, k = 3, 300_007, 3_000
     ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
     e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
