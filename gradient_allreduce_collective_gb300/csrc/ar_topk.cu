@@ -21,6 +21,7 @@
 // every kept element its slot. All ranks of a call share each launch
 // (grid.y = rank): six launches per call whatever the number of ranks.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -923,6 +924,20 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
   }
 }
 
+// The staged pass needs more than the default 48 KiB of dynamic shared
+// memory; the attribute is set once per device (setting it is a host call
+// that costs far more than a launch).
+cudaError_t allow_staged_smem() {
+  static std::atomic<bool> done[kMaxRanks];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < kMaxRanks && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  err = cudaFuncSetAttribute(k_topk_split_staged, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSplitStagedSmem);
+  if (err == cudaSuccess && dev >= 0 && dev < kMaxRanks) done[dev].store(true, std::memory_order_release);
+  return err;
+}
+
 template <bool VEC>
 cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 one(1, a.nranks);
@@ -949,9 +964,7 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
     unsigned qx = (unsigned)(kSms / a.nranks);
     if (qx < 1) qx = 1;
     if (qx > a.nb) qx = (unsigned)a.nb;
-    if ((err = cudaFuncSetAttribute(k_topk_split_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSplitStagedSmem)) != cudaSuccess)
-      return err;
+    if ((err = allow_staged_smem()) != cudaSuccess) return err;
     if ((err = pdl_launch(k_topk_split_staged, dim3(qx, a.nranks), kSplitStagedSmem, s, a)) != cudaSuccess)
       return err;
   } else if ((err = pdl_launch(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) {
