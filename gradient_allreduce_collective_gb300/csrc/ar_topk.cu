@@ -21,7 +21,6 @@
 // every kept element its slot. All ranks of a call share each launch
 // (grid.y = rank): six launches per call whatever the number of ranks.
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -383,141 +382,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
       w.n_s[tile] = n;
       if (n > S) atomicOr(&w.st->overflow, 1u);
     }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
-    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
-  if (last_block(&w.st->ticket[1])) find_digit<1024>(w.hist, 10, w.st);
-}
-
-// Asynchronous 16-byte global-to-shared copies (completion per thread).
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// The end of pass 2 for one tile, given each run's mask of keys >= lo and the
-// values: slot positions in index order (all runs of u = 0, then u = 1, ...;
-// runs 0 and 1, and runs 2 and 3, share one scan of two 16-bit counts), the
-// set bits written to the slots, the histogram of the keys in bin d1.
-template <class ValueAt>
-__device__ __forceinline__ void split_tile_finish(const RankWs& w, uint64_t tile, uint32_t S, const uint32_t (&m)[4],
-                                                  uint32_t d1, uint32_t* sh, ValueAt value_at) {
-  uint32_t t01, t23;
-  const uint32_t e01 = block_exclusive_scan((uint32_t)__popc(m[0]) | ((uint32_t)__popc(m[1]) << 16), &t01);
-  const uint32_t e23 = block_exclusive_scan((uint32_t)__popc(m[2]) | ((uint32_t)__popc(m[3]) << 16), &t23);
-  const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
-  uint32_t pos[kTopkRuns];
-  pos[0] = e01 & 0xFFFFu;
-  pos[1] = tot0 + (e01 >> 16);
-  pos[2] = tot0 + tot1 + (e23 & 0xFFFFu);
-  pos[3] = tot0 + tot1 + tot2 + (e23 >> 16);
-  uint32_t* __restrict__ si = slot_idx(w, tile, S);
-  float* __restrict__ sv = slot_val(w, tile, S);
-#pragma unroll
-  for (int u = 0; u < kTopkRuns; ++u) {
-    const uint64_t base = run_base(tile, u);
-    uint32_t bits = m[u];
-    uint32_t p = pos[u];
-    while (bits) {
-      const int j = __ffs(bits) - 1;
-      bits &= bits - 1;
-      const float x = value_at(u, j);
-      const uint32_t key = mag_key(x);
-      if ((key >> 20) == d1) atomicAdd(&sh[(key >> 10) & 1023u], 1u);
-      if (p < S) {
-        si[p] = (uint32_t)(base + j);
-        sv[p] = x;
-      }
-      ++p;
-    }
-  }
-  if (threadIdx.x == 0) {
-    const uint32_t n = tot0 + tot1 + tot2 + tot3;
-    w.n_s[tile] = n;
-    if (n > S) atomicOr(&w.st->overflow, 1u);
-  }
-}
-
-constexpr int kSplitStages = 3;  // tiles of 64 KiB in shared memory per block
-constexpr size_t kSplitStagedSmem = (size_t)kSplitStages * kTopkBlock * sizeof(float);
-
-// Pass 2 for 16-byte-aligned data, one block per SM: each block's whole
-// tiles are copied into a ring of kSplitStages shared-memory buffers with
-// asynchronous copies, kSplitStages - 1 tiles ahead of the tile being
-// processed, so the copies stay in flight through each tile's scans and slot
-// writes. Each thread copies exactly the 256 bytes it later reads (and only
-// then overwrites them), so no barrier has to order the copies. A partial
-// last tile is read directly.
-__global__ void __launch_bounds__(kThreads, 1) k_topk_split_staged(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
-  extern __shared__ float4 stage[];  // kSplitStages x (kTopkBlock / 4)
-  __shared__ uint32_t sh[1024];
-  const int r = blockIdx.y;
-  const RankWs w = rank_ws(A, r);
-  const uint64_t count = A.count;
-  const float* __restrict__ a = A.e[r];
-  const uint32_t S = A.slots;
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
-  const uint32_t d1 = w.st->prefix >> 20;
-  const uint32_t lo = d1 << 20;
-  __syncthreads();
-  const uint64_t nfull = count / kTopkBlock;
-  const uint64_t mine = nfull > blockIdx.x ? (nfull - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  auto issue = [&](uint64_t k) {  // this block's k-th whole tile into stage k % kSplitStages
-    if (k < mine) {
-      const float4* src = reinterpret_cast<const float4*>(a + (blockIdx.x + k * gridDim.x) * kTopkBlock);
-      float4* dst = stage + (k % kSplitStages) * (kTopkBlock / 4);
-#pragma unroll
-      for (int u = 0; u < kTopkRuns; ++u)
-#pragma unroll
-        for (int q = 0; q < kTopkElems / 4; ++q) {
-          const int i4 = (u * kThreads + threadIdx.x) * (kTopkElems / 4) + q;
-          cp_async16(dst + i4, src + i4);
-        }
-    }
-    cp_async_commit();  // one group per k, empty past the end, so the wait count below holds
-  };
-#pragma unroll
-  for (int k = 0; k < kSplitStages - 1; ++k) issue(k);
-  for (uint64_t k = 0; k < mine; ++k) {
-    issue(k + kSplitStages - 1);        // into the stage this thread finished reading at k - 1
-    cp_async_wait<kSplitStages - 1>();  // this thread's copies of tile k have landed
-    const uint64_t tile = blockIdx.x + k * gridDim.x;
-    const float4* buf = stage + (k % kSplitStages) * (kTopkBlock / 4);
-    uint32_t m[kTopkRuns];
-#pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) {
-      uint32_t b = 0;
-#pragma unroll
-      for (int q = 0; q < kTopkElems / 4; ++q) {
-        const float4 x = buf[(u * kThreads + threadIdx.x) * (kTopkElems / 4) + q];
-        if (mag_key(x.x) >= lo) b |= 1u << (4 * q);
-        if (mag_key(x.y) >= lo) b |= 2u << (4 * q);
-        if (mag_key(x.z) >= lo) b |= 4u << (4 * q);
-        if (mag_key(x.w) >= lo) b |= 8u << (4 * q);
-      }
-      m[u] = b;
-    }
-    const float* fb = reinterpret_cast<const float*>(buf);
-    split_tile_finish(w, tile, S, m, d1, sh, [&](int u, int j) {
-      return fb[(u * kThreads + threadIdx.x) * kTopkElems + j];
-    });
-  }
-  cp_async_wait<0>();
-  if (nfull < A.nb && nfull % gridDim.x == blockIdx.x) {  // the partial last tile
-    const uint64_t tile = nfull;
-    float v[kTopkRuns][kTopkElems];
-#pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) load_run<true>(a, run_base(tile, u), count, v[u]);
-    uint32_t m[kTopkRuns];
-#pragma unroll
-    for (int u = 0; u < kTopkRuns; ++u) m[u] = ge_mask(v[u], run_base(tile, u), count, lo);
-    split_tile_finish(w, tile, S, m, d1, sh, [&](int u, int j) { return a[run_base(tile, u) + j]; });
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 1024; i += blockDim.x)
@@ -924,20 +788,6 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
   }
 }
 
-// The staged pass needs more than the default 48 KiB of dynamic shared
-// memory; the attribute is set once per device (setting it is a host call
-// that costs far more than a launch).
-cudaError_t allow_staged_smem() {
-  static std::atomic<bool> done[kMaxRanks];
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev >= 0 && dev < kMaxRanks && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  err = cudaFuncSetAttribute(k_topk_split_staged, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSplitStagedSmem);
-  if (err == cudaSuccess && dev >= 0 && dev < kMaxRanks) done[dev].store(true, std::memory_order_release);
-  return err;
-}
-
 template <bool VEC>
 cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   const dim3 one(1, a.nranks);
@@ -959,17 +809,7 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   unsigned sx = (unsigned)(kSms * kSplitBlocksPerSm / a.nranks);
   if (sx < 1) sx = 1;
   if (sx > a.nb) sx = (unsigned)a.nb;
-  if (VEC) {
-    // one block per SM over all ranks, three 64 KiB stages each
-    unsigned qx = (unsigned)(kSms / a.nranks);
-    if (qx < 1) qx = 1;
-    if (qx > a.nb) qx = (unsigned)a.nb;
-    if ((err = allow_staged_smem()) != cudaSuccess) return err;
-    if ((err = pdl_launch(k_topk_split_staged, dim3(qx, a.nranks), kSplitStagedSmem, s, a)) != cudaSuccess)
-      return err;
-  } else if ((err = pdl_launch(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) {
-    return err;
-  }
+  if ((err = pdl_launch(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) return err;
   if ((err = pdl_launch(k_topk_pass3<VEC>, hgrid, 0, s, a)) != cudaSuccess) return err;
   const dim3 wgrid((unsigned)((a.nb + kWarps - 1) / kWarps), a.nranks);
   if ((err = pdl_launch(k_topk_count<VEC>, wgrid, 0, s, a)) != cudaSuccess) return err;
