@@ -311,3 +311,69 @@ def test_topk_workspace_reused_across_steps(offset):
             assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), (step, r)
             assert np.array_equal(_bits(from_dev(val[r])), _bits(ov)), (step, r)
             assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
+
+
+@pytest.mark.parametrize("n", [16, 64])
+def test_topk_and_sparse_allreduce_many_ranks(n):
+    # the most ranks one call takes: a shared-memory fold tile of 8192 / N values
+    count, k = 20_011, 150
+    g_np = [synthgen.normal_f32(count, 900 + r, 1.0) for r in range(n)]
+    e_np = [synthgen.normal_f32(count, 1900 + r, 0.1) for r in range(n)]
+    grads = [to_dev(x, "f32") for x in g_np]
+    res = [to_dev(x, "f32") for x in e_np]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    ws = torch.empty(gar.ar_topk_workspace_bytes(n, count, k), dtype=torch.uint8, device="cuda")
+    gar.ar_topk_compress(grads, res, k, idx, val, ws)
+    out = [torch.empty(count, device="cuda") for _ in range(n)]
+    sws = torch.empty(gar.ar_sparse_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    algo = "tree" if n & (n - 1) == 0 else "fused"
+    gar.ar_sparse_allreduce(idx, val, [k] * n, out, "avg", algo, sws)
+    torch.cuda.synchronize()
+    o_idx, o_val = [], []
+    for r in range(n):
+        oi, ov, oe = oracle.topk_compress(g_np[r], e_np[r], k)
+        assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), r
+        assert np.array_equal(_bits(from_dev(val[r])), _bits(ov)), r
+        assert np.array_equal(_bits(from_dev(res[r])), _bits(oe)), r
+        o_idx.append(oi)
+        o_val.append(ov)
+    dense = [oracle.sparse_to_dense(i, v, count) for i, v in zip(o_idx, o_val)]
+    want = oracle.tree_allreduce(dense, "f32", "avg")[0]
+    for r in range(n):
+        assert np.array_equal(_bits(from_dev(out[r])), _bits(want)), r
+
+
+def test_topk_step_captured_in_a_cuda_graph():
+    # the launches of one step (programmatic dependent launches included)
+    # replay from a CUDA graph with the same bits as eager calls
+    n, count, k = 4, 100_003, 1_000
+    g_np = [synthgen.normal_f32(count, 950 + r, 1.0) for r in range(n)]
+    grads = [to_dev(x, "f32") for x in g_np]
+    res = [torch.zeros(count, device="cuda") for _ in range(n)]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    out = [torch.empty(count, device="cuda") for _ in range(n)]
+    ws = torch.empty(gar.ar_topk_workspace_bytes(n, count, k), dtype=torch.uint8, device="cuda")
+    sws = torch.empty(gar.ar_sparse_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        g.capture_begin()
+        gar.ar_topk_compress(grads, res, k, idx, val, ws, side)
+        gar.ar_sparse_allreduce(idx, val, [k] * n, out, "sum", "fused", sws, side)
+        g.capture_end()
+    torch.cuda.current_stream().wait_stream(side)
+    e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
+    for step in range(3):  # capture itself ran nothing; three replays are three steps of feedback
+        g.replay()
+        torch.cuda.synchronize()
+        pairs = []
+        for r in range(n):
+            oi, ov, e_np[r] = oracle.topk_compress(g_np[r], e_np[r], k)
+            assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), (step, r)
+            assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
+            pairs.append((oi, ov))
+        want = oracle.sparse_ring_allreduce([p[0] for p in pairs], [p[1] for p in pairs], count, "sum")[0]
+        assert np.array_equal(_bits(from_dev(out[0])), _bits(want)), step
