@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constan
     }
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = __fdiv_rn(amax, 448.0f);
+    const float s = scale_of(amax);
     uint32_t word[V / 4];
     quantise_lane<V>(x, amax, s, word);
     if (b < nfull) {
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_scalar(const __grid_cons
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = __fdiv_rn(amax, 448.0f);
+    const float s = scale_of(amax);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint64_t e = lo + lane + 32 * k;

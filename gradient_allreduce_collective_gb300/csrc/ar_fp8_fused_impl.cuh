@@ -57,7 +57,7 @@ template <int IDT> struct Fp8FusedLd {
     }
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = __fdiv_rn(amax, 448.0f);
+    const float s = scale_of(amax);
     qdq_lane<V>(x, amax, s, d);
   }
   __device__ __forceinline__ static Acc comb(Acc a, Acc b) { return __fadd_rn(a, b); }
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_consta
       }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float s = __fdiv_rn(amax, 448.0f);
+      const float s = scale_of(amax);
       float t[4];
       qdq_lane<4>(x, amax, s, t);
 #pragma unroll

@@ -30,7 +30,7 @@ __device__ __forceinline__ void qdq_block(float (&p)[4]) {
   for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(p[k]));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float s = __fdiv_rn(amax, 448.0f);
+  const float s = scale_of(amax);
   const float x[4] = {p[0], p[1], p[2], p[3]};
   qdq_lane<4>(x, amax, s, p);
 }

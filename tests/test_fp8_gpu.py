@@ -46,6 +46,30 @@ def test_quantize_matches_oracle(in_dtype):
             assert _same_bits(from_dev(q), wq) and _same_bits(from_dev(s), ws), (count, off)
 
 
+@pytest.mark.parametrize("offset", [0, 4])
+def test_block_scales_over_the_binary32_range(offset):
+    # one block per amax: amax = random binary32 patterns over the whole
+    # positive range (the division-free scale's domain, its edges, subnormals,
+    # FLT_MAX) in slot 0 and zeros elsewhere; every scale and code bit-exact
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0x00000001, 0x7F800000, size=1 << 18, dtype=np.uint32)
+    edges = np.array([0x05800000, 0x057FFFFF, 0x05800001, 0x7F7FFFFF, 0x7F7FFFFE, 0x00800000, 0x007FFFFF,
+                      0x3F800000, 0x43E00000, 0x43E00001, 0x3B124925, 0x3B124924], dtype=np.uint32)
+    amax = np.concatenate([edges, bits]).view(np.float32)
+    x = np.zeros(amax.size * 128, dtype=np.float32)
+    x[::128] = amax
+    x[1::128] = -amax / np.float32(3.0)  # a second value per block (its code depends on the scale too)
+    g = Guarded(1, x.size, "f32", offset)
+    g.views[0].copy_(to_dev(x, "f32"))
+    q = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(amax.size, dtype=torch.float32, device="cuda")
+    gar.ar_quantize_fp8_blocks(g.views[0], q, sc)
+    wq, ws = oracle.fp8_quantize(x, "f32")
+    assert _same_bits(from_dev(sc), ws)
+    assert _same_bits(from_dev(q), wq)
+    g.check()
+
+
 def _e4m3_midpoints():
     codes = np.arange(0x7F, dtype=np.uint8)
     v = np.sort(oracle.e4m3_to_f32(codes).astype(np.float64))
