@@ -10,16 +10,23 @@
 // entries zeroed.
 //
 // Exact selection without sorting: the key T of the k-th largest magnitude
-// comes from a three-pass radix select over the 31 magnitude bits — a
-// histogram of bits 30..20 (fused with a = g + e), then of bits 19..10 and
-// 9..0 among the keys that match the prefix found so far. The block of each
-// pass that finishes last picks the digit (a block-wide scan of the
-// histogram from the top), so the state never leaves the device and no
-// launch is spent on it. Keys above T are all kept; of the keys equal to T,
-// the first (k - #above) in index order are kept: per-block counts, scanned
-// by the count pass's last block, and block-wide scans in the emit pass give
-// every kept element its slot. All ranks of a call share each launch
-// (grid.y = rank): six launches per call whatever the number of ranks.
+// comes from a three-digit radix select over the 31 magnitude bits (11 + 10
+// + 10 bits). Pass 1 reads g and e once, writes a, and histograms the first
+// digit. Pass 2 reads a once more, histograms the second digit among the keys
+// in the first digit's bin, and compacts every key at or above that bin (all
+// that can still be kept, about 2 % of the values) in index order into the
+// tile's slots. Pass 3, the count of keys above and equal to T per tile, and
+// the emission read only the slots; if some tile's keys do not fit its slots
+// they read the data instead (same results). The block of each pass that
+// finishes last picks the digit or scans the per-tile counts, so the state
+// never leaves the device and no launch is spent on it. Keys above T are all
+// kept; of the keys equal to T, the first (k - #above) in index order. All
+// ranks of a call share each launch (grid.y = rank): six launches per call.
+//
+// The sparse allreduce (SUM, AVG) densifies each output tile from every
+// rank's pairs in shared memory and folds it in the dense order, so only the
+// N replicas are written; MIN and MAX go through dense copies and the dense
+// allreduce.
 #include <algorithm>
 #include <cstdint>
 #include <string>
