@@ -86,6 +86,20 @@ __global__ void __launch_bounds__(kThreads, 4) k_fp8_hop(const __grid_constant__
 #pragma unroll
     for (int k = 0; k < 4; ++k) valid[k] = full || lo + lane + 32 * k < hi;
     const int s0 = (c + 1 == N) ? 0 : c + 1;
+    if (VEC) {
+      // this lane's vectors of the warp's next block, every rank, into L2:
+      // their loads then wait on L2 rather than DRAM
+      const uint64_t tn = t + nwarps;
+      if (tn < tasks) {
+        const int cn = (int)(tn / A.nbc);
+        const uint64_t lon = (uint64_t)cn * A.L + (tn - (uint64_t)cn * A.nbc) * kFp8Block;
+        if (lon + kFp8Block <= A.count) {
+          for (int r = 0; r < N; ++r)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(A.src[r]) +
+                                                            (lon + 4 * lane) * Fmt<IDT>::bytes));
+        }
+      }
+    }
     float p[4];
 #pragma unroll
     for (int b0 = 0; b0 < MAXN; b0 += 8) {
@@ -153,7 +167,10 @@ template <int IDT, int ODT, int OP>
 cudaError_t launch_hop_op(const Fp8HopArgs& a, cudaStream_t s) {
   const uint64_t tasks = (uint64_t)a.nranks * a.nbc;
   if (tasks == 0) return cudaSuccess;
-  const unsigned grid = grid_for(tasks * 32);
+  // a resident grid (4 blocks of 8 warps per SM), each warp looping over
+  // blocks, so that it can prefetch its next block while folding this one
+  const uint64_t resident = 152ull * 4;
+  const unsigned grid = grid_for(tasks * 32) < resident ? grid_for(tasks * 32) : (unsigned)resident;
   // 4-element vectors when every buffer allows them (block starts are
   // multiples of 4 elements: chunk lengths are multiples of 16 bytes of the
   // output type)
