@@ -377,3 +377,27 @@ def test_topk_step_captured_in_a_cuda_graph():
             pairs.append((oi, ov))
         want = oracle.sparse_ring_allreduce([p[0] for p in pairs], [p[1] for p in pairs], count, "sum")[0]
         assert np.array_equal(_bits(from_dev(out[0])), _bits(want)), step
+
+
+def test_sparse_allreduce_unaligned_outputs_and_ragged_tiles():
+    # outputs one float off 16-byte alignment take the element stores; a count
+    # that is not a multiple of the fold tile or of 4 leaves a ragged last tile
+    from tests._dev import Guarded
+    n, count = 6, 9_999
+    rng = np.random.default_rng(3)
+    idx_np, val_np = [], []
+    for r in range(n):
+        i = np.sort(rng.choice(count, size=[0, 1, 57, 999, count, 5][r], replace=False)).astype(np.uint32)
+        idx_np.append(i)
+        val_np.append(rng.standard_normal(i.size).astype(np.float32))
+    idx = [torch.from_numpy(i.view(np.int32)).cuda() if i.size else torch.empty(0, dtype=torch.int32, device="cuda")
+           for i in idx_np]
+    val = [to_dev(v, "f32") if v.size else torch.empty(0, dtype=torch.float32, device="cuda") for v in val_np]
+    ws = torch.empty(gar.ar_sparse_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+    for op in ("sum", "avg"):
+        out = Guarded(n, count, "f32", offset_bytes=4)
+        gar.ar_sparse_allreduce(idx, val, [i.size for i in idx_np], out.views, op, "fused", ws)
+        out.check()
+        want = oracle.sparse_ring_allreduce(idx_np, val_np, count, op)[0]
+        for r in range(n):
+            assert np.array_equal(_bits(from_dev(out.views[r])), _bits(want)), (op, r)
