@@ -24,7 +24,8 @@ N(0, 1e-3), op = avg), one fused ring-order pass per step. Inputs are
 
 `--workload sweep` prints one line per message size (8 ranks, 4 KiB..1 GiB
 per rank, fp32 sum; ring, tree and fused; warm and cold L2).
-`--workload fp8` and `--workload topk` print only that row.
+`--workload fp8` and `--workload topk` print only that row; `--workload
+strong` splits the bucket's elements over the GPUs (ar_allreduce_slice).
 `--impl reference` times the oracle alone on the bucket (rank 0 only).
 Under torchrun each GPU runs its own full workload (weak scaling: the
 virtual ranks already live on one device, so there is no exchange between
@@ -834,6 +835,60 @@ def run_ours(args):
     return 0
 
 
+# ----------------------------------------------------------------- GPU arm: strong scaling
+
+
+def run_strong(args):
+    """The bucket shared by all GPUs: GPU g computes elements [g*count/G,
+    (g+1)*count/G) of every rank with ar_allreduce_slice (the whole problem's
+    chunk plan, no exchange between GPUs); value = the bucket's busbw at the
+    slowest GPU's time."""
+    import torch
+
+    world, rank, local = dist_env()
+    dist = init_dist(world)
+    torch.cuda.set_device(local)
+    import gradient_allreduce_collective_gb300 as gar
+    import synthgen
+
+    gar.build()
+    gar.lib()
+    stream = torch.cuda.current_stream()
+    lo, hi = COUNT * rank // world, COUNT * (rank + 1) // world
+    lo -= lo % 4
+    hi = COUNT if rank == world - 1 else hi - hi % 4
+    send_np = synthgen.ranks_normal(NRANKS, COUNT, SIGMA, base_seed=0)
+    send = [torch.from_numpy(a[lo:hi].copy()).cuda() for a in send_np]
+    recv = [torch.empty_like(x) for x in send]
+
+    def step():
+        gar.ar_allreduce_slice(send, recv, COUNT, lo, OP, "fused", stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device_uuid(local))
+    clocks.start()
+    barrier(dist)
+    torch.cuda.synchronize()
+    ms = time_steps(step, args.steps, stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop()
+    ms_max = reduce_over_ranks(dist, ms, "max")
+    if rank != 0:
+        return 0
+    M = COUNT * 4
+    print(json.dumps({
+        "metric": METRIC, "value": busbw_gbs(M, ms_max * 1e-3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config("fused"), parallelism=f"the bucket's elements split over {world} GPU(s)"),
+        "hbm_gbs_per_gpu": 2 * NRANKS * (hi - lo) * 4 / (ms * 1e-3) / 1e9, "clocks": clk,
+        "gpu_launches": args.steps * max(1, NRANKS // world + 1)}))
+    return 0
+
+
 # ----------------------------------------------------------------- GPU arm: size sweep
 
 
@@ -933,7 +988,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("bucket", "sweep", "fp8", "topk"), default="bucket")
+    ap.add_argument("--workload", choices=("bucket", "sweep", "fp8", "topk", "strong"), default="bucket")
     ap.add_argument("--fp8-count", type=int, default=134_217_728, help="elements per rank for --workload fp8")
     ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
@@ -946,6 +1001,8 @@ def main(argv=None):
         return run_reference(args)
     if args.workload == "sweep":
         return run_sweep(args)
+    if args.workload == "strong":
+        return run_strong(args)
     if args.workload == "fp8":
         import torch
 

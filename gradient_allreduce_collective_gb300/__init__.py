@@ -17,7 +17,7 @@ import torch  # noqa: F401  (loads the shared CUDA runtime first)
 from ._build import build, lib_path
 
 __all__ = [
-    "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_reduce_scatter", "ar_all_gather",
+    "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_allreduce_slice", "ar_reduce_scatter", "ar_all_gather",
     "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
     "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops", "ar_allreduce_fp8_noalloc",
     "ar_topk_workspace_bytes", "ar_topk_compress", "ar_sparse_workspace_bytes", "ar_sparse_allreduce",
@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
     pp = ctypes.POINTER(ctypes.c_void_p)
     L.ar_allreduce.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
     L.ar_reduce_scatter.argtypes = [pp, pp, ci, sz, ci, ci, vp]
+    L.ar_allreduce_slice.argtypes = [pp, pp, ci, sz, sz, sz, ci, ci, ci, vp]
     L.ar_all_gather.argtypes = [pp, pp, ci, sz, ci, vp]
     L.ar_bucket_plan.argtypes = [vp, ci, ci, sz, vp, vp, vp, vp]
     L.ar_bucket_flatten.argtypes = [pp, vp, vp, ci, ci, vp, vp]
@@ -83,7 +84,7 @@ def lib() -> ctypes.CDLL:
     L.ar_sparse_workspace_bytes.argtypes = [ci, sz]
     L.ar_sparse_workspace_bytes.restype = sz
     L.ar_sparse_allreduce.argtypes = [pp, pp, vp, ci, sz, ci, ci, pp, vp, sz, vp]
-    for name in ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
+    for name in ("ar_allreduce", "ar_allreduce_slice", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
                  "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops",
                  "ar_topk_compress", "ar_sparse_allreduce"):
         getattr(L, name).restype = ci
@@ -155,6 +156,18 @@ def ar_allreduce(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tens
     _same(recvbufs, "recvbufs")
     _check(lib().ar_allreduce(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], OPS[op],
                               ALGOS[algo], _stream(stream)))
+
+
+def ar_allreduce_slice(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], count: int, first: int,
+                       op: str = "sum", algo: str = "fused", stream=None) -> None:
+    """Elements [first, first + n) of the allreduce of `count` elements per rank,
+    from each rank's slice of n elements (see include/ar.h)."""
+    dt, n = _same(sendbufs, "sendbufs")
+    if len(recvbufs) != len(sendbufs):
+        raise ValueError("one output per rank")
+    _same(recvbufs, "recvbufs")
+    _check(lib().ar_allreduce_slice(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), count, first, n, DTYPES[dt],
+                                    OPS[op], ALGOS[algo], _stream(stream)))
 
 
 def ar_reduce_scatter(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], op: str = "sum",

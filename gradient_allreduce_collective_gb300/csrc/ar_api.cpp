@@ -407,6 +407,68 @@ ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int
   return ok();
 }
 
+ar_status_t ar_allreduce_slice(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                               size_t first, size_t n, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo,
+                               ar_stream_t stream) {
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
+  if (st != AR_SUCCESS) return st;
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (!valid_any_algo(algo)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown algo");
+  // the stepwise executors give the ring and tree orders' bits; a slice takes those orders one pass at a time
+  if (algo == AR_ALGO_AUTO || algo == AR_ALGO_RING || algo == AR_ALGO_STEP_RING) algo = AR_ALGO_FUSED;
+  if (algo == AR_ALGO_STEP_TREE) algo = AR_ALGO_TREE;
+  if (algo == AR_ALGO_TREE && !pow2(nranks)) return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
+  const size_t es = elem_size(dtype);
+  if (count > SIZE_MAX / es / 2) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if (first > count || n > count - first) return fail(AR_ERR_INVALID_ARGUMENT, "slice outside the problem");
+  if (n == 0) return ok();
+  if ((st = check_ptrs(sendbufs, nranks, es, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, es, "recvbufs")) != AR_SUCCESS) return st;
+  std::vector<Span> spans;
+  std::vector<int> pair_in(nranks);
+  std::vector<uintptr_t> pair_off(nranks, 0);
+  for (int r = 0; r < nranks; ++r) {
+    spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + n * es, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + n * es, true, r});
+    pair_in[r] = r;  // in place: recvbufs[r] == sendbufs[r]
+  }
+  if (!overlap_ok(spans, pair_in, pair_off)) return fail(AR_ERR_ALIAS, "buffers overlap");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t V = 16 / es;
+  auto launch_piece = [&](size_t lo, size_t len, int rot, int mode) -> ar_status_t {
+    // elements [lo, lo + len) of the slice as one local chunk whose fold
+    // starts at the rank after `rot` (rank pointers rotated by rot)
+    ReduceArgs a{};
+    a.nranks = nranks;
+    a.count = len;
+    a.L = (len + V - 1) / V * V;
+    bool vec = true;
+    for (int r = 0; r < nranks; ++r) {
+      const int q = (r + rot) % nranks;
+      a.src[r] = static_cast<const char*>(sendbufs[q]) + lo * es;
+      a.dst[r] = static_cast<char*>(recvbufs[q]) + lo * es;
+      vec = vec && aligned(a.src[r], 16) && aligned(a.dst[r], 16);
+    }
+    a.vec = vec ? 1 : 0;
+    const cudaError_t e = launch_reduce(dtype, op, mode, a, s);
+    return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "slice allreduce launch");
+  };
+  if (algo == AR_ALGO_TREE) {  // the tree order does not depend on the chunk plan
+    st = launch_piece(0, n, 0, MODE_FUSED_TREE);
+    return st == AR_SUCCESS ? ok() : st;
+  }
+  // ring order: one launch per chunk of the whole problem that the slice
+  // meets; chunk c folds from rank c + 1, which the rotation by c provides
+  const size_t L = chunk_len(count, nranks, V);
+  for (size_t g = first; g < first + n;) {
+    const size_t c = g / L;
+    const size_t end = std::min(first + n, (c + 1) * L);
+    if ((st = launch_piece(g - first, end - g, (int)(c % (size_t)nranks), MODE_FUSED_RING)) != AR_SUCCESS) return st;
+    g = end;
+  }
+  return ok();
+}
+
 ar_status_t ar_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t recvcount,
                               ar_dtype_t dtype, ar_op_t op, ar_stream_t stream) {
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);

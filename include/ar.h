@@ -125,6 +125,23 @@ typedef enum {
 ar_status_t ar_allreduce(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
                          ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, ar_stream_t stream);
 
+/* A slice of an allreduce: elements [first, first + n) of the result of
+ * ar_allreduce over `count` elements per rank, bit-identical to them (same
+ * chunk plan, same summation order), computed from those elements alone.
+ * The pages have no counterpart: this is how several GPUs share one problem,
+ * each holding a contiguous slice of every rank's buffer, with no exchange
+ * between them (the result of element i depends only on the N values at i).
+ *   sendbufs[r], recvbufs[r] — rank r's slice (n elements each, device):
+ *                 element j of the slice is element first + j of the problem.
+ *   algo        — RING, FUSED, AUTO and STEP_RING give the ring order, TREE
+ *                 and STEP_TREE the recursive-halving order; in the ring order
+ *                 a slice that meets k chunks of the problem costs k launches.
+ * In place and overlap rules: as ar_allreduce. first + n > count gives
+ * AR_ERR_INVALID_ARGUMENT; n == 0 is a no-op. */
+ar_status_t ar_allreduce_slice(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
+                               size_t first, size_t n, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo,
+                               ar_stream_t stream);
+
 /* Reduce-scatter ([VL] §Reduce-Scatterは集約後の結果をrankへ分ける: reduce
  * element-wise, split into equal chunks, rank r keeps chunk r; [AW]
  * primitives table). Ring order with chunk length `recvcount`.

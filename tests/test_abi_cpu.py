@@ -238,3 +238,20 @@ def test_sparse_allreduce_argument_errors(L):
     assert f(idx=idx[:3] + [out[0] + 8]) == gar.AR_ERR_ALIAS                            # an index array inside an output
     assert f(count=1 << 32) == gar.AR_ERR_INVALID_ARGUMENT
     assert f(count=0) == gar.AR_SUCCESS
+
+
+def test_allreduce_slice_argument_errors(L):
+    n, count = 4, 1000
+    s = [0x1000000 * (r + 1) for r in range(n)]
+    d = [0x20000000 + 0x1000000 * r for r in range(n)]
+    f = L.ar_allreduce_slice
+    assert f(_arr(s), _arr(d), n, count, 990, 11, 0, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT  # past the end
+    assert f(_arr(s), _arr(d), n, count, 1001, 0, 0, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(_arr(s), _arr(d), n, count, 10, 0, 0, 0, 1, None) == gar.AR_SUCCESS                  # empty slice
+    assert f(_arr(s[:3]), _arr(d[:3]), 3, count, 0, 10, 0, 0, 2, None) == gar.AR_ERR_UNSUPPORTED  # tree, N=3
+    assert f(_arr(s[:3]), _arr(d[:3]), 3, count, 0, 10, 0, 0, 4, None) == gar.AR_ERR_UNSUPPORTED  # step tree, N=3
+    assert f(_arr(s), _arr(d), n, count, 0, 10, 0, 7, 1, None) == gar.AR_ERR_INVALID_ARGUMENT     # op
+    assert f(_arr(s), _arr(d), n, count, 0, 10, 0, 0, 9, None) == gar.AR_ERR_INVALID_ARGUMENT     # algo
+    over = list(d)
+    over[1] = d[0] + 8
+    assert f(_arr(s), _arr(over), n, count, 0, 10, 0, 0, 1, None) == gar.AR_ERR_ALIAS

@@ -308,3 +308,27 @@ def test_communicator_threads_launch_one_allreduce():
         assert _same_bits(from_dev(recv[r]), want)
     rec = comm.last_record(0)
     assert rec.seq == 1 and rec.arrived_mask == (1 << n) - 1
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("n", [3, 8])
+def test_slices_reassemble_the_allreduce(dtype, n):
+    # G "GPUs" each hold a contiguous slice of every rank's buffer (separate
+    # allocations, boundaries anywhere); their slice results concatenated are
+    # the whole problem's allreduce, bit for bit, in the ring and tree orders
+    count = 100_003
+    send_np = _rand(dtype, n, count, seed=77 + n)
+    rng = np.random.default_rng(n)
+    for op in ("sum", "avg", "max"):
+        for algo in ["fused", "ring", "auto", "step_ring"] + (["tree", "step_tree"] if n & (n - 1) == 0 else []):
+            want = _expect(send_np, dtype, op, algo)
+            for G in (1, 2, 3, 5):
+                cuts = [0] + sorted(int(x) for x in rng.integers(1, count, G - 1)) + [count]
+                got = []
+                for lo, hi in zip(cuts[:-1], cuts[1:]):
+                    send = [to_dev(a[lo:hi].copy(), dtype) for a in send_np]
+                    recv = [torch.empty_like(x) for x in send]
+                    gar.ar_allreduce_slice(send, recv, count, lo, op, algo)
+                    got.append([from_dev(x) for x in recv])
+                for r in range(n):
+                    assert _same_bits(np.concatenate([g[r] for g in got]), want), (op, algo, G, r)
