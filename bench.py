@@ -885,7 +885,7 @@ def run_strong(args):
         "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(workload_config("fused"), parallelism=f"the bucket's elements split over {world} GPU(s)"),
         "hbm_gbs_per_gpu": 2 * NRANKS * (hi - lo) * 4 / (ms * 1e-3) / 1e9, "clocks": clk,
-        "gpu_launches": args.steps * max(1, NRANKS // world + 1)}))
+        "gpu_launches": args.steps * (1 if lo % (-(-COUNT // NRANKS)) == 0 else 2)}))
     return 0
 
 

@@ -435,13 +435,14 @@ ar_status_t ar_allreduce_slice(const void* const* sendbufs, void* const* recvbuf
   if (!overlap_ok(spans, pair_in, pair_off)) return fail(AR_ERR_ALIAS, "buffers overlap");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t V = 16 / es;
-  auto launch_piece = [&](size_t lo, size_t len, int rot, int mode) -> ar_status_t {
-    // elements [lo, lo + len) of the slice as one local chunk whose fold
-    // starts at the rank after `rot` (rank pointers rotated by rot)
+  auto launch_piece = [&](size_t lo, size_t len, int rot, size_t Lp, int mode) -> ar_status_t {
+    // elements [lo, lo + len) of the slice in local chunks of Lp elements,
+    // local chunk c folded from the rank after c + rot (rank pointers
+    // rotated by rot)
     ReduceArgs a{};
     a.nranks = nranks;
     a.count = len;
-    a.L = (len + V - 1) / V * V;
+    a.L = Lp;
     bool vec = true;
     for (int r = 0; r < nranks; ++r) {
       const int q = (r + rot) % nranks;
@@ -454,17 +455,28 @@ ar_status_t ar_allreduce_slice(const void* const* sendbufs, void* const* recvbuf
     return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "slice allreduce launch");
   };
   if (algo == AR_ALGO_TREE) {  // the tree order does not depend on the chunk plan
-    st = launch_piece(0, n, 0, MODE_FUSED_TREE);
+    st = launch_piece(0, n, 0, (n + V - 1) / V * V, MODE_FUSED_TREE);
     return st == AR_SUCCESS ? ok() : st;
   }
-  // ring order: one launch per chunk of the whole problem that the slice
-  // meets; chunk c folds from rank c + 1, which the rotation by c provides
+  // ring order: chunk c of the whole problem folds from rank c + 1. The part
+  // of the slice before its first chunk boundary is one launch rotated by its
+  // chunk; from that boundary on, the problem's own chunk length with the
+  // rotation by the boundary's chunk index gives every later chunk its start
+  // rank: two launches at most.
   const size_t L = chunk_len(count, nranks, V);
-  for (size_t g = first; g < first + n;) {
+  size_t g = first;
+  if (g % L != 0) {
     const size_t c = g / L;
     const size_t end = std::min(first + n, (c + 1) * L);
-    if ((st = launch_piece(g - first, end - g, (int)(c % (size_t)nranks), MODE_FUSED_RING)) != AR_SUCCESS) return st;
+    if ((st = launch_piece(0, end - g, (int)(c % (size_t)nranks), (end - g + V - 1) / V * V, MODE_FUSED_RING)) !=
+        AR_SUCCESS)
+      return st;
     g = end;
+  }
+  if (g < first + n) {
+    if ((st = launch_piece(g - first, first + n - g, (int)((g / L) % (size_t)nranks), L, MODE_FUSED_RING)) !=
+        AR_SUCCESS)
+      return st;
   }
   return ok();
 }

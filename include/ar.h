@@ -134,8 +134,8 @@ ar_status_t ar_allreduce(const void *const *sendbufs, void *const *recvbufs, int
  *   sendbufs[r], recvbufs[r] — rank r's slice (n elements each, device):
  *                 element j of the slice is element first + j of the problem.
  *   algo        — RING, FUSED, AUTO and STEP_RING give the ring order, TREE
- *                 and STEP_TREE the recursive-halving order; in the ring order
- *                 a slice that meets k chunks of the problem costs k launches.
+ *                 and STEP_TREE the recursive-halving order; one launch, or
+ *                 two in the ring order when the slice starts inside a chunk.
  * In place and overlap rules: as ar_allreduce. first + n > count gives
  * AR_ERR_INVALID_ARGUMENT; n == 0 is a no-op. */
 ar_status_t ar_allreduce_slice(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
