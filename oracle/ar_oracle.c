@@ -27,7 +27,14 @@
  * and needs quantise/dequantise plus a scale exchange, [GL] §NCCLにおける
  * AllReduce, §勾配圧縮技術, [VL] §data typeと圧縮): parity unpinned for the
  * choice of block size and scale rule; the arithmetic itself is pinned by
- * format anchors, brute-force rounding and error bounds.
+ * format anchors, brute-force rounding and error bounds. The same holds for
+ * the per-hop FP8 reading (fp8-hop: pinned by a hand-computed example, the
+ * N = 1 reduction to quantise-once, a second per-block formulation and error
+ * bounds) and for Top-K (topk: the pages fix neither the tie rule nor the
+ * order of the pairs; pinned by hand-computed ties, k = 0 and k = count,
+ * brute force over subsets, the exact partition a = pairs + residual and
+ * gradient-mass conservation). The range form of the per-element fold is
+ * pinned by equality with the literal ring simulator.
  */
 #include <math.h>
 #include <stddef.h>
