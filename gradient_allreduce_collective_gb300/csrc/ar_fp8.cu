@@ -54,8 +54,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constan
       x[k] = to_f32<DT>(get_lane<B>(raw[u], k));
       amax = fmaxf(amax, fabsf(x[k]));
     }
-#pragma unroll
-    for (int o = G / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    amax = group_amax<G>(amax);
     const float s = scale_of(amax);
     uint32_t word[V / 4];
     quantise_lane<V>(x, amax, s, word);
@@ -95,8 +94,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_scalar(const __grid_cons
       x[k] = to_f32<DT>(bits);
       amax = fmaxf(amax, fabsf(x[k]));
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    amax = group_amax<32>(amax);
     const float s = scale_of(amax);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {

@@ -55,8 +55,7 @@ template <int IDT> struct Fp8FusedLd {
       x[k] = to_f32<IDT>(get_lane<B>(raw, k));
       amax = fmaxf(amax, fabsf(x[k]));
     }
-#pragma unroll
-    for (int o = G / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    amax = group_amax<G>(amax);
     const float s = scale_of(amax);
     qdq_lane<V>(x, amax, s, d);
   }
@@ -128,8 +127,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_consta
         x[k] = to_f32<IDT>(bits);
         amax = fmaxf(amax, fabsf(x[k]));
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      amax = group_amax<32>(amax);
       const float s = scale_of(amax);
       float t[4];
       qdq_lane<4>(x, amax, s, t);

@@ -28,8 +28,7 @@ __device__ __forceinline__ void qdq_block(float (&p)[4]) {
   float amax = 0.0f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(p[k]));
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  amax = group_amax<32>(amax);
   const float s = scale_of(amax);
   const float x[4] = {p[0], p[1], p[2], p[3]};
   qdq_lane<4>(x, amax, s, p);
