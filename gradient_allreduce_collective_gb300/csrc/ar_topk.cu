@@ -305,6 +305,54 @@ __device__ __forceinline__ uint32_t ge_mask(const float (&v)[kTopkElems], uint64
   return m;
 }
 
+// Slot positions of a tile's four runs per thread, in index order (all runs
+// of u = 0, then u = 1, ...), with one barrier: each warp scans its lanes'
+// counts with shuffles (runs 0 and 1, and 2 and 3, packed as two 16-bit
+// fields), publishes its four totals, and every thread adds up the totals of
+// the earlier runs and of the earlier warps. `tot` is a per-block buffer of
+// 2 x kWarps x 4 words used alternately by consecutive tiles (`parity`), so a
+// warp may start writing the next tile's totals while a slower one still
+// reads this tile's. Returns the tile's total in *n.
+__device__ __forceinline__ void run_positions(const uint32_t (&m)[kTopkRuns], uint32_t* tot, int parity,
+                                              uint32_t (&pos)[kTopkRuns], uint32_t* n) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t mine01 = (uint32_t)__popc(m[0]) | ((uint32_t)__popc(m[1]) << 16);
+  const uint32_t mine23 = (uint32_t)__popc(m[2]) | ((uint32_t)__popc(m[3]) << 16);
+  uint32_t s01 = mine01, s23 = mine23;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t a = __shfl_up_sync(0xffffffffu, s01, o), b = __shfl_up_sync(0xffffffffu, s23, o);
+    if (lane >= o) {
+      s01 += a;
+      s23 += b;
+    }
+  }
+  uint32_t* t = tot + parity * (kWarps * 4);
+  if (lane == 31) {  // the warp's totals per run (at most 512 each: no field overflows)
+    t[wid * 4 + 0] = s01 & 0xFFFFu;
+    t[wid * 4 + 1] = s01 >> 16;
+    t[wid * 4 + 2] = s23 & 0xFFFFu;
+    t[wid * 4 + 3] = s23 >> 16;
+  }
+  __syncthreads();
+  uint32_t run_tot[kTopkRuns] = {0, 0, 0, 0}, before[kTopkRuns] = {0, 0, 0, 0};
+#pragma unroll
+  for (int w2 = 0; w2 < kWarps; ++w2) {
+#pragma unroll
+    for (int u = 0; u < kTopkRuns; ++u) {
+      const uint32_t v = t[w2 * 4 + u];
+      run_tot[u] += v;
+      if (w2 < wid) before[u] += v;
+    }
+  }
+  const uint32_t ex01 = s01 - mine01, ex23 = s23 - mine23;
+  pos[0] = before[0] + (ex01 & 0xFFFFu);
+  pos[1] = run_tot[0] + before[1] + (ex01 >> 16);
+  pos[2] = run_tot[0] + run_tot[1] + before[2] + (ex23 & 0xFFFFu);
+  pos[3] = run_tot[0] + run_tot[1] + run_tot[2] + before[3] + (ex23 >> 16);
+  *n = run_tot[0] + run_tot[1] + run_tot[2] + run_tot[3];
+}
+
 // Pass 2, a resident grid looping over the tiles: each tile's keys at or
 // above the first digit's bin (every key that can still be kept) compacted in
 // index order into the tile's slots, and the histogram of bits 19..10 of the
@@ -315,6 +363,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__ TopkArgs A) {
   pdl_enter();
   __shared__ uint32_t sh[1024];
+  __shared__ uint32_t tot[2 * kWarps * 4];
+  int parity = 0;
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   const uint64_t count = A.count;
@@ -353,17 +403,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
 #pragma unroll
       for (int u = 0; u < kTopkRuns; ++u) m[u] = ge_mask(v[u], run_base(tile, u), count, lo);
     }
-    // slot positions in index order (all runs of u = 0, then u = 1, ...):
-    // runs 0 and 1, and runs 2 and 3, share one scan of two 16-bit counts
-    uint32_t t01, t23;
-    const uint32_t e01 = block_exclusive_scan((uint32_t)__popc(m[0]) | ((uint32_t)__popc(m[1]) << 16), &t01);
-    const uint32_t e23 = block_exclusive_scan((uint32_t)__popc(m[2]) | ((uint32_t)__popc(m[3]) << 16), &t23);
-    const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
-    uint32_t pos[kTopkRuns];
-    pos[0] = e01 & 0xFFFFu;
-    pos[1] = tot0 + (e01 >> 16);
-    pos[2] = tot0 + tot1 + (e23 & 0xFFFFu);
-    pos[3] = tot0 + tot1 + tot2 + (e23 >> 16);
+    uint32_t pos[kTopkRuns], ntile;
+    run_positions(m, tot, parity, pos, &ntile);
+    parity ^= 1;
     uint32_t* __restrict__ si = slot_idx(w, tile, S);
     float* __restrict__ sv = slot_val(w, tile, S);
 #pragma unroll
@@ -385,9 +427,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
       }
     }
     if (threadIdx.x == 0) {
-      const uint32_t n = tot0 + tot1 + tot2 + tot3;
-      w.n_s[tile] = n;
-      if (n > S) atomicOr(&w.st->overflow, 1u);
+      w.n_s[tile] = ntile;
+      if (ntile > S) atomicOr(&w.st->overflow, 1u);
     }
   }
   __syncthreads();
