@@ -83,9 +83,6 @@ struct RankWs {
   uint32_t* eq_before;
   uint32_t* out_off;
   uint32_t* n_s;
-  uint32_t* n_above;
-  uint32_t* n_dig;
-  uint16_t* digits;
   uint32_t* masks;
   uint32_t* slots;
 };
@@ -100,10 +97,7 @@ __device__ __forceinline__ RankWs rank_ws(const TopkArgs& A, int r) {
   w.eq_before = w.n_eq + A.nb;
   w.out_off = w.eq_before + A.nb;
   w.n_s = w.out_off + A.nb;
-  w.n_above = w.n_s + A.nb;
-  w.n_dig = w.n_above + A.nb;
-  w.digits = reinterpret_cast<uint16_t*>(w.n_dig + A.nb);
-  w.masks = w.n_dig + A.nb + A.nb * (kTopkDigitCap / 2);
+  w.masks = w.n_s + A.nb;
   w.slots = w.masks + A.nb * kThreads * kTopkRuns;
   return w;
 }
@@ -208,8 +202,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ 
     w.st->gt = 0;
     for (int p = 0; p < 4; ++p) w.st->ticket[p] = 0;
     w.st->overflow = 0;
-    w.st->digit_over = 0;
-    w.st->counted = 0;
   }
 }
 
@@ -445,15 +437,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   if (last_block(&w.st->ticket[1])) find_digit<1024>(w.hist, 10, w.st);
 }
 
-__device__ void scan_blocks(const RankWs& w, uint64_t nb);
-
-// Pass 3: histogram of bits 9..0 among the keys that match the prefix; then
-// (last block) the last digit, which completes T. From the slots, one warp
-// per tile also records the tile's keys above the prefix and the last digits
-// of the keys inside it, so that the last block can write every tile's
-// counts of keys above and equal to T and scan them (the count pass then
-// has nothing to do). After an overflow the data is read instead and the
-// count pass counts.
+// Pass 3: histogram of bits 9..0 among the keys that match the prefix, read
+// from the slots (or, after an overflow, from the data); then (last block)
+// the last digit, which completes T.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__ TopkArgs A) {
   pdl_enter();
@@ -463,40 +449,18 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
   for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
   __syncthreads();
   const uint32_t mask = w.st->mask, prefix = w.st->prefix;
-  const bool slots = !w.st->overflow;  // the same for every block
-  if (slots) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const uint32_t lt = (1u << lane) - 1u;
-    for (uint64_t tile = (uint64_t)blockIdx.x * kWarps + wid; tile < A.nb; tile += (uint64_t)gridDim.x * kWarps) {
+  auto add = [&](float x) {
+    const uint32_t key = mag_key(x);
+    if ((key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
+  };
+  if (!w.st->overflow) {
+    for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
       const float* sv = slot_val(w, tile, A.slots);
-      uint16_t* dig = w.digits + tile * kTopkDigitCap;
       const uint32_t n = w.n_s[tile];
-      uint32_t na = 0, nd = 0;
-      for (uint32_t c0 = 0; c0 < n; c0 += 32) {
-        const uint32_t c = c0 + lane;
-        const uint32_t key = c < n ? mag_key(sv[c]) : 0u;
-        const bool above = c < n && (key & mask) > prefix;
-        const bool match = c < n && (key & mask) == prefix;
-        const uint32_t mb = __ballot_sync(0xffffffffu, match);
-        na += (uint32_t)__popc(__ballot_sync(0xffffffffu, above));
-        if (match) {
-          atomicAdd(&sh[key & 1023u], 1u);
-          const uint32_t p = nd + (uint32_t)__popc(mb & lt);
-          if (p < (uint32_t)kTopkDigitCap) dig[p] = (uint16_t)(key & 1023u);
-        }
-        nd += (uint32_t)__popc(mb);
-      }
-      if (lane == 0) {
-        w.n_above[tile] = na;
-        w.n_dig[tile] = nd;
-        if (nd > (uint32_t)kTopkDigitCap) atomicOr(&w.st->digit_over, 1u);
-      }
+#pragma unroll 4
+      for (uint32_t c = threadIdx.x; c < n; c += blockDim.x) add(sv[c]);
     }
   } else {
-    auto add = [&](float x) {
-      const uint32_t key = mag_key(x);
-      if ((key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
-    };
     const float* __restrict__ a = A.e[r];
     const uint64_t count = A.count;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -519,29 +483,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
   __syncthreads();
   for (int i = threadIdx.x; i < 1024; i += blockDim.x)
     if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
-  if (last_block(&w.st->ticket[2])) {
-    find_digit<1024>(w.hist, 0, w.st);
-    __syncthreads();
-    if (slots && !__ldcg(&w.st->digit_over)) {
-      const uint32_t d3 = w.st->prefix & 1023u;
-      for (uint64_t t = threadIdx.x; t < A.nb; t += blockDim.x) {
-        const uint32_t nd = __ldcg(w.n_dig + t);
-        const uint16_t* dig = w.digits + t * kTopkDigitCap;
-        uint32_t gt = __ldcg(w.n_above + t), eq = 0;
-        for (uint32_t q = 0; q < nd; ++q) {
-          const uint32_t d = __ldcg(dig + q);
-          gt += d > d3;
-          eq += d == d3;
-        }
-        w.n_gt[t] = gt;
-        w.n_eq[t] = eq;
-      }
-      __threadfence();
-      __syncthreads();
-      scan_blocks(w, A.nb);
-      if (threadIdx.x == 0) w.st->counted = 1u;
-    }
-  }
+  if (last_block(&w.st->ticket[2])) find_digit<1024>(w.hist, 0, w.st);
 }
 
 // run mask: bit j set if value j's key is above T, bit 16 + j if it equals T
@@ -607,7 +549,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__
   pdl_enter();
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
-  if (w.st->counted) return;  // pass 3 wrote the counts and their scans (the same for every block)
   const uint32_t T = w.st->prefix;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (!w.st->overflow) {

@@ -22,16 +22,12 @@ constexpr uint32_t kTopkMaxSlots = 8192;                       // slot cap per t
 //   [0, 2048)        histogram of the current radix pass
 //   [2048, 2064)     TopkState
 //   then nb words each of n_gt, n_eq, eq_before, out_off, n_s (nb = tiles)
-//   then nb words each of n_above and n_dig, and nb * kTopkDigitCap / 2 words
-//   of digits: per tile, from the slots, the keys above the second digit's
-//   prefix and the last digits (bits 9..0) of the keys inside it (pass 3)
 //   then nb * kThreads * kTopkRuns words of run masks (used only when a
 //   tile's slots overflow): for the kTopkElems values of a run, bit j (j < 16)
 //   set if value j's key is above T, bit 16 + j if it equals T
 //   then per tile 2 * S words of slots: the indices, then the values, of the
 //   tile's keys at or above the first digit's bin (every key that can be
 //   kept), in index order; n_s[tile] of them
-constexpr int kTopkDigitCap = 32;  // last digits kept per tile by pass 3 (16 bits each)
 constexpr int kTopkHistWords = 2048;
 constexpr int kTopkStateWords = 16;
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
@@ -50,7 +46,7 @@ inline uint32_t topk_slots(uint64_t count, uint64_t k) {
 
 inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
   const uint64_t nb = topk_blocks(count);
-  return (kTopkHistWords + kTopkStateWords + (7 + kTopkDigitCap / 2 + (uint64_t)kThreads * kTopkRuns) * nb +
+  return (kTopkHistWords + kTopkStateWords + (5 + (uint64_t)kThreads * kTopkRuns) * nb +
           2ull * topk_slots(count, k) * nb + 63) / 64 * 64;
 }
 
@@ -66,10 +62,6 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //   overflow:    nonzero if some tile had more keys at or above the first
 //                digit's bin than its slots hold; the later passes then read
 //                the data instead
-//   digit_over:  nonzero if some tile had more than kTopkDigitCap keys inside
-//                the second digit's prefix (the count pass then counts)
-//   counted:     1 once pass 3's last block has written the per-tile counts
-//                and their scans (the count pass then has nothing to do)
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -77,9 +69,7 @@ struct TopkState {
   uint32_t gt;
   uint32_t ticket[4];
   uint32_t overflow;
-  uint32_t digit_over;
-  uint32_t counted;
-  uint32_t pad[5];
+  uint32_t pad[7];
 };
 static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 
