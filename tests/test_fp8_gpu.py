@@ -257,6 +257,32 @@ def test_fp8_hops_matches_oracle(in_dtype, out_dtype):
                     assert _same_bits(from_dev(v), want), (n, count, op)
 
 
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_fp8_hops_scales_over_the_binary32_range(out_dtype):
+    # every block of every rank at its own magnitude, 2^-140 .. 2^100 (block
+    # scales below, inside and above the range of the kernel's division-free
+    # path, subnormal values), some blocks zero: both blocks of a pair, one or
+    # neither, on the general path
+    rng = np.random.default_rng(12)
+    n, nblk = 3, 200
+    count = 128 * nblk + 40
+    send_np = []
+    for r in range(n):
+        x = rng.standard_normal(count)
+        e = rng.integers(-140, 100, size=nblk + 1)
+        scale = np.exp2(e.astype(np.float64))
+        scale[rng.random(nblk + 1) < 0.1] = 0.0
+        send_np.append((x * np.repeat(scale, 128)[:count]).astype(np.float32))
+    send = [to_dev(a, "f32") for a in send_np]
+    for op in ("sum", "avg"):
+        want = oracle.fp8_hop_ring_allreduce(send_np, "f32", out_dtype, op)[0]
+        out = Guarded(n, count, out_dtype, 0)
+        gar.ar_allreduce_fp8_hops(send, out.views, op)
+        out.check()
+        for v in out.views:
+            assert _same_bits(from_dev(v), want), op
+
+
 def test_fp8_hops_example():
     g = G.load("fp8_hop_example.txt")
     send = [to_dev(synthgen.to_dtype(np.array(G.nums(g[f"rank{r}"]), dtype=np.float32), "bf16"), "bf16")
