@@ -257,22 +257,47 @@ def test_fp8_hops_matches_oracle(in_dtype, out_dtype):
                     assert _same_bits(from_dev(v), want), (n, count, op)
 
 
-@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
-def test_fp8_hops_scales_over_the_binary32_range(out_dtype):
+def _wide_scale_ranks(n, nblk, seed, dtype):
     # every block of every rank at its own magnitude, 2^-140 .. 2^100 (block
-    # scales below, inside and above the range of the kernel's division-free
-    # path, subnormal values), some blocks zero: both blocks of a pair, one or
-    # neither, on the general path
-    rng = np.random.default_rng(12)
-    n, nblk = 3, 200
+    # scales below, inside and above the range of the kernels' division-free
+    # path, subnormal values), some blocks zero
+    rng = np.random.default_rng(seed)
     count = 128 * nblk + 40
-    send_np = []
+    out = []
     for r in range(n):
         x = rng.standard_normal(count)
         e = rng.integers(-140, 100, size=nblk + 1)
         scale = np.exp2(e.astype(np.float64))
         scale[rng.random(nblk + 1) < 0.1] = 0.0
-        send_np.append((x * np.repeat(scale, 128)[:count]).astype(np.float32))
+        out.append(synthgen.to_dtype((x * np.repeat(scale, 128)[:count]).astype(np.float32), dtype))
+    return out
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+def test_fp8_fused_scales_over_the_binary32_range(in_dtype):
+    for n in (3, 4):
+        send_np = _wide_scale_ranks(n, 300, 13 + n, in_dtype)
+        count = send_np[0].size
+        send = [to_dev(a, in_dtype) for a in send_np]
+        for op in ("sum", "avg"):
+            for algo in (("fused", "tree") if n == 4 else ("fused",)):
+                if algo == "tree":
+                    want = oracle.fp8_tree_allreduce(send_np, in_dtype, "bf16", op)[0]
+                else:
+                    want = oracle.fp8_ring_allreduce(send_np, in_dtype, "bf16", op)[0]
+                out = Guarded(n, count, "bf16")
+                gar.ar_allreduce_fp8_fused(send, out.views, op, algo)
+                out.check()
+                for v in out.views:
+                    assert _same_bits(from_dev(v), want), (n, op, algo)
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_fp8_hops_scales_over_the_binary32_range(out_dtype):
+    # both blocks of a pair, one or neither on the general path
+    n = 3
+    send_np = _wide_scale_ranks(n, 200, 12, "f32")
+    count = send_np[0].size
     send = [to_dev(a, "f32") for a in send_np]
     for op in ("sum", "avg"):
         want = oracle.fp8_hop_ring_allreduce(send_np, "f32", out_dtype, op)[0]
