@@ -11,11 +11,18 @@
 // format is what a multi-device ring would exchange, and its rounding is kept
 // exactly.
 //
+//  k_fp8_fused_pair  ring order, bf16/fp16 inputs: a warp per two blocks,
+//                    lane l holding elements 4l..4l+3 of each; block amax by a
+//                    warp max-reduction; every rank's pair quantised on the
+//                    call-free division-free path (the general path redoes a
+//                    warp whose scales leave its range), so that successive
+//                    ranks' quantisations overlap.
 //  k_fp8_fused_vec   16-byte loads, one lane group per block (16 lanes for
-//                    bf16/fp16, 32 for fp32); a warp whose elements all lie in
+//                    bf16/fp16, 32 for fp32); the tree order, and fp32 inputs.
+//                    In both vector kernels a warp whose elements all lie in
 //                    one ring chunk shares one start rank, so the fold needs no
-//                    per-rank storage. Warps that straddle a chunk boundary are
-//                    left to the element-wise kernel.
+//                    per-rank storage; warps that straddle a chunk boundary
+//                    are left to the element-wise kernel.
 //  k_fp8_fused_elem  one warp per block, elements lane + 32k: every rank's
 //                    dequantised values first, then each element folded in its
 //                    own chunk's order (straddling warps, the short last block,
@@ -99,6 +106,148 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_FUSED_TREE ? 1 : 4) k_f
   }
 }
 
+// Ring order, 16-bit inputs: the same two blocks per warp as
+// k_fp8_fused_vec, laid out as in the per-hop kernel: lane l holds elements
+// 4l..4l+3 of each block, each block's amax is one warp max-reduction, and
+// every rank's two blocks are quantised on the division-free path with no
+// branch or call, so that the quantisations of successive ranks (independent
+// of the running sum) overlap. If some block's scale lies outside
+// [2^-90, 2^90] the warp folds its blocks again on the general path.
+template <int IDT>
+__device__ __forceinline__ void fused_pair_load(const Fp8FusedArgs& A, int r, uint64_t ea, bool vb, uint2& a,
+                                                uint2& b) {
+  const uint16_t* src = static_cast<const uint16_t*>(A.src[r]);
+  a = __ldcs(reinterpret_cast<const uint2*>(src + ea));
+  b = vb ? __ldcs(reinterpret_cast<const uint2*>(src + ea + kFp8Block)) : make_uint2(0, 0);
+}
+
+template <int IDT>
+__device__ __forceinline__ void unpack4x16(uint2 v, float (&x)[4]) {
+  x[0] = to_f32<IDT>(v.x & 0xFFFFu);
+  x[1] = to_f32<IDT>(v.x >> 16);
+  x[2] = to_f32<IDT>(v.y & 0xFFFFu);
+  x[3] = to_f32<IDT>(v.y >> 16);
+}
+
+// dequantised values of one rank's two blocks; FAST: the division-free path,
+// returning false if a scale is outside its range
+template <bool FAST>
+__device__ __forceinline__ bool qdq_two(const float (&xa)[4], const float (&xb)[4], float (&da)[4],
+                                        float (&db)[4]) {
+  float ma = 0.0f, mb = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ma = fmaxf(ma, fabsf(xa[k]));
+    mb = fmaxf(mb, fabsf(xb[k]));
+  }
+  ma = group_amax<32>(ma);
+  mb = group_amax<32>(mb);
+  if constexpr (FAST) {
+    const float sa = scale_fast(ma), sb = scale_fast(mb);
+    qdq_fast<4>(xa, sa, recip_in_range(sa), da);
+    qdq_fast<4>(xb, sb, recip_in_range(sb), db);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      da[k] = ma == 0.0f ? 0.0f : da[k];
+      db[k] = mb == 0.0f ? 0.0f : db[k];
+    }
+    return (ma == 0.0f || scale_in_range(sa)) && (mb == 0.0f || scale_in_range(sb));
+  } else {
+    qdq_lane<4>(xa, ma, scale_of(ma), da);
+    qdq_lane<4>(xb, mb, scale_of(mb), db);
+    return true;
+  }
+}
+
+// ring-order fold of every rank's dequantised pair of blocks, starting at
+// rank s; ranks loaded eight at a time before they are folded
+template <int IDT, int MAXN, bool FAST>
+__device__ __forceinline__ bool fused_pair_ring(const Fp8FusedArgs& A, uint64_t ea, bool vb, int s,
+                                                float (&pa)[4], float (&pb)[4]) {
+  const int N = A.nranks;
+  bool ok = true;
+#pragma unroll 1
+  for (int b0 = 0; b0 < MAXN; b0 += 8) {
+    if (b0 >= N) break;
+    uint2 ra[8], rb[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (b0 + m < N) {
+        int r = s + b0 + m;
+        r = (r >= N) ? r - N : r;
+        fused_pair_load<IDT>(A, r, ea, vb, ra[m], rb[m]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (b0 + m < N) {
+        float xa[4], xb[4], da[4], db[4];
+        unpack4x16<IDT>(ra[m], xa);
+        unpack4x16<IDT>(rb[m], xb);
+        if (FAST) ok &= qdq_two<true>(xa, xb, da, db);
+        else qdq_two<false>(xa, xb, da, db);
+        if (b0 + m == 0) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            pa[k] = da[k];
+            pb[k] = db[k];
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            pa[k] = __fadd_rn(pa[k], da[k]);
+            pb[k] = __fadd_rn(pb[k], db[k]);
+          }
+        }
+      }
+    }
+  }
+  return ok;
+}
+
+template <int IDT, int MAXN>
+static __device__ __noinline__ void fused_pair_ring_general(const Fp8FusedArgs& A, uint64_t ea, bool vb, int s,
+                                                            float (&pa)[4], float (&pb)[4]) {
+  fused_pair_ring<IDT, MAXN, false>(A, ea, vb, s, pa, pb);
+}
+
+constexpr int kFusedPairBlocksPerSm = 3;
+
+template <int IDT, int ODT, int OP, int MAXN>
+__global__ void __launch_bounds__(kThreads, kFusedPairBlocksPerSm) k_fp8_fused_pair(const __grid_constant__ Fp8FusedArgs A) {
+  static_assert(Fmt<IDT>::bytes == 2, "16-bit inputs");
+  const int N = A.nranks;
+  const uint64_t nfull = A.count / kFp8Block;
+  const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t wb0 = warp * 2;
+  if (wb0 >= nfull) return;  // warp-uniform
+  const uint64_t wb1 = (wb0 + 2 < nfull) ? wb0 + 2 : nfull;
+  const uint64_t c_lo = (wb0 * kFp8Block) / A.L, c_hi = (wb1 * kFp8Block - 1) / A.L;
+  if (c_lo != c_hi) return;  // straddles a chunk boundary: the element-wise kernel's
+  const int s = ((int)c_lo + 1 == N) ? 0 : (int)c_lo + 1;
+  const bool vb = wb0 + 1 < nfull;  // the second block is whole
+  const uint64_t ea = wb0 * kFp8Block + 4 * lane;
+  float pa[4], pb[4];
+  if (!fused_pair_ring<IDT, MAXN, true>(A, ea, vb, s, pa, pb)) fused_pair_ring_general<IDT, MAXN>(A, ea, vb, s, pa, pb);
+  uint32_t ba[4], bb[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ba[k] = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(pa[k], (float)N) : pa[k]);
+    bb[k] = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(pb[k], (float)N) : pb[k]);
+  }
+  for (int r = 0; r < N; ++r) {
+    char* dst = static_cast<char*>(A.dst[r]);
+    if constexpr (Fmt<ODT>::bytes == 4) {
+      __stcs(reinterpret_cast<uint4*>(dst + ea * 4), make_uint4(ba[0], ba[1], ba[2], ba[3]));
+      if (vb) __stcs(reinterpret_cast<uint4*>(dst + (ea + kFp8Block) * 4), make_uint4(bb[0], bb[1], bb[2], bb[3]));
+    } else {
+      __stcs(reinterpret_cast<uint2*>(dst + ea * 2), make_uint2(ba[0] | (ba[1] << 16), ba[2] | (ba[3] << 16)));
+      if (vb) __stcs(reinterpret_cast<uint2*>(dst + (ea + kFp8Block) * 2), make_uint2(bb[0] | (bb[1] << 16), bb[2] | (bb[3] << 16)));
+    }
+  }
+}
+
 template <int IDT, int ODT, int OP, int MODE, int MAXN>
 __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_constant__ Fp8FusedArgs A) {
   constexpr int IB = Fmt<IDT>::bytes, OB = Fmt<ODT>::bytes;
@@ -171,7 +320,10 @@ cudaError_t launch_fused_n(bool vec, const Fp8FusedArgs& a, cudaStream_t stream)
     const uint64_t nfull = a.count / kFp8Block;
     if (nfull > 0) {
       const uint64_t warps = (nfull + BPW - 1) / BPW;
-      k_fp8_fused_vec<IDT, ODT, OP, MODE, MAXN><<<grid_for(warps * 32), kThreads, 0, stream>>>(a);
+      if constexpr (MODE == MODE_FUSED_RING && Fmt<IDT>::bytes == 2)
+        k_fp8_fused_pair<IDT, ODT, OP, MAXN><<<grid_for(warps * 32), kThreads, 0, stream>>>(a);
+      else
+        k_fp8_fused_vec<IDT, ODT, OP, MODE, MAXN><<<grid_for(warps * 32), kThreads, 0, stream>>>(a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
