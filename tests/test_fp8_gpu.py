@@ -199,6 +199,23 @@ FUSED_IO = [("bf16", "bf16"), ("bf16", "f16"), ("f16", "f16"), ("f16", "bf16"), 
             ("f32", "f16")]
 
 
+def test_fp8_fused_many_ranks():
+    # 33 ranks: the kernels' largest rank tier (batches of eight ranks in a loop)
+    n = 33
+    for in_dtype in ("bf16", "f32"):
+        for count in (128 * 66 + 24, 128 * 200):
+            send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=count, dtype=in_dtype, outlier_p=1e-2,
+                                            outlier_scale=100.0)
+            send = [to_dev(a, in_dtype) for a in send_np]
+            for op in ("sum", "avg"):
+                want = oracle.fp8_ring_allreduce(send_np, in_dtype, "bf16", op)[0]
+                out = Guarded(n, count, "bf16")
+                gar.ar_allreduce_fp8_fused(send, out.views, op, "fused")
+                out.check()
+                for v in out.views:
+                    assert _same_bits(from_dev(v), want), (in_dtype, count, op)
+
+
 @pytest.mark.parametrize("in_dtype,out_dtype", FUSED_IO)
 def test_fp8_fused_matches_oracle(in_dtype, out_dtype):
     # counts put chunk boundaries inside vector-kernel warps (element-wise path),
