@@ -144,13 +144,8 @@ __device__ __forceinline__ bool qdq_two(const float (&xa)[4], const float (&xb)[
   mb = group_amax<32>(mb);
   if constexpr (FAST) {
     const float sa = scale_fast(ma), sb = scale_fast(mb);
-    qdq_fast<4>(xa, sa, recip_in_range(sa), da);
-    qdq_fast<4>(xb, sb, recip_in_range(sb), db);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      da[k] = ma == 0.0f ? 0.0f : da[k];
-      db[k] = mb == 0.0f ? 0.0f : db[k];
-    }
+    qdq_fast_z<4>(xa, ma, sa, da);
+    qdq_fast_z<4>(xb, mb, sb, db);
     return (ma == 0.0f || scale_in_range(sa)) && (mb == 0.0f || scale_in_range(sb));
   } else {
     qdq_lane<4>(xa, ma, scale_of(ma), da);

@@ -58,13 +58,8 @@ __device__ __forceinline__ bool qdq_block_pair(float (&pa)[4], float (&pb)[4]) {
   mb = group_amax<32>(mb);
   const float sa = scale_fast(ma), sb = scale_fast(mb);
   const float xa[4] = {pa[0], pa[1], pa[2], pa[3]}, xb[4] = {pb[0], pb[1], pb[2], pb[3]};
-  qdq_fast<4>(xa, sa, recip_in_range(sa), pa);
-  qdq_fast<4>(xb, sb, recip_in_range(sb), pb);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    pa[k] = ma == 0.0f ? 0.0f : pa[k];
-    pb[k] = mb == 0.0f ? 0.0f : pb[k];
-  }
+  qdq_fast_z<4>(xa, ma, sa, pa);
+  qdq_fast_z<4>(xb, mb, sb, pb);
   return (ma == 0.0f || scale_in_range(sa)) && (mb == 0.0f || scale_in_range(sb));
 }
 

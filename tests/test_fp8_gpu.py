@@ -290,6 +290,52 @@ def _wide_scale_ranks(n, nblk, seed, dtype):
     return out
 
 
+def _signed_zero_ranks(n, nblk, seed, dtype):
+    # normal blocks with a fifth of their elements set to -0 or +0, blocks of
+    # mixed -0 / +0 only, and blocks of -0 only
+    rng = np.random.default_rng(seed)
+    count = 128 * nblk + 40
+    out = []
+    for r in range(n):
+        x = (rng.standard_normal(count) * 1e-3).astype(np.float32)
+        x[rng.random(count) < 0.1] = np.float32(-0.0)
+        x[rng.random(count) < 0.1] = np.float32(0.0)
+        kind = rng.integers(0, 4, size=nblk + 1)
+        for b in range(nblk + 1):
+            if kind[b] == 1:
+                x[128 * b:128 * (b + 1)] = np.where(rng.random(min(128, count - 128 * b)) < 0.5, -0.0, 0.0)
+            elif kind[b] == 2:
+                x[128 * b:128 * (b + 1)] = -0.0
+        out.append(synthgen.to_dtype(x, dtype))
+    return out
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+def test_fp8_signed_zeros(in_dtype):
+    # the sign of zero through quantisation, the fold and the output, on the
+    # fused, per-hop and materialised paths (every rank's block kinds differ,
+    # so some chunks fold only zeros)
+    for n in (3, 4):
+        send_np = _signed_zero_ranks(n, 120, 21 + n, in_dtype)
+        count = send_np[0].size
+        send = [to_dev(a, in_dtype) for a in send_np]
+        for op in ("sum", "avg"):
+            want = oracle.fp8_ring_allreduce(send_np, in_dtype, "bf16", op)[0]
+            out = Guarded(n, count, "bf16")
+            gar.ar_allreduce_fp8_fused(send, out.views, op, "fused")
+            out.check()
+            for v in out.views:
+                assert _same_bits(from_dev(v), want), ("fused", n, op)
+            gar.ar_allreduce_fp8(send, out.views, _ws(n, count), op, "fused")
+            for v in out.views:
+                assert _same_bits(from_dev(v), want), ("materialised", n, op)
+            want_hop = oracle.fp8_hop_ring_allreduce(send_np, in_dtype, "bf16", op)[0]
+            gar.ar_allreduce_fp8_hops(send, out.views, op)
+            out.check()
+            for v in out.views:
+                assert _same_bits(from_dev(v), want_hop), ("hops", n, op)
+
+
 @pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
 def test_fp8_fused_scales_over_the_binary32_range(in_dtype):
     for n in (3, 4):
