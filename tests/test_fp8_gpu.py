@@ -355,15 +355,16 @@ def test_fp8_fused_scales_over_the_binary32_range(in_dtype):
                     assert _same_bits(from_dev(v), want), (n, op, algo)
 
 
-@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
-def test_fp8_hops_scales_over_the_binary32_range(out_dtype):
-    # both blocks of a pair, one or neither on the general path
-    n = 3
-    send_np = _wide_scale_ranks(n, 200, 12, "f32")
+@pytest.mark.parametrize("in_dtype,out_dtype", [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16")])
+def test_fp8_hops_scales_over_the_binary32_range(in_dtype, out_dtype):
+    # both blocks of a pair, one or neither on the general path (binary32
+    # inputs fold four ranks per batch, 16-bit inputs eight)
+    n = 3 if in_dtype == "f32" else 10
+    send_np = _wide_scale_ranks(n, 200, 12, in_dtype)
     count = send_np[0].size
-    send = [to_dev(a, "f32") for a in send_np]
+    send = [to_dev(a, in_dtype) for a in send_np]
     for op in ("sum", "avg"):
-        want = oracle.fp8_hop_ring_allreduce(send_np, "f32", out_dtype, op)[0]
+        want = oracle.fp8_hop_ring_allreduce(send_np, in_dtype, out_dtype, op)[0]
         out = Guarded(n, count, out_dtype, 0)
         gar.ar_allreduce_fp8_hops(send, out.views, op)
         out.check()
