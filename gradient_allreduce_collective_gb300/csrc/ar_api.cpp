@@ -12,6 +12,7 @@
 
 #include "ar.h"
 #include "ar_internal.h"
+#include "ar_trace.h"
 
 namespace gar {
 
@@ -352,6 +353,7 @@ const char* ar_last_error(void) { return g_last_error.c_str(); }
 
 ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
                          ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, ar_stream_t stream) {
+  AR_TRACE("ar_allreduce");
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
   if (st != AR_SUCCESS) return st;
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
@@ -410,6 +412,7 @@ ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int
 ar_status_t ar_allreduce_slice(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
                                size_t first, size_t n, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo,
                                ar_stream_t stream) {
+  AR_TRACE("ar_allreduce_slice");
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
   if (st != AR_SUCCESS) return st;
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
@@ -483,6 +486,7 @@ ar_status_t ar_allreduce_slice(const void* const* sendbufs, void* const* recvbuf
 
 ar_status_t ar_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t recvcount,
                               ar_dtype_t dtype, ar_op_t op, ar_stream_t stream) {
+  AR_TRACE("ar_reduce_scatter");
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
   if (st != AR_SUCCESS) return st;
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
@@ -517,6 +521,7 @@ ar_status_t ar_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
 
 ar_status_t ar_all_gather(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t sendcount,
                           ar_dtype_t dtype, ar_stream_t stream) {
+  AR_TRACE("ar_all_gather");
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
   if (st != AR_SUCCESS) return st;
   if (sendcount == 0) return ok();
@@ -653,6 +658,7 @@ extern "C" {
 
 ar_status_t ar_bucket_flatten(const void* const* tensors, const size_t* counts, const size_t* offsets, int ntensors,
                               ar_dtype_t dtype, void* bucket, ar_stream_t stream) {
+  AR_TRACE("ar_bucket_flatten");
   if (!bucket && ntensors > 0) return fail(AR_ERR_INVALID_ARGUMENT, "null bucket");
   return bucket_copy(tensors, nullptr, nullptr, bucket, counts, offsets, ntensors, dtype,
                      reinterpret_cast<cudaStream_t>(stream));
@@ -660,6 +666,7 @@ ar_status_t ar_bucket_flatten(const void* const* tensors, const size_t* counts, 
 
 ar_status_t ar_bucket_unflatten(const void* bucket, void* const* tensors, const size_t* counts, const size_t* offsets,
                                 int ntensors, ar_dtype_t dtype, ar_stream_t stream) {
+  AR_TRACE("ar_bucket_unflatten");
   if (!bucket && ntensors > 0) return fail(AR_ERR_INVALID_ARGUMENT, "null bucket");
   return bucket_copy(nullptr, tensors, bucket, nullptr, counts, offsets, ntensors, dtype,
                      reinterpret_cast<cudaStream_t>(stream));
@@ -668,6 +675,7 @@ ar_status_t ar_bucket_unflatten(const void* bucket, void* const* tensors, const 
 ar_status_t ar_bucket_allreduce(const void* const* tensors, void* const* out_tensors, int nranks, int ntensors,
                                 const size_t* counts, const size_t* offsets, size_t bucket_count, ar_dtype_t dtype,
                                 ar_op_t op, ar_algo_t algo, ar_stream_t stream) {
+  AR_TRACE("ar_bucket_allreduce");
   ar_status_t st = common_checks(tensors, out_tensors, nranks, dtype);
   if (st != AR_SUCCESS) return st;
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
@@ -770,6 +778,7 @@ size_t ar_fp8_workspace_bytes(int nranks, size_t count) {
 
 ar_status_t ar_quantize_fp8_blocks(const void* in, ar_dtype_t in_dtype, size_t count, uint8_t* q, float* scales,
                                    ar_stream_t stream) {
+  AR_TRACE("ar_quantize_fp8_blocks");
   if (in_dtype != AR_F32 && in_dtype != AR_F16 && in_dtype != AR_BF16)
     return fail(AR_ERR_INVALID_ARGUMENT, "in_dtype must be F32, F16 or BF16");
   if (count == 0) return ok();
@@ -797,6 +806,7 @@ ar_status_t ar_quantize_fp8_blocks(const void* in, ar_dtype_t in_dtype, size_t c
 ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
                              ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo, void* workspace,
                              size_t ws_bytes, ar_stream_t stream) {
+  AR_TRACE("ar_allreduce_fp8");
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, in_dtype);
   if (st != AR_SUCCESS) return st;
   if (in_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating input type");
@@ -867,6 +877,7 @@ ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs,
 
 ar_status_t ar_allreduce_fp8_hops(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
                                   ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_stream_t stream) {
+  AR_TRACE("ar_allreduce_fp8_hops");
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, in_dtype);
   if (st != AR_SUCCESS) return st;
   if (in_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating input type");
@@ -901,6 +912,7 @@ ar_status_t ar_allreduce_fp8_hops(const void* const* sendbufs, void* const* recv
 ar_status_t ar_allreduce_fp8_fused(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
                                    ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo,
                                    ar_stream_t stream) {
+  AR_TRACE("ar_allreduce_fp8_fused");
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, in_dtype);
   if (st != AR_SUCCESS) return st;
   if (in_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating input type");

@@ -34,6 +34,7 @@
 
 #include "ar.h"
 #include "ar_topk_internal.h"
+#include "ar_trace.h"
 
 namespace gar {
 
@@ -926,6 +927,7 @@ size_t ar_topk_workspace_bytes(int nranks, size_t count, size_t k) {
 ar_status_t ar_topk_compress(const float* const* grads, float* const* residuals, int nranks, size_t count, size_t k,
                              uint32_t* const* idx, float* const* val, void* workspace, size_t ws_bytes,
                              ar_stream_t stream) {
+  AR_TRACE("ar_topk_compress");
   if (!grads || !residuals || !idx || !val) return tk_fail(AR_ERR_INVALID_ARGUMENT, "null buffer array");
   if (nranks < 1 || nranks > AR_MAX_RANKS) return tk_fail(AR_ERR_INVALID_ARGUMENT, "nranks must be in 1..64");
   if (count > 0xFFFFFFFFull) return tk_fail(AR_ERR_INVALID_ARGUMENT, "count must fit 32-bit indices");
@@ -980,6 +982,7 @@ size_t ar_sparse_workspace_bytes(int nranks, size_t count) {
 ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* val, const size_t* nnz, int nranks,
                                 size_t count, ar_op_t op, ar_algo_t algo, float* const* recvbufs, void* workspace,
                                 size_t ws_bytes, ar_stream_t stream) {
+  AR_TRACE("ar_sparse_allreduce");
   if (!idx || !val || !nnz || !recvbufs) return tk_fail(AR_ERR_INVALID_ARGUMENT, "null array");
   if (nranks < 1 || nranks > AR_MAX_RANKS) return tk_fail(AR_ERR_INVALID_ARGUMENT, "nranks must be in 1..64");
   if (op < AR_SUM || op > AR_MAX) return tk_fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
