@@ -23,7 +23,9 @@ N(0, 1e-3), op = avg), one fused ring-order pass per step. Inputs are
           same bucket, a bounded number of repetitions.
 
 `--workload sweep` prints one line per message size (8 ranks, 4 KiB..1 GiB
-per rank, fp32 sum; ring, tree and fused; warm and cold L2).
+per rank; fp32 uniform(-1,1) sum, or with `--sweep-dtype i32 --sweep-op
+min|max` int32 uniform[-2^20, 2^20]; ring, tree, fused and the stepwise
+executors; warm and cold L2).
 `--workload fp8` and `--workload topk` print only that row; `--workload
 strong` splits the bucket's elements over the GPUs (ar_allreduce_slice).
 `--impl reference` times the oracle alone on the bucket (rank 0 only).
@@ -304,6 +306,24 @@ def run_reference(args):
 # ----------------------------------------------------------------- GPU helpers
 
 
+# About half a millisecond of SM cycles at the GB300's 2.07 GHz maximum clock.
+HOLD_CYCLES = 1_000_000
+
+
+def hold_stream(stream) -> None:
+    """Keep `stream` busy for about 0.5 ms with PyTorch's spin kernel before a
+    start event is recorded behind it. The host then has the first timed
+    launches queued by the time the start event fires, so the timed region
+    holds the device time of the steps and not the host's latency to issue
+    the first one into an idle stream (the blocking-kernel idea of NVIDIA's
+    NVBench). The steps themselves still run back to back as the host issues
+    them; nothing of theirs is outside the region."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HOLD_CYCLES)
+
+
 def time_steps(fn, steps: int, stream) -> float:
     """Average ms per call of fn() over `steps` calls, CUDA events on `stream`."""
     import torch
@@ -311,6 +331,7 @@ def time_steps(fn, steps: int, stream) -> float:
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    hold_stream(stream)
     start.record(stream)
     for _ in range(steps):
         fn()
@@ -676,6 +697,37 @@ def measure_topk(gar, steps: int, warmup: int, count: int = COUNT, frac: float =
 # ----------------------------------------------------------------- GPU arm: headline
 
 
+def rows_summary(rows: dict, other: dict, ms_headline: float, peak: float) -> dict:
+    """Milliseconds per step and fraction of the measured HBM peak of every
+    row, compact, so that they survive a truncated log next to the headline."""
+    alg = 2 * NRANKS * COUNT * 4
+
+    def ent(ms, moved):
+        return {"ms": round(ms, 4), "frac": round(moved / (ms * 1e-3) / 1e9 / peak, 3)}
+
+    out = {"fused_ring": ent(ms_headline, alg), "tree": ent(other["tree"], alg),
+           "ring_rs_ag": ent(other["ring"], (2 * NRANKS + 1) * COUNT * 4)}  # reduce-scatter + all-gather bytes
+    ddp = rows.get("ddp_bucket_sync")
+    if ddp:
+        for name in ("direct", "three_step"):
+            r = ddp[name]
+            best = min(r["ms_per_step_eager"], r["ms_per_step_cuda_graph"])
+            out[f"ddp_{name}"] = {"ms": round(best, 4), "frac": round(r["frac_hbm"], 3)}
+    fp8 = rows.get("fp8_allreduce")
+    if fp8:
+        for name in ("materialised", "fused_quantisation", "per_hop"):
+            r = fp8[name]
+            out[f"fp8_{name}"] = {"ms": round(r["ms_per_step"], 4), "frac": round(r["frac_hbm"], 3)}
+    tk = rows.get("topk_sparse_allreduce")
+    if tk:
+        c = tk["compress"]
+        out["topk_compress"] = {"ms": round(c["ms"], 4), "frac_min_bytes": round(c["hbm_gbs_min_bytes"] / peak, 3),
+                                "frac_structure": round(c["frac_hbm_structure"], 3)}
+        sp = tk["sparse_allreduce"]
+        out["sparse_allreduce"] = {"ms": round(sp["ms"], 4), "frac": round(sp["frac_hbm"], 3)}
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -769,7 +821,9 @@ def run_ours(args):
     e2e_steps = max(5, min(args.steps, 200))
     barrier(dist)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(stream)
     start.record(stream)
+    s_in.wait_stream(stream)  # the first upload starts after the start event, not during the hold
     for _ in range(e2e_steps):
         step_e2e()
     stream.wait_stream(s_out)
@@ -801,6 +855,7 @@ def run_ours(args):
         cpu = oracle_baseline(args.cpu_budget)
     if rank != 0:
         return 0
+    summary = rows_summary(rows, other, ms_max, peak)
     line = {
         "metric": METRIC,
         "value": value,
@@ -815,6 +870,7 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic (seeded SplitMix64 + Box-Muller N(0, 1e-3), rank r uses seed r)",
         "config": workload_config("fused"),
+        "rows_summary": summary,
         "algbw_gbs": M / (ms_max * 1e-3) / 1e9,
         "hbm_gbs": achieved,
         "pct_hbm_roofline": 100.0 * achieved / peak,
@@ -904,9 +960,15 @@ def run_sweep(args):
     n = 8
     max_bytes = args.sweep_max_bytes
     nmax = max_bytes // 4
-    host = synthgen.ranks_uniform(n, nmax, -1.0, 1.0, base_seed=0)
-    send = [torch.from_numpy(a).cuda() for a in host]
-    del host
+    dtype, op = args.sweep_dtype, args.sweep_op
+    if dtype == "i32" and op not in ("min", "max"):
+        raise SystemExit("the int32 leg of the sweep takes --sweep-op min or max")
+    send = []
+    for r in range(n):  # one rank at a time on the host: 1 GiB each at the largest size
+        host = (synthgen.uniform_i32(nmax, r, -(2**20), 2**20) if dtype == "i32"
+                else synthgen.uniform_f32(nmax, r, -1.0, 1.0))
+        send.append(torch.from_numpy(host).cuda())
+        del host
     recv = [torch.empty_like(s) for s in send]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
@@ -921,7 +983,7 @@ def run_sweep(args):
         res = {}
         for algo in ("fused", "tree", "ring"):
             def f(a=algo):
-                gar.ar_allreduce(s_v, r_v, "sum", a, stream)
+                gar.ar_allreduce(s_v, r_v, op, a, stream)
             for _ in range(5):
                 f()
             reps = max(5, min(2000, int(2e9 / (2 * n * size))))
@@ -948,7 +1010,7 @@ def run_sweep(args):
             with torch.cuda.stream(side):
                 g.capture_begin()
                 for _ in range(reps):
-                    gar.ar_allreduce(s_v, r_v, "sum", algo, side)
+                    gar.ar_allreduce(s_v, r_v, op, algo, side)
                 g.capture_end()
             stream.wait_stream(side)
             g.replay()
@@ -956,7 +1018,7 @@ def run_sweep(args):
             del g
         for algo, us in graph_us.items():
             fits.setdefault(algo, []).append((size, us))
-        print(json.dumps({"workload": "size sweep", "nranks": n, "bytes_per_rank": size, "dtype": "f32", "op": "sum",
+        print(json.dumps({"workload": "size sweep", "nranks": n, "bytes_per_rank": size, "dtype": dtype, "op": op,
                           "in_l2": 2 * n * size <= l2, "graph_us": graph_us, **res}))
         sys.stdout.flush()
         size *= 2
@@ -977,7 +1039,7 @@ def run_sweep(args):
         pred = {al: v["alpha_us_per_launch"] * v["launches_per_call"] + traffic[al] * m / 1e3 / v["beta_gbs"]
                 for al, v in model.items() if v["beta_gbs"]}
         best[m] = min(pred, key=pred.get)
-    print(json.dumps({"workload": "alpha-beta fit", "nranks": n, "model": model,
+    print(json.dumps({"workload": "alpha-beta fit", "nranks": n, "dtype": dtype, "op": op, "model": model,
                       "fastest_by_model": {str(k): v for k, v in best.items()}}))
     return 0
 
@@ -991,6 +1053,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=("bucket", "sweep", "fp8", "topk", "strong"), default="bucket")
     ap.add_argument("--fp8-count", type=int, default=134_217_728, help="elements per rank for --workload fp8")
     ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
+    ap.add_argument("--sweep-dtype", choices=("f32", "i32"), default="f32",
+                    help="f32 uniform(-1,1) or int32 uniform[-2^20, 2^20] per rank")
+    ap.add_argument("--sweep-op", choices=("sum", "min", "max"), default="sum")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true", help="skip the DDP, FP8 and Top-K rows")
