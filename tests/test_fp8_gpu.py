@@ -173,6 +173,24 @@ def test_fp8_block_example():
                 assert y.float().cpu().tolist() == G.nums(g[f"expect_{op}"]), (op, algo)
 
 
+def test_fp8_tree_example():
+    # the hand-computed recursive-halving pairing after E4M3 quantisation, on
+    # the materialised and the fused paths (the ring order gives other values)
+    g = G.load("fp8_tree_example.txt")
+    send = [to_dev(synthgen.to_dtype(np.array(G.nums(g[f"rank{r}"]), dtype=np.float32), "bf16"), "bf16")
+            for r in range(4)]
+    for op in ("sum", "avg"):
+        for algo, key in (("tree", "tree"), ("fused", "ring"), ("ring", "ring")):
+            for path in ("materialised", "fused"):
+                recv = [torch.empty(4, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+                if path == "materialised":
+                    gar.ar_allreduce_fp8(send, recv, _ws(4, 4), op, algo)
+                else:
+                    gar.ar_allreduce_fp8_fused(send, recv, op, algo)
+                for y in recv:
+                    assert y.float().cpu().tolist() == G.nums(g[f"expect_{key}_{op}"]), (op, algo, path)
+
+
 @pytest.mark.parametrize("in_dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f16", "f32"])
 def test_fp8_allreduce_matches_oracle(in_dtype, out_dtype):

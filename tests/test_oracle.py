@@ -324,6 +324,18 @@ def test_fp8_blocks_match_full():
         assert np.array_equal(out[j, : blen[j]], full[first[j]: first[j] + blen[j]])
 
 
+def test_fp8_tree_example():
+    # hand-computed: the recursive-halving pairing (x0 + x2) + (x1 + x3) after E4M3 quantisation,
+    # distinct from the ring order and from the adjacent pairing
+    g = G.load("fp8_tree_example.txt")
+    send = [_as("bf16", G.nums(g[f"rank{r}"])) for r in range(4)]
+    for op in ("sum", "avg"):
+        for y in oracle.fp8_tree_allreduce(send, "bf16", "bf16", op):
+            assert oracle.bf16_to_f32(y).tolist() == G.nums(g[f"expect_tree_{op}"])
+        for y in oracle.fp8_ring_allreduce(send, "bf16", "bf16", op):
+            assert oracle.bf16_to_f32(y).tolist() == G.nums(g[f"expect_ring_{op}"])
+
+
 def test_fp8_tree_and_ring_agree_up_to_order():
     n, count = 8, 4096
     send = synthgen.ranks_normal(n, count, 1e-3, base_seed=8, dtype="bf16")
