@@ -3,6 +3,7 @@
 // by-value kernel argument blocks. Everything here runs on the host; nothing
 // allocates device memory or synchronises.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <string>
@@ -68,6 +69,31 @@ cudaError_t launch_fp8_hop(int in_dtype, int out_dtype, int op, const Fp8HopArgs
     case DT_F32: return launch_fp8_hop_f32(out_dtype, op, a, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];  // 0: not read yet
+}  // namespace
+
+cudaError_t sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return cudaSuccess;
+    }
+  }
+  int c = 0;
+  e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (c < 1) c = 1;
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(c, std::memory_order_relaxed);
+  *out = c;
+  return cudaSuccess;
 }
 
 cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream) {
@@ -803,10 +829,14 @@ ar_status_t ar_quantize_fp8_blocks(const void* in, ar_dtype_t in_dtype, size_t c
   return e == cudaSuccess ? ok() : cuda_fail(e, "quantise launch");
 }
 
-ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
-                             ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo, void* workspace,
-                             size_t ws_bytes, ar_stream_t stream) {
-  AR_TRACE("ar_allreduce_fp8");
+}  // extern "C"
+
+namespace gar {
+
+// The checks of ar_allreduce_fp8 that come before its workspace: buffer
+// arrays, rank count, types, op and order (AUTO resolves to the fused order).
+ar_status_t fp8_arg_checks(const void* const* sendbufs, void* const* recvbufs, int nranks, ar_dtype_t in_dtype,
+                           ar_dtype_t out_dtype, ar_op_t op, ar_algo_t* algo) {
   ar_status_t st = common_checks(sendbufs, recvbufs, nranks, in_dtype);
   if (st != AR_SUCCESS) return st;
   if (in_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating input type");
@@ -814,9 +844,22 @@ ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs,
   if (out_dtype == AR_I32) return fail(AR_ERR_UNSUPPORTED, "FP8 path needs a floating output type");
   if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
   if (op != AR_SUM && op != AR_AVG) return fail(AR_ERR_UNSUPPORTED, "FP8 path supports SUM and AVG");
-  if ((st = basic_algo(&algo)) != AR_SUCCESS) return st;
-  if (algo == AR_ALGO_TREE && !pow2(nranks))
+  if ((st = basic_algo(algo)) != AR_SUCCESS) return st;
+  if (*algo == AR_ALGO_TREE && !pow2(nranks))
     return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
+  return AR_SUCCESS;
+}
+
+}  // namespace gar
+
+extern "C" {
+
+ar_status_t ar_allreduce_fp8(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                             ar_dtype_t in_dtype, ar_dtype_t out_dtype, ar_op_t op, ar_algo_t algo, void* workspace,
+                             size_t ws_bytes, ar_stream_t stream) {
+  AR_TRACE("ar_allreduce_fp8");
+  ar_status_t st = gar::fp8_arg_checks(sendbufs, recvbufs, nranks, in_dtype, out_dtype, op, &algo);
+  if (st != AR_SUCCESS) return st;
   if (count == 0) return ok();
   const size_t need = ar_fp8_workspace_bytes(nranks, count);
   if (need == 0) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");

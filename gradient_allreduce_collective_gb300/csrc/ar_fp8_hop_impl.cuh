@@ -287,7 +287,10 @@ cudaError_t launch_hop_op(const Fp8HopArgs& a, cudaStream_t s) {
   // a resident grid (kHopBlocksPerSm blocks per SM), each warp looping over
   // pairs of blocks: measured faster than one warp per pair (1.42 against
   // 1.46 ms for 16 x 134,217,728 bf16)
-  const uint64_t resident = 152ull * kHopBlocksPerSm;
+  int sms = 0;
+  const cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  const uint64_t resident = (uint64_t)sms * kHopBlocksPerSm;
   const unsigned grid = grid_for(tasks * 32) < resident ? grid_for(tasks * 32) : (unsigned)resident;
   // 4-element vectors when every buffer allows them (block starts are
   // multiples of 4 elements: chunk lengths are multiples of 16 bytes of the

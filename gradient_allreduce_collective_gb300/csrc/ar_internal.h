@@ -149,6 +149,12 @@ struct StepArgs {
   int vec;     // all pointers 16-byte aligned: items are 16-byte vectors
 };
 
+// Number of SMs of the calling thread's current device
+// (cudaDevAttrMultiProcessorCount), read once per device and cached; sizes
+// the resident grids, so that they follow the part (152 SMs on a GB300, fewer
+// on a partition of one).
+cudaError_t sm_count(int* out);
+
 // Launchers: enqueue on `stream`, return the launch status.
 cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cudaStream_t stream);
 cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream);

@@ -45,7 +45,6 @@ namespace {
 constexpr int kHistBlocksPerSm = 8;
 constexpr int kSplitBlocksPerSm = 3;  // the register budget of k_topk_split
 constexpr int kPass1BlocksPerSm = 5;  // k_topk_pass1 keeps 8 float4 loads in flight per thread
-constexpr int kSms = 152;
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
 
@@ -839,23 +838,26 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
 
 template <bool VEC>
 cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
+  int sms = 0;
+  cudaError_t err = sm_count(&sms);
+  if (err != cudaSuccess) return err;
   const dim3 one(1, a.nranks);
-  cudaError_t err = pdl_launch(k_topk_init, one, 0, s, a);
+  err = pdl_launch(k_topk_init, one, 0, s, a);
   if (err != cudaSuccess) return err;
   // histogram passes over the data: a resident grid looping over it, so that
   // each block flushes its shared histogram once
   const uint64_t items = VEC ? (a.count + 3) / 4 : a.count;
-  unsigned per_rank = (unsigned)(kSms * kHistBlocksPerSm / a.nranks);
+  unsigned per_rank = (unsigned)(sms * kHistBlocksPerSm / a.nranks);
   if (per_rank < 1) per_rank = 1;
   const unsigned hx = grid_for(items) < per_rank ? grid_for(items) : per_rank;
   const dim3 hgrid(hx, a.nranks);
-  unsigned p1 = (unsigned)(kSms * kPass1BlocksPerSm / a.nranks);
+  unsigned p1 = (unsigned)(sms * kPass1BlocksPerSm / a.nranks);
   if (p1 < 1) p1 = 1;
   const unsigned p1x = grid_for(items) < p1 ? grid_for(items) : p1;
   err = pdl_launch(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);
   if (err != cudaSuccess) return err;
   if (a.k == 0) return cudaSuccess;  // nothing kept: e = a
-  unsigned sx = (unsigned)(kSms * kSplitBlocksPerSm / a.nranks);
+  unsigned sx = (unsigned)(sms * kSplitBlocksPerSm / a.nranks);
   if (sx < 1) sx = 1;
   if (sx > a.nb) sx = (unsigned)a.nb;
   if ((err = pdl_launch(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) return err;

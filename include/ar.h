@@ -293,9 +293,14 @@ ar_status_t ar_allreduce_fp8_hops(const void *const *sendbufs, void *const *recv
  *   Limit: ar_fp8_workspace_bytes(nranks, count) must not exceed
  *   AR_FP8_STATIC_WS_BYTES (for example 8 ranks x 2,000,000 elements fit);
  *   larger calls return AR_ERR_INVALID_ARGUMENT and ar_last_error() says why.
- *   Set-up: the first call made while a device is current looks up that
- *   device's address of the array (cudaGetSymbolAddress) and caches it; make
- *   that first call before any stream capture.
+ *   Set-up: the first call made in a CUDA context (normally the device's
+ *   primary context, so once per device) looks up the array's address in
+ *   that context (cudaGetSymbolAddress) and caches it with the context's ID;
+ *   make that first call before any stream capture. A later call in another
+ *   context, for example after cudaDeviceReset, looks the address up again.
+ *   Argument errors are reported as by ar_allreduce_fp8 and take precedence
+ *   over the size limit; a count whose workspace size overflows is "count
+ *   too large".
  *   Sharing: all calls on a device use the same array and leave their data in
  *   it; each call writes every byte it later reads, so nothing needs
  *   clearing, but calls that overlap on the GPU (different streams, or host

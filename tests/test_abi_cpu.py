@@ -127,6 +127,32 @@ def test_fp8_argument_errors(L):
     assert gar.ar_fp8_workspace_bytes(0, 10) == 0
 
 
+def test_fp8_noalloc_reports_argument_errors_before_its_size_limit(L):
+    # every case returns before any CUDA call: fake device addresses suffice
+    n, big = 8, 2_100_000  # big: needs more than the library's 16 MiB array
+    s = [0x1000000 * (r + 1) for r in range(n)]
+    d = [0x20000000 + 0x1000000 * r for r in range(n)]
+    f = L.ar_allreduce_fp8_noalloc
+    assert gar.ar_fp8_workspace_bytes(n, big) > 16 * 1024 * 1024
+    assert f(_arr(s), _arr(d), n, big, 7, 2, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert "unknown dtype" in gar.ar_last_error()
+    assert f(_arr(s), _arr(d), n, big, 2, 2, 9, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert "unknown op" in gar.ar_last_error()
+    assert f(_arr(s), _arr(d), n, big, 2, 2, 2, 1, None) == gar.AR_ERR_UNSUPPORTED  # MIN
+    assert f(_arr(s), _arr(d), n, big, 2, 2, 0, 9, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert "unknown algo" in gar.ar_last_error()
+    assert f(_arr(s[:3]), _arr(d[:3]), 3, big, 2, 2, 0, 2, None) == gar.AR_ERR_UNSUPPORTED  # tree, 3 ranks
+    assert f(None, _arr(d), n, big, 2, 2, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    # a count whose workspace size overflows is "count too large", not "needs 0 bytes"
+    assert f(_arr(s), _arr(d), n, 1 << 62, 2, 2, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert "count too large" in gar.ar_last_error()
+    # valid arguments beyond the array: the size limit, with the sizes in the message
+    assert f(_arr(s), _arr(d), n, big, 2, 2, 0, 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert "static FP8 workspace holds 16777216 bytes" in gar.ar_last_error()
+    assert str(gar.ar_fp8_workspace_bytes(n, big)) in gar.ar_last_error()
+    assert f(_arr(s), _arr(d), n, 0, 2, 2, 0, 1, None) == gar.AR_SUCCESS  # count 0: no-op
+
+
 def test_bucket_plan_matches_hand_derivation(L):
     import torch
     g = G.load("gpt2_buckets.txt")
