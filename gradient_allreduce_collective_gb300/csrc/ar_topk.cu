@@ -374,7 +374,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   const uint32_t d1 = w.st->prefix >> 20;
   const uint32_t lo = d1 << 20;
   __syncthreads();
-  for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
+  // highest tiles first: pass 1 wrote them last, so some are still in L2
+  for (uint64_t step = blockIdx.x; step < A.nb; step += gridDim.x) {
+    const uint64_t tile = A.nb - 1 - step;
     uint32_t m[kTopkRuns];
     if (VEC && (tile + 1) * kTopkBlock <= count) {
       // a whole tile: no bounds checks (the same for every thread of the block)
@@ -454,11 +456,22 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     if ((key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
   };
   if (!w.st->overflow) {
-    for (uint64_t tile = blockIdx.x; tile < A.nb; tile += gridDim.x) {
+    // one warp per tile, eight slot loads in flight per lane
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (uint64_t tile = (uint64_t)blockIdx.x * kWarps + wid; tile < A.nb; tile += (uint64_t)gridDim.x * kWarps) {
       const float* sv = slot_val(w, tile, A.slots);
       const uint32_t n = w.n_s[tile];
-#pragma unroll 4
-      for (uint32_t c = threadIdx.x; c < n; c += blockDim.x) add(sv[c]);
+      for (uint32_t c0 = 0; c0 < n; c0 += 32 * 8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t c = c0 + 32 * u + lane;
+          x[u] = c < n ? sv[c] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c0 + 32 * u + lane < n) add(x[u]);
+      }
     }
   } else {
     const float* __restrict__ a = A.e[r];
@@ -557,11 +570,19 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__
       const float* sv = slot_val(w, tile, A.slots);
       const uint32_t n = w.n_s[tile];
       uint32_t gt = 0, eq = 0;
-#pragma unroll 4
-      for (uint32_t c = lane; c < n; c += 32) {
-        const uint32_t key = mag_key(sv[c]);
-        gt += key > T;
-        eq += key == T;
+      for (uint32_t c0 = 0; c0 < n; c0 += 32 * 8) {  // eight slot loads in flight per lane
+        uint32_t key[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t c = c0 + 32 * u + lane;
+          key[u] = c < n ? mag_key(sv[c]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool in = c0 + 32 * u + lane < n;
+          gt += in && key[u] > T;
+          eq += in && key[u] == T;
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
