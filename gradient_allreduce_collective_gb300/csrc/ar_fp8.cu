@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constan
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       x[k] = to_f32<DT>(get_lane<B>(raw[u], k));
-      amax = fmaxf(amax, fabsf(x[k]));
+      amax = fmax_nan(amax, fabsf(x[k]));
     }
     amax = group_amax<G>(amax);
     const float s = scale_of(amax);
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_scalar(const __grid_cons
         else bits = *reinterpret_cast<const uint16_t*>(src + e * 2);
       }
       x[k] = to_f32<DT>(bits);
-      amax = fmaxf(amax, fabsf(x[k]));
+      amax = fmax_nan(amax, fabsf(x[k]));
     }
     amax = group_amax<32>(amax);
     const float s = scale_of(amax);

@@ -60,7 +60,7 @@ template <int IDT> struct Fp8FusedLd {
 #pragma unroll
     for (int k = 0; k < V; ++k) {
       x[k] = to_f32<IDT>(get_lane<B>(raw, k));
-      amax = fmaxf(amax, fabsf(x[k]));
+      amax = fmax_nan(amax, fabsf(x[k]));
     }
     amax = group_amax<G>(amax);
     const float s = scale_of(amax);
@@ -137,8 +137,8 @@ __device__ __forceinline__ bool qdq_two(const float (&xa)[4], const float (&xb)[
   float ma = 0.0f, mb = 0.0f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    ma = fmaxf(ma, fabsf(xa[k]));
-    mb = fmaxf(mb, fabsf(xb[k]));
+    ma = fmax_nan(ma, fabsf(xa[k]));
+    mb = fmax_nan(mb, fabsf(xb[k]));
   }
   ma = group_amax<32>(ma);
   mb = group_amax<32>(mb);
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_consta
           else bits = *reinterpret_cast<const uint16_t*>(src + e * 2);
         }
         x[k] = to_f32<IDT>(bits);
-        amax = fmaxf(amax, fabsf(x[k]));
+        amax = fmax_nan(amax, fabsf(x[k]));
       }
       amax = group_amax<32>(amax);
       const float s = scale_of(amax);

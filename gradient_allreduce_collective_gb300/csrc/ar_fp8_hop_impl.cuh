@@ -34,7 +34,7 @@ namespace gar {
 __device__ __forceinline__ void qdq_block(float (&p)[4]) {
   float amax = 0.0f;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(p[k]));
+  for (int k = 0; k < 4; ++k) amax = fmax_nan(amax, fabsf(p[k]));
   amax = group_amax<32>(amax);
   const float s = scale_of(amax);
   const float x[4] = {p[0], p[1], p[2], p[3]};
@@ -51,8 +51,8 @@ __device__ __forceinline__ bool qdq_block_pair(float (&pa)[4], float (&pb)[4]) {
   float ma = 0.0f, mb = 0.0f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    ma = fmaxf(ma, fabsf(pa[k]));
-    mb = fmaxf(mb, fabsf(pb[k]));
+    ma = fmax_nan(ma, fabsf(pa[k]));
+    mb = fmax_nan(mb, fabsf(pb[k]));
   }
   ma = group_amax<32>(ma);
   mb = group_amax<32>(mb);

@@ -221,8 +221,10 @@ ar_status_t ar_bucket_allreduce(const void *const *tensors, void *const *out_ten
  * into blocks of AR_FP8_BLOCK = 128 consecutive elements (the last block may
  * be shorter); per block amax = max|x| in binary32, s = amax / 448, and
  * q = E4M3(x / s) rounded to nearest even with saturation to +-448
- * (amax == 0 gives s = 0 and q = 0). Non-finite inputs give unspecified
- * values in their block.
+ * (amax == 0 gives s = 0 and q = 0). The maximum propagates a NaN, so a
+ * block holding a NaN has s = NaN and dequantises to NaN throughout, on every
+ * FP8 entry point; a block holding an infinity has s = inf and dequantises
+ * to NaN as well (inf/inf and 0 * inf).
  *
  * Workspace layout (bytes, all regions 256-byte aligned):
  *   [0, N*QS)            q of rank r at r*QS,  QS = round_up(count, 256)

@@ -551,8 +551,10 @@ int or_reference_f64(const void *const *send, int N, size_t count, int dt, int o
 /* carries q and s. Dequantisation is one binary32 multiply float(q) * s;    */
 /* the dequantised values are reduced in the ring order in binary32 (sum or  */
 /* avg), rounded once to the output type, and all-gathered. Chunks use       */
-/* V = 16 bytes / output element size. Non-finite inputs are outside the     */
-/* method's domain.                                                          */
+/* V = 16 bytes / output element size. The amax propagates a NaN (the      */
+/* NaN-propagating maximum), so a block holding a NaN gets s = NaN and       */
+/* dequantises to NaN throughout; a block holding an infinity gets s = inf  */
+/* and dequantises to NaN as well (inf/inf, 0 * inf).                        */
 /* ------------------------------------------------------------------------- */
 
 #define OR_FP8_BLOCK 128
@@ -565,7 +567,7 @@ void or_fp8_quantize(const void *x, int in_dt, size_t count, uint8_t *q, float *
         float amax = 0.0f;
         for (size_t i = lo; i < hi; ++i) {
             float a = fabsf(or_load(in_dt, x, i).f);
-            if (a > amax) amax = a;
+            if (a > amax || a != a) amax = a;  /* a NaN stays: nothing compares above it */
         }
         float s = amax / 448.0f;
         scales[b] = s;
@@ -673,11 +675,12 @@ int or_fp8_ring_blocks(const void *blocks, const int64_t *first, const int32_t *
 /* change the numerical error). At reduce-scatter step s the sender          */
 /* quantises its partial of the chunk it sends in blocks of 128 elements     */
 /* counted from the chunk's start (s = amax/448, E4M3 nearest-even with      */
-/* saturation, amax = 0 -> 0) and the receiver adds the dequantised values   */
-/* float(q)*s to its own value in binary32 (received first). The owner       */
-/* finishes the chunk (AVG divides by N), quantises it the same way once     */
-/* more for the all-gather, and every rank, the owner included, keeps the    */
-/* dequantised chunk rounded to the output type, so replicas are identical.  */
+/* saturation, amax = 0 -> 0, a NaN amax as in fp8) and the receiver adds   */
+/* the dequantised values float(q)*s to its own value in binary32 (received  */
+/* first). The owner finishes the chunk (AVG divides by N), quantises it the */
+/* same way once more for the all-gather, and every rank, the owner          */
+/* included, keeps the dequantised chunk rounded to the output type, so      */
+/* replicas are identical.                                                   */
 /* Parity unpinned as far as the pages go (they fix no block rule); pinned   */
 /* by a hand-computed example, N = 1 against the quantise-once path, a       */
 /* second formulation and error bounds.                                      */
@@ -691,7 +694,7 @@ static void or_qdq_run(float *v, size_t n)
         float amax = 0.0f;
         for (size_t i = lo; i < hi; ++i) {
             float a = fabsf(v[i]);
-            if (a > amax) amax = a;
+            if (a > amax || a != a) amax = a;  /* a NaN stays: nothing compares above it */
         }
         float s = amax / 448.0f;
         for (size_t i = lo; i < hi; ++i)

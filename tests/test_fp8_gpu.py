@@ -191,6 +191,50 @@ def test_fp8_tree_example():
                     assert y.float().cpu().tolist() == G.nums(g[f"expect_{key}_{op}"]), (op, algo, path)
 
 
+def _nan_blocks(n, nblk, seed, dtype):
+    """Ranks of nblk blocks: block 0 of every rank all zeros but one NaN,
+    block 1 normal values with one NaN, the rest normal values."""
+    x = synthgen.ranks_normal(n, nblk * 128, 1e-3, base_seed=seed)
+    for r, a in enumerate(x):
+        a[:128] = 0.0
+        a[5 + r] = np.nan
+        a[128 + 17 * r] = np.nan
+    return [a if dtype == "f32" else synthgen.to_dtype(a, dtype) for a in x]
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+def test_fp8_nan_blocks_agree_on_every_path(in_dtype):
+    # the block amax propagates a NaN: a block holding one (among zeros or among
+    # normal values) has a NaN scale and dequantises to NaN throughout, on the
+    # materialised, fused and per-hop paths alike, as in the oracle; the other
+    # blocks are bit-exact
+    n, nblk = 4, 8  # chunks of 2 blocks: the per-hop path's blocks are the same
+    send_np = _nan_blocks(n, nblk, 21, in_dtype)
+    send = [to_dev(a, in_dtype) for a in send_np]
+    count = nblk * 128
+    want_once = oracle.fp8_ring_allreduce(send_np, in_dtype, "bf16", "sum")[0]
+    want_hops = oracle.fp8_hop_ring_allreduce(send_np, in_dtype, "bf16", "sum")[0]
+    for w in (want_once, want_hops):
+        f = oracle.bf16_to_f32(w)
+        assert np.isnan(f[:256]).all() and not np.isnan(f[256:]).any()
+    runs = {
+        "materialised": lambda out: gar.ar_allreduce_fp8(send, out, _ws(n, count), "sum", "fused"),
+        "fused": lambda out: gar.ar_allreduce_fp8_fused(send, out, "sum", "fused"),
+        "hops": lambda out: gar.ar_allreduce_fp8_hops(send, out, "sum"),
+    }
+    for name, run in runs.items():
+        out = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        run(out)
+        want = want_hops if name == "hops" else want_once
+        wf = oracle.bf16_to_f32(want)
+        for o in out:
+            got = from_dev(o)
+            gf = oracle.bf16_to_f32(got)
+            nan = np.isnan(wf)
+            assert np.array_equal(np.isnan(gf), nan), name
+            assert np.array_equal(got[~nan], want[~nan]), name
+
+
 @pytest.mark.parametrize("in_dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f16", "f32"])
 def test_fp8_allreduce_matches_oracle(in_dtype, out_dtype):

@@ -324,6 +324,28 @@ def test_fp8_blocks_match_full():
         assert np.array_equal(out[j, : blen[j]], full[first[j]: first[j] + blen[j]])
 
 
+def test_fp8_nan_makes_its_block_nan():
+    # the block amax is the NaN-propagating maximum: a NaN anywhere in a block
+    # (here the last element, after every larger magnitude, and a block of
+    # zeros) makes its scale NaN and the whole block NaN; an infinity makes
+    # the scale inf and the block NaN (inf/inf, 0*inf); other blocks unchanged
+    # 2 ranks x 768 values: chunks of 384 = 3 blocks, so the per-hop path's
+    # blocks (counted from each chunk's start) are the same 128-value blocks
+    x = np.zeros(6 * 128, dtype=np.float32)
+    x[128:] = np.linspace(-3, 3, 5 * 128, dtype=np.float32)
+    x[127] = np.nan           # block 0: zeros and a NaN
+    x[255] = np.nan           # block 1: values, the NaN last
+    x[300] = np.inf           # block 2: an infinity
+    q, s = oracle.fp8_quantize(x, "f32")
+    assert np.isnan(s[0]) and np.isnan(s[1]) and np.isinf(s[2]) and np.isfinite(s[3:]).all()
+    other = np.zeros_like(x)
+    for fn in (oracle.fp8_ring_allreduce, oracle.fp8_hop_ring_allreduce):
+        y = fn([x, other], "f32", "f32", "sum")[0]
+        assert np.isnan(y[:384]).all() and not np.isnan(y[384:]).any(), fn.__name__
+    y = oracle.fp8_ring_allreduce([x, other], "f32", "f32", "sum")[0]
+    assert np.array_equal(y[384:], oracle.fp8_ring_allreduce([x[384:], other[384:]], "f32", "f32", "sum")[0])
+
+
 def test_fp8_tree_example():
     # hand-computed: the recursive-halving pairing (x0 + x2) + (x1 + x3) after E4M3 quantisation,
     # distinct from the ring order and from the adjacent pairing
