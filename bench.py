@@ -948,6 +948,24 @@ def run_strong(args):
 # ----------------------------------------------------------------- GPU arm: size sweep
 
 
+def stepwise16_traffic(algo: str, n: int) -> float:
+    """Bytes per call of the 16-bit stepwise orders, in units of M (bytes per
+    rank, 2 per element): reduce-scatter steps read 2-byte inputs or 4-byte
+    binary32 partials and write partials (the last step 2-byte results); the
+    all-gather steps copy 2-byte values."""
+    if algo == "step_ring":  # N-1 steps over every chunk: 8, 10, ..., 10, 8 bytes per element
+        rs = 8 * 2 + 10 * (n - 3) if n >= 3 else 6
+    else:  # level i combines N * count / 2^(i+1) elements: 8 (2+2+4), 12 (4+4+4), ..., 10 (4+4+2) bytes each
+        levels = int(math.log2(n))
+        rs = 0.0
+        for i in range(levels):
+            a = 2 if i == 0 else 4
+            w = 2 if i == levels - 1 else 4
+            rs += n / 2 ** (i + 1) * (2 * a + w)
+    ag = 4 * (n - 1)  # N-1 copies of count elements of 2 bytes, read and written
+    return (rs + ag) / 2
+
+
 def run_sweep(args):
     import torch
 
@@ -959,16 +977,25 @@ def run_sweep(args):
     gar.lib()
     n = 8
     max_bytes = args.sweep_max_bytes
-    nmax = max_bytes // 4
     dtype, op = args.sweep_dtype, args.sweep_op
+    es = 2 if dtype == "bf16" else 4
+    nmax = max_bytes // es
     if dtype == "i32" and op not in ("min", "max"):
         raise SystemExit("the int32 leg of the sweep takes --sweep-op min or max")
     send = []
     for r in range(n):  # one rank at a time on the host: 1 GiB each at the largest size
-        host = (synthgen.uniform_i32(nmax, r, -(2**20), 2**20) if dtype == "i32"
-                else synthgen.uniform_f32(nmax, r, -1.0, 1.0))
-        send.append(torch.from_numpy(host).cuda())
-        del host
+        if dtype == "i32":
+            t = torch.from_numpy(synthgen.uniform_i32(nmax, r, -(2**20), 2**20))
+        elif dtype == "bf16":
+            t = torch.from_numpy(synthgen.to_dtype(synthgen.uniform_f32(nmax, r, -1.0, 1.0), "bf16")).view(
+                torch.int16).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(synthgen.uniform_f32(nmax, r, -1.0, 1.0))
+        send.append(t.cuda())
+        del t
+    # binary32 partials of the 16-bit stepwise orders
+    ws = (torch.empty(gar.ar_stepwise_workspace_bytes(n, nmax, dtype), dtype=torch.uint8, device="cuda")
+          if es == 2 else None)
     recv = [torch.empty_like(s) for s in send]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
@@ -977,7 +1004,7 @@ def run_sweep(args):
     fits: dict[str, list] = {}
     size = 4096
     while size <= max_bytes:
-        cnt = size // 4
+        cnt = size // es
         s_v = [t[:cnt] for t in send]
         r_v = [t[:cnt] for t in recv]
         res = {}
@@ -1010,7 +1037,10 @@ def run_sweep(args):
             with torch.cuda.stream(side):
                 g.capture_begin()
                 for _ in range(reps):
-                    gar.ar_allreduce(s_v, r_v, op, algo, side)
+                    if algo.startswith("step") and es == 2:
+                        gar.ar_allreduce_stepwise(s_v, r_v, ws, op, algo, side)
+                    else:
+                        gar.ar_allreduce(s_v, r_v, op, algo, side)
                 g.capture_end()
             stream.wait_stream(side)
             g.replay()
@@ -1027,6 +1057,9 @@ def run_sweep(args):
     import numpy as np
     launches = {"fused": 1, "tree": 1, "ring": 2, "step_ring": 2 * (n - 1), "step_tree": 2 * int(math.log2(n))}
     traffic = {"fused": 2 * n, "tree": 2 * n, "ring": 2 * n + 1, "step_ring": 5 * (n - 1), "step_tree": 5 * (n - 1)}
+    if es == 2:  # binary32 partials: bytes per call in units of M = 2 * count
+        traffic["step_ring"] = stepwise16_traffic("step_ring", n)
+        traffic["step_tree"] = stepwise16_traffic("step_tree", n)
     model = {}
     for algo, pts in fits.items():
         a = np.array([[launches[algo], traffic[algo] * m / 1e3] for m, _ in pts])  # us, (bytes/1e3) -> us at GB/s
@@ -1053,8 +1086,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=("bucket", "sweep", "fp8", "topk", "strong"), default="bucket")
     ap.add_argument("--fp8-count", type=int, default=134_217_728, help="elements per rank for --workload fp8")
     ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
-    ap.add_argument("--sweep-dtype", choices=("f32", "i32"), default="f32",
-                    help="f32 uniform(-1,1) or int32 uniform[-2^20, 2^20] per rank")
+    ap.add_argument("--sweep-dtype", choices=("f32", "i32", "bf16"), default="f32",
+                    help="f32 or bf16 uniform(-1,1), or int32 uniform[-2^20, 2^20] per rank")
     ap.add_argument("--sweep-op", choices=("sum", "min", "max"), default="sum")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -20,7 +20,7 @@ __all__ = [
     "ArError", "build", "lib", "lib_path", "ar_allreduce", "ar_allreduce_slice", "ar_reduce_scatter", "ar_all_gather",
     "ar_bucket_plan", "ar_bucket_flatten", "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_fp8_workspace_bytes",
     "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops", "ar_allreduce_fp8_noalloc",
-    "ar_topk_workspace_bytes", "ar_topk_compress", "ar_sparse_workspace_bytes", "ar_sparse_allreduce",
+    "ar_stepwise_workspace_bytes", "ar_allreduce_stepwise", "ar_topk_workspace_bytes", "ar_topk_compress", "ar_sparse_workspace_bytes", "ar_sparse_allreduce",
     "ar_status_string", "ar_last_error", "ar_version",
     "DTYPES", "OPS", "ALGOS", "Comm", "CallRecord",
 ]
@@ -78,13 +78,16 @@ def lib() -> ctypes.CDLL:
     L.ar_allreduce_fp8_noalloc.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_fused.argtypes = [pp, pp, ci, sz, ci, ci, ci, ci, vp]
     L.ar_allreduce_fp8_hops.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp]
+    L.ar_stepwise_workspace_bytes.argtypes = [ci, sz, ci]
+    L.ar_stepwise_workspace_bytes.restype = sz
+    L.ar_allreduce_stepwise.argtypes = [pp, pp, ci, sz, ci, ci, ci, vp, sz, vp]
     L.ar_topk_workspace_bytes.argtypes = [ci, sz, sz]
     L.ar_topk_workspace_bytes.restype = sz
     L.ar_topk_compress.argtypes = [pp, pp, ci, sz, sz, pp, pp, vp, sz, vp]
     L.ar_sparse_workspace_bytes.argtypes = [ci, sz]
     L.ar_sparse_workspace_bytes.restype = sz
     L.ar_sparse_allreduce.argtypes = [pp, pp, vp, ci, sz, ci, ci, pp, vp, sz, vp]
-    for name in ("ar_allreduce", "ar_allreduce_slice", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
+    for name in ("ar_allreduce", "ar_allreduce_stepwise", "ar_allreduce_slice", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucket_flatten",
                  "ar_bucket_unflatten", "ar_bucket_allreduce", "ar_quantize_fp8_blocks", "ar_allreduce_fp8", "ar_allreduce_fp8_noalloc", "ar_allreduce_fp8_fused", "ar_allreduce_fp8_hops",
                  "ar_topk_compress", "ar_sparse_allreduce"):
         getattr(L, name).restype = ci
@@ -156,6 +159,25 @@ def ar_allreduce(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tens
     _same(recvbufs, "recvbufs")
     _check(lib().ar_allreduce(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], OPS[op],
                               ALGOS[algo], _stream(stream)))
+
+
+def ar_stepwise_workspace_bytes(nranks: int, count: int, dtype) -> int:
+    dt = DTYPES[dtype] if isinstance(dtype, torch.dtype) else DTYPE_NAMES[dtype]
+    return int(lib().ar_stepwise_workspace_bytes(nranks, count, dt))
+
+
+def ar_allreduce_stepwise(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], workspace,
+                          op: str = "sum", algo: str = "step_ring", stream=None) -> None:
+    """The stepwise ring / recursive halving-doubling for every element type;
+    `workspace` (a device tensor or None) holds the binary32 partials of
+    16-bit inputs (ar_stepwise_workspace_bytes)."""
+    dt, n = _same(sendbufs, "sendbufs")
+    if len(recvbufs) != len(sendbufs):
+        raise ValueError("one output per rank")
+    _same(recvbufs, "recvbufs")
+    ws, wsb = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    _check(lib().ar_allreduce_stepwise(_ptrs(sendbufs), _ptrs(recvbufs), len(sendbufs), n, DTYPES[dt], OPS[op],
+                                       ALGOS[algo], ws, wsb, _stream(stream)))
 
 
 def ar_allreduce_slice(sendbufs: Sequence[torch.Tensor], recvbufs: Sequence[torch.Tensor], count: int, first: int,

@@ -356,6 +356,109 @@ ar_status_t step_tree(const void* const* send, void* const* recv, int n, size_t 
   return AR_SUCCESS;
 }
 
+// --- 16-bit element types: partial sums in binary32, in a workspace of one
+// count-long partial array per rank (P[r]); the last reduce-scatter step
+// writes the finished 16-bit values into the outputs, whose all-gather steps
+// are the 16-bit copies above.
+
+const char* at2(const void* p, uint64_t elems) { return static_cast<const char*>(p) + elems * 2; }
+char* at2(void* p, uint64_t elems) { return static_cast<char*>(p) + elems * 2; }
+
+ar_status_t step_combine16(int dtype, int op, int nranks, bool a32, bool b32, bool finish, bool vec,
+                           const std::vector<StepTask>& tasks, cudaStream_t s) {
+  StepArgs a{};
+  a.nranks = nranks;
+  a.finish = finish ? 1 : 0;
+  a.vec = vec ? 1 : 0;
+  uint64_t tiles = 0;
+  for (const StepTask& t : tasks) {
+    if (t.len == 0) continue;
+    const int k = a.ntasks++;
+    a.a[k] = t.a;
+    a.b[k] = t.b;
+    a.dst[k] = t.dst;
+    a.len[k] = t.len;
+    a.tile_start[k] = (uint32_t)tiles;
+    tiles += ((t.len + 3) / 4 + kThreads - 1) / kThreads;
+  }
+  a.tile_start[a.ntasks] = (uint32_t)tiles;
+  const cudaError_t e = launch_step_combine16(dtype, op, a32, b32, a, s);
+  return e == cudaSuccess ? AR_SUCCESS : cuda_fail(e, "reduce-scatter step launch");
+}
+
+// Ring, literally, as step_ring: step st, rank r's partial of chunk
+// (r-st-1) mod N (its input at step 0, else P[r]) plus rank r+1's input goes
+// to P[r+1] (or, on the last step, finished into the output of r+1). Within
+// a step rank d writes one chunk of P[d] while rank d+1 reads another.
+ar_status_t step_ring16(const void* const* send, void* const* recv, char* const* P, int n, size_t count, int dtype,
+                        int op, bool vec, cudaStream_t s) {
+  const size_t L = chunk_len(count, n, 8);
+  auto lo_of = [&](int c) { return std::min((size_t)c * L, count); };
+  auto hi_of = [&](int c) { return std::min((size_t)(c + 1) * L, count); };
+  for (int st = 0; st < n - 1; ++st) {
+    const bool last = st == n - 2;
+    std::vector<StepTask> tasks;
+    for (int r = 0; r < n; ++r) {
+      const int c = ((r - st - 1) % n + n) % n, d = (r + 1) % n;
+      const size_t lo = lo_of(c), hi = hi_of(c);
+      tasks.push_back({st == 0 ? at2(send[r], lo) : at(P[r], lo), at2(send[d], lo),
+                       last ? static_cast<void*>(at2(recv[d], lo)) : static_cast<void*>(at(P[d], lo)), hi - lo});
+    }
+    if (ar_status_t e = step_combine16(dtype, op, n, st > 0, false, last, vec, tasks, s); e != AR_SUCCESS) return e;
+  }
+  for (int st = 0; st < n - 1; ++st) {
+    std::vector<CopyItem> items;
+    for (int r = 0; r < n; ++r) {
+      const int c = ((r - st) % n + n) % n, d = (r + 1) % n;
+      const size_t lo = lo_of(c), hi = hi_of(c);
+      items.push_back({at2(recv[r], lo), at2(recv[d], lo), (hi - lo) * 2});
+    }
+    if (ar_status_t e = step_copies(items, s); e != AR_SUCCESS) return e;
+  }
+  return AR_SUCCESS;
+}
+
+// Recursive halving / doubling, as step_tree: at each level partners keep
+// the two halves of their common segment; the partials of a level live in
+// P, each rank writing the half it keeps while its partner reads the other.
+ar_status_t step_tree16(const void* const* send, void* const* recv, char* const* P, int n, size_t count, int dtype,
+                        int op, bool vec, cudaStream_t s) {
+  int levels = 0;
+  while ((1 << levels) < n) ++levels;
+  std::vector<std::vector<std::pair<size_t, size_t>>> seg(levels + 1,
+                                                          std::vector<std::pair<size_t, size_t>>(n));
+  for (int r = 0; r < n; ++r) seg[0][r] = {0, count};
+  for (int i = 0; i < levels; ++i) {
+    const int d = n >> (i + 1);
+    const bool last = i == levels - 1;
+    std::vector<StepTask> tasks;
+    for (int r = 0; r < n; ++r) {
+      const size_t lo = seg[i][r].first, hi = seg[i][r].second;
+      const size_t half = ((hi - lo + 1) / 2 + 3) / 4 * 4;
+      const size_t mid = std::min(lo + half, hi);
+      seg[i + 1][r] = (r & d) ? std::make_pair(mid, hi) : std::make_pair(lo, mid);
+      const int p = r ^ d;
+      const size_t klo = seg[i + 1][r].first, khi = seg[i + 1][r].second;
+      tasks.push_back({i == 0 ? at2(send[r], klo) : at(P[r], klo), i == 0 ? at2(send[p], klo) : at(P[p], klo),
+                       last ? static_cast<void*>(at2(recv[r], klo)) : static_cast<void*>(at(P[r], klo)),
+                       khi - klo});
+    }
+    if (ar_status_t e = step_combine16(dtype, op, n, i > 0, i > 0, last, vec, tasks, s); e != AR_SUCCESS) return e;
+  }
+  for (int i = levels - 1; i >= 0; --i) {
+    const int d = n >> (i + 1);
+    std::vector<CopyItem> items;
+    for (int r = 0; r < n; ++r) {
+      const size_t lo = seg[i + 1][r].first, hi = seg[i + 1][r].second;
+      items.push_back({at2(recv[r], lo), at2(recv[r ^ d], lo), (hi - lo) * 2});
+    }
+    if (ar_status_t e = step_copies(items, s); e != AR_SUCCESS) return e;
+  }
+  return AR_SUCCESS;
+}
+
+size_t stepwise_rank_bytes(size_t count) { return (count * 4 + 255) / 256 * 256; }
+
 }  // namespace
 
 extern "C" {
@@ -390,7 +493,8 @@ ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int
   const size_t es = elem_size(dtype);
   const bool stepwise = algo == AR_ALGO_STEP_RING || algo == AR_ALGO_STEP_TREE;
   if (stepwise && es != 4)
-    return fail(AR_ERR_UNSUPPORTED, "stepwise orders keep partials in the element type: F32 or I32 only");
+    return fail(AR_ERR_UNSUPPORTED,
+                "stepwise orders of 16-bit types keep binary32 partials in a workspace: use ar_allreduce_stepwise");
   if (count == 0) return ok();
   if (count > SIZE_MAX / es / 2) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
   if ((st = check_ptrs(sendbufs, nranks, es, "sendbufs")) != AR_SUCCESS) return st;
@@ -433,6 +537,55 @@ ar_status_t ar_allreduce(const void* const* sendbufs, void* const* recvbufs, int
   const cudaError_t e = launch_reduce(dtype, op, algo == AR_ALGO_TREE ? MODE_FUSED_TREE : MODE_FUSED_RING, a, s);
   if (e != cudaSuccess) return cuda_fail(e, "allreduce launch");
   return ok();
+}
+
+size_t ar_stepwise_workspace_bytes(int nranks, size_t count, ar_dtype_t dtype) {
+  if (nranks < 1 || nranks > AR_MAX_RANKS || elem_size(dtype) != 2 || count > SIZE_MAX / 8 / AR_MAX_RANKS) return 0;
+  return (size_t)nranks * stepwise_rank_bytes(count);
+}
+
+ar_status_t ar_allreduce_stepwise(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                                  ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, void* workspace, size_t ws_bytes,
+                                  ar_stream_t stream) {
+  AR_TRACE("ar_allreduce_stepwise");
+  ar_status_t st = common_checks(sendbufs, recvbufs, nranks, dtype);
+  if (st != AR_SUCCESS) return st;
+  if (!valid_op(op)) return fail(AR_ERR_INVALID_ARGUMENT, "unknown op");
+  if (algo != AR_ALGO_STEP_RING && algo != AR_ALGO_STEP_TREE)
+    return fail(AR_ERR_INVALID_ARGUMENT, "ar_allreduce_stepwise takes STEP_RING or STEP_TREE");
+  if (algo == AR_ALGO_STEP_TREE && !pow2(nranks))
+    return fail(AR_ERR_UNSUPPORTED, "TREE needs nranks to be a power of two");
+  const size_t es = elem_size(dtype);
+  if (es == 4)  // partials in the element type, in the outputs: no workspace
+    return ar_allreduce(sendbufs, recvbufs, nranks, count, dtype, op, algo, stream);
+  if (count == 0) return ok();
+  if (count > SIZE_MAX / 8 / AR_MAX_RANKS) return fail(AR_ERR_INVALID_ARGUMENT, "count too large");
+  if (nranks == 1)  // nothing to combine: the one-pass kernel copies (and finishes) the input
+    return ar_allreduce(sendbufs, recvbufs, nranks, count, dtype, op, AR_ALGO_FUSED, stream);
+  const size_t need = ar_stepwise_workspace_bytes(nranks, count, dtype);
+  if (!workspace) return fail(AR_ERR_INVALID_ARGUMENT, "null workspace");
+  if (ws_bytes < need) return fail(AR_ERR_INVALID_ARGUMENT, "workspace too small");
+  if (!aligned(workspace, 16)) return fail(AR_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+  if ((st = check_ptrs(sendbufs, nranks, es, "sendbufs")) != AR_SUCCESS) return st;
+  if ((st = check_ptrs(recvbufs, nranks, es, "recvbufs")) != AR_SUCCESS) return st;
+  const size_t bytes = count * es;
+  std::vector<Span> spans;
+  std::vector<int> pair_in(nranks + 1, -1);
+  std::vector<uintptr_t> pair_off(nranks + 1, 0);
+  for (int r = 0; r < nranks; ++r) {
+    spans.push_back({addr(sendbufs[r]), addr(sendbufs[r]) + bytes, false, r});
+    spans.push_back({addr(recvbufs[r]), addr(recvbufs[r]) + bytes, true, r});
+    pair_in[r] = r;  // in place: recvbufs[r] == sendbufs[r]
+  }
+  spans.push_back({addr(workspace), addr(workspace) + need, true, nranks});
+  if (!overlap_ok(spans, pair_in, pair_off)) return fail(AR_ERR_ALIAS, "buffers overlap");
+  std::vector<char*> P(nranks);
+  for (int r = 0; r < nranks; ++r) P[r] = static_cast<char*>(workspace) + (size_t)r * stepwise_rank_bytes(count);
+  const bool vec = all_aligned16(sendbufs, nranks) && all_aligned16(recvbufs, nranks);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = algo == AR_ALGO_STEP_RING ? step_ring16(sendbufs, recvbufs, P.data(), nranks, count, dtype, op, vec, s)
+                                 : step_tree16(sendbufs, recvbufs, P.data(), nranks, count, dtype, op, vec, s);
+  return st == AR_SUCCESS ? ok() : st;
 }
 
 ar_status_t ar_allreduce_slice(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,

@@ -160,6 +160,10 @@ cudaError_t launch_reduce(int dtype, int op, int mode, const ReduceArgs& a, cuda
 cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_step_combine(int dtype, int op, const StepArgs& a, cudaStream_t stream);
+// bf16/fp16 with binary32 partials: a32/b32 — operand a/b is a partial word
+// (else a 16-bit input); a.finish — the result is the finished 16-bit value
+// (else a partial word). Items are 4 elements.
+cudaError_t launch_step_combine16(int dtype, int op, bool a32, bool b32, const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_bucket_reduce(int dtype, int op, int mode, const BucketArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cudaStream_t stream);
 cudaError_t launch_fp8_reduce(int out_dtype, int op, int mode, const Fp8ReduceArgs& a, cudaStream_t stream);

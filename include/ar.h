@@ -97,8 +97,10 @@ typedef enum { AR_SUM = 0, AR_AVG = 1, AR_MIN = 2, AR_MAX = 3 } ar_op_t;
  *                   segment) then recursive doubling all-gather ([AW] table,
  *                   Rabenseifner). Same bits as TREE; 5(N-1)*M bytes in
  *                   2*log2(N) launches.
- *   The stepwise orders keep partial sums in the output buffers, so they
- *   take 4-byte element types (F32, I32) only; AR_ERR_UNSUPPORTED otherwise.
+ *   Through ar_allreduce the stepwise orders keep partial sums in the output
+ *   buffers, so they take 4-byte element types (F32, I32) only
+ *   (AR_ERR_UNSUPPORTED otherwise); ar_allreduce_stepwise runs them for
+ *   BF16 and F16 with binary32 partials in a caller workspace.
  *   AR_ALGO_AUTO      — chosen by the library: the one-pass FUSED kernel, which
  *                   measured fastest at every message size on one device. */
 typedef enum {
@@ -124,6 +126,28 @@ typedef enum {
  * overlap each other (they are only read). */
 ar_status_t ar_allreduce(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
                          ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, ar_stream_t stream);
+
+/* Workspace bytes of ar_allreduce_stepwise for BF16/F16: one binary32
+ * partial array of `count` values per rank (each rounded up to 256 bytes);
+ * 0 for other types (they need none) or when nranks or count is out of
+ * range. */
+size_t ar_stepwise_workspace_bytes(int nranks, size_t count, ar_dtype_t dtype);
+
+/* The stepwise orders (AR_ALGO_STEP_RING, AR_ALGO_STEP_TREE; the literal
+ * ring and recursive halving-doubling of [GL]'s algorithm table, one launch
+ * per step) for every element type. BF16/F16 inputs are widened exactly, the
+ * reduce-scatter steps keep their partial sums in binary32 in `workspace`
+ * (device, at least ar_stepwise_workspace_bytes, 16-byte aligned, owned by
+ * the caller, contents meaningless before and after), and the last step
+ * rounds once to the output type, so the results are bit-identical to
+ * AR_ALGO_RING / AR_ALGO_TREE; the all-gather steps copy 16-bit values. F32
+ * and I32 need no workspace (it may be null) and run as ar_allreduce does.
+ * Other algo values give AR_ERR_INVALID_ARGUMENT; the workspace must not
+ * overlap any buffer (AR_ERR_ALIAS). In place and other rules: as
+ * ar_allreduce. */
+ar_status_t ar_allreduce_stepwise(const void *const *sendbufs, void *const *recvbufs, int nranks, size_t count,
+                                  ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, void *workspace, size_t ws_bytes,
+                                  ar_stream_t stream);
 
 /* A slice of an allreduce: elements [first, first + n) of the result of
  * ar_allreduce over `count` elements per rank, bit-identical to them (same

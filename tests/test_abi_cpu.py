@@ -127,6 +127,31 @@ def test_fp8_argument_errors(L):
     assert gar.ar_fp8_workspace_bytes(0, 10) == 0
 
 
+def test_stepwise_workspace_and_argument_errors(L):
+    n, count = 8, 1000
+    s = [0x1000000 * (r + 1) for r in range(n)]
+    d = [0x20000000 + 0x1000000 * r for r in range(n)]
+    per = (count * 4 + 255) // 256 * 256
+    assert gar.ar_stepwise_workspace_bytes(n, count, "bf16") == n * per
+    assert gar.ar_stepwise_workspace_bytes(n, count, "f16") == n * per
+    assert gar.ar_stepwise_workspace_bytes(n, count, "f32") == 0  # partials in the outputs
+    assert gar.ar_stepwise_workspace_bytes(0, count, "bf16") == 0
+    f = L.ar_allreduce_stepwise
+    ws = 0x40000000
+    need = n * per
+    assert f(_arr(s), _arr(d), n, count, 2, 0, 1, ws, need, None) == gar.AR_ERR_INVALID_ARGUMENT  # FUSED
+    assert "STEP_RING or STEP_TREE" in gar.ar_last_error()
+    assert f(_arr(s[:3]), _arr(d[:3]), 3, count, 2, 0, 4, ws, need, None) == gar.AR_ERR_UNSUPPORTED  # tree, 3 ranks
+    assert f(_arr(s), _arr(d), n, count, 2, 0, 3, None, 0, None) == gar.AR_ERR_INVALID_ARGUMENT  # no workspace
+    assert f(_arr(s), _arr(d), n, count, 2, 0, 3, ws, need - 1, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(_arr(s), _arr(d), n, count, 2, 0, 3, ws + 8, need, None) == gar.AR_ERR_INVALID_ARGUMENT
+    assert f(_arr(s), _arr(d), n, count, 2, 0, 3, d[2] + 64, need, None) == gar.AR_ERR_ALIAS
+    assert f(_arr(s), _arr(d), n, 0, 2, 0, 3, None, 0, None) == gar.AR_SUCCESS  # count 0: no-op
+    # through ar_allreduce the 16-bit stepwise orders point to this entry point
+    assert _ar(L, s, d, n, 16, dt=2, algo=3) == gar.AR_ERR_UNSUPPORTED
+    assert "ar_allreduce_stepwise" in gar.ar_last_error()
+
+
 def test_fp8_noalloc_reports_argument_errors_before_its_size_limit(L):
     # every case returns before any CUDA call: fake device addresses suffice
     n, big = 8, 2_100_000  # big: needs more than the library's 16 MiB array

@@ -40,7 +40,12 @@ def _gpu_allreduce(send_np, dtype, op, algo, offset=0, in_offset=0):
     else:
         send = [to_dev(a, dtype) for a in send_np]
     out = Guarded(n, count, dtype, offset)
-    gar.ar_allreduce(send, out.views, op, algo)
+    if algo.startswith("step") and ESIZE[dtype] == 2:  # binary32 partials in a workspace
+        wsb = gar.ar_stepwise_workspace_bytes(n, count, dtype)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+        gar.ar_allreduce_stepwise(send, out.views, ws, op, algo)
+    else:
+        gar.ar_allreduce(send, out.views, op, algo)
     out.check()
     return [from_dev(v) for v in out.views]
 
@@ -56,11 +61,11 @@ def _same_bits(a, b):
 
 
 def _algos(n, dtype="f32"):
-    """Orders to check: the one-pass ones, AUTO, and (4-byte types) the stepwise executors."""
+    """Orders to check: the one-pass ones, AUTO, and the stepwise executors (16-bit
+    types through ar_allreduce_stepwise with binary32 partials)."""
     pow2 = n & (n - 1) == 0
     algos = ["ring", "fused", "auto"] + (["tree"] if pow2 else [])
-    if dtype in ("f32", "i32"):
-        algos += ["step_ring"] + (["step_tree"] if pow2 else [])
+    algos += ["step_ring"] + (["step_tree"] if pow2 else [])
     return tuple(algos)
 
 
@@ -194,7 +199,11 @@ def test_in_place_forms():
         send_np = _rand(dtype, n, count, seed=3)
         for algo in _algos(n, dtype):
             bufs = [to_dev(a, dtype) for a in send_np]
-            gar.ar_allreduce(bufs, bufs, "sum", algo)
+            if algo.startswith("step") and ESIZE[dtype] == 2:
+                ws = torch.empty(gar.ar_stepwise_workspace_bytes(n, count, dtype), dtype=torch.uint8, device="cuda")
+                gar.ar_allreduce_stepwise(bufs, bufs, ws, "sum", algo)
+            else:
+                gar.ar_allreduce(bufs, bufs, "sum", algo)
             want = _expect(send_np, dtype, "sum", algo)
             for b in bufs:
                 assert _same_bits(from_dev(b), want)
