@@ -45,6 +45,7 @@ namespace {
 constexpr int kHistBlocksPerSm = 8;
 constexpr int kSplitBlocksPerSm = 3;  // the register budget of k_topk_split
 constexpr int kPass1BlocksPerSm = 5;  // k_topk_pass1 keeps 8 float4 loads in flight per thread
+constexpr int kSpecBlocksPerSm = 3;   // k_topk_pass1_spec keeps 16 float4 loads in flight per lane
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
 
@@ -157,9 +158,12 @@ __device__ __forceinline__ bool last_block(uint32_t* ticket) {
 
 // The last block of a radix pass: the highest digit whose count from the top
 // reaches `need` (a block-wide scan over BINS bins, highest first); fold it
-// into the prefix and clear the bins for the next pass.
+// into the prefix and clear the bins for the next pass. With target2 > 0 the
+// same scan also stores in *hint (pre-set by the caller) the lowest key of the
+// highest digit whose count from the top reaches target2, if there is one.
 template <int BINS>
-__device__ void find_digit(uint32_t* hist, int shift, TopkState* st) {
+__device__ void find_digit(uint32_t* hist, int shift, TopkState* st, uint32_t target2 = 0,
+                           uint32_t* hint = nullptr) {
   constexpr int R = BINS / kThreads;
   const int top = BINS - threadIdx.x * R;  // this thread: bins [top - R, top)
   const uint32_t need = st->need;
@@ -171,6 +175,19 @@ __device__ void find_digit(uint32_t* hist, int shift, TopkState* st) {
     local += h[j];
   }
   const uint32_t above0 = block_exclusive_scan(local, nullptr);
+  if (target2 > 0 && above0 < target2 && above0 + local >= target2) {  // at most one thread
+    uint32_t above = above0;
+    int pick = top - R;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (above + h[j] >= target2) {
+        pick = top - 1 - j;
+        break;
+      }
+      above += h[j];
+    }
+    *hint = (uint32_t)pick << shift;
+  }
   if (above0 < need && above0 + local >= need) {  // exactly one thread
     uint32_t above = above0;
     int pick = top - R;
@@ -202,6 +219,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ 
     w.st->gt = 0;
     for (int p = 0; p < 4; ++p) w.st->ticket[p] = 0;
     w.st->overflow = 0;
+    w.st->spec_ok = 0;  // the hint is left as the previous call set it
+    w.st->spec_overflow = 0;
   }
 }
 
@@ -268,6 +287,139 @@ __global__ void __launch_bounds__(kThreads, kPass1BlocksPerSm) k_topk_pass1(cons
     if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
   if (A.k == 0) return;  // nothing to select
   if (last_block(&w.st->ticket[0])) find_digit<2048>(w.hist, 20, w.st);
+}
+
+// Pass 1 with speculative candidate slots (every buffer 16-byte aligned and
+// enough tiles for a warp each): as k_topk_pass1, and each warp walks whole
+// tiles of kTopkBlock values in index order, compacting the values whose key
+// is at or above the hint into the tile's slots, in the layout the split
+// pass fills. A warp takes 512 values at a time, lane l the float4 at
+// offsets 128 q + 4 l (q = 0..3), so index order is q-major; the four
+// per-q candidate counts of a lane are scanned across the warp as one word
+// of 8-bit fields. The last block finds the first digit, decides whether the
+// slots hold every key that can be kept (the hint at or below the first
+// digit's bin, no tile overflowing) and leaves the next call's hint.
+constexpr int kSpecSeg = 512;  // values of a warp in one segment
+
+__global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(const __grid_constant__ TopkArgs A) {
+  pdl_enter();
+  __shared__ uint32_t sh[2048];
+  const int r = blockIdx.y;
+  const RankWs w = rank_ws(A, r);
+  const float* __restrict__ g = A.g[r];
+  float* __restrict__ e = A.e[r];
+  const uint64_t count = A.count;
+  const uint32_t tau = w.st->hint;
+  const uint32_t S = A.slots;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  // tiles interleaved over the blocks (tile = warp * gridDim.x + block), so
+  // that every block, and so every SM, gets an equal share
+  for (uint64_t tile = (uint64_t)wid * gridDim.x + blockIdx.x; tile < A.nb; tile += (uint64_t)gridDim.x * kWarps) {
+    uint32_t* __restrict__ si = slot_idx(w, tile, S);
+    float* __restrict__ sv = slot_val(w, tile, S);
+    uint32_t pos = 0;
+    const uint64_t t_end = (tile + 1) * kTopkBlock < count ? (tile + 1) * kTopkBlock : count;
+    // two 512-value segments per round: 8 float4 of g and of e in flight per lane
+    for (uint64_t e0 = tile * kTopkBlock; e0 < t_end; e0 += 2 * kSpecSeg) {
+      const bool full = e0 + 2 * kSpecSeg <= count;  // the same for the whole warp
+      float v[8][4];
+      if (full) {
+        float4 x[8], y[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          x[q] = __ldcs(reinterpret_cast<const float4*>(g + e0 + 128 * q) + lane);
+          y[q] = reinterpret_cast<const float4*>(e + e0 + 128 * q)[lane];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 s4 = add4(x[q], y[q]);
+          reinterpret_cast<float4*>(e + e0 + 128 * q)[lane] = s4;
+          v[q][0] = s4.x;
+          v[q][1] = s4.y;
+          v[q][2] = s4.z;
+          v[q][3] = s4.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t i = e0 + 128 * q + 4 * lane + j;
+            v[q][j] = 0.0f;
+            if (i < count) {
+              v[q][j] = __fadd_rn(g[i], e[i]);
+              e[i] = v[q][j];
+            }
+          }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // the two segments in index order
+        uint32_t m = 0;  // bit 4q + j: value (4h + q, j) is a candidate
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const bool in = full || e0 + 128 * (4 * h + q) + 4 * lane + j < count;
+            const uint32_t key = mag_key(v[4 * h + q][j]);
+            if (in) atomicAdd(&sh[key >> 20], 1u);
+            if (in && key >= tau) m |= 1u << (4 * q + j);
+          }
+        const uint32_t c = (uint32_t)__popc(m & 0xFu) | ((uint32_t)__popc(m & 0xF0u) << 8) |
+                           ((uint32_t)__popc(m & 0xF00u) << 16) | ((uint32_t)__popc(m & 0xF000u) << 24);
+        uint32_t inc = c;  // no field overflows: at most 128 each
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += t;
+        }
+        const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31), exc = inc - c;
+        uint32_t before = pos;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t p = before + ((exc >> (8 * q)) & 0xFFu);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if ((m >> (4 * q + j)) & 1u) {
+              if (p < S) {
+                si[p] = (uint32_t)(e0 + 128 * (4 * h + q) + 4 * lane + j);
+                sv[p] = v[4 * h + q][j];
+              }
+              ++p;
+            }
+          }
+          before += (tot >> (8 * q)) & 0xFFu;
+        }
+        pos = before;
+      }
+    }
+    if (lane == 0) {
+      w.n_s[tile] = pos;
+      if (pos > S) atomicOr(&w.st->spec_overflow, 1u);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
+    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
+  if (A.k == 0) return;
+  if (last_block(&w.st->ticket[0])) {
+    // the next call's hint: the lowest key of the bin where the count from
+    // the top reaches 4k (about four times the kept keys; 0, that is every
+    // key, when there are fewer), so that a moderate growth or shrinkage of
+    // the gradients between calls still finds the hint valid
+    __shared__ uint32_t s_hint;
+    if (threadIdx.x == 0) s_hint = 0;
+    __syncthreads();
+    const uint64_t t2 = 4ull * A.k;
+    find_digit<2048>(w.hist, 20, w.st, t2 < 0xFFFFFFFFull ? (uint32_t)t2 : 0xFFFFFFFFu, &s_hint);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t d1 = w.st->prefix >> 20;
+      w.st->spec_ok = (tau <= (d1 << 20) && __ldcg(&w.st->spec_overflow) == 0) ? 1u : 0u;
+      w.st->hint = s_hint;
+    }
+  }
 }
 
 // kTopkElems consecutive values starting at `base` (zero past the end)
@@ -374,6 +526,32 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   const uint32_t d1 = w.st->prefix >> 20;
   const uint32_t lo = d1 << 20;
   __syncthreads();
+  if (w.st->spec_ok) {
+    // pass 1 left every candidate in the slots: only the histogram of bits
+    // 19..10 of the keys in the first digit's bin, from the slots (a warp per
+    // tile, eight slot loads in flight per lane)
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (uint64_t tile = (uint64_t)blockIdx.x * kWarps + wid; tile < A.nb; tile += (uint64_t)gridDim.x * kWarps) {
+      const float* sv = slot_val(w, tile, S);
+      const uint32_t n = w.n_s[tile];
+      for (uint32_t c0 = 0; c0 < n; c0 += 32 * 8) {
+        uint32_t key[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t c = c0 + 32 * u + lane;
+          key[u] = c < n ? mag_key(sv[c]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c0 + 32 * u + lane < n && (key[u] >> 20) == d1) atomicAdd(&sh[(key[u] >> 10) & 1023u], 1u);
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+      if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
+    if (last_block(&w.st->ticket[1])) find_digit<1024>(w.hist, 10, w.st);
+    return;
+  }
   // highest tiles first: pass 1 wrote them last, so some are still in L2
   for (uint64_t step = blockIdx.x; step < A.nb; step += gridDim.x) {
     const uint64_t tile = A.nb - 1 - step;
@@ -875,7 +1053,15 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   unsigned p1 = (unsigned)(sms * kPass1BlocksPerSm / a.nranks);
   if (p1 < 1) p1 = 1;
   const unsigned p1x = grid_for(items) < p1 ? grid_for(items) : p1;
-  err = pdl_launch(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);
+  // the speculative pass 1 takes a warp per tile: used when the tiles of all
+  // ranks keep at least 16 warps per SM busy
+  if (VEC && a.k > 0 && a.nb * (uint64_t)a.nranks >= (uint64_t)sms * 16) {
+    unsigned sbx = (unsigned)(sms * kSpecBlocksPerSm / a.nranks);
+    if (sbx < 1) sbx = 1;
+    err = pdl_launch(k_topk_pass1_spec, dim3(sbx, a.nranks), 0, s, a);
+  } else {
+    err = pdl_launch(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);
+  }
   if (err != cudaSuccess) return err;
   if (a.k == 0) return cudaSuccess;  // nothing kept: e = a
   unsigned sx = (unsigned)(sms * kSplitBlocksPerSm / a.nranks);

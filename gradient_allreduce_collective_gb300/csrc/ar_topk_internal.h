@@ -62,6 +62,15 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //   overflow:    nonzero if some tile had more keys at or above the first
 //                digit's bin than its slots hold; the later passes then read
 //                the data instead
+//   hint:        a key below which the next call's pass 1 need not keep
+//                candidates (the lowest key of the bin where this call's
+//                count from the top reaches 4k); kept from call to call, any
+//                value is safe (a wrong one only costs the split pass over
+//                the data)
+//   spec_ok:     pass 1 filled the slots with every key at or above its hint,
+//                the hint lies at or below the first digit's bin and no
+//                tile's slots overflowed: the split pass reads the slots only
+//   spec_overflow: some tile had more candidates than its slots hold in pass 1
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -69,7 +78,10 @@ struct TopkState {
   uint32_t gt;
   uint32_t ticket[4];
   uint32_t overflow;
-  uint32_t pad[7];
+  uint32_t hint;
+  uint32_t spec_ok;
+  uint32_t spec_overflow;
+  uint32_t pad[4];
 };
 static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 

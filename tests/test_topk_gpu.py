@@ -313,6 +313,62 @@ def test_topk_workspace_reused_across_steps(offset):
             assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
 
 
+def _spec_decision(a: np.ndarray, hint: int, k: int, slots: int):
+    """Whether pass 1's speculative slots serve the split pass for values a,
+    and the hint the call leaves: the first digit (bits 30..20 of |a|) is the
+    highest bin whose count from the top reaches k; the slots serve when the
+    hint is at or below that bin's lowest key and no tile of 16,384 values has
+    more keys at or above the hint than its slots hold; the next hint is the
+    lowest key of the highest bin whose count from the top reaches 4k."""
+    key = a.view(np.uint32) & 0x7FFFFFFF
+    cum = np.cumsum(np.bincount(key >> 20, minlength=2048)[::-1])[::-1]
+    d1 = int(np.nonzero(cum >= k)[0].max())
+    nb = -(-key.size // 16384)
+    tiles = np.zeros(nb * 16384, dtype=np.uint32)
+    tiles[:key.size] = key
+    cand = np.count_nonzero(tiles.reshape(nb, 16384) >= np.uint32(hint), axis=1)
+    if hint == 0:  # padding counts too; only the real keys matter
+        cand[-1] -= nb * 16384 - key.size
+    ok = hint <= (d1 << 20) and int(cand.max()) <= slots
+    nxt = (int(np.nonzero(cum >= 4 * k)[0].max()) << 20) if cum[0] >= 4 * k else 0
+    return ok, nxt
+
+
+def test_topk_speculative_first_pass_across_steps():
+    # Large enough for pass 1 to compact its candidates speculatively (a warp
+    # per tile of 16,384 values). The hint it uses comes from the previous
+    # call on the same workspace: garbage on the first call, too high or too
+    # low while error feedback builds up the residual and after the gradient
+    # scale jumps by 1e3, valid once the scale holds. The bits must equal the
+    # oracle's every step whichever path ran, and the path taken (rank 0's
+    # spec_ok word in the workspace) must be the one the rule gives.
+    n, count, k = 8, 5_242_880, 52_428
+    share = -(-k * 16384 // count)
+    slots = min(8192, -(-(8 * share + 512) // 32) * 32)
+    ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
+    state_spec_ok = 2048 + 10  # 32-bit word of rank 0's workspace
+    hint = 0x5A5A5A5A
+    e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
+    res = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    spec_steps = 0
+    for step, scale in enumerate([1.0, 1.0, 1.0, 1e3, 1e-3, 1.0, 1.0, 1.0]):
+        g_np = [synthgen.normal_f32(count, 900 + 10 * step + r, 1e-3 * scale) for r in range(n)]
+        want_ok, hint = _spec_decision(g_np[0] + e_np[0], hint, k, slots)
+        grads = [to_dev(x, "f32") for x in g_np]
+        gar.ar_topk_compress(grads, res, k, idx, val, ws)
+        torch.cuda.synchronize()
+        assert int(ws.view(torch.int32)[state_spec_ok]) == int(want_ok), step
+        spec_steps += int(want_ok)
+        for r in range(n):
+            oi, ov, e_np[r] = oracle.topk_compress(g_np[r], e_np[r], k)
+            assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), (step, r)
+            assert np.array_equal(_bits(from_dev(val[r])), _bits(ov)), (step, r)
+            assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
+    assert spec_steps >= 3
+
+
 @pytest.mark.parametrize("n", [16, 64])
 def test_topk_and_sparse_allreduce_many_ranks(n):
     # the most ranks one call takes: a shared-memory fold tile of 8192 / N values
