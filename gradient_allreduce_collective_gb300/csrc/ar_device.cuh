@@ -67,6 +67,15 @@ template <int DT> __device__ __forceinline__ uint32_t order_key(uint32_t b) {
   return (b & Fmt<DT>::sign) ? (~b & Fmt<DT>::all) : (b | Fmt<DT>::sign);
 }
 
+// x / n of the AVG operator, the correctly rounded binary32 quotient. For n a
+// power of two, 1/n is exact and x * (1/n) rounds the same real number x/n
+// once, so one multiply gives the division's bits (subnormal results
+// included); other n take the IEEE division.
+__device__ __forceinline__ float avg_div(float x, int n) {
+  if ((n & (n - 1)) == 0) return __fmul_rn(x, __int_as_float((128 - __ffs(n)) << 23));
+  return __fdiv_rn(x, (float)n);
+}
+
 // ---------------------------------------------------------------- operator
 //
 // Sum, min, max and average are the element-wise operators of the "All-reduce"
@@ -113,7 +122,7 @@ template <int DT, int OP> struct Red {
       if constexpr (OP == OP_AVG) return (uint32_t)((int32_t)a / n);
       else return a;
     } else {
-      if constexpr (OP == OP_AVG) return from_f32<DT>(__fdiv_rn(a, (float)n));
+      if constexpr (OP == OP_AVG) return from_f32<DT>(avg_div(a, n));
       else return from_f32<DT>(a);
     }
   }

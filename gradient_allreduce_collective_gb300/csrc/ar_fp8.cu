@@ -189,7 +189,7 @@ __device__ __forceinline__ void fp8_item(const Fp8ReduceArgs& A, uint64_t i, int
   }
   uint32_t bits[V];
 #pragma unroll
-  for (int k = 0; k < V; ++k) bits[k] = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(acc[k], (float)N) : acc[k]);
+  for (int k = 0; k < V; ++k) bits[k] = from_f32<ODT>(OP == OP_AVG ? avg_div(acc[k], N) : acc[k]);
   if constexpr (VEC) {
     uint4 out = make_uint4(0, 0, 0, 0);
 #pragma unroll

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_FUSED_TREE ? 1 : 4) k_f
   if (!ld.valid) return;
   uint32_t bits[V];
 #pragma unroll
-  for (int k = 0; k < V; ++k) bits[k] = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(acc[k], (float)N) : acc[k]);
+  for (int k = 0; k < V; ++k) bits[k] = from_f32<ODT>(OP == OP_AVG ? avg_div(acc[k], N) : acc[k]);
   if constexpr (V * OB == 16) {
     uint4 out = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -228,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, kFusedPairBlocksPerSm) k_fp8_fused_p
   uint32_t ba[4], bb[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    ba[k] = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(pa[k], (float)N) : pa[k]);
-    bb[k] = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(pb[k], (float)N) : pb[k]);
+    ba[k] = from_f32<ODT>(OP == OP_AVG ? avg_div(pa[k], N) : pa[k]);
+    bb[k] = from_f32<ODT>(OP == OP_AVG ? avg_div(pb[k], N) : pb[k]);
   }
   for (int r = 0; r < N; ++r) {
     char* dst = static_cast<char*>(A.dst[r]);
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_consta
           acc = __fadd_rn(acc, d[r][k]);
         }
       }
-      const uint32_t out = from_f32<ODT>(OP == OP_AVG ? __fdiv_rn(acc, (float)N) : acc);
+      const uint32_t out = from_f32<ODT>(OP == OP_AVG ? avg_div(acc, N) : acc);
       for (int r = 0; r < N; ++r) {
         char* p = static_cast<char*>(A.dst[r]);
         if constexpr (OB == 4) *reinterpret_cast<uint32_t*>(p + e * 4) = out;

@@ -145,7 +145,7 @@ __device__ __forceinline__ void hop_block(const Fp8HopArgs& A, uint64_t lo, uint
   }
   if constexpr (OP == OP_AVG) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) p[k] = __fdiv_rn(p[k], (float)N);
+    for (int k = 0; k < 4; ++k) p[k] = avg_div(p[k], N);
   }
   qdq_block(p);  // the finished chunk, as the all-gather sends it
   if (full) {
@@ -228,8 +228,8 @@ __device__ __forceinline__ void hop_pair(const Fp8HopArgs& A, uint64_t lo, int s
   if constexpr (OP == OP_AVG) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      pa[k] = __fdiv_rn(pa[k], (float)N);
-      pb[k] = __fdiv_rn(pb[k], (float)N);
+      pa[k] = avg_div(pa[k], N);
+      pb[k] = avg_div(pb[k], N);
     }
   }
   ok &= qdq_block_pair(pa, pb);  // the finished chunk, as the all-gather sends it

@@ -33,6 +33,7 @@
 #include <vector>
 
 #include "ar.h"
+#include "ar_device.cuh"
 #include "ar_topk_internal.h"
 #include "ar_trace.h"
 
@@ -1021,10 +1022,7 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
         acc = make_float4(__fadd_rn(acc.x, y.x), __fadd_rn(acc.y, y.y), __fadd_rn(acc.z, y.z), __fadd_rn(acc.w, y.w));
       }
     }
-    if (A.avg) {
-      const float n = (float)N;
-      acc = make_float4(__fdiv_rn(acc.x, n), __fdiv_rn(acc.y, n), __fdiv_rn(acc.z, n), __fdiv_rn(acc.w, n));
-    }
+    if (A.avg) acc = make_float4(avg_div(acc.x, N), avg_div(acc.y, N), avg_div(acc.z, N), avg_div(acc.w, N));
     if (A.vec && 4 * q + 4 <= len) {
       for (int r = 0; r < N; ++r) __stcs(reinterpret_cast<float4*>(A.dst[r] + i), acc);
     } else {
