@@ -164,10 +164,18 @@ template <class Ld> struct PairAdd<Ld, std::void_t<decltype(Ld::kPairAdd)>> {
   static constexpr bool value = Ld::kPairAdd;
 };
 
+// A loader may declare `static constexpr int kBatch`: how many ranks' loads
+// the ring order issues before folding them (8 unless it says otherwise).
+template <class Ld, class = void> struct LoadBatch { static constexpr int value = 8; };
+template <class Ld> struct LoadBatch<Ld, std::void_t<decltype(Ld::kBatch)>> {
+  static constexpr int value = Ld::kBatch;
+};
+
 template <class Ld> struct Fold {
   using Acc = typename Ld::Acc;
   using Raw = typename Ld::Raw;
   static constexpr int V = Ld::V;
+  static constexpr int kB = LoadBatch<Ld>::value;
 
   __device__ __forceinline__ static void comb_into(Acc (&a)[V], const Acc (&b)[V]) {
     if constexpr (PairAdd<Ld>::value && V % 2 == 0) {
@@ -184,13 +192,14 @@ template <class Ld> struct Fold {
   }
 
   // ring order starting at rank s (0 <= s < N): acc = x_s (+) x_{s+1} (+) ...
-  // MAXN: compile-time bound on N (8 drops the code for further batches).
+  // MAXN: compile-time bound on N (it drops the code for further batches);
+  // the loads of kB ranks are issued before they are folded.
   template <int MAXN>
   __device__ __forceinline__ static void ring(const Ld& ld, int N, int s, Acc (&acc)[V]) {
     {
-      Raw raw[8];
+      Raw raw[kB];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kB; ++j) {
         if (j < N) {
           int r = s + j;
           r = (r >= N) ? r - N : r;
@@ -199,7 +208,7 @@ template <class Ld> struct Fold {
       }
       ld.unpack(raw[0], acc);
 #pragma unroll
-      for (int j = 1; j < 8; ++j) {
+      for (int j = 1; j < kB; ++j) {
         if (j < N) {
           Acc x[V];
           ld.unpack(raw[j], x);
@@ -207,13 +216,13 @@ template <class Ld> struct Fold {
         }
       }
     }
-    if constexpr (MAXN > 8) {
+    if constexpr (MAXN > kB) {
 #pragma unroll
-      for (int b0 = 8; b0 < MAXN; b0 += 8) {
+      for (int b0 = kB; b0 < MAXN; b0 += kB) {
         if (b0 >= N) break;
-        Raw raw[8];
+        Raw raw[kB];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kB; ++j) {
           if (b0 + j < N) {
             int r = s + b0 + j;
             r = (r >= N) ? r - N : r;
@@ -221,7 +230,7 @@ template <class Ld> struct Fold {
           }
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kB; ++j) {
           if (b0 + j < N) {
             Acc x[V];
             ld.unpack(raw[j], x);

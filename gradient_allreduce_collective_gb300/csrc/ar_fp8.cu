@@ -143,6 +143,10 @@ cudaError_t launch_fp8_quant(int in_dtype, bool vec, const Fp8QuantArgs& a, cuda
 
 template <int VV> struct Fp8Ld {
   static constexpr int V = VV;
+  // every rank's codes and scale (12 bytes each at V = 8) loaded before the
+  // fold: one round trip for up to 16 ranks (2.165 against 2.239 ms per
+  // materialised step of 16 x 134,217,728 bf16 with batches of 8 on GB300)
+  static constexpr int kBatch = 16;
   static constexpr bool kPairAdd = true;  // comb is a binary32 add: pairs may use the packed add
   using Acc = float;
   struct Raw {
