@@ -24,8 +24,9 @@
 namespace gar {
 
 // Blocks handled by one lane group per launch row: every lane issues the loads
-// of kQuantUnroll blocks before any arithmetic, so 4 x 16 bytes are in flight.
-constexpr int kQuantUnroll = 4;
+// of kQuantUnroll blocks before any arithmetic, so 8 x 16 bytes are in flight
+// (2.120 against 2.150 ms per materialised step with 4 on GB300).
+constexpr int kQuantUnroll = 8;
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constant__ Fp8QuantArgs A) {
