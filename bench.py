@@ -632,7 +632,10 @@ def measure_topk(gar, steps: int, warmup: int, count: int = COUNT, frac: float =
         compress()
         sparse_ar()
 
-    for _ in range(warmup):
+    # at least 40 untimed steps: with the same gradients every step the residual
+    # grows from call to call at first, and the threshold hint that lets pass 1
+    # collect the candidates (so the data is read once) settles after ~30 calls
+    for _ in range(max(warmup, 40)):
         step()
     ms = time_steps(step, steps, stream)
     ms_c = time_steps(compress, steps, stream)
