@@ -620,7 +620,10 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
 
 // Pass 3: histogram of bits 9..0 among the keys that match the prefix, read
 // from the slots (or, after an overflow, from the data); then (last block)
-// the last digit, which completes T.
+// the last digit, which completes T. From the slots, each tile's run is also
+// compacted in place to the keys at or above the prefix (every key that can
+// still be kept: about the tile's share of k), in index order, so that the
+// count and the emission read only those.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__ TopkArgs A) {
   pdl_enter();
@@ -635,22 +638,43 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     if ((key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
   };
   if (!w.st->overflow) {
-    // one warp per tile, eight slot loads in flight per lane
+    // one warp per tile, eight slots (index and value) loaded per lane before
+    // any is written back: a kept entry moves to the count of kept entries
+    // before it, never past an entry not yet loaded
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const uint32_t lt = (1u << lane) - 1u;
     for (uint64_t tile = (uint64_t)blockIdx.x * kWarps + wid; tile < A.nb; tile += (uint64_t)gridDim.x * kWarps) {
-      const float* sv = slot_val(w, tile, A.slots);
+      uint32_t* si = slot_idx(w, tile, A.slots);
+      float* sv = slot_val(w, tile, A.slots);
       const uint32_t n = w.n_s[tile];
+      uint32_t kept = 0;
       for (uint32_t c0 = 0; c0 < n; c0 += 32 * 8) {
         float x[8];
+        uint32_t ii[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const uint32_t c = c0 + 32 * u + lane;
           x[u] = c < n ? sv[c] : 0.0f;
+          ii[u] = c < n ? si[c] : 0u;
         }
+        __syncwarp();
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (c0 + 32 * u + lane < n) add(x[u]);
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t key = mag_key(x[u]);
+          const bool in = c0 + 32 * u + lane < n;
+          if (in && (key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
+          const bool keep = in && key >= prefix;
+          const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+          if (keep) {
+            const uint32_t p = kept + (uint32_t)__popc(bal & lt);
+            si[p] = ii[u];
+            sv[p] = x[u];
+          }
+          kept += (uint32_t)__popc(bal);
+        }
+        __syncwarp();
       }
+      if (lane == 0) w.n_s[tile] = kept;
     }
   } else {
     const float* __restrict__ a = A.e[r];

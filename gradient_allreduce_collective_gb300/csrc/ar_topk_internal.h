@@ -32,12 +32,14 @@ constexpr int kTopkHistWords = 2048;
 constexpr int kTopkStateWords = 16;
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
 
-// Slot capacity per tile: eight times the tile's share of k plus a margin, a
-// multiple of 32, at most kTopkMaxSlots and at most a tile.
+// Slot capacity per tile: sixteen times the tile's share of k plus a margin,
+// a multiple of 32, at most kTopkMaxSlots and at most a tile. The speculative
+// pass 1 keeps every value at or above the previous call's 4k-quantile bin,
+// which under error feedback is 6 to 15 times the share of k per tile.
 inline uint32_t topk_slots(uint64_t count, uint64_t k) {
   if (count == 0) return 32;
   const uint64_t share = (k * kTopkBlock + count - 1) / count;
-  uint64_t s = (8 * share + 512 + 31) / 32 * 32;
+  uint64_t s = (16 * share + 1024 + 31) / 32 * 32;
   const uint64_t tile = count < (uint64_t)kTopkBlock ? (count + 31) / 32 * 32 : (uint64_t)kTopkBlock;
   if (s > tile) s = tile;
   if (s > kTopkMaxSlots) s = kTopkMaxSlots;

@@ -317,26 +317,25 @@ def _spec_decision(a: np.ndarray, hint: int, k: int, slots: int):
     """Whether pass 1's speculative slots serve the split pass for values a,
     and the hint the call leaves: the first digit (bits 30..20 of |a|) is the
     highest bin whose count from the top reaches k; the slots serve when the
-    hint is at or below that bin's lowest key and no tile of 16,384 values has
-    more keys at or above the hint than its slots hold; the next hint is the
-    lowest key of the highest bin whose count from the top reaches 4k."""
+    hint is at or below that bin's lowest key and no sixteenth of a tile
+    (1,024 values) has more keys at or above the hint than its sixteenth of
+    the tile's slots holds; the next hint is the lowest key of the highest bin
+    whose count from the top reaches 4k."""
     key = a.view(np.uint32) & 0x7FFFFFFF
     cum = np.cumsum(np.bincount(key >> 20, minlength=2048)[::-1])[::-1]
     d1 = int(np.nonzero(cum >= k)[0].max())
-    nb = -(-key.size // 16384)
-    tiles = np.zeros(nb * 16384, dtype=np.uint32)
-    tiles[:key.size] = key
-    cand = np.count_nonzero(tiles.reshape(nb, 16384) >= np.uint32(hint), axis=1)
-    if hint == 0:  # padding counts too; only the real keys matter
-        cand[-1] -= nb * 16384 - key.size
-    ok = hint <= (d1 << 20) and int(cand.max()) <= slots
+    nsub = -(-key.size // 1024)
+    above = np.zeros(nsub * 1024, dtype=bool)  # padding past the end never counts
+    above[:key.size] = key >= np.uint32(hint)
+    cand = np.count_nonzero(above.reshape(nsub, 1024), axis=1)
+    ok = hint <= (d1 << 20) and int(cand.max()) <= slots // 16
     nxt = (int(np.nonzero(cum >= 4 * k)[0].max()) << 20) if cum[0] >= 4 * k else 0
     return ok, nxt
 
 
 def test_topk_speculative_first_pass_across_steps():
     # Large enough for pass 1 to compact its candidates speculatively (a warp
-    # per tile of 16,384 values). The hint it uses comes from the previous
+    # per 1,024-value sixteenth of a tile). The hint it uses comes from the previous
     # call on the same workspace: garbage on the first call, too high or too
     # low while error feedback builds up the residual and after the gradient
     # scale jumps by 1e3, valid once the scale holds. The bits must equal the
@@ -344,7 +343,7 @@ def test_topk_speculative_first_pass_across_steps():
     # spec_ok word in the workspace) must be the one the rule gives.
     n, count, k = 8, 5_242_880, 52_428
     share = -(-k * 16384 // count)
-    slots = min(8192, -(-(8 * share + 512) // 32) * 32)
+    slots = min(8192, -(-(16 * share + 1024) // 32) * 32)
     ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
     state_spec_ok = 2048 + 10  # 32-bit word of rank 0's workspace
     hint = 0x5A5A5A5A
