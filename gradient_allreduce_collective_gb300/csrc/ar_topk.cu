@@ -159,12 +159,9 @@ __device__ __forceinline__ bool last_block(uint32_t* ticket) {
 
 // The last block of a radix pass: the highest digit whose count from the top
 // reaches `need` (a block-wide scan over BINS bins, highest first); fold it
-// into the prefix and clear the bins for the next pass. With target2 > 0 the
-// same scan also stores in *hint (pre-set by the caller) the lowest key of the
-// highest digit whose count from the top reaches target2, if there is one.
+// into the prefix and clear the bins for the next pass.
 template <int BINS>
-__device__ void find_digit(uint32_t* hist, int shift, TopkState* st, uint32_t target2 = 0,
-                           uint32_t* hint = nullptr) {
+__device__ void find_digit(uint32_t* hist, int shift, TopkState* st) {
   constexpr int R = BINS / kThreads;
   const int top = BINS - threadIdx.x * R;  // this thread: bins [top - R, top)
   const uint32_t need = st->need;
@@ -176,19 +173,6 @@ __device__ void find_digit(uint32_t* hist, int shift, TopkState* st, uint32_t ta
     local += h[j];
   }
   const uint32_t above0 = block_exclusive_scan(local, nullptr);
-  if (target2 > 0 && above0 < target2 && above0 + local >= target2) {  // at most one thread
-    uint32_t above = above0;
-    int pick = top - R;
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-      if (above + h[j] >= target2) {
-        pick = top - 1 - j;
-        break;
-      }
-      above += h[j];
-    }
-    *hint = (uint32_t)pick << shift;
-  }
   if (above0 < need && above0 + local >= need) {  // exactly one thread
     uint32_t above = above0;
     int pick = top - R;
@@ -222,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ 
     w.st->overflow = 0;
     w.st->spec_ok = 0;  // the hint is left as the previous call set it
     w.st->spec_overflow = 0;
+    w.st->spec_count = 0;
   }
 }
 
@@ -297,10 +282,103 @@ __global__ void __launch_bounds__(kThreads, kPass1BlocksPerSm) k_topk_pass1(cons
 // pass fills. A warp takes 512 values at a time, lane l the float4 at
 // offsets 128 q + 4 l (q = 0..3), so index order is q-major; the four
 // per-q candidate counts of a lane are scanned across the warp as one word
-// of 8-bit fields. The last block finds the first digit, decides whether the
-// slots hold every key that can be kept (the hint at or below the first
-// digit's bin, no tile overflowing) and leaves the next call's hint.
+// of 8-bit fields. The last block finds the first digit and decides whether
+// the slots hold every key that can be kept: at least k keys at or above the
+// hint (then T is at or above it, and so is every key kept) and no tile
+// overflowing.
 constexpr int kSpecSeg = 512;  // values of a warp in one segment
+
+// The candidates (bit 4q + j of m: value (q, j) of the segment) of one lane
+// to the slots from position p on, in index order; lb = the index of the
+// lane's value (0, 0). CHECKED: positions at or past S are counted, not written.
+template <bool CHECKED>
+__device__ __forceinline__ void spec_emit(uint32_t m, uint32_t exc, uint32_t tot, uint32_t before,
+                                          uint32_t lb, const float (&v)[4][4], uint32_t S,
+                                          uint32_t* __restrict__ si, float* __restrict__ sv) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t p = before + ((exc >> (8 * q)) & 0xFFu);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((m >> (4 * q + j)) & 1u) {
+        if (!CHECKED || p < S) {
+          si[p] = lb + 128 * q + j;
+          sv[p] = v[q][j];
+        }
+        ++p;
+      }
+    }
+    before += (tot >> (8 * q)) & 0xFFu;
+  }
+}
+
+// Two 512-value segments of a tile from e0 on (lane l: the float4 at offsets
+// 128 q + 4 l of each); rem = count - e0. FULL: both lie inside the data.
+// The indices of values inside the data fit 32 bits (count does).
+template <bool FULL>
+__device__ __forceinline__ void spec_round(const float* __restrict__ g, float* __restrict__ e, uint32_t e0,
+                                           uint32_t rem, uint32_t tau, uint32_t S, uint32_t* __restrict__ si,
+                                           float* __restrict__ sv, uint32_t* sh, uint32_t& pos, int lane) {
+  float v[2][4][4];
+  if (FULL) {
+    float4 x[8], y[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      x[q] = __ldcs(reinterpret_cast<const float4*>(g + e0 + 128 * q) + lane);
+      y[q] = reinterpret_cast<const float4*>(e + e0 + 128 * q)[lane];
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 s4 = add4(x[q], y[q]);
+      reinterpret_cast<float4*>(e + e0 + 128 * q)[lane] = s4;
+      v[q >> 2][q & 3][0] = s4.x;
+      v[q >> 2][q & 3][1] = s4.y;
+      v[q >> 2][q & 3][2] = s4.z;
+      v[q >> 2][q & 3][3] = s4.w;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t o = 128 * q + 4 * lane + j;
+        v[q >> 2][q & 3][j] = 0.0f;
+        if (o < rem) {
+          v[q >> 2][q & 3][j] = __fadd_rn(g[e0 + o], e[e0 + o]);
+          e[e0 + o] = v[q >> 2][q & 3][j];
+        }
+      }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // the two segments in index order
+    const uint32_t lb = e0 + kSpecSeg * h + 4 * lane;
+    uint32_t m = 0;  // bit 4q + j: value (h, q, j) is a candidate
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool in = FULL || (uint32_t)(kSpecSeg * h + 4 * lane + 128 * q + j) < rem;
+        const uint32_t key = mag_key(v[h][q][j]);
+        if (in) atomicAdd(&sh[key >> 20], 1u);
+        if (in && key >= tau) m |= 1u << (4 * q + j);
+      }
+    const uint32_t c = (uint32_t)__popc(m & 0xFu) | ((uint32_t)__popc(m & 0xF0u) << 8) |
+                       ((uint32_t)__popc(m & 0xF00u) << 16) | ((uint32_t)__popc(m & 0xF000u) << 24);
+    uint32_t inc = c;  // no field overflows: at most 128 each
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31), exc = inc - c;
+    const uint32_t seg = (tot & 0xFFu) + ((tot >> 8) & 0xFFu) + ((tot >> 16) & 0xFFu) + (tot >> 24);
+    if (pos + seg <= S)  // the same for the whole warp
+      spec_emit<false>(m, exc, tot, pos, lb, v[h], S, si, sv);
+    else
+      spec_emit<true>(m, exc, tot, pos, lb, v[h], S, si, sv);
+    pos += seg;
+  }
+}
 
 __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(const __grid_constant__ TopkArgs A) {
   pdl_enter();
@@ -309,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(
   const RankWs w = rank_ws(A, r);
   const float* __restrict__ g = A.g[r];
   float* __restrict__ e = A.e[r];
-  const uint64_t count = A.count;
+  const uint32_t count = (uint32_t)A.count;
   const uint32_t tau = w.st->hint;
   const uint32_t S = A.slots;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -321,83 +399,23 @@ __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(
     uint32_t* __restrict__ si = slot_idx(w, tile, S);
     float* __restrict__ sv = slot_val(w, tile, S);
     uint32_t pos = 0;
-    const uint64_t t_end = (tile + 1) * kTopkBlock < count ? (tile + 1) * kTopkBlock : count;
-    // two 512-value segments per round: 8 float4 of g and of e in flight per lane
-    for (uint64_t e0 = tile * kTopkBlock; e0 < t_end; e0 += 2 * kSpecSeg) {
-      const bool full = e0 + 2 * kSpecSeg <= count;  // the same for the whole warp
-      float v[8][4];
-      if (full) {
-        float4 x[8], y[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          x[q] = __ldcs(reinterpret_cast<const float4*>(g + e0 + 128 * q) + lane);
-          y[q] = reinterpret_cast<const float4*>(e + e0 + 128 * q)[lane];
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 s4 = add4(x[q], y[q]);
-          reinterpret_cast<float4*>(e + e0 + 128 * q)[lane] = s4;
-          v[q][0] = s4.x;
-          v[q][1] = s4.y;
-          v[q][2] = s4.z;
-          v[q][3] = s4.w;
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t i = e0 + 128 * q + 4 * lane + j;
-            v[q][j] = 0.0f;
-            if (i < count) {
-              v[q][j] = __fadd_rn(g[i], e[i]);
-              e[i] = v[q][j];
-            }
-          }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // the two segments in index order
-        uint32_t m = 0;  // bit 4q + j: value (4h + q, j) is a candidate
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const bool in = full || e0 + 128 * (4 * h + q) + 4 * lane + j < count;
-            const uint32_t key = mag_key(v[4 * h + q][j]);
-            if (in) atomicAdd(&sh[key >> 20], 1u);
-            if (in && key >= tau) m |= 1u << (4 * q + j);
-          }
-        const uint32_t c = (uint32_t)__popc(m & 0xFu) | ((uint32_t)__popc(m & 0xF0u) << 8) |
-                           ((uint32_t)__popc(m & 0xF00u) << 16) | ((uint32_t)__popc(m & 0xF000u) << 24);
-        uint32_t inc = c;  // no field overflows: at most 128 each
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += t;
-        }
-        const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31), exc = inc - c;
-        uint32_t before = pos;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t p = before + ((exc >> (8 * q)) & 0xFFu);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if ((m >> (4 * q + j)) & 1u) {
-              if (p < S) {
-                si[p] = (uint32_t)(e0 + 128 * (4 * h + q) + 4 * lane + j);
-                sv[p] = v[4 * h + q][j];
-              }
-              ++p;
-            }
-          }
-          before += (tot >> (8 * q)) & 0xFFu;
-        }
-        pos = before;
+    const uint32_t t0 = (uint32_t)tile * kTopkBlock;
+    if ((uint64_t)t0 + kTopkBlock <= count) {  // a whole tile: no bounds checks
+      for (uint32_t e0 = t0; e0 < t0 + kTopkBlock; e0 += 2 * kSpecSeg)
+        spec_round<true>(g, e, e0, 0u, tau, S, si, sv, sh, pos, lane);
+    } else {
+      for (uint64_t e0 = t0; e0 < count; e0 += 2 * kSpecSeg) {
+        const uint32_t rem = (uint32_t)(count - e0);
+        if (rem >= 2 * kSpecSeg)
+          spec_round<true>(g, e, (uint32_t)e0, rem, tau, S, si, sv, sh, pos, lane);
+        else
+          spec_round<false>(g, e, (uint32_t)e0, rem, tau, S, si, sv, sh, pos, lane);
       }
     }
     if (lane == 0) {
       w.n_s[tile] = pos;
       if (pos > S) atomicOr(&w.st->spec_overflow, 1u);
+      if (pos) atomicAdd(&w.st->spec_count, pos);
     }
   }
   __syncthreads();
@@ -405,21 +423,9 @@ __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(
     if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
   if (A.k == 0) return;
   if (last_block(&w.st->ticket[0])) {
-    // the next call's hint: the lowest key of the bin where the count from
-    // the top reaches 4k (about four times the kept keys; 0, that is every
-    // key, when there are fewer), so that a moderate growth or shrinkage of
-    // the gradients between calls still finds the hint valid
-    __shared__ uint32_t s_hint;
-    if (threadIdx.x == 0) s_hint = 0;
-    __syncthreads();
-    const uint64_t t2 = 4ull * A.k;
-    find_digit<2048>(w.hist, 20, w.st, t2 < 0xFFFFFFFFull ? (uint32_t)t2 : 0xFFFFFFFFu, &s_hint);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t d1 = w.st->prefix >> 20;
-      w.st->spec_ok = (tau <= (d1 << 20) && __ldcg(&w.st->spec_overflow) == 0) ? 1u : 0u;
-      w.st->hint = s_hint;
-    }
+    find_digit<2048>(w.hist, 20, w.st);
+    if (threadIdx.x == 0)
+      w.st->spec_ok = (__ldcg(&w.st->spec_count) >= A.k && __ldcg(&w.st->spec_overflow) == 0) ? 1u : 0u;
   }
 }
 
@@ -699,7 +705,16 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
   __syncthreads();
   for (int i = threadIdx.x; i < 1024; i += blockDim.x)
     if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
-  if (last_block(&w.st->ticket[2])) find_digit<1024>(w.hist, 0, w.st);
+  if (last_block(&w.st->ticket[2])) {
+    find_digit<1024>(w.hist, 0, w.st);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // the next call's hint: T's magnitude scaled down a little (for an
+      // infinity or a NaN, the infinity's key)
+      const uint32_t T = w.st->prefix;
+      w.st->hint = T >= 0x7F800000u ? 0x7F800000u : __float_as_uint(__fmul_rn(__uint_as_float(T), kTopkHintScale));
+    }
+  }
 }
 
 // run mask: bit j set if value j's key is above T, bit 16 + j if it equals T

@@ -30,12 +30,17 @@ constexpr uint32_t kTopkMaxSlots = 8192;                       // slot cap per t
 //   kept), in index order; n_s[tile] of them
 constexpr int kTopkHistWords = 2048;
 constexpr int kTopkStateWords = 16;
+// The next call's hint: T's magnitude times this (rounded to nearest), a
+// margin for thresholds that fall from call to call.
+constexpr float kTopkHintScale = 0.95f;
+
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
 
 // Slot capacity per tile: sixteen times the tile's share of k plus a margin,
-// a multiple of 32, at most kTopkMaxSlots and at most a tile. The speculative
-// pass 1 keeps every value at or above the previous call's 4k-quantile bin,
-// which under error feedback is 6 to 15 times the share of k per tile.
+// a multiple of 32, at most kTopkMaxSlots and at most a tile. The split pass
+// keeps every key in the first digit's bin and above (under error feedback
+// 6 to 15 times the share of k per tile: the values pile up just below the
+// threshold); the speculative pass 1 keeps those at or above its hint.
 inline uint32_t topk_slots(uint64_t count, uint64_t k) {
   if (count == 0) return 32;
   const uint64_t share = (k * kTopkBlock + count - 1) / count;
@@ -64,15 +69,15 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //   overflow:    nonzero if some tile had more keys at or above the first
 //                digit's bin than its slots hold; the later passes then read
 //                the data instead
-//   hint:        a key below which the next call's pass 1 need not keep
-//                candidates (the lowest key of the bin where this call's
-//                count from the top reaches 4k); kept from call to call, any
-//                value is safe (a wrong one only costs the split pass over
-//                the data)
+//   hint:        the key below which the next call's pass 1 keeps no
+//                candidates: this call's T with its magnitude scaled by
+//                kTopkHintScale; kept from call to call, any value is safe
+//                (a wrong one only costs the split pass over the data)
 //   spec_ok:     pass 1 filled the slots with every key at or above its hint,
-//                the hint lies at or below the first digit's bin and no
-//                tile's slots overflowed: the split pass reads the slots only
+//                at least k of them (so T is among them) and no tile's slots
+//                overflowed: the split pass reads the slots only
 //   spec_overflow: some tile had more candidates than its slots hold in pass 1
+//   spec_count:  the candidates of pass 1, all tiles
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -83,7 +88,8 @@ struct TopkState {
   uint32_t hint;
   uint32_t spec_ok;
   uint32_t spec_overflow;
-  uint32_t pad[4];
+  uint32_t spec_count;
+  uint32_t pad[3];
 };
 static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 

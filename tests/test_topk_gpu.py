@@ -313,39 +313,42 @@ def test_topk_workspace_reused_across_steps(offset):
             assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
 
 
+HINT_SCALE = np.float32(0.95)  # the next call's hint: T's magnitude times this
+
+
 def _spec_decision(a: np.ndarray, hint: int, k: int, slots: int):
     """Whether pass 1's speculative slots serve the split pass for values a,
-    and the hint the call leaves: the first digit (bits 30..20 of |a|) is the
-    highest bin whose count from the top reaches k; the slots serve when the
-    hint is at or below that bin's lowest key and no sixteenth of a tile
-    (1,024 values) has more keys at or above the hint than its sixteenth of
-    the tile's slots holds; the next hint is the lowest key of the highest bin
-    whose count from the top reaches 4k."""
+    and the hint the call leaves: the slots serve when at least k keys (bits
+    30..0 of a) are at or above the hint (so T, the k-th largest key, is one
+    of them) and no tile of 16,384 values has more of them than its slots
+    hold; the next hint is the key of T's magnitude times 0.95, rounded to
+    nearest (the infinity's key for an infinite or NaN T)."""
     key = a.view(np.uint32) & 0x7FFFFFFF
-    cum = np.cumsum(np.bincount(key >> 20, minlength=2048)[::-1])[::-1]
-    d1 = int(np.nonzero(cum >= k)[0].max())
-    nsub = -(-key.size // 1024)
-    above = np.zeros(nsub * 1024, dtype=bool)  # padding past the end never counts
+    nb = -(-key.size // 16384)
+    above = np.zeros(nb * 16384, dtype=bool)  # padding past the end never counts
     above[:key.size] = key >= np.uint32(hint)
-    cand = np.count_nonzero(above.reshape(nsub, 1024), axis=1)
-    ok = hint <= (d1 << 20) and int(cand.max()) <= slots // 16
-    nxt = (int(np.nonzero(cum >= 4 * k)[0].max()) << 20) if cum[0] >= 4 * k else 0
+    cand = np.count_nonzero(above.reshape(nb, 16384), axis=1)
+    ok = int(cand.sum()) >= k and int(cand.max()) <= slots
+    T = int(np.sort(key)[key.size - k])
+    nxt = 0x7F800000 if T >= 0x7F800000 else int((np.uint32(T).view(np.float32) * HINT_SCALE).view(np.uint32))
     return ok, nxt
 
 
 def test_topk_speculative_first_pass_across_steps():
     # Large enough for pass 1 to compact its candidates speculatively (a warp
-    # per 1,024-value sixteenth of a tile). The hint it uses comes from the previous
-    # call on the same workspace: garbage on the first call, too high or too
-    # low while error feedback builds up the residual and after the gradient
-    # scale jumps by 1e3, valid once the scale holds. The bits must equal the
-    # oracle's every step whichever path ran, and the path taken (rank 0's
-    # spec_ok word in the workspace) must be the one the rule gives.
+    # per tile of 16,384 values). The hint it uses comes from the previous
+    # call on the same workspace: garbage on the first call, far too low
+    # (every tile overflowing) when the gradient scale jumps by 1e3, too high
+    # (fewer than k keys above it) while the residual that jump left decays,
+    # valid again once the threshold holds. The bits must equal the oracle's every step
+    # whichever path ran; the path taken (rank 0's spec_ok word in the
+    # workspace) and the hint left for the next call must be the ones the
+    # rule gives.
     n, count, k = 8, 5_242_880, 52_428
     share = -(-k * 16384 // count)
     slots = min(8192, -(-(16 * share + 1024) // 32) * 32)
     ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
-    state_spec_ok = 2048 + 10  # 32-bit word of rank 0's workspace
+    state_hint, state_spec_ok = 2048 + 9, 2048 + 10  # 32-bit words of rank 0's workspace
     hint = 0x5A5A5A5A
     e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
     res = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
@@ -359,6 +362,7 @@ def test_topk_speculative_first_pass_across_steps():
         gar.ar_topk_compress(grads, res, k, idx, val, ws)
         torch.cuda.synchronize()
         assert int(ws.view(torch.int32)[state_spec_ok]) == int(want_ok), step
+        assert int(ws.view(torch.int32)[state_hint]) == hint, step
         spec_steps += int(want_ok)
         for r in range(n):
             oi, ov, e_np[r] = oracle.topk_compress(g_np[r], e_np[r], k)
