@@ -659,11 +659,14 @@ def measure_topk(gar, steps: int, warmup: int, count: int = COUNT, frac: float =
     # how often pass 1's speculative candidate slots served the split pass
     # (one full pass over the data instead of two): rank 0's spec_ok word after
     # each of SPEC_PROBES further steps, untimed
-    spec_hits = 0
+    # and how often pass 1 also found the second digit (the previous call's
+    # first digit held), so that the split pass returned at once
+    spec_hits = pre2_hits = 0
     for _ in range(SPEC_PROBES):
         step()
         torch.cuda.synchronize()
         spec_hits += int(ws.view(torch.int32)[2048 + 10]) == 1
+        pre2_hits += int(ws.view(torch.int32)[2048 + 14]) == 1
     spec = spec_hits / SPEC_PROBES
     M = count * 4
     min_c = n * 3 * M + n * k * 8          # read g and e, write e; the pairs
@@ -699,6 +702,7 @@ def measure_topk(gar, steps: int, warmup: int, count: int = COUNT, frac: float =
         "ms_per_step_graph": ms_graph,
         "compress": {"ms": ms_c, "launches": 6, "min_bytes": min_c, "structure_bytes": struct_c,
                      "full_data_passes": round(2 - spec, 3), "speculative_share": spec,
+                     "second_digit_in_pass1_share": pre2_hits / SPEC_PROBES,
                      "hbm_gbs_min_bytes": min_c / (ms_c * 1e-3) / 1e9,
                      "hbm_gbs_structure": struct_c / (ms_c * 1e-3) / 1e9,
                      "frac_hbm_structure": struct_c / (ms_c * 1e-3) / 1e9 / peak},

@@ -204,10 +204,13 @@ __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ 
     w.st->gt = 0;
     for (int p = 0; p < 4; ++p) w.st->ticket[p] = 0;
     w.st->overflow = 0;
-    w.st->spec_ok = 0;  // the hint is left as the previous call set it
+    w.st->spec_ok = 0;  // the hint and t_prev are left as the previous call set them
     w.st->spec_overflow = 0;
     w.st->spec_count = 0;
+    w.st->pre2 = 0;
   }
+  if (A.nb > 0)  // pass 1's second-digit histogram
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x) w.masks[i] = 0;
 }
 
 __device__ __forceinline__ float4 add4(float4 x, float4 y) {
@@ -312,13 +315,18 @@ __device__ __forceinline__ void spec_emit(uint32_t m, uint32_t exc, uint32_t tot
   }
 }
 
+// The speculative pass 1's block histogram, one count per key: bins 0..2047
+// by bits 30..20, except that a key in the guessed first-digit bin d1g counts
+// in bin 2048 + bits 19..10 instead (bin d1g is their sum).
+__shared__ uint32_t s_spec_h[3072];
+
 // Two 512-value segments of a tile from e0 on (lane l: the float4 at offsets
 // 128 q + 4 l of each); rem = count - e0. FULL: both lie inside the data.
 // The indices of values inside the data fit 32 bits (count does).
 template <bool FULL>
 __device__ __forceinline__ void spec_round(const float* __restrict__ g, float* __restrict__ e, uint32_t e0,
                                            uint32_t rem, uint32_t tau, uint32_t S, uint32_t* __restrict__ si,
-                                           float* __restrict__ sv, uint32_t* sh, uint32_t& pos, int lane) {
+                                           float* __restrict__ sv, uint32_t d1g, uint32_t& pos, int lane) {
   float v[2][4][4];
   if (FULL) {
     float4 x[8], y[8];
@@ -359,7 +367,8 @@ __device__ __forceinline__ void spec_round(const float* __restrict__ g, float* _
       for (int j = 0; j < 4; ++j) {
         const bool in = FULL || (uint32_t)(kSpecSeg * h + 4 * lane + 128 * q + j) < rem;
         const uint32_t key = mag_key(v[h][q][j]);
-        if (in) atomicAdd(&sh[key >> 20], 1u);
+        const uint32_t hi = key >> 20;
+        if (in) atomicAdd(&s_spec_h[hi == d1g ? 2048u + ((key >> 10) & 1023u) : hi], 1u);
         if (in && key >= tau) m |= 1u << (4 * q + j);
       }
     const uint32_t c = (uint32_t)__popc(m & 0xFu) | ((uint32_t)__popc(m & 0xF0u) << 8) |
@@ -382,16 +391,16 @@ __device__ __forceinline__ void spec_round(const float* __restrict__ g, float* _
 
 __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(const __grid_constant__ TopkArgs A) {
   pdl_enter();
-  __shared__ uint32_t sh[2048];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   const float* __restrict__ g = A.g[r];
   float* __restrict__ e = A.e[r];
   const uint32_t count = (uint32_t)A.count;
   const uint32_t tau = w.st->hint;
+  const uint32_t d1g = w.st->t_prev >> 20;  // the first digit guessed
   const uint32_t S = A.slots;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x) sh[i] = 0;
+  for (int i = threadIdx.x; i < 3072; i += blockDim.x) s_spec_h[i] = 0;
   __syncthreads();
   // tiles interleaved over the blocks (tile = warp * gridDim.x + block), so
   // that every block, and so every SM, gets an equal share
@@ -402,14 +411,14 @@ __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(
     const uint32_t t0 = (uint32_t)tile * kTopkBlock;
     if ((uint64_t)t0 + kTopkBlock <= count) {  // a whole tile: no bounds checks
       for (uint32_t e0 = t0; e0 < t0 + kTopkBlock; e0 += 2 * kSpecSeg)
-        spec_round<true>(g, e, e0, 0u, tau, S, si, sv, sh, pos, lane);
+        spec_round<true>(g, e, e0, 0u, tau, S, si, sv, d1g, pos, lane);
     } else {
       for (uint64_t e0 = t0; e0 < count; e0 += 2 * kSpecSeg) {
         const uint32_t rem = (uint32_t)(count - e0);
         if (rem >= 2 * kSpecSeg)
-          spec_round<true>(g, e, (uint32_t)e0, rem, tau, S, si, sv, sh, pos, lane);
+          spec_round<true>(g, e, (uint32_t)e0, rem, tau, S, si, sv, d1g, pos, lane);
         else
-          spec_round<false>(g, e, (uint32_t)e0, rem, tau, S, si, sv, sh, pos, lane);
+          spec_round<false>(g, e, (uint32_t)e0, rem, tau, S, si, sv, d1g, pos, lane);
       }
     }
     if (lane == 0) {
@@ -420,12 +429,33 @@ __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 2048; i += blockDim.x)
-    if (sh[i]) atomicAdd(&w.hist[i], sh[i]);
+    if (s_spec_h[i]) atomicAdd(&w.hist[i], s_spec_h[i]);
+  if (d1g < 2048) {  // a garbage t_prev gives a bin no key falls in
+    uint32_t part = 0;
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x) {
+      const uint32_t c = s_spec_h[2048 + i];
+      part += c;
+      if (c) atomicAdd(&w.masks[i], c);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if ((threadIdx.x & 31) == 0 && part) atomicAdd(&w.hist[d1g], part);
+  }
   if (A.k == 0) return;
   if (last_block(&w.st->ticket[0])) {
     find_digit<2048>(w.hist, 20, w.st);
-    if (threadIdx.x == 0)
-      w.st->spec_ok = (__ldcg(&w.st->spec_count) >= A.k && __ldcg(&w.st->spec_overflow) == 0) ? 1u : 0u;
+    __shared__ uint32_t s_pre2;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const bool ok = __ldcg(&w.st->spec_count) >= A.k && __ldcg(&w.st->spec_overflow) == 0;
+      w.st->spec_ok = ok ? 1u : 0u;
+      s_pre2 = (ok && (w.st->prefix >> 20) == d1g) ? 1u : 0u;
+      w.st->pre2 = s_pre2;
+    }
+    __syncthreads();
+    // the guessed bin is the first digit: the second digit from pass 1's own
+    // histogram of that bin (the split pass would count the same keys)
+    if (s_pre2) find_digit<1024>(w.masks, 10, w.st);
   }
 }
 
@@ -526,6 +556,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   int parity = 0;
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
+  if (w.st->pre2) return;  // pass 1 found the second digit (the same for the whole block)
   const uint64_t count = A.count;
   const float* __restrict__ a = A.e[r];
   const uint32_t S = A.slots;
@@ -710,9 +741,10 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     __syncthreads();
     if (threadIdx.x == 0) {
       // the next call's hint: T's magnitude scaled down a little (for an
-      // infinity or a NaN, the infinity's key)
+      // infinity or a NaN, the infinity's key); and T itself
       const uint32_t T = w.st->prefix;
       w.st->hint = T >= 0x7F800000u ? 0x7F800000u : __float_as_uint(__fmul_rn(__uint_as_float(T), kTopkHintScale));
+      w.st->t_prev = T;
     }
   }
 }

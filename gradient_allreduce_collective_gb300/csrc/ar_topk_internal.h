@@ -24,7 +24,9 @@ constexpr uint32_t kTopkMaxSlots = 8192;                       // slot cap per t
 //   then nb words each of n_gt, n_eq, eq_before, out_off, n_s (nb = tiles)
 //   then nb * kThreads * kTopkRuns words of run masks (used only when a
 //   tile's slots overflow): for the kTopkElems values of a run, bit j (j < 16)
-//   set if value j's key is above T, bit 16 + j if it equals T
+//   set if value j's key is above T, bit 16 + j if it equals T; the first
+//   1024 of them also hold the speculative pass 1's second-digit histogram
+//   (consumed before any mask is written)
 //   then per tile 2 * S words of slots: the indices, then the values, of the
 //   tile's keys at or above the first digit's bin (every key that can be
 //   kept), in index order; n_s[tile] of them
@@ -78,6 +80,11 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //                overflowed: the split pass reads the slots only
 //   spec_overflow: some tile had more candidates than its slots hold in pass 1
 //   spec_count:  the candidates of pass 1, all tiles
+//   t_prev:      the previous call's T (kept from call to call, like hint);
+//                the speculative pass 1 also counts, by bits 19..10, the
+//                keys in t_prev's first-digit bin
+//   pre2:        that bin was this call's first digit and the slots serve:
+//                pass 1 found the second digit too, the split pass is skipped
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -89,7 +96,9 @@ struct TopkState {
   uint32_t spec_ok;
   uint32_t spec_overflow;
   uint32_t spec_count;
-  uint32_t pad[3];
+  uint32_t t_prev;
+  uint32_t pre2;
+  uint32_t pad[1];
 };
 static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 

@@ -348,7 +348,8 @@ def test_topk_speculative_first_pass_across_steps():
     share = -(-k * 16384 // count)
     slots = min(8192, -(-(16 * share + 1024) // 32) * 32)
     ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
-    state_hint, state_spec_ok = 2048 + 9, 2048 + 10  # 32-bit words of rank 0's workspace
+    state_hint, state_spec_ok, state_pre2 = 2048 + 9, 2048 + 10, 2048 + 14  # words of rank 0's workspace
+    t_prev = 0x5A5A5A5A
     hint = 0x5A5A5A5A
     e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
     res = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
@@ -357,12 +358,17 @@ def test_topk_speculative_first_pass_across_steps():
     spec_steps = 0
     for step, scale in enumerate([1.0, 1.0, 1.0, 1e3, 1e-3, 1.0, 1.0, 1.0]):
         g_np = [synthgen.normal_f32(count, 900 + 10 * step + r, 1e-3 * scale) for r in range(n)]
-        want_ok, hint = _spec_decision(g_np[0] + e_np[0], hint, k, slots)
+        a0 = g_np[0] + e_np[0]
+        want_ok, hint = _spec_decision(a0, hint, k, slots)
+        T = int(np.sort(a0.view(np.uint32) & 0x7FFFFFFF)[count - k])
+        want_pre2 = want_ok and (T >> 20) == (t_prev >> 20)  # the previous T's first digit held
+        t_prev = T
         grads = [to_dev(x, "f32") for x in g_np]
         gar.ar_topk_compress(grads, res, k, idx, val, ws)
         torch.cuda.synchronize()
         assert int(ws.view(torch.int32)[state_spec_ok]) == int(want_ok), step
         assert int(ws.view(torch.int32)[state_hint]) == hint, step
+        assert int(ws.view(torch.int32)[state_pre2]) == int(want_pre2), step
         spec_steps += int(want_ok)
         for r in range(n):
             oi, ov, e_np[r] = oracle.topk_compress(g_np[r], e_np[r], k)
@@ -370,6 +376,32 @@ def test_topk_speculative_first_pass_across_steps():
             assert np.array_equal(_bits(from_dev(val[r])), _bits(ov)), (step, r)
             assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
     assert spec_steps >= 3
+
+
+def test_topk_first_digit_guess_skips_the_split_pass():
+    # The same gradients and a zero residual on every call: from the second
+    # call on the hint holds and T's first digit is the previous call's, so
+    # pass 1 finds the second digit from its own histogram of the candidates
+    # in that bin and the split pass returns at once. The bits must not
+    # change.
+    n, count, k = 8, 5_242_880, 52_428
+    g_np = [synthgen.normal_f32(count, 700 + r, 1e-3) for r in range(n)]
+    want = [oracle.topk_compress(g, np.zeros(count, dtype=np.float32), k) for g in g_np]
+    ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
+    grads = [to_dev(x, "f32") for x in g_np]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    for call in range(3):
+        res = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+        gar.ar_topk_compress(grads, res, k, idx, val, ws)
+        torch.cuda.synchronize()
+        words = ws.view(torch.int32)
+        assert int(words[2048 + 10]) == int(call > 0) and int(words[2048 + 14]) == int(call > 0), call
+        for r in range(n):
+            wi, wv, we = want[r]
+            assert np.array_equal(from_dev(idx[r]).view(np.uint32), wi), (call, r)
+            assert np.array_equal(_bits(from_dev(val[r])), _bits(wv)), (call, r)
+            assert np.array_equal(_bits(from_dev(res[r])), _bits(we)), (call, r)
 
 
 @pytest.mark.parametrize("n", [16, 64])
