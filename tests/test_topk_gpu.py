@@ -199,6 +199,40 @@ def test_sparse_allreduce_matches_oracle(n):
                 assert np.array_equal(_bits(from_dev(out[r])), _bits(want)), (op, algo, r)
 
 
+@pytest.mark.parametrize("n", [3, 4])
+def test_sparse_allreduce_signed_zeros_and_overlaps(n):
+    # Values with signed zeros, opposite signs and rounding-sensitive
+    # magnitudes on indices that several ranks share: the fold reads only the
+    # present values, an absent one counting as +0 in the same order, so the
+    # bits (-0 only where every rank holds -0) must equal the dense forms'.
+    count = 9_001
+    pick = np.array([-0.0, 0.0, 1.0, -1.0, 1e-8, -1e-8, 3.0e38, -3.0e38, 0.1, -0.3], dtype=np.float32)
+    rng = np.random.default_rng(5)
+    idx_np, val_np = [], []
+    for r in range(n):
+        i = np.union1d([0], np.arange(r % 2, count, 1 + r % 3)).astype(np.uint32)
+        v = pick[rng.integers(0, pick.size, i.size)]
+        v[0] = np.float32(-0.0)  # every rank holds -0 at index 0
+        idx_np.append(i)
+        val_np.append(v)
+    idx = [torch.from_numpy(i.view(np.int32)).cuda() for i in idx_np]
+    val = [to_dev(v, "f32") for v in val_np]
+    nnz = [i.size for i in idx_np]
+    dense = [oracle.sparse_to_dense(i, v, count) for i, v in zip(idx_np, val_np)]
+    for op in ("sum", "avg"):
+        for algo in _algos(n):
+            out = [torch.full((count,), float("nan"), device="cuda") for _ in range(n)]
+            ws = torch.empty(gar.ar_sparse_workspace_bytes(n, count), dtype=torch.uint8, device="cuda")
+            gar.ar_sparse_allreduce(idx, val, nnz, out, op, algo, ws)
+            torch.cuda.synchronize()
+            if algo in ("tree", "step_tree"):
+                want = oracle.tree_allreduce(dense, "f32", op)[0]
+            else:
+                want = oracle.sparse_ring_allreduce(idx_np, val_np, count, op)[0]
+            for r in range(n):
+                assert np.array_equal(_bits(from_dev(out[r])), _bits(want)), (op, algo, r)
+
+
 def test_sparse_allreduce_drops_out_of_range_indices():
     count = 1000
     idx = torch.tensor([0, 999, 1000, 5000], dtype=torch.int32, device="cuda")
