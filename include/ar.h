@@ -363,12 +363,14 @@ size_t ar_topk_workspace_bytes(int nranks, size_t count, size_t k);
  *     16-byte aligned the vector path runs; results are identical either way).
  *   workspace: device memory of at least ar_topk_workspace_bytes(nranks,
  *     count, k), 16-byte aligned, owned by the caller; its contents need no
- *     initialisation. A call leaves in it a threshold hint that the next
- *     call on the same workspace uses to collect its candidates during the
- *     pass that forms a = g + e (large calls, 16-byte aligned buffers): when
- *     the hint holds, the data is read once instead of twice. Results never
- *     depend on the workspace's contents; a stale or garbage hint only
- *     costs the second pass.
+ *     initialisation. A call leaves in it its threshold, which the next
+ *     call on the same workspace uses to collect its candidates (the values
+ *     at or above 0.95 times it) during the pass that forms a = g + e (large
+ *     calls, 16-byte aligned buffers): when at least k values are collected
+ *     and they fit, the data is read once instead of twice, and when the
+ *     threshold's leading 11 bits also hold, that pass narrows the
+ *     selection one step further. Results never depend on the workspace's
+ *     contents; a stale or garbage threshold only costs the second pass.
  *   Errors: AR_ERR_INVALID_ARGUMENT for k > count, count >= 2^32, a null or
  *   misaligned pointer or a short workspace; AR_ERR_ALIAS if an output
  *   (residual, idx, val, workspace) overlaps another output or an input
