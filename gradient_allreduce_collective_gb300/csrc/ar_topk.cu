@@ -740,10 +740,25 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     find_digit<1024>(w.hist, 0, w.st);
     __syncthreads();
     if (threadIdx.x == 0) {
-      // the next call's hint: T's magnitude scaled down a little (for an
-      // infinity or a NaN, the infinity's key); and T itself
+      // the margin for the next call: wider after too few candidates,
+      // narrower after a run of calls whose candidates served
+      uint32_t level = w.st->margin & 0xFFu, run = w.st->margin >> 8;
+      if (level >= (uint32_t)kTopkHintLevels) level = kTopkHintStart, run = 0;
+      if (w.st->spec_ok) {
+        if (++run >= kTopkTightenRun) {
+          run = level > 0 ? 0 : kTopkTightenRun;
+          if (level > 0) --level;
+        }
+      } else {
+        run = 0;
+        if (w.st->spec_count < A.k && level + 1 < (uint32_t)kTopkHintLevels) ++level;
+      }
+      w.st->margin = level | run << 8;
+      // the next call's hint: T's magnitude scaled down by the margin (for
+      // an infinity or a NaN, the infinity's key); and T itself
       const uint32_t T = w.st->prefix;
-      w.st->hint = T >= 0x7F800000u ? 0x7F800000u : __float_as_uint(__fmul_rn(__uint_as_float(T), kTopkHintScale));
+      w.st->hint =
+          T >= 0x7F800000u ? 0x7F800000u : __float_as_uint(__fmul_rn(__uint_as_float(T), topk_hint_scale(level)));
       w.st->t_prev = T;
     }
   }

@@ -32,9 +32,24 @@ constexpr uint32_t kTopkMaxSlots = 8192;                       // slot cap per t
 //   kept), in index order; n_s[tile] of them
 constexpr int kTopkHistWords = 2048;
 constexpr int kTopkStateWords = 16;
-// The next call's hint: T's magnitude times this (rounded to nearest), a
-// margin for thresholds that fall from call to call.
-constexpr float kTopkHintScale = 0.95f;
+// The next call's hint is T's magnitude times the factor of a margin level
+// (rounded to nearest): a call whose candidates fell short of k (T dropped
+// below its hint) widens the margin one level, kTopkTightenRun calls in a
+// row that kept their candidates narrow it one level. A level outside the
+// table (a fresh workspace) counts as kTopkHintStart.
+constexpr int kTopkHintLevels = 6;
+constexpr uint32_t kTopkHintStart = 2;
+constexpr uint32_t kTopkTightenRun = 16;
+__host__ __device__ inline float topk_hint_scale(uint32_t level) {
+  switch (level) {
+    case 0: return 0.99f;
+    case 1: return 0.98f;
+    case 2: return 0.95f;
+    case 3: return 0.9f;
+    case 4: return 0.8f;
+    default: return 0.5f;
+  }
+}
 
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
 
@@ -72,8 +87,8 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //                digit's bin than its slots hold; the later passes then read
 //                the data instead
 //   hint:        the key below which the next call's pass 1 keeps no
-//                candidates: this call's T with its magnitude scaled by
-//                kTopkHintScale; kept from call to call, any value is safe
+//                candidates: this call's T with its magnitude scaled by the
+//                margin's factor; kept from call to call, any value is safe
 //                (a wrong one only costs the split pass over the data)
 //   spec_ok:     pass 1 filled the slots with every key at or above its hint,
 //                at least k of them (so T is among them) and no tile's slots
@@ -85,6 +100,9 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //                keys in t_prev's first-digit bin
 //   pre2:        that bin was this call's first digit and the slots serve:
 //                pass 1 found the second digit too, the split pass is skipped
+//   margin:      bits 0..7 the level of the hint's factor (topk_hint_scale),
+//                bits 8.. the run of calls since it last changed that kept
+//                their candidates in the slots; kept from call to call
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -98,7 +116,7 @@ struct TopkState {
   uint32_t spec_count;
   uint32_t t_prev;
   uint32_t pre2;
-  uint32_t pad[1];
+  uint32_t margin;
 };
 static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 

@@ -347,34 +347,58 @@ def test_topk_workspace_reused_across_steps(offset):
             assert np.array_equal(_bits(from_dev(res[r])), _bits(e_np[r])), (step, r)
 
 
-HINT_SCALE = np.float32(0.95)  # the next call's hint: T's magnitude times this
+HINT_SCALES = np.array([0.99, 0.98, 0.95, 0.9, 0.8, 0.5], dtype=np.float32)  # by margin level
 
 
 def _spec_decision(a: np.ndarray, hint: int, k: int, slots: int):
     """Whether pass 1's speculative slots serve the split pass for values a,
-    and the hint the call leaves: the slots serve when at least k keys (bits
-    30..0 of a) are at or above the hint (so T, the k-th largest key, is one
-    of them) and no tile of 16,384 values has more of them than its slots
-    hold; the next hint is the key of T's magnitude times 0.95, rounded to
-    nearest (the infinity's key for an infinite or NaN T)."""
+    whether fewer than k keys (bits 30..0 of a) lie at or above the hint, and
+    T, the k-th largest key: the slots serve when at least k keys are at or
+    above the hint (so T is one of them) and no tile of 16,384 values has
+    more of them than its slots hold."""
     key = a.view(np.uint32) & 0x7FFFFFFF
     nb = -(-key.size // 16384)
     above = np.zeros(nb * 16384, dtype=bool)  # padding past the end never counts
     above[:key.size] = key >= np.uint32(hint)
     cand = np.count_nonzero(above.reshape(nb, 16384), axis=1)
-    ok = int(cand.sum()) >= k and int(cand.max()) <= slots
-    T = int(np.sort(key)[key.size - k])
-    nxt = 0x7F800000 if T >= 0x7F800000 else int((np.uint32(T).view(np.float32) * HINT_SCALE).view(np.uint32))
-    return ok, nxt
+    short = int(cand.sum()) < k
+    ok = not short and int(cand.max()) <= slots
+    return ok, short, int(np.sort(key)[key.size - k])
+
+
+def _next_hint(T: int, margin: int, ok: bool, short: bool):
+    """The hint and margin word a call leaves: the margin level (bits 0..7;
+    outside the table it counts as 2, with an empty run) widens by one after
+    a call whose candidates fell short of k, and narrows by one after 16
+    calls in a row whose slots served (the run, bits 8..); the hint is the
+    key of T's magnitude times the level's factor, rounded to nearest (the
+    infinity's key for an infinite or NaN T)."""
+    level, run = margin & 0xFF, margin >> 8
+    if level >= HINT_SCALES.size:
+        level, run = 2, 0
+    if ok:
+        run += 1
+        if run >= 16:
+            if level > 0:
+                level, run = level - 1, 0
+            else:
+                run = 16
+    else:
+        run = 0
+        if short and level + 1 < HINT_SCALES.size:
+            level += 1
+    if T >= 0x7F800000:
+        return 0x7F800000, level | run << 8
+    return int((np.uint32(T).view(np.float32) * HINT_SCALES[level]).view(np.uint32)), level | run << 8
 
 
 def test_topk_speculative_first_pass_across_steps():
     # Large enough for pass 1 to compact its candidates speculatively (a warp
     # per tile of 16,384 values). The hint it uses comes from the previous
-    # call on the same workspace: garbage on the first call, far too low
-    # (every tile overflowing) when the gradient scale jumps by 1e3, too high
-    # (fewer than k keys above it) while the residual that jump left decays,
-    # valid again once the threshold holds. The bits must equal the oracle's every step
+    # call on the same workspace: garbage on the first call (too high: the
+    # margin widens), far too low (every tile overflowing) when the gradient
+    # scale jumps by 1e3, valid while the residual that jump left decays and
+    # once the scale holds. The bits must equal the oracle's every step
     # whichever path ran; the path taken (rank 0's spec_ok word in the
     # workspace) and the hint left for the next call must be the ones the
     # rule gives.
@@ -383,7 +407,7 @@ def test_topk_speculative_first_pass_across_steps():
     slots = min(8192, -(-(16 * share + 1024) // 32) * 32)
     ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
     state_hint, state_spec_ok, state_pre2 = 2048 + 9, 2048 + 10, 2048 + 14  # words of rank 0's workspace
-    t_prev = 0x5A5A5A5A
+    t_prev = margin = 0x5A5A5A5A
     hint = 0x5A5A5A5A
     e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
     res = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
@@ -392,10 +416,9 @@ def test_topk_speculative_first_pass_across_steps():
     spec_steps = 0
     for step, scale in enumerate([1.0, 1.0, 1.0, 1e3, 1e-3, 1.0, 1.0, 1.0]):
         g_np = [synthgen.normal_f32(count, 900 + 10 * step + r, 1e-3 * scale) for r in range(n)]
-        a0 = g_np[0] + e_np[0]
-        want_ok, hint = _spec_decision(a0, hint, k, slots)
-        T = int(np.sort(a0.view(np.uint32) & 0x7FFFFFFF)[count - k])
+        want_ok, short, T = _spec_decision(g_np[0] + e_np[0], hint, k, slots)
         want_pre2 = want_ok and (T >> 20) == (t_prev >> 20)  # the previous T's first digit held
+        hint, margin = _next_hint(T, margin, want_ok, short)
         t_prev = T
         grads = [to_dev(x, "f32") for x in g_np]
         gar.ar_topk_compress(grads, res, k, idx, val, ws)
@@ -436,6 +459,49 @@ def test_topk_first_digit_guess_skips_the_split_pass():
             assert np.array_equal(from_dev(idx[r]).view(np.uint32), wi), (call, r)
             assert np.array_equal(_bits(from_dev(val[r])), _bits(wv)), (call, r)
             assert np.array_equal(_bits(from_dev(res[r])), _bits(we)), (call, r)
+
+
+def test_topk_hint_margin_widens_and_narrows():
+    # The margin word of rank 0's state is set by hand between calls to reach
+    # every transition: a run of 16 served calls narrows the level, a run at
+    # the narrowest level stays capped, and a threshold that falls by 3 %
+    # below a 0.99 hint (fewer than k candidates) costs that call the pass
+    # over the data and widens the level. The residual is reset each call, so
+    # a = g * scale; the bits must equal the oracle's on every call.
+    n, count, k = 8, 5_242_880, 52_428
+    share = -(-k * 16384 // count)
+    slots = min(8192, -(-(16 * share + 1024) // 32) * 32)
+    g1 = [synthgen.normal_f32(count, 800 + r, 1e-3) for r in range(n)]
+    inputs = {1.0: g1, 0.97: [x * np.float32(0.97) for x in g1]}
+    zero = np.zeros(count, dtype=np.float32)
+    want = {sc: [oracle.topk_compress(x, zero, k) for x in xs] for sc, xs in inputs.items()}
+    dev = {sc: [to_dev(x, "f32") for x in xs] for sc, xs in inputs.items()}
+    ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
+    words = ws.view(torch.int32)
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    hint, margin = 0x5A5A5A5A, 0x5A5A5A5A
+    # (input scale, margin word written before the call or None, expected spec_ok)
+    plan = [(1.0, None, False), (1.0, 2 | 15 << 8, True), (1.0, 0, True), (0.97, None, False),
+            (0.97, None, True), (0.97, 0 | 15 << 8, True)]
+    for call, (sc, set_margin, want_ok) in enumerate(plan):
+        if set_margin is not None:
+            words[2048 + 15] = set_margin
+            margin = set_margin
+        ok, short, T = _spec_decision(inputs[sc][0], hint, k, slots)
+        assert ok == want_ok, call  # the plan itself follows the rule
+        hint, margin = _next_hint(T, margin, ok, short)
+        res = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+        gar.ar_topk_compress(dev[sc], res, k, idx, val, ws)
+        torch.cuda.synchronize()
+        assert int(words[2048 + 10]) == int(ok), call
+        assert int(words[2048 + 9]) == hint and int(words[2048 + 15]) == margin, (call, hex(margin))
+        for r in range(n):
+            wi, wv, we = want[sc][r]
+            assert np.array_equal(from_dev(idx[r]).view(np.uint32), wi), (call, r)
+            assert np.array_equal(_bits(from_dev(val[r])), _bits(wv)), (call, r)
+            assert np.array_equal(_bits(from_dev(res[r])), _bits(we)), (call, r)
+    assert margin == 0 | 16 << 8  # the last call capped the run at the narrowest level
 
 
 @pytest.mark.parametrize("n", [16, 64])
