@@ -365,7 +365,9 @@ size_t ar_topk_workspace_bytes(int nranks, size_t count, size_t k);
  *     count, k), 16-byte aligned, owned by the caller; its contents need no
  *     initialisation. A call leaves in it its threshold, which the next
  *     call on the same workspace uses to collect its candidates (the values
- *     at or above 0.95 times it) during the pass that forms a = g + e (large
+ *     at or above 0.5 to 0.99 times it, a margin that widens after a call
+ *     whose threshold fell below it and narrows while it holds) during the
+ *     pass that forms a = g + e (large
  *     calls, 16-byte aligned buffers): when at least k values are collected
  *     and they fit, the data is read once instead of twice, and when the
  *     threshold's leading 11 bits also hold, that pass narrows the
