@@ -208,6 +208,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ 
     w.st->spec_overflow = 0;
     w.st->spec_count = 0;
     w.st->pre2 = 0;
+    w.st->mcount = 0;
+    w.st->counted = 0;
   }
   if (A.nb > 0)  // pass 1's second-digit histogram
     for (int i = threadIdx.x; i < 1024; i += blockDim.x) w.masks[i] = 0;
@@ -655,12 +657,18 @@ __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__
   if (last_block(&w.st->ticket[1])) find_digit<1024>(w.hist, 10, w.st);
 }
 
+template <bool GLOBAL>
+__device__ void scan_tiles(const RankWs& w, uint64_t nb, const uint32_t* gt, const uint32_t* eq);
+
 // Pass 3: histogram of bits 9..0 among the keys that match the prefix, read
 // from the slots (or, after an overflow, from the data); then (last block)
 // the last digit, which completes T. From the slots, each tile's run is also
 // compacted in place to the keys at or above the prefix (every key that can
 // still be kept: about the tile's share of k), in index order, so that the
-// count and the emission read only those.
+// count and the emission read only those; and the keys equal to the prefix
+// in its 21 bits (few) are listed, so that the last block, once T is known,
+// derives each tile's counts of keys above and equal to T from its run
+// length and the list, and scans them: the count pass then has nothing to do.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__ TopkArgs A) {
   pdl_enter();
@@ -680,6 +688,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     // before it, never past an entry not yet loaded
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t cap = topk_match_cap(A.nb);
+    uint32_t* list = w.masks + 1024;
     for (uint64_t tile = (uint64_t)blockIdx.x * kWarps + wid; tile < A.nb; tile += (uint64_t)gridDim.x * kWarps) {
       uint32_t* si = slot_idx(w, tile, A.slots);
       float* sv = slot_val(w, tile, A.slots);
@@ -699,7 +709,14 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
         for (int u = 0; u < 8; ++u) {
           const uint32_t key = mag_key(x[u]);
           const bool in = c0 + 32 * u + lane < n;
-          if (in && (key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
+          if (in && (key & mask) == prefix) {
+            atomicAdd(&sh[key & 1023u], 1u);
+            const uint32_t m = atomicAdd(&w.st->mcount, 1u);
+            if (m < cap) {
+              list[2 * m] = ii[u];
+              list[2 * m + 1] = key;
+            }
+          }
           const bool keep = in && key >= prefix;
           const uint32_t bal = __ballot_sync(0xffffffffu, keep);
           if (keep) {
@@ -761,6 +778,35 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
           T >= 0x7F800000u ? 0x7F800000u : __float_as_uint(__fmul_rn(__uint_as_float(T), topk_hint_scale(level)));
       w.st->t_prev = T;
     }
+    __syncthreads();
+    const uint32_t m = __ldcg(&w.st->mcount);
+    if (!w.st->overflow && m <= topk_match_cap(A.nb)) {  // the same for the whole block
+      // each run holds the tile's keys at or above the prefix: all above T
+      // but the listed ones at or below it. Up to 512 tiles the counts stay
+      // in this block's shared memory (the histogram is done with).
+      const uint32_t T = w.st->prefix;
+      const bool smem = A.nb <= 512;
+      uint32_t* gt = smem ? sh : w.n_gt;
+      uint32_t* eq = smem ? sh + 512 : w.n_eq;
+      for (uint64_t t = threadIdx.x; t < A.nb; t += blockDim.x) {
+        gt[t] = __ldcg(w.n_s + t);
+        eq[t] = 0;
+      }
+      __syncthreads();
+      const uint32_t* list = w.masks + 1024;
+      for (uint32_t i = threadIdx.x; i < m; i += blockDim.x) {
+        const uint32_t key = __ldcg(list + 2 * i + 1);
+        const uint64_t t = __ldcg(list + 2 * i) / kTopkBlock;
+        if (key <= T) atomicSub(gt + t, 1u);
+        if (key == T) atomicAdd(eq + t, 1u);
+      }
+      __syncthreads();
+      if (smem)
+        scan_tiles<false>(w, A.nb, gt, eq);
+      else
+        scan_tiles<true>(w, A.nb, gt, eq);
+      if (threadIdx.x == 0) w.st->counted = 1;
+    }
   }
 }
 
@@ -787,26 +833,30 @@ __device__ __forceinline__ uint32_t mask_counts(uint32_t m) {
 
 // The count pass's last block: eq_before[b] = keys equal to T in earlier
 // tiles; out_off[b] = kept elements in earlier tiles, where tile b keeps all
-// its keys above T and min(n_eq[b], max(0, need - eq_before[b])) of its keys
-// equal to T. Each thread scans a contiguous run of tiles.
-__device__ void scan_blocks(const RankWs& w, uint64_t nb) {
+// its keys above T and min(eq[b], max(0, need - eq_before[b])) of its keys
+// equal to T, gt[b] and eq[b] being its keys above and equal to T (global
+// arrays read through L2, or shared memory). Each thread scans a contiguous
+// run of tiles.
+template <bool GLOBAL>
+__device__ void scan_tiles(const RankWs& w, uint64_t nb, const uint32_t* gt, const uint32_t* eq) {
+  auto ld = [](const uint32_t* p) { return GLOBAL ? __ldcg(p) : *p; };
   const uint32_t need = w.st->need;
   const uint64_t m = (nb + kThreads - 1) / kThreads;
   const uint64_t lo = (uint64_t)threadIdx.x * m < nb ? (uint64_t)threadIdx.x * m : nb;
   const uint64_t hi = lo + m < nb ? lo + m : nb;
   uint32_t se = 0;
-  for (uint64_t b = lo; b < hi; ++b) se += __ldcg(w.n_eq + b);
+  for (uint64_t b = lo; b < hi; ++b) se += ld(eq + b);
   const uint32_t eq0 = block_exclusive_scan(se, nullptr);
   auto take_of = [&](uint64_t b, uint32_t eqb) {
-    const uint32_t e = __ldcg(w.n_eq + b);
+    const uint32_t e = ld(eq + b);
     const uint32_t rest = need > eqb ? need - eqb : 0u;
-    return __ldcg(w.n_gt + b) + (e < rest ? e : rest);
+    return ld(gt + b) + (e < rest ? e : rest);
   };
   uint32_t st = 0;
   uint32_t eqb = eq0;
   for (uint64_t b = lo; b < hi; ++b) {
     st += take_of(b, eqb);
-    eqb += __ldcg(w.n_eq + b);
+    eqb += ld(eq + b);
   }
   uint32_t off = block_exclusive_scan(st, nullptr);
   eqb = eq0;
@@ -815,18 +865,20 @@ __device__ void scan_blocks(const RankWs& w, uint64_t nb) {
     w.eq_before[b] = eqb;
     w.out_off[b] = off;
     off += t;
-    eqb += __ldcg(w.n_eq + b);
+    eqb += ld(eq + b);
   }
 }
 
-// Keys above T and equal to T per tile. From the slots: one warp per tile.
-// After an overflow: the block takes its kWarps tiles one after another from
-// the data, writing the run masks. The last block scans all tiles' counts.
+// Keys above T and equal to T per tile, unless pass 3 derived them. From the
+// slots: one warp per tile. After an overflow: the block takes its kWarps
+// tiles one after another from the data, writing the run masks. The last
+// block scans all tiles' counts.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
   pdl_enter();
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
+  if (w.st->counted) return;  // pass 3 did it (the same for the whole block)
   const uint32_t T = w.st->prefix;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (!w.st->overflow) {
@@ -881,7 +933,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__
       }
     }
   }
-  if (last_block(&w.st->ticket[3])) scan_blocks(w, A.nb);
+  if (last_block(&w.st->ticket[3])) scan_tiles<true>(w, A.nb, w.n_gt, w.n_eq);
 }
 
 // Emission from the slots, one warp per tile: the slots are in index order,

@@ -26,12 +26,14 @@ constexpr uint32_t kTopkMaxSlots = 8192;                       // slot cap per t
 //   tile's slots overflow): for the kTopkElems values of a run, bit j (j < 16)
 //   set if value j's key is above T, bit 16 + j if it equals T; the first
 //   1024 of them also hold the speculative pass 1's second-digit histogram
-//   (consumed before any mask is written)
+//   (consumed before any mask is written), the next ones pass 3's match
+//   list (topk_match_cap entries of two words; masks are written only when
+//   the list is not used)
 //   then per tile 2 * S words of slots: the indices, then the values, of the
 //   tile's keys at or above the first digit's bin (every key that can be
 //   kept), in index order; n_s[tile] of them
 constexpr int kTopkHistWords = 2048;
-constexpr int kTopkStateWords = 16;
+constexpr int kTopkStateWords = 32;
 // The next call's hint is T's magnitude times the factor of a margin level
 // (rounded to nearest): a call whose candidates fell short of k (T dropped
 // below its hint) widens the margin one level, kTopkTightenRun calls in a
@@ -49,6 +51,13 @@ __host__ __device__ inline float topk_hint_scale(uint32_t level) {
     case 4: return 0.8f;
     default: return 0.5f;
   }
+}
+
+// Entries of pass 3's match list: what the run masks hold past the second-
+// digit histogram, at most 4096.
+__host__ __device__ inline uint32_t topk_match_cap(uint64_t nb) {
+  const uint64_t room = nb * 1024 > 1024 ? (nb * 1024 - 1024) / 2 : 0;
+  return room < 4096 ? (uint32_t)room : 4096u;
 }
 
 inline uint64_t topk_blocks(uint64_t count) { return (count + kTopkBlock - 1) / kTopkBlock; }
@@ -103,6 +112,10 @@ inline uint64_t topk_rank_words(uint64_t count, uint64_t k) {
 //   margin:      bits 0..7 the level of the hint's factor (topk_hint_scale),
 //                bits 8.. the run of calls since it last changed that kept
 //                their candidates in the slots; kept from call to call
+//   mcount:      keys pass 3 found equal to the two-digit prefix (listed,
+//                index and key, while they fit the match list)
+//   counted:     pass 3's last block derived the per-tile counts and their
+//                scans from the match list: the count pass is skipped
 struct TopkState {
   uint32_t prefix;
   uint32_t mask;
@@ -117,6 +130,9 @@ struct TopkState {
   uint32_t t_prev;
   uint32_t pre2;
   uint32_t margin;
+  uint32_t mcount;
+  uint32_t counted;
+  uint32_t pad[14];
 };
 static_assert(sizeof(TopkState) == kTopkStateWords * 4, "state size");
 

@@ -233,7 +233,7 @@ def test_topk_workspace_and_argument_errors(L):
     nb = math.ceil(count / 16384)
     share = math.ceil(k10 * 16384 / count)
     slots = min(16384, 8192, math.ceil((16 * share + 1024) / 32) * 32)
-    assert need == n * math.ceil((2048 + 16 + (5 + 1024) * nb + 2 * slots * nb) / 64) * 64 * 4
+    assert need == n * math.ceil((2048 + 32 + (5 + 1024) * nb + 2 * slots * nb) / 64) * 64 * 4
     assert gar.ar_topk_workspace_bytes(1, 1 << 32, 1) == 0 and gar.ar_topk_workspace_bytes(0, 10, 1) == 0
     assert gar.ar_topk_workspace_bytes(1, 10, 11) == 0
     # at most about 4.25 bytes per value plus the fixed part, whatever k is

@@ -123,6 +123,33 @@ def test_topk_heavy_ties_and_signed_zeros(offset):
         _check_against_oracle(g, e, k, offset)
 
 
+@pytest.mark.parametrize("every,k,listed", [(600, 200, True), (40, 2000, False)])
+def test_topk_match_list_with_ties(every, k, listed):
+    # Ties at +-0.5 spread over every tile hold the threshold, all else is
+    # small: the keys equal to T's two-digit prefix are the ties. With 334 of
+    # them pass 3 lists them and derives the per-tile counts itself (the ties
+    # kept in index order across tiles); with 5,000 the list overflows while
+    # the slots still fit, and the count pass reads the slots instead.
+    count = 200_000
+    g = synthgen.normal_f32(count, 61, 1e-3)
+    pos = np.arange(0, count, every)
+    g[pos] = np.where(pos % 3 == 0, -0.5, 0.5).astype(np.float32)
+    e = np.zeros(count, dtype=np.float32)
+    ws = torch.full((gar.ar_topk_workspace_bytes(1, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
+    res = [to_dev(e, "f32")]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda")]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda")]
+    gar.ar_topk_compress([to_dev(g, "f32")], res, k, idx, val, ws)
+    torch.cuda.synchronize()
+    words = ws.view(torch.int32)
+    assert int(words[2048 + 8]) == 0  # no slot overflow
+    assert int(words[2048 + 16]) == pos.size and int(words[2048 + 17]) == int(listed)
+    oi, ov, oe = oracle.topk_compress(g, e, k)
+    assert np.array_equal(from_dev(idx[0]).view(np.uint32), oi)
+    assert np.array_equal(_bits(from_dev(val[0])), _bits(ov))
+    assert np.array_equal(_bits(from_dev(res[0])), _bits(oe))
+
+
 def test_topk_one_overflowing_tile():
     # a block of equal magnitudes inside one tile holds the threshold: that
     # tile's candidates overflow their slots while every other tile's fit
@@ -454,6 +481,7 @@ def test_topk_first_digit_guess_skips_the_split_pass():
         torch.cuda.synchronize()
         words = ws.view(torch.int32)
         assert int(words[2048 + 10]) == int(call > 0) and int(words[2048 + 14]) == int(call > 0), call
+        assert int(words[2048 + 17]) == 1, call  # pass 3 derived the counts
         for r in range(n):
             wi, wv, we = want[r]
             assert np.array_equal(from_dev(idx[r]).view(np.uint32), wi), (call, r)
