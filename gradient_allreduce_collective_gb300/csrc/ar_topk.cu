@@ -690,6 +690,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     const uint32_t lt = (1u << lane) - 1u;
     const uint32_t cap = topk_match_cap(A.nb);
     uint32_t* list = w.masks + 1024;
+    const float* er = A.e[r];
     for (uint64_t tile = (uint64_t)blockIdx.x * kWarps + wid; tile < A.nb; tile += (uint64_t)gridDim.x * kWarps) {
       uint32_t* si = slot_idx(w, tile, A.slots);
       float* sv = slot_val(w, tile, A.slots);
@@ -723,6 +724,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
             const uint32_t p = kept + (uint32_t)__popc(bal & lt);
             si[p] = ii[u];
             sv[p] = x[u];
+            // the emission zeroes this residual: bring its sector into L2 now
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(er + ii[u]));
           }
           kept += (uint32_t)__popc(bal);
         }
