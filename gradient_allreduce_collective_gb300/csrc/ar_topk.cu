@@ -59,6 +59,11 @@ __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
+// Only the wait: the kernel's dependents launch as its blocks exit. For a
+// grid of many waves whose dependents would otherwise hold SM resources,
+// waiting, while its last waves still need them.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Launch with programmatic stream serialization allowed.
 template <typename... KArgs, typename... Args>
 cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
@@ -1096,12 +1101,17 @@ __global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constan
   for (int64_t t = prev + 1; t <= cur; ++t) st[t] = (uint32_t)j;
 }
 
+// resident blocks of k_sparse_fold (32 KiB of shared memory each): the ring
+// order fits 32 registers; the recursive halving takes what it needs
+template <bool TREE> constexpr int kSparseBlocksPerSm = TREE ? 1 : 7;
+
 // One tile per block: every rank's pairs of the tile scattered into shared
 // memory (zeros elsewhere), folded per element in the ring order of its
 // chunk (or recursive halving), divided by N for AVG, and stored to all N
 // outputs. The dense allreduce of the densified vectors gives the same bits.
-__global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant__ SparseArgs A) {
-  pdl_enter();
+template <bool TREE>
+__global__ void __launch_bounds__(kThreads, kSparseBlocksPerSm<TREE>) k_sparse_fold(const __grid_constant__ SparseArgs A) {
+  pdl_wait();  // six waves: the next call's kernels launch as its last blocks exit
   extern __shared__ float sm[];  // nranks x tile
   const int N = A.nranks;
   const uint32_t T = A.tile;
@@ -1145,7 +1155,7 @@ __global__ void __launch_bounds__(kThreads) k_sparse_fold(const __grid_constant_
   for (uint32_t q = threadIdx.x; q * 4 < len; q += blockDim.x) {
     const uint64_t i = i0 + 4ull * q;
     float4 acc;
-    if (A.tree) {
+    if (TREE) {
       for (int d = N >> 1; d >= 1; d >>= 1)
         for (int r = 0; r < d; ++r) {
           const float4 x = s4[(uint32_t)r * T4 + q], y = s4[(uint32_t)(r + d) * T4 + q];
@@ -1222,7 +1232,9 @@ cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream) {
 cudaError_t launch_sparse_fold(const SparseArgs& a, uint64_t max_nnz, cudaStream_t stream) {
   const cudaError_t err = pdl_launch(k_sparse_bounds, dim3(grid_for(max_nnz + 1), a.nranks), 0, stream, a);
   if (err != cudaSuccess) return err;
-  return pdl_launch(k_sparse_fold, dim3(a.ntiles), (size_t)a.nranks * a.tile * sizeof(float), stream, a);
+  const size_t smem = (size_t)a.nranks * a.tile * sizeof(float);
+  return a.tree ? pdl_launch(k_sparse_fold<true>, dim3(a.ntiles), smem, stream, a)
+                : pdl_launch(k_sparse_fold<false>, dim3(a.ntiles), smem, stream, a);
 }
 
 cudaError_t launch_sparse_scatter(const ScatterArgs& a, cudaStream_t stream) {
