@@ -1102,8 +1102,9 @@ __global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constan
 }
 
 // resident blocks of k_sparse_fold (32 KiB of shared memory each): the ring
-// order fits 32 registers; the recursive halving takes what it needs
-template <bool TREE> constexpr int kSparseBlocksPerSm = TREE ? 1 : 7;
+// order fits 32 registers, the recursive halving 48 (a 12-byte spill,
+// measured faster than 64 registers at 4 blocks)
+template <bool TREE> constexpr int kSparseBlocksPerSm = TREE ? 5 : 7;
 
 // One tile per block: every rank's pairs of the tile scattered into shared
 // memory (zeros elsewhere), folded per element in the ring order of its
