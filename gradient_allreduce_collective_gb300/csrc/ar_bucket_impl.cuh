@@ -85,6 +85,7 @@ __device__ __forceinline__ void bucket_item(const BucketArgs& A, int t, uint64_t
 
 template <int DT, int OP, int MODE, int MAXN>
 __global__ void __launch_bounds__(kThreads) k_bucket_reduce(const __grid_constant__ BucketArgs A) {
+  pdl_begin();
   constexpr int V = 16 / Fmt<DT>::bytes;
   const uint32_t total = A.tile_start[A.nt];
   for (uint32_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -118,8 +119,8 @@ cudaError_t launch_bucket_t(const BucketArgs& a, cudaStream_t stream) {
   const uint32_t total = a.tile_start[a.nt];
   if (total == 0) return cudaSuccess;
   const unsigned grid = total < 0x7FFFFFFFu ? total : 0x7FFFFFFFu;  // one block per tile
-  if (a.nranks <= 8) k_bucket_reduce<DT, OP, MODE, 8><<<grid, kThreads, 0, stream>>>(a);
-  else k_bucket_reduce<DT, OP, MODE, kMaxRanks><<<grid, kThreads, 0, stream>>>(a);
+  if (a.nranks <= 8) launch_pdl(k_bucket_reduce<DT, OP, MODE, 8>, dim3(grid), 0, stream, a);
+  else launch_pdl(k_bucket_reduce<DT, OP, MODE, kMaxRanks>, dim3(grid), 0, stream, a);
   return cudaGetLastError();
 }
 

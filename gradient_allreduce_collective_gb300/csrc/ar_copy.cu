@@ -34,6 +34,7 @@ template <int U> __device__ __forceinline__ void st_unit(void* p, typename Unit<
 
 template <int U>
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ GatherArgs A) {
+  pdl_begin();
   const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t nt = (uint64_t)gridDim.x * blockDim.x;
   const int N = A.nranks;
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
 
 template <int U> cudaError_t launch_gather_u(const GatherArgs& a, cudaStream_t stream) {
   const uint64_t items = a.units > a.tail_bytes ? a.units : a.tail_bytes;
-  k_gather<U><<<grid_for(items), kThreads, 0, stream>>>(a);
+  launch_pdl(k_gather<U>, dim3(grid_for(items)), 0, stream, a);
   return cudaGetLastError();
 }
 
@@ -85,6 +86,7 @@ cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stre
 
 // One block copies one kCopyTile-byte tile at a time; 4 x 16 bytes in flight per thread.
 __global__ void __launch_bounds__(kThreads) k_multicopy(const __grid_constant__ MultiCopyArgs A) {
+  pdl_begin();
   const uint32_t total = A.tile_start[A.nitems];
   for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
     int lo = 0, hi = A.nitems - 1;  // last item whose first tile is <= t
@@ -124,7 +126,7 @@ cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream) {
   if (total == 0) return cudaSuccess;
   // one block per tile
   const unsigned grid = total < 0x7FFFFFFFu ? total : 0x7FFFFFFFu;
-  k_multicopy<<<grid, kThreads, 0, stream>>>(a);
+  launch_pdl(k_multicopy, dim3(grid), 0, stream, a);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,7 @@ constexpr int kQuantUnroll = 8;
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constant__ Fp8QuantArgs A) {
+  pdl_begin();
   constexpr int B = Fmt<DT>::bytes, V = 16 / B, G = kFp8Block / V, BPW = 32 / G;
   const int r = blockIdx.y;
   const uint64_t nfull = A.count / kFp8Block;
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constan
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_fp8_quant_scalar(const __grid_constant__ Fp8QuantArgs A) {
+  pdl_begin();
   constexpr int B = Fmt<DT>::bytes;
   const uint64_t nblocks = (A.count + kFp8Block - 1) / kFp8Block;
   const uint64_t nb = nblocks - A.first_block;
@@ -115,7 +117,7 @@ template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& 
     if (nfull > 0) {
       const uint64_t warps = (nfull + kQuantUnroll * BPW - 1) / (kQuantUnroll * BPW);
       const dim3 grid(grid_for(warps * 32), (unsigned)a.nranks);
-      k_fp8_quant_vec<DT><<<grid, kThreads, 0, stream>>>(a);
+      launch_pdl(k_fp8_quant_vec<DT>, dim3(grid), 0, stream, a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -125,7 +127,7 @@ template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& 
   }
   if (b.first_block < nblocks) {
     const uint64_t warps = (uint64_t)a.nranks * (nblocks - b.first_block);
-    k_fp8_quant_scalar<DT><<<grid_for(warps * 32), kThreads, 0, stream>>>(b);
+    launch_pdl(k_fp8_quant_scalar<DT>, dim3(grid_for(warps * 32)), 0, stream, b);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -235,6 +237,7 @@ __device__ __forceinline__ void fp8_range(const Fp8ReduceArgs& A, uint64_t t0, u
 
 template <int ODT, int OP, int MODE, int MAXN>
 __global__ void __launch_bounds__(kThreads) k_fp8_reduce(const __grid_constant__ Fp8ReduceArgs A) {
+  pdl_begin();
   const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t nt = (uint64_t)gridDim.x * blockDim.x;
   if (A.vec) {
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_reduce(const __grid_constant__
 template <int ODT, int OP, int MODE, int MAXN>
 cudaError_t launch_fp8_reduce_n(const Fp8ReduceArgs& a, cudaStream_t stream) {
   const uint64_t items = a.vec ? a.count / (16 / Fmt<ODT>::bytes) : a.count;
-  k_fp8_reduce<ODT, OP, MODE, MAXN><<<grid_for(items > 0 ? items : a.count), kThreads, 0, stream>>>(a);
+  launch_pdl(k_fp8_reduce<ODT, OP, MODE, MAXN>, dim3(grid_for(items > 0 ? items : a.count)), 0, stream, a);
   return cudaGetLastError();
 }
 

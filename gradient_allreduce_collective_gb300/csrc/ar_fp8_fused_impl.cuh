@@ -71,6 +71,7 @@ template <int IDT> struct Fp8FusedLd {
 
 template <int IDT, int ODT, int OP, int MODE, int MAXN>
 __global__ void __launch_bounds__(kThreads, MODE == MODE_FUSED_TREE ? 1 : 4) k_fp8_fused_vec(const __grid_constant__ Fp8FusedArgs A) {
+  pdl_begin();
   using Ld = Fp8FusedLd<IDT>;
   constexpr int V = Ld::V, G = Ld::G, BPW = 32 / G, OB = Fmt<ODT>::bytes;
   const int N = A.nranks;
@@ -210,6 +211,7 @@ constexpr int kFusedPairBlocksPerSm = 3;
 
 template <int IDT, int ODT, int OP, int MAXN>
 __global__ void __launch_bounds__(kThreads, kFusedPairBlocksPerSm) k_fp8_fused_pair(const __grid_constant__ Fp8FusedArgs A) {
+  pdl_begin();
   static_assert(Fmt<IDT>::bytes == 2, "16-bit inputs");
   const int N = A.nranks;
   const uint64_t nfull = A.count / kFp8Block;
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, kFusedPairBlocksPerSm) k_fp8_fused_p
 
 template <int IDT, int ODT, int OP, int MODE, int MAXN>
 __global__ void __launch_bounds__(kThreads) k_fp8_fused_elem(const __grid_constant__ Fp8FusedArgs A) {
+  pdl_begin();
   constexpr int IB = Fmt<IDT>::bytes, OB = Fmt<ODT>::bytes;
   const int N = A.nranks;
   const uint64_t nblocks = (A.count + kFp8Block - 1) / kFp8Block;
@@ -316,9 +319,9 @@ cudaError_t launch_fused_n(bool vec, const Fp8FusedArgs& a, cudaStream_t stream)
     if (nfull > 0) {
       const uint64_t warps = (nfull + BPW - 1) / BPW;
       if constexpr (MODE == MODE_FUSED_RING && Fmt<IDT>::bytes == 2)
-        k_fp8_fused_pair<IDT, ODT, OP, MAXN><<<grid_for(warps * 32), kThreads, 0, stream>>>(a);
+        launch_pdl(k_fp8_fused_pair<IDT, ODT, OP, MAXN>, dim3(grid_for(warps * 32)), 0, stream, a);
       else
-        k_fp8_fused_vec<IDT, ODT, OP, MODE, MAXN><<<grid_for(warps * 32), kThreads, 0, stream>>>(a);
+        launch_pdl(k_fp8_fused_vec<IDT, ODT, OP, MODE, MAXN>, dim3(grid_for(warps * 32)), 0, stream, a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -326,7 +329,7 @@ cudaError_t launch_fused_n(bool vec, const Fp8FusedArgs& a, cudaStream_t stream)
   const uint64_t nblocks = (a.count + kFp8Block - 1) / kFp8Block;
   const uint64_t tasks = (uint64_t)a.nlist + (nblocks - a.first_block);
   if (tasks == 0) return cudaSuccess;
-  k_fp8_fused_elem<IDT, ODT, OP, MODE, MAXN><<<grid_for(tasks * 32), kThreads, 0, stream>>>(a);
+  launch_pdl(k_fp8_fused_elem<IDT, ODT, OP, MODE, MAXN>, dim3(grid_for(tasks * 32)), 0, stream, a);
   return cudaGetLastError();
 }
 

@@ -256,6 +256,7 @@ constexpr int kHopBlocksPerSm = 3;
 // its start), the resident grid's warps looping over the pairs.
 template <int IDT, int ODT, int OP, int MAXN, bool VEC>
 __global__ void __launch_bounds__(kThreads, kHopBlocksPerSm) k_fp8_hop(const __grid_constant__ Fp8HopArgs A) {
+  pdl_begin();
   const int N = A.nranks;
   const int lane = threadIdx.x & 31;
   const uint64_t npairs = (A.nbc + 1) / 2;
@@ -300,8 +301,8 @@ cudaError_t launch_hop_op(const Fp8HopArgs& a, cudaStream_t s) {
     vec = vec && reinterpret_cast<uintptr_t>(a.src[r]) % (4 * Fmt<IDT>::bytes) == 0 &&
           reinterpret_cast<uintptr_t>(a.dst[r]) % (4 * Fmt<ODT>::bytes) == 0;
 #define GAR_HOP(MAXNV)                                                        \
-  if (vec) k_fp8_hop<IDT, ODT, OP, MAXNV, true><<<grid, kThreads, 0, s>>>(a); \
-  else k_fp8_hop<IDT, ODT, OP, MAXNV, false><<<grid, kThreads, 0, s>>>(a);
+  if (vec) launch_pdl(k_fp8_hop<IDT, ODT, OP, MAXNV, true>, dim3(grid), 0, s, a); \
+  else launch_pdl(k_fp8_hop<IDT, ODT, OP, MAXNV, false>, dim3(grid), 0, s, a);
   if (a.nranks <= 8) {
     GAR_HOP(8)
   } else if (a.nranks <= 16) {

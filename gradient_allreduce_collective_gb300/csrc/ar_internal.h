@@ -186,4 +186,34 @@ inline unsigned grid_for(uint64_t items) {
   return (unsigned)(need > 0 ? need : 1);
 }
 
+#ifdef __CUDACC__
+// First statement of a kernel launched by launch_pdl: wait until the previous
+// grid in the stream has completed and its writes are visible (a no-op after
+// an ordinary launch), then let the next grid be placed on the SMs this
+// grid's last wave frees, so that it starts as soon as this one completes.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+#endif
+
+// Launch with programmatic stream serialization: the grid may be placed on
+// the SMs while the previous grid in the stream finishes. The kernel must
+// call pdl_begin() before it touches memory that an earlier kernel writes or
+// reads; stream order and results stay as for <<<...>>>.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace gar

@@ -98,12 +98,7 @@ __device__ __forceinline__ void reduce_range(const ReduceArgs& A, uint64_t t0, u
 
 template <int DT, int OP, int MODE, int MAXN>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ ReduceArgs A) {
-  // programmatic dependent launch: wait until the previous grid in the
-  // stream has completed (its writes visible), then let the next one be
-  // placed on the SMs that this grid's last wave frees, so that it starts as
-  // soon as this one completes
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" :::);
+  pdl_begin();
   const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t nt = (uint64_t)gridDim.x * blockDim.x;
   if (A.vec) {
@@ -125,17 +120,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Red
 template <int DT, int OP, int MODE, int MAXN>
 cudaError_t launch_reduce_n(const ReduceArgs& a, cudaStream_t stream) {
   const uint64_t items = a.vec ? a.count / (16 / Fmt<DT>::bytes) : a.count;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid_for(items > 0 ? items : a.count));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_reduce<DT, OP, MODE, MAXN>, a);
+  return launch_pdl(k_reduce<DT, OP, MODE, MAXN>, dim3(grid_for(items > 0 ? items : a.count)), 0, stream, a);
 }
 
 template <int DT, int OP, int MODE>

@@ -24,6 +24,7 @@ template <class Acc> __device__ __forceinline__ uint32_t partial_bits(Acc v) {
 
 template <int DT, int OP>
 __global__ void __launch_bounds__(kThreads) k_step_combine(const __grid_constant__ StepArgs A) {
+  pdl_begin();
   using R = Red<DT, OP>;
   constexpr int B = Fmt<DT>::bytes;
   constexpr int V = 16 / B;
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) k_step_combine(const __grid_constant
 template <int DT, int OP> cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
   const uint32_t total = a.tile_start[a.ntasks];
   if (total == 0) return cudaSuccess;
-  k_step_combine<DT, OP><<<total, kThreads, 0, s>>>(a);  // one block per tile
+  launch_pdl(k_step_combine<DT, OP>, dim3(total), 0, s, a);  // one block per tile
   return cudaGetLastError();
 }
 
@@ -129,6 +130,7 @@ __device__ __forceinline__ typename Red<DT, OP>::Acc load1(const void* base, uin
 
 template <int DT, int OP, bool A32, bool B32, bool FIN>
 __global__ void __launch_bounds__(kThreads) k_step_combine16(const __grid_constant__ StepArgs A) {
+  pdl_begin();
   using R = Red<DT, OP>;
   using Acc = typename R::Acc;
   const uint32_t total = A.tile_start[A.ntasks];
@@ -173,8 +175,8 @@ template <int DT, int OP, bool A32, bool B32>
 cudaError_t launch_step16_ab(bool fin, const StepArgs& a, cudaStream_t s) {
   const uint32_t total = a.tile_start[a.ntasks];
   if (total == 0) return cudaSuccess;
-  if (fin) k_step_combine16<DT, OP, A32, B32, true><<<total, kThreads, 0, s>>>(a);
-  else k_step_combine16<DT, OP, A32, B32, false><<<total, kThreads, 0, s>>>(a);
+  if (fin) launch_pdl(k_step_combine16<DT, OP, A32, B32, true>, dim3(total), 0, s, a);
+  else launch_pdl(k_step_combine16<DT, OP, A32, B32, false>, dim3(total), 0, s, a);
   return cudaGetLastError();
 }
 

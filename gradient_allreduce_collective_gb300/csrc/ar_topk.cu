@@ -50,35 +50,13 @@ constexpr int kSpecBlocksPerSm = 3;   // k_topk_pass1_spec keeps 16 float4 loads
 
 __device__ __forceinline__ uint32_t mag_key(float a) { return __float_as_uint(a) & 0x7FFFFFFFu; }
 
-// Programmatic dependent launch: every kernel here is launched so that it may
-// be scheduled while the previous kernel on the stream drains; it waits for
-// that kernel's completion (and its memory) before touching global memory,
-// then lets its own dependents be scheduled.
-__device__ __forceinline__ void pdl_enter() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" :::);
-}
+// Programmatic dependent launch: every kernel here is launched by launch_pdl
+// and begins with pdl_begin (ar_internal.h), or with pdl_wait.
 
 // Only the wait: the kernel's dependents launch as its blocks exit. For a
 // grid of many waves whose dependents would otherwise hold SM resources,
 // waiting, while its last waves still need them.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Launch with programmatic stream serialization allowed.
-template <typename... KArgs, typename... Args>
-cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
 
 constexpr int kWarps = kThreads / 32;  // tiles per block in the slot-reading passes
 
@@ -199,7 +177,7 @@ __device__ void find_digit(uint32_t* hist, int shift, TopkState* st) {
 }
 
 __global__ void __launch_bounds__(kThreads) k_topk_init(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
+  pdl_begin();
   const RankWs w = rank_ws(A, blockIdx.y);
   for (int i = threadIdx.x; i < kTopkHistWords; i += blockDim.x) w.hist[i] = 0;
   if (threadIdx.x == 0) {
@@ -228,7 +206,7 @@ __device__ __forceinline__ float4 add4(float4 x, float4 y) {
 // block, if k > 0) the first digit.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads, kPass1BlocksPerSm) k_topk_pass1(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
+  pdl_begin();
   __shared__ uint32_t sh[2048];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
@@ -397,7 +375,7 @@ __device__ __forceinline__ void spec_round(const float* __restrict__ g, float* _
 }
 
 __global__ void __launch_bounds__(kThreads, kSpecBlocksPerSm) k_topk_pass1_spec(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
+  pdl_begin();
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   const float* __restrict__ g = A.g[r];
@@ -557,7 +535,7 @@ __device__ __forceinline__ void run_positions(const uint32_t (&m)[kTopkRuns], ui
 // from the cache.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_split(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
+  pdl_begin();
   __shared__ uint32_t sh[1024];
   __shared__ uint32_t tot[2 * kWarps * 4];
   int parity = 0;
@@ -676,7 +654,7 @@ __device__ void scan_tiles(const RankWs& w, uint64_t nb, const uint32_t* gt, con
 // length and the list, and scans them: the count pass then has nothing to do.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
+  pdl_begin();
   __shared__ uint32_t sh[1024];
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
@@ -883,7 +861,7 @@ __device__ void scan_tiles(const RankWs& w, uint64_t nb, const uint32_t* gt, con
 // block scans all tiles' counts.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_topk_count(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
+  pdl_begin();
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   if (w.st->counted) return;  // pass 3 did it (the same for the whole block)
@@ -1045,7 +1023,7 @@ __device__ void emit_masks(const TopkArgs& A, const RankWs& w, int r, uint64_t t
 // Kept elements to (index, value) in index order; zero their residual. Each
 // block covers kWarps tiles.
 __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ TopkArgs A) {
-  pdl_enter();
+  pdl_begin();
   const int r = blockIdx.y;
   const RankWs w = rank_ws(A, r);
   if (!w.st->overflow) {
@@ -1061,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_emit(const __grid_constant__ 
 
 // recv[r][idx_r[j]] = val_r[j] for every rank (outputs already zeroed)
 __global__ void __launch_bounds__(kThreads) k_sparse_scatter(const __grid_constant__ ScatterArgs A) {
-  pdl_enter();
+  pdl_begin();
   const uint32_t total = A.tile_start[A.nranks];
   for (uint32_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
     int lo = 0, hi = A.nranks - 1;
@@ -1084,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads) k_sparse_scatter(const __grid_consta
 // ntiles). With ascending indices every entry is written once; otherwise the
 // fold clamps what it reads.
 __global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constant__ SparseArgs A) {
-  pdl_enter();
+  pdl_begin();
   const int r = blockIdx.y;
   const uint64_t nnz = A.nnz[r];
   const uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1191,7 +1169,7 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   cudaError_t err = sm_count(&sms);
   if (err != cudaSuccess) return err;
   const dim3 one(1, a.nranks);
-  err = pdl_launch(k_topk_init, one, 0, s, a);
+  err = launch_pdl(k_topk_init, one, 0, s, a);
   if (err != cudaSuccess) return err;
   // histogram passes over the data: a resident grid looping over it, so that
   // each block flushes its shared histogram once
@@ -1208,20 +1186,20 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
   if (VEC && a.k > 0 && a.nb * (uint64_t)a.nranks >= (uint64_t)sms * 16) {
     unsigned sbx = (unsigned)(sms * kSpecBlocksPerSm / a.nranks);
     if (sbx < 1) sbx = 1;
-    err = pdl_launch(k_topk_pass1_spec, dim3(sbx, a.nranks), 0, s, a);
+    err = launch_pdl(k_topk_pass1_spec, dim3(sbx, a.nranks), 0, s, a);
   } else {
-    err = pdl_launch(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);
+    err = launch_pdl(k_topk_pass1<VEC>, dim3(p1x, a.nranks), 0, s, a);
   }
   if (err != cudaSuccess) return err;
   if (a.k == 0) return cudaSuccess;  // nothing kept: e = a
   unsigned sx = (unsigned)(sms * kSplitBlocksPerSm / a.nranks);
   if (sx < 1) sx = 1;
   if (sx > a.nb) sx = (unsigned)a.nb;
-  if ((err = pdl_launch(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) return err;
-  if ((err = pdl_launch(k_topk_pass3<VEC>, hgrid, 0, s, a)) != cudaSuccess) return err;
+  if ((err = launch_pdl(k_topk_split<VEC>, dim3(sx, a.nranks), 0, s, a)) != cudaSuccess) return err;
+  if ((err = launch_pdl(k_topk_pass3<VEC>, hgrid, 0, s, a)) != cudaSuccess) return err;
   const dim3 wgrid((unsigned)((a.nb + kWarps - 1) / kWarps), a.nranks);
-  if ((err = pdl_launch(k_topk_count<VEC>, wgrid, 0, s, a)) != cudaSuccess) return err;
-  return pdl_launch(k_topk_emit, wgrid, 0, s, a);
+  if ((err = launch_pdl(k_topk_count<VEC>, wgrid, 0, s, a)) != cudaSuccess) return err;
+  return launch_pdl(k_topk_emit, wgrid, 0, s, a);
 }
 
 }  // namespace
@@ -1231,11 +1209,11 @@ cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream) {
 }
 
 cudaError_t launch_sparse_fold(const SparseArgs& a, uint64_t max_nnz, cudaStream_t stream) {
-  const cudaError_t err = pdl_launch(k_sparse_bounds, dim3(grid_for(max_nnz + 1), a.nranks), 0, stream, a);
+  const cudaError_t err = launch_pdl(k_sparse_bounds, dim3(grid_for(max_nnz + 1), a.nranks), 0, stream, a);
   if (err != cudaSuccess) return err;
   const size_t smem = (size_t)a.nranks * a.tile * sizeof(float);
-  return a.tree ? pdl_launch(k_sparse_fold<true>, dim3(a.ntiles), smem, stream, a)
-                : pdl_launch(k_sparse_fold<false>, dim3(a.ntiles), smem, stream, a);
+  return a.tree ? launch_pdl(k_sparse_fold<true>, dim3(a.ntiles), smem, stream, a)
+                : launch_pdl(k_sparse_fold<false>, dim3(a.ntiles), smem, stream, a);
 }
 
 cudaError_t launch_sparse_scatter(const ScatterArgs& a, cudaStream_t stream) {
