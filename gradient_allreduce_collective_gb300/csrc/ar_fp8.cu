@@ -29,7 +29,7 @@ namespace gar {
 constexpr int kQuantUnroll = 8;
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constant__ Fp8QuantArgs A) {
+__device__ __forceinline__ void fp8_quant_vec_body(const Fp8QuantArgs& A) {
   pdl_begin();
   constexpr int B = Fmt<DT>::bytes, V = 16 / B, G = kFp8Block / V, BPW = 32 / G;
   const int r = blockIdx.y;
@@ -67,6 +67,19 @@ __global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constan
       if (gl == 0) A.s[r][b] = s;
     }
   }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_fp8_quant_vec(const __grid_constant__ Fp8QuantArgs A) {
+  fp8_quant_vec_body<DT>(A);
+}
+
+// 16-bit inputs at 5 resident blocks per SM (48 registers, a 16-byte spill,
+// against 4 blocks at 63): materialised step 2.013 -> 1.987 ms. The binary32
+// input kernel already fits 5 blocks at 49 registers and keeps k_fp8_quant_vec.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 5) k_fp8_quant_vec16(const __grid_constant__ Fp8QuantArgs A) {
+  fp8_quant_vec_body<DT>(A);
 }
 
 template <int DT>
@@ -117,7 +130,10 @@ template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& 
     if (nfull > 0) {
       const uint64_t warps = (nfull + kQuantUnroll * BPW - 1) / (kQuantUnroll * BPW);
       const dim3 grid(grid_for(warps * 32), (unsigned)a.nranks);
-      launch_pdl(k_fp8_quant_vec<DT>, dim3(grid), 0, stream, a);
+      if constexpr (Fmt<DT>::bytes == 2)
+        launch_pdl(k_fp8_quant_vec16<DT>, grid, 0, stream, a);
+      else
+        launch_pdl(k_fp8_quant_vec<DT>, grid, 0, stream, a);
       const cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
