@@ -666,9 +666,10 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
     if ((key & mask) == prefix) atomicAdd(&sh[key & 1023u], 1u);
   };
   if (!w.st->overflow) {
-    // one warp per tile, eight slots (index and value) loaded per lane before
+    // one warp per tile, kP3 slots (index and value) loaded per lane before
     // any is written back: a kept entry moves to the count of kept entries
     // before it, never past an entry not yet loaded
+    constexpr int kP3 = 16;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const uint32_t lt = (1u << lane) - 1u;
     const uint32_t cap = topk_match_cap(A.nb);
@@ -679,18 +680,18 @@ __global__ void __launch_bounds__(kThreads) k_topk_pass3(const __grid_constant__
       float* sv = slot_val(w, tile, A.slots);
       const uint32_t n = w.n_s[tile];
       uint32_t kept = 0;
-      for (uint32_t c0 = 0; c0 < n; c0 += 32 * 8) {
-        float x[8];
-        uint32_t ii[8];
+      for (uint32_t c0 = 0; c0 < n; c0 += 32 * kP3) {
+        float x[kP3];
+        uint32_t ii[kP3];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kP3; ++u) {
           const uint32_t c = c0 + 32 * u + lane;
           x[u] = c < n ? sv[c] : 0.0f;
           ii[u] = c < n ? si[c] : 0u;
         }
         __syncwarp();
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kP3; ++u) {
           const uint32_t key = mag_key(x[u]);
           const bool in = c0 + 32 * u + lane < n;
           if (in && (key & mask) == prefix) {
@@ -938,7 +939,7 @@ __device__ void emit_slots(const TopkArgs& A, const RankWs& w, int r) {
   uint32_t* __restrict__ idx = A.idx[r];
   float* __restrict__ val = A.val[r];
   const uint32_t lt = (1u << lane) - 1u;
-  constexpr int U = 4;  // rounds of 32 slots whose loads are issued together
+  constexpr int U = 8;  // rounds of 32 slots whose loads are issued together
   for (uint32_t c0 = 0; c0 < n; c0 += 32 * U) {
     float x[U];
     uint32_t ii[U];
