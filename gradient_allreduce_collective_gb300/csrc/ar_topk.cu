@@ -1057,27 +1057,38 @@ __global__ void __launch_bounds__(kThreads) k_sparse_scatter(const __grid_consta
   }
 }
 
-// Tile starts of the sparse fold: thread j of rank r (0 <= j <= nnz) writes
-// starts[t] = j for the tiles t after the tile of pair j - 1 up to the tile
-// of pair j (pairs with an index >= count, and j = nnz, count as tile
-// ntiles). With ascending indices every entry is written once; otherwise the
-// fold clamps what it reads.
+// Tile starts of the sparse fold: for each pair position p of rank r
+// (0 <= p <= nnz), starts[t] = p for the tiles t after the tile of pair p - 1
+// up to the tile of pair p (pairs with an index >= count, and p = nnz, count
+// as tile ntiles). A thread takes four consecutive positions, its five index
+// loads issued together. With ascending indices every entry is written once;
+// otherwise the fold clamps what it reads.
+constexpr int kBoundsPerThread = 4;
+
 __global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constant__ SparseArgs A) {
   pdl_begin();
   const int r = blockIdx.y;
   const uint64_t nnz = A.nnz[r];
-  const uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j > nnz) return;
+  const uint64_t p0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) * kBoundsPerThread;
+  if (p0 > nnz) return;
   const uint32_t* __restrict__ ix = A.idx[r];
-  auto tile_of = [&](uint64_t p) -> int64_t {
-    if (p >= nnz) return A.ntiles;
-    const uint32_t i = ix[p];
-    return i < A.count ? (int64_t)(i / A.tile) : (int64_t)A.ntiles;
-  };
-  const int64_t prev = j == 0 ? -1 : tile_of(j - 1);
-  const int64_t cur = tile_of(j);
+  // tiles of pairs p0 - 1 .. p0 + 3 (-1 before the first pair, ntiles past the last)
+  int64_t tl[kBoundsPerThread + 1];
+#pragma unroll
+  for (int u = 0; u <= kBoundsPerThread; ++u) {
+    const uint64_t q = p0 + u - 1;  // wraps to 2^64 - 1 for p0 = 0, u = 0
+    uint32_t i = 0;
+    if (q < nnz) i = ix[q];
+    tl[u] = (u == 0 && p0 == 0) ? -1
+          : (q >= nnz || i >= A.count) ? (int64_t)A.ntiles : (int64_t)(i / A.tile);
+  }
   uint32_t* st = A.starts + (uint64_t)r * (A.ntiles + 1);
-  for (int64_t t = prev + 1; t <= cur; ++t) st[t] = (uint32_t)j;
+#pragma unroll
+  for (int u = 0; u < kBoundsPerThread; ++u) {
+    const uint64_t p = p0 + u;
+    if (p > nnz) break;
+    for (int64_t t = tl[u] + 1; t <= tl[u + 1]; ++t) st[t] = (uint32_t)p;
+  }
 }
 
 // resident blocks of k_sparse_fold (32 KiB of shared memory each): the ring
@@ -1210,7 +1221,8 @@ cudaError_t launch_topk(const TopkArgs& a, bool vec, cudaStream_t stream) {
 }
 
 cudaError_t launch_sparse_fold(const SparseArgs& a, uint64_t max_nnz, cudaStream_t stream) {
-  const cudaError_t err = launch_pdl(k_sparse_bounds, dim3(grid_for(max_nnz + 1), a.nranks), 0, stream, a);
+  const cudaError_t err = launch_pdl(
+      k_sparse_bounds, dim3(grid_for((max_nnz + kBoundsPerThread) / kBoundsPerThread), a.nranks), 0, stream, a);
   if (err != cudaSuccess) return err;
   const size_t smem = (size_t)a.nranks * a.tile * sizeof(float);
   return a.tree ? launch_pdl(k_sparse_fold<true>, dim3(a.ntiles), smem, stream, a)
