@@ -4,11 +4,11 @@ callbacks, on a path where allocation is forbidden, or without the CUDA
 allocation API). It keeps its quantised codes and scales in a fixed array
 inside the library instead of a caller workspace.
 
-Its results must equal those of ar_allreduce_fp8 with a caller-provided
-workspace bit for bit (the same kernels run in the same order; the FP8 tests
-compare bit-exactly), on two calls in a row with different shapes, so the
-second call runs on the array the first one left filled. A call that needs
-more than the built-in array is refused with a clear error.
+Its results must equal the oracle's FP8 ring allreduce bit for bit, and those
+of ar_allreduce_fp8 with a caller-provided workspace on two calls in a row
+with different shapes, so the second call runs on the array the first one
+left filled. A call that needs more than the built-in array is refused with a
+clear error.
 
 This file is collected last, so a run that stops at the first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -18,6 +18,7 @@ import pytest
 import torch
 
 import gradient_allreduce_collective_gb300 as gar
+import oracle
 import synthgen
 from tests._dev import from_dev, to_dev
 
@@ -38,6 +39,24 @@ def _case(n, count, in_dtype, out_dtype, seed):
     send = [to_dev(a, in_dtype) for a in send_np]
     tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[out_dtype]
     return send, tdt
+
+
+@pytest.mark.parametrize("n,count,idt,odt,op,algo", [
+    (8, 128 * 700 + 77, "bf16", "bf16", "sum", "fused"),
+    (4, 128 * 300 + 5, "f32", "f16", "avg", "ring"),
+    (3, 128 * 41 + 100, "f16", "f32", "sum", "fused"),
+])
+def test_noalloc_matches_the_oracle(n, count, idt, odt, op, algo):
+    send_np = synthgen.ranks_normal(n, count, 1e-3, base_seed=300 + n, dtype=idt, outlier_p=1e-3, outlier_scale=100.0)
+    send = [to_dev(a, idt) for a in send_np]
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[odt]
+    out = [torch.full((count,), float("nan"), dtype=tdt, device="cuda") for _ in range(n)]
+    gar.ar_allreduce_fp8_noalloc(send, out, op, algo)
+    torch.cuda.synchronize()
+    want = oracle.fp8_ring_allreduce(send_np, idt, odt, op)[0]
+    for o in out:
+        got = from_dev(o)
+        assert got.tobytes() == np.ascontiguousarray(want).tobytes(), (n, count, op, algo)
 
 
 def test_noalloc_matches_caller_workspace_on_two_calls_in_a_row():
