@@ -741,7 +741,9 @@ def rows_summary(rows: dict, other: dict, ms_headline: float, peak: float) -> di
     if tk:
         c = tk["compress"]
         out["topk_compress"] = {"ms": round(c["ms"], 4), "frac_min_bytes": round(c["hbm_gbs_min_bytes"] / peak, 3),
-                                "frac_structure": round(c["frac_hbm_structure"], 3)}
+                                "frac_structure": round(c["frac_hbm_structure"], 3),
+                                "speculative_share": c.get("speculative_share"),
+                                "second_digit_in_pass1_share": c.get("second_digit_in_pass1_share")}
         sp = tk["sparse_allreduce"]
         out["sparse_allreduce"] = {"ms": round(sp["ms"], 4), "frac": round(sp["frac_hbm"], 3)}
     return out
