@@ -798,15 +798,27 @@ int or_fp8_hop_blocks_allreduce(const void *const *send, void *const *recv, int 
 /* vectors is the allreduce of their dense forms (zeros elsewhere) in the    */
 /* ring order. Parity unpinned as far as the pages go (they fix no tie rule */
 /* or formula); pinned by hand-computed ties, k = 0 and k = count, the       */
-/* partition a = s + e and brute force.                                      */
+/* partition a = s + e and brute force. |a| is compared as the binary32      */
+/* bit pattern with the sign cleared: for every number that is the order of  */
+/* the magnitudes (-0 and +0 tie). The pages leave NaN open; here a NaN      */
+/* ranks above every number and all NaNs tie (their payload is unspecified, */
+/* reading nan-order), so among NaNs the lower index comes first.            */
 /* ------------------------------------------------------------------------- */
 
 static const float *or_topk_keys;
 
+static uint32_t or_mag_key(float a)
+{
+    uint32_t u;
+    if (a != a) return 0x7FFFFFFFu;  /* every NaN: one key above +inf's */
+    memcpy(&u, &a, sizeof u);
+    return u & 0x7FFFFFFFu;
+}
+
 static int or_topk_cmp(const void *x, const void *y)
 {
     uint32_t i = *(const uint32_t *)x, j = *(const uint32_t *)y;
-    float a = fabsf(or_topk_keys[i]), b = fabsf(or_topk_keys[j]);
+    uint32_t a = or_mag_key(or_topk_keys[i]), b = or_mag_key(or_topk_keys[j]);
     if (a > b) return -1;
     if (a < b) return 1;
     return (i < j) ? -1 : (i > j);

@@ -440,6 +440,35 @@ def test_topk_hand_ties():
     assert e.tolist() == G.nums(g["k2_residual"])
 
 
+def _nan_class_equal(got, want):
+    """Bit-equal where `want` is a number, NaN where it is NaN (NaN payloads
+    are unspecified, reading nan-order)."""
+    got, want = np.asarray(got, dtype=np.float32), np.asarray(want, dtype=np.float32)
+    nan = np.isnan(want)
+    return np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+def test_topk_nans_rank_above_every_number_and_tie():
+    # Worked by hand: a NaN ranks above every number, +-inf included, and all
+    # NaNs tie whatever their sign and payload (the lower index first); -0 + 0
+    # is +0. Ranking: NaN (1), NaN (4), NaN (7), -inf (2), 3 (6), 2 (3), 1 (0), +0 (5).
+    bits = [0x3F800000, 0x7FC00001, 0xFF800000, 0x40000000, 0xFFC12345, 0x80000000, 0x40400000, 0x7FA00000]
+    grad = np.array(bits, dtype=np.uint32).view(np.float32)
+    res = np.zeros(8, dtype=np.float32)
+    nan = np.float32("nan")
+    cases = {
+        2: ([1, 4], [nan, nan], [1.0, 0.0, -np.inf, 2.0, 0.0, 0.0, 3.0, nan]),
+        4: ([1, 2, 4, 7], [nan, -np.inf, nan, nan], [1.0, 0.0, 0.0, 2.0, 0.0, 0.0, 3.0, 0.0]),
+        6: ([1, 2, 3, 4, 6, 7], [nan, -np.inf, 2.0, nan, 3.0, nan], [1.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0]),
+    }
+    for k, (want_idx, want_val, want_res) in cases.items():
+        idx, val, e = oracle.topk_compress(grad, res, k)
+        assert idx.tolist() == want_idx, k
+        assert _nan_class_equal(val, want_val), k
+        assert _nan_class_equal(e, want_res), k
+        assert not np.any(e.view(np.uint32) == 0x80000000)  # the kept entries and -0 + 0 are +0
+
+
 def test_topk_extremes_partition_and_brute_force():
     rng = np.random.default_rng(4)
     for count in (1, 7, 300, 5000):

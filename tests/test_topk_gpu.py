@@ -174,6 +174,63 @@ def test_topk_special_values():
         _check_against_oracle(g, e, k)
 
 
+def _nan_class_equal(got, want):
+    """Bit-equal where `want` is a number, NaN where it is NaN (NaN payloads
+    are unspecified: the device's add returns its own canonical NaN)."""
+    got, want = np.asarray(got, dtype=np.float32), np.asarray(want, dtype=np.float32)
+    nan = np.isnan(want)
+    return np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+def _nan_inputs(count, seed, n_nan, n_inf):
+    g = synthgen.normal_f32(count, seed, 1e-3)
+    rng = np.random.default_rng(seed)
+    pos = rng.choice(count, size=n_nan + n_inf, replace=False)
+    payload = rng.integers(1, 1 << 22, size=n_nan, dtype=np.uint32) | np.uint32(0x7F800000)
+    sign = rng.integers(0, 2, size=n_nan, dtype=np.uint32) << np.uint32(31)
+    g[pos[:n_nan]] = (payload | sign).view(np.float32)  # quiet and signalling, both signs
+    g[pos[n_nan:]] = np.where(rng.integers(0, 2, size=n_inf) == 1, np.inf, -np.inf).astype(np.float32)
+    return g
+
+
+@pytest.mark.parametrize("k", [50, 299, 300, 301, 2000])
+def test_topk_nans_rank_above_every_number(k):
+    # 300 NaNs (random payloads and signs, some signalling) and 40 infinities
+    # among small values: the NaNs tie above every number, the lower index
+    # first; k below, at and above the NaN count.
+    count = 50_000
+    g = _nan_inputs(count, 71, 300, 40)
+    e = np.zeros(count, dtype=np.float32)
+    gi, gv, ge = _gpu_topk(g, e, k)
+    oi, ov, oe = oracle.topk_compress(g, e, k)
+    assert np.array_equal(gi, oi)
+    assert _nan_class_equal(gv, ov) and _nan_class_equal(ge, oe)
+
+
+def test_topk_nans_on_the_speculative_path():
+    # Eight ranks large enough for the speculative pass 1, two calls on one
+    # workspace: rank 0 with fewer NaNs than k (T a number), rank 1 with more
+    # (T a NaN: the next hint is the infinity's key), the rest without.
+    n, count, k = 8, 5_242_880, 52_428
+    g_np = [synthgen.normal_f32(count, 500 + r, 1e-3) for r in range(n)]
+    g_np[0] = _nan_inputs(count, 501, 10_000, 100)
+    g_np[1] = _nan_inputs(count, 502, 60_000, 100)
+    grads = [to_dev(x, "f32") for x in g_np]
+    ws = torch.full((gar.ar_topk_workspace_bytes(n, count, k),), 0x5A, dtype=torch.uint8, device="cuda")
+    e_np = [np.zeros(count, dtype=np.float32) for _ in range(n)]
+    res = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(n)]
+    val = [torch.empty(k, dtype=torch.float32, device="cuda") for _ in range(n)]
+    for call in range(2):
+        gar.ar_topk_compress(grads, res, k, idx, val, ws)
+        torch.cuda.synchronize()
+        for r in (0, 1, 2):
+            oi, ov, e_np[r] = oracle.topk_compress(g_np[r], e_np[r], k)
+            assert np.array_equal(from_dev(idx[r]).view(np.uint32), oi), (call, r)
+            assert _nan_class_equal(from_dev(val[r]), ov), (call, r)
+            assert _nan_class_equal(from_dev(res[r]), e_np[r]), (call, r)
+
+
 def test_error_feedback_over_several_steps():
     count, k = 200_000, 2_000
     e_host = np.zeros(count, dtype=np.float32)
