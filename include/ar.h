@@ -348,11 +348,12 @@ ar_status_t ar_allreduce_fp8_noalloc(const void *const *sendbufs, void *const *r
  *   residuals[r] = a with the kept entries set to +0
  * so the dense form of (idx, val) plus the new residual equals a exactly.
  * |a| is compared through its bit pattern with the sign cleared (so -0 ties
- * +0, and a NaN ranks above every number).
+ * +0, and a NaN ranks above every number); a = g + e of a NaN is the device's
+ * one canonical NaN, so all NaNs tie and the lower index comes first.
  *
  * Workspace bytes for ar_topk_compress over nranks x `count` values keeping
- * k per rank (per rank about count / 4 bytes plus 32 * max(k, count / 256)
- * bytes, at most 4.25 bytes per value, plus 8 KiB; a multiple of 256 bytes);
+ * k per rank (per rank about 3 * count / 4 + 128 * k bytes, at most 4.25
+ * bytes per value, plus 8 KiB; a multiple of 256 bytes);
  * 0 if nranks is outside 1..AR_MAX_RANKS, count >= 2^32 or k > count. */
 size_t ar_topk_workspace_bytes(int nranks, size_t count, size_t k);
 
