@@ -14,14 +14,23 @@
 // + 10 bits). Pass 1 reads g and e once, writes a, and histograms the first
 // digit. Pass 2 reads a once more, histograms the second digit among the keys
 // in the first digit's bin, and compacts every key at or above that bin (all
-// that can still be kept, about 2 % of the values) in index order into the
-// tile's slots. Pass 3, the count of keys above and equal to T per tile, and
-// the emission read only the slots; if some tile's keys do not fit its slots
-// they read the data instead (same results). The block of each pass that
-// finishes last picks the digit or scans the per-tile counts, so the state
-// never leaves the device and no launch is spent on it. Keys above T are all
-// kept; of the keys equal to T, the first (k - #above) in index order. All
-// ranks of a call share each launch (grid.y = rank): six launches per call.
+// that can still be kept) in index order into the tile's slots. Pass 3, the
+// count of keys above and equal to T per tile, and the emission read only
+// the slots; if some tile's keys do not fit its slots they read the data
+// instead (same results). The block of each pass that finishes last picks
+// the digit or scans the per-tile counts, so the state never leaves the
+// device and no launch is spent on it. Keys above T are all kept; of the keys
+// equal to T, the first (k - #above) in index order. All ranks of a call
+// share each launch (grid.y = rank): six launches per call.
+//
+// On large calls the previous call's T, kept in the workspace, makes the
+// common case cheaper without changing any result: pass 1 also compacts the
+// values at or above T times a margin into the slots, and when at least k of
+// them fit, pass 2 reads the slots instead of the data (or, when T's first
+// digit held, has nothing left to do: pass 1 found the second digit too).
+// Pass 3 then compacts each tile's slots to the keys at or above the
+// two-digit prefix and, from a short list of the keys equal to it, derives
+// the per-tile counts itself, so the count pass only reads its flag.
 //
 // The sparse allreduce (SUM, AVG) densifies each output tile from every
 // rank's pairs in shared memory and folds it in the dense order, so only the
