@@ -1100,10 +1100,10 @@ __global__ void __launch_bounds__(kThreads) k_sparse_bounds(const __grid_constan
   }
 }
 
-// resident blocks of k_sparse_fold (32 KiB of shared memory each): the ring
-// order fits 32 registers, the recursive halving 48 (a 12-byte spill,
-// measured faster than 64 registers at 4 blocks)
-template <bool TREE> constexpr int kSparseBlocksPerSm = TREE ? 5 : 7;
+// resident blocks of k_sparse_fold (24 KiB of shared memory each): the ring
+// order fits 32 registers, eight blocks of 256 threads; the recursive
+// halving 48 (a 12-byte spill, measured faster than 64 registers at 4 blocks)
+template <bool TREE> constexpr int kSparseBlocksPerSm = TREE ? 5 : 8;
 
 // One tile per block: every rank's pairs of the tile scattered into shared
 // memory (zeros elsewhere), folded per element in the ring order of its
@@ -1111,7 +1111,7 @@ template <bool TREE> constexpr int kSparseBlocksPerSm = TREE ? 5 : 7;
 // outputs. The dense allreduce of the densified vectors gives the same bits.
 template <bool TREE>
 __global__ void __launch_bounds__(kThreads, kSparseBlocksPerSm<TREE>) k_sparse_fold(const __grid_constant__ SparseArgs A) {
-  pdl_wait();  // six waves: the next call's kernels launch as its last blocks exit
+  pdl_wait();  // seven waves: the next call's kernels launch as its last blocks exit
   extern __shared__ float sm[];  // nranks x tile
   const int N = A.nranks;
   const uint32_t T = A.tile;

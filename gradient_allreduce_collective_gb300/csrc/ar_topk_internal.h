@@ -187,9 +187,10 @@ struct SparseArgs {
 };
 
 // Tile length of the sparse fold for N ranks: N * tile floats of shared
-// memory stay at 32 KiB (a multiple of 128 elements, 128..4096).
+// memory stay at 24 KiB (a multiple of 128 elements, 128..4096), so that
+// eight blocks (plus the 1 KiB each reserves) fit the SM's 228 KiB.
 inline uint32_t sparse_tile(int nranks) {
-  uint32_t t = 8192u / (uint32_t)nranks / 128u * 128u;
+  uint32_t t = 6144u / (uint32_t)nranks / 128u * 128u;
   if (t < 128) t = 128;
   if (t > 4096) t = 4096;
   return t;

@@ -269,7 +269,7 @@ def test_sparse_allreduce_argument_errors(L):
     out = [0x20000000 + 0x1000000 * r for r in range(n)]
     ws = 0x30000000
     need = gar.ar_sparse_workspace_bytes(n, count)
-    tile = max(128, min(4096, 8192 // n // 128 * 128))
+    tile = max(128, min(4096, 6144 // n // 128 * 128))
     assert need == math.ceil(n * (math.ceil(count / tile) + 1) * 4 / 256) * 256
     assert gar.ar_sparse_workspace_bytes(0, 10) == 0 and gar.ar_sparse_workspace_bytes(1, 1 << 32) == 0
     nnz = (ctypes.c_size_t * n)(10, 0, 1000, 5)
