@@ -119,9 +119,8 @@ cudaError_t launch_bucket_t(const BucketArgs& a, cudaStream_t stream) {
   const uint32_t total = a.tile_start[a.nt];
   if (total == 0) return cudaSuccess;
   const unsigned grid = total < 0x7FFFFFFFu ? total : 0x7FFFFFFFu;  // one block per tile
-  if (a.nranks <= 8) launch_pdl(k_bucket_reduce<DT, OP, MODE, 8>, dim3(grid), 0, stream, a);
-  else launch_pdl(k_bucket_reduce<DT, OP, MODE, kMaxRanks>, dim3(grid), 0, stream, a);
-  return cudaGetLastError();
+  return a.nranks <= 8 ? launch_pdl(k_bucket_reduce<DT, OP, MODE, 8>, dim3(grid), 0, stream, a)
+                       : launch_pdl(k_bucket_reduce<DT, OP, MODE, kMaxRanks>, dim3(grid), 0, stream, a);
 }
 
 template <int DT> cudaError_t launch_bucket_dt(int op, int mode, const BucketArgs& a, cudaStream_t s) {

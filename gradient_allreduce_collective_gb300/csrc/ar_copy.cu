@@ -70,8 +70,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
 
 template <int U> cudaError_t launch_gather_u(const GatherArgs& a, cudaStream_t stream) {
   const uint64_t items = a.units > a.tail_bytes ? a.units : a.tail_bytes;
-  launch_pdl(k_gather<U>, dim3(grid_for(items)), 0, stream, a);
-  return cudaGetLastError();
+  return launch_pdl(k_gather<U>, dim3(grid_for(items)), 0, stream, a);
 }
 
 cudaError_t launch_gather(int unit_bytes, const GatherArgs& a, cudaStream_t stream) {
@@ -126,8 +125,7 @@ cudaError_t launch_multicopy(const MultiCopyArgs& a, cudaStream_t stream) {
   if (total == 0) return cudaSuccess;
   // one block per tile
   const unsigned grid = total < 0x7FFFFFFFu ? total : 0x7FFFFFFFu;
-  launch_pdl(k_multicopy, dim3(grid), 0, stream, a);
-  return cudaGetLastError();
+  return launch_pdl(k_multicopy, dim3(grid), 0, stream, a);
 }
 
 }  // namespace gar

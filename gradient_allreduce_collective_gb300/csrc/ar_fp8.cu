@@ -130,11 +130,8 @@ template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& 
     if (nfull > 0) {
       const uint64_t warps = (nfull + kQuantUnroll * BPW - 1) / (kQuantUnroll * BPW);
       const dim3 grid(grid_for(warps * 32), (unsigned)a.nranks);
-      if constexpr (Fmt<DT>::bytes == 2)
-        launch_pdl(k_fp8_quant_vec16<DT>, grid, 0, stream, a);
-      else
-        launch_pdl(k_fp8_quant_vec<DT>, grid, 0, stream, a);
-      const cudaError_t e = cudaGetLastError();
+      const cudaError_t e = Fmt<DT>::bytes == 2 ? launch_pdl(k_fp8_quant_vec16<DT>, grid, 0, stream, a)
+                                                : launch_pdl(k_fp8_quant_vec<DT>, grid, 0, stream, a);
       if (e != cudaSuccess) return e;
     }
     b.first_block = nfull;
@@ -143,8 +140,7 @@ template <int DT> cudaError_t launch_fp8_quant_dt(bool vec, const Fp8QuantArgs& 
   }
   if (b.first_block < nblocks) {
     const uint64_t warps = (uint64_t)a.nranks * (nblocks - b.first_block);
-    launch_pdl(k_fp8_quant_scalar<DT>, dim3(grid_for(warps * 32)), 0, stream, b);
-    return cudaGetLastError();
+    return launch_pdl(k_fp8_quant_scalar<DT>, dim3(grid_for(warps * 32)), 0, stream, b);
   }
   return cudaSuccess;
 }
@@ -291,10 +287,9 @@ cudaError_t launch_fp8_reduce_n(const Fp8ReduceArgs& a, cudaStream_t stream) {
   const uint64_t items = a.vec ? a.count / (16 / Fmt<ODT>::bytes) : a.count;
   const dim3 grid(grid_for(items > 0 ? items : a.count));
   if constexpr (MODE == MODE_FUSED_RING && MAXN <= 16 && OP != OP_AVG && Fmt<ODT>::bytes == 2)
-    launch_pdl(k_fp8_reduce_sum16<ODT, OP, MAXN>, grid, 0, stream, a);
+    return launch_pdl(k_fp8_reduce_sum16<ODT, OP, MAXN>, grid, 0, stream, a);
   else
-    launch_pdl(k_fp8_reduce<ODT, OP, MODE, MAXN>, grid, 0, stream, a);
-  return cudaGetLastError();
+    return launch_pdl(k_fp8_reduce<ODT, OP, MODE, MAXN>, grid, 0, stream, a);
 }
 
 template <int ODT, int OP>

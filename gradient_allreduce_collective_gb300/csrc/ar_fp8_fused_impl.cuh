@@ -318,19 +318,18 @@ cudaError_t launch_fused_n(bool vec, const Fp8FusedArgs& a, cudaStream_t stream)
     const uint64_t nfull = a.count / kFp8Block;
     if (nfull > 0) {
       const uint64_t warps = (nfull + BPW - 1) / BPW;
+      cudaError_t e;
       if constexpr (MODE == MODE_FUSED_RING && Fmt<IDT>::bytes == 2)
-        launch_pdl(k_fp8_fused_pair<IDT, ODT, OP, MAXN>, dim3(grid_for(warps * 32)), 0, stream, a);
+        e = launch_pdl(k_fp8_fused_pair<IDT, ODT, OP, MAXN>, dim3(grid_for(warps * 32)), 0, stream, a);
       else
-        launch_pdl(k_fp8_fused_vec<IDT, ODT, OP, MODE, MAXN>, dim3(grid_for(warps * 32)), 0, stream, a);
-      const cudaError_t e = cudaGetLastError();
+        e = launch_pdl(k_fp8_fused_vec<IDT, ODT, OP, MODE, MAXN>, dim3(grid_for(warps * 32)), 0, stream, a);
       if (e != cudaSuccess) return e;
     }
   }
   const uint64_t nblocks = (a.count + kFp8Block - 1) / kFp8Block;
   const uint64_t tasks = (uint64_t)a.nlist + (nblocks - a.first_block);
   if (tasks == 0) return cudaSuccess;
-  launch_pdl(k_fp8_fused_elem<IDT, ODT, OP, MODE, MAXN>, dim3(grid_for(tasks * 32)), 0, stream, a);
-  return cudaGetLastError();
+  return launch_pdl(k_fp8_fused_elem<IDT, ODT, OP, MODE, MAXN>, dim3(grid_for(tasks * 32)), 0, stream, a);
 }
 
 template <int IDT, int ODT, int OP>

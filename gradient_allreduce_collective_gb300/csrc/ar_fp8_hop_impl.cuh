@@ -300,9 +300,9 @@ cudaError_t launch_hop_op(const Fp8HopArgs& a, cudaStream_t s) {
   for (int r = 0; r < a.nranks; ++r)
     vec = vec && reinterpret_cast<uintptr_t>(a.src[r]) % (4 * Fmt<IDT>::bytes) == 0 &&
           reinterpret_cast<uintptr_t>(a.dst[r]) % (4 * Fmt<ODT>::bytes) == 0;
-#define GAR_HOP(MAXNV)                                                        \
-  if (vec) launch_pdl(k_fp8_hop<IDT, ODT, OP, MAXNV, true>, dim3(grid), 0, s, a); \
-  else launch_pdl(k_fp8_hop<IDT, ODT, OP, MAXNV, false>, dim3(grid), 0, s, a);
+#define GAR_HOP(MAXNV)                                                                 \
+  return vec ? launch_pdl(k_fp8_hop<IDT, ODT, OP, MAXNV, true>, dim3(grid), 0, s, a) \
+             : launch_pdl(k_fp8_hop<IDT, ODT, OP, MAXNV, false>, dim3(grid), 0, s, a);
   if (a.nranks <= 8) {
     GAR_HOP(8)
   } else if (a.nranks <= 16) {
@@ -311,7 +311,6 @@ cudaError_t launch_hop_op(const Fp8HopArgs& a, cudaStream_t s) {
     GAR_HOP(kMaxRanks)
   }
 #undef GAR_HOP
-  return cudaGetLastError();
 }
 
 template <int IDT, int ODT> cudaError_t launch_hop_io(int op, const Fp8HopArgs& a, cudaStream_t s) {

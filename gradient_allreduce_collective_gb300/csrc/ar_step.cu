@@ -65,8 +65,7 @@ __global__ void __launch_bounds__(kThreads) k_step_combine(const __grid_constant
 template <int DT, int OP> cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
   const uint32_t total = a.tile_start[a.ntasks];
   if (total == 0) return cudaSuccess;
-  launch_pdl(k_step_combine<DT, OP>, dim3(total), 0, s, a);  // one block per tile
-  return cudaGetLastError();
+  return launch_pdl(k_step_combine<DT, OP>, dim3(total), 0, s, a);  // one block per tile
 }
 
 template <int DT> cudaError_t launch_step_dt(int op, const StepArgs& a, cudaStream_t s) {
@@ -175,9 +174,8 @@ template <int DT, int OP, bool A32, bool B32>
 cudaError_t launch_step16_ab(bool fin, const StepArgs& a, cudaStream_t s) {
   const uint32_t total = a.tile_start[a.ntasks];
   if (total == 0) return cudaSuccess;
-  if (fin) launch_pdl(k_step_combine16<DT, OP, A32, B32, true>, dim3(total), 0, s, a);
-  else launch_pdl(k_step_combine16<DT, OP, A32, B32, false>, dim3(total), 0, s, a);
-  return cudaGetLastError();
+  return fin ? launch_pdl(k_step_combine16<DT, OP, A32, B32, true>, dim3(total), 0, s, a)
+             : launch_pdl(k_step_combine16<DT, OP, A32, B32, false>, dim3(total), 0, s, a);
 }
 
 template <int DT, int OP>
