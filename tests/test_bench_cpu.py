@@ -1,7 +1,8 @@
 """Host-side helpers of bench.py, without a GPU: the byte models the bench
 divides its times by, the compact per-row summary that travels with the
-headline line, and the lookup of a profiled DRAM traffic figure (used only
-while the profiled kernel's sources are unchanged)."""
+headline line, the lookup of a profiled DRAM traffic figure (used only
+while the profiled kernel's sources are unchanged), and the reference arm's
+JSON line (the CPU oracle, timed on a small bucket here)."""
 import bench
 
 
@@ -69,3 +70,34 @@ def test_profiled_traffic_only_while_the_sources_match():
     assert bench.profiled_traffic("no_such_profile.md") is None
     # hashed over other sources, the recorded hash no longer matches
     assert bench.profiled_traffic(name, files=bench.FUSED_KERNEL_SOURCES[:1]) is None
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    # the reference arm times the CPU oracle; a small bucket keeps it quick
+    import json
+
+    monkeypatch.setattr(bench, "COUNT", 8192)
+    for key in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(key, raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1"]) == 0
+    lines = [s for s in capsys.readouterr().out.splitlines() if s.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3  # at least 3 warm-up steps
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None and d["dtype"] == "f32"
+    assert d["config"]["count_per_rank"] == 8192 and "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["value"] == d["value"] and cb["kind"] == "oracle" and cb["cores"] == 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # value is the busbw of the timed sample: 2 (N-1)/N x bytes per rank / time
+    n = 8192
+    assert abs(d["value"] - bench.busbw_gbs(n * 4, d["ms_per_step"] * 1e-3)) < 1e-6 * d["value"]
+
+
+def test_reference_arm_other_ranks_print_nothing(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
