@@ -124,7 +124,12 @@ ar_status_t ok() {
   return AR_SUCCESS;
 }
 
+// A CUDA error is reported once, through this library's status and message:
+// it is also taken off the runtime's per-thread last-error slot, so that a
+// later check elsewhere (a framework's own launch check) does not report it
+// again.
 ar_status_t cuda_fail(cudaError_t e, const char* what) {
+  (void)cudaGetLastError();
   return fail(AR_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 

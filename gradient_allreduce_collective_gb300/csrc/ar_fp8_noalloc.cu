@@ -77,6 +77,7 @@ const DriverFns& driver_fns() {
 }
 
 ar_status_t cuda_error(const char* what, cudaError_t e) {
+  (void)cudaGetLastError();  // reported here, not again by a later check elsewhere
   gar::set_last_error(std::string(what) + ": " + cudaGetErrorString(e));
   return AR_ERR_CUDA;
 }

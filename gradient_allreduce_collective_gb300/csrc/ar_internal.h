@@ -200,10 +200,7 @@ __device__ __forceinline__ void pdl_begin() {
 // Launch with programmatic stream serialization: the grid may be placed on
 // the SMs while the previous grid in the stream finishes. The kernel must
 // call pdl_begin() before it touches memory that an earlier kernel writes or
-// reads; stream order and results stay as for <<<...>>>. Returns the launch's
-// status; a failed launch's error is taken off the thread's last-error slot
-// here, so the caller reports it once and a later check elsewhere does not
-// see it again.
+// reads; stream order and results stay as for <<<...>>>.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg{};
@@ -216,9 +213,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, size_t smem, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
-  if (e != cudaSuccess) (void)cudaGetLastError();
-  return e;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace gar

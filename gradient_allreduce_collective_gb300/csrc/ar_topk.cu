@@ -1256,6 +1256,11 @@ ar_status_t tk_fail(ar_status_t st, const std::string& msg) {
   gar::set_last_error(msg);
   return st;
 }
+// a CUDA error, reported here and taken off the runtime's last-error slot
+ar_status_t tk_cuda_fail(const char* what, cudaError_t e) {
+  (void)cudaGetLastError();
+  return tk_fail(AR_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
 ar_status_t tk_ok() {
   gar::set_last_error("");
   return AR_SUCCESS;
@@ -1331,7 +1336,7 @@ ar_status_t ar_topk_compress(const float* const* grads, float* const* residuals,
   a.k = (uint32_t)k;
   a.nranks = nranks;
   const cudaError_t e = gar::launch_topk(a, vec, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("top-k launch: ") + cudaGetErrorString(e));
+  if (e != cudaSuccess) return tk_cuda_fail("top-k launch", e);
   return tk_ok();
 }
 
@@ -1403,16 +1408,16 @@ ar_status_t ar_sparse_allreduce(const uint32_t* const* idx, const float* const* 
     f.vec = 1;
     for (int r = 0; r < nranks; ++r) f.vec = f.vec && tk_addr(recvbufs[r]) % 16 == 0;
     const cudaError_t e = gar::launch_sparse_fold(f, max_nnz, s);
-    if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("sparse fold launch: ") + cudaGetErrorString(e));
+    if (e != cudaSuccess) return tk_cuda_fail("sparse fold launch", e);
     return tk_ok();
   }
   // MIN / MAX: the dense forms in the outputs, then the dense allreduce in place
   for (int r = 0; r < nranks; ++r) {
     const cudaError_t e = cudaMemsetAsync(recvbufs[r], 0, b, s);
-    if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("zeroing the outputs: ") + cudaGetErrorString(e));
+    if (e != cudaSuccess) return tk_cuda_fail("zeroing the outputs", e);
   }
   const cudaError_t e = gar::launch_sparse_scatter(a, s);
-  if (e != cudaSuccess) return tk_fail(AR_ERR_CUDA, std::string("sparse scatter launch: ") + cudaGetErrorString(e));
+  if (e != cudaSuccess) return tk_cuda_fail("sparse scatter launch", e);
   std::vector<const void*> in(recvbufs, recvbufs + nranks);
   std::vector<void*> out(recvbufs, recvbufs + nranks);
   return ar_allreduce(in.data(), out.data(), nranks, count, AR_F32, op, algo, stream);
