@@ -383,9 +383,12 @@ ar_status_t ar_topk_compress(const float *const *grads, float *const *residuals,
                              size_t k, uint32_t *const *idx, float *const *val, void *workspace, size_t ws_bytes,
                              ar_stream_t stream);
 
-/* Workspace bytes for ar_sparse_allreduce with SUM or AVG (a multiple of
- * 256; about nranks * count / 2048 bytes); 0 if nranks is outside
- * 1..AR_MAX_RANKS or count >= 2^32. */
+/* Workspace bytes for ar_sparse_allreduce with SUM or AVG: one uint32 per
+ * rank and output tile boundary, 4 * nranks * (ceil(count / T) + 1) rounded
+ * up to a multiple of 256, where the tile T is 6144 / nranks rounded down to
+ * a multiple of 128 and kept within 128..4096 (768 values at 8 ranks, about
+ * count / 24 bytes); 0 if nranks is outside 1..AR_MAX_RANKS or
+ * count >= 2^32. */
 size_t ar_sparse_workspace_bytes(int nranks, size_t count);
 
 /* Allreduce of sparse vectors ([GL] §勾配圧縮技術): rank r contributes the

@@ -269,8 +269,13 @@ def test_sparse_allreduce_argument_errors(L):
     out = [0x20000000 + 0x1000000 * r for r in range(n)]
     ws = 0x30000000
     need = gar.ar_sparse_workspace_bytes(n, count)
-    tile = max(128, min(4096, 6144 // n // 128 * 128))
-    assert need == math.ceil(n * (math.ceil(count / tile) + 1) * 4 / 256) * 256
+    # one boundary word per rank and output tile; the tile keeps N x tile
+    # floats of shared memory at most 24 KiB (within 128..4096 values)
+    for nn, cc in [(n, count), (1, 5), (2, 10**6), (3, 6145), (8, 6_553_600), (16, 767), (48, 10**5), (49, 129),
+                   (64, 10**7 + 3)]:
+        tile = max(128, min(4096, 6144 // nn // 128 * 128))
+        assert gar.ar_sparse_workspace_bytes(nn, cc) == math.ceil(nn * (math.ceil(cc / tile) + 1) * 4 / 256) * 256
+    assert gar.ar_sparse_workspace_bytes(8, 6_553_600) == 273_152  # 8 x 8,534 words: 768-value tiles
     assert gar.ar_sparse_workspace_bytes(0, 10) == 0 and gar.ar_sparse_workspace_bytes(1, 1 << 32) == 0
     nnz = (ctypes.c_size_t * n)(10, 0, 1000, 5)
 
